@@ -1,0 +1,413 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct CPU reference for the weight-only
+ * quantized GEMV formats.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the oracle that the CUDA library is
+ * checked against.  Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load it.  It shares no code, header, table or constant
+ * with the CUDA library, and the CUDA library never loads it.
+ *
+ * Every dot product accumulates in double and is returned in double.  With the
+ * workloads' value ranges each product term is exact in double (int4 x f32
+ * scale x f32/bf16 activation, e4m3 x f32 x bf16, fp16-affine x bf16), so the
+ * only rounding is the order of summation.  Each function cites the passage
+ * of the page it follows:
+ *
+ *   [colibri #457]  "metal: grouped-int4 (fmt=4) GEMV support", sections 3-5, 11
+ *   [colibri #528]  "fmt=7: fp8-e4m3-b128 passthrough weight format", Design
+ *   [hipfire MQ4V2] "MQ4 V2" docs, sections 1e, 2, 3, 4
+ *
+ * No function here blocks, fuses or reorders beyond what its definition
+ * states; loops run in the order the definition reads.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Scalar number formats                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* OCP 8-bit floating point, E4M3 "FN" variant ([colibri #528] Design: the
+ * decode table is exact OCP E4M3-FN; the only NaN codes have every exponent
+ * bit and every mantissa bit set; an all-ones exponent is NOT infinity).
+ *   sign s = bit 7, exponent e = bits 6..3 (bias 7), mantissa m = bits 2..0
+ *   e == 15 && m == 7 : NaN (codes 0x7F and 0xFF)
+ *   e == 0            : subnormal, (-1)^s * 2^(1-7) * (m/8)
+ *   otherwise         : normal,    (-1)^s * 2^(e-7) * (1 + m/8)            */
+double oracle_e4m3_value(uint8_t code)
+{
+    int s = (code >> 7) & 1;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, 1 - 7);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* IEEE 754 binary16: sign bit 15, exponent bits 14..10 (bias 15), fraction
+ * bits 9..0.  Used for the MQ4-V2 header ([hipfire MQ4V2] section 2).        */
+double oracle_f16_value(uint16_t h)
+{
+    int s = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double v;
+    if (e == 31)
+        v = f ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)f, -24);                 /* subnormal: f * 2^-24 */
+    else
+        v = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    return s ? -v : v;
+}
+
+/* binary32 -> binary16, round to nearest, ties to even (IEEE 754 default).
+ * Written from the definition: find the binade, scale the value so that one
+ * unit in the last place of the target is 1.0, round to the nearest integer
+ * with ties going to even, and re-assemble.  All the double arithmetic here
+ * is exact (power-of-two scaling of a value with at most 24 significant
+ * bits), so rint() does the only rounding, in the default rounding mode.    */
+uint16_t oracle_f16_from_f32(float f)
+{
+    double a = fabs((double)f);
+    uint16_t sign = signbit(f) ? 0x8000u : 0u;
+    if (isnan(f))
+        return (uint16_t)(sign | 0x7E00u);
+    if (a >= 65520.0)            /* halfway between 65504 and 2^16 and above */
+        return (uint16_t)(sign | 0x7C00u);
+    if (a < ldexp(1.0, -14)) {   /* subnormal range: ulp is 2^-24 */
+        double q = rint(a / ldexp(1.0, -24));
+        /* q == 1024 rounds up into the smallest normal; the bit pattern
+         * 0x0400 is exactly that, so no special case is needed.            */
+        return (uint16_t)(sign | (uint16_t)q);
+    }
+    int e2;
+    (void)frexp(a, &e2);         /* a = fr * 2^e2 with fr in [0.5, 1) */
+    int e = e2 - 1;              /* a in [2^e, 2^(e+1)) */
+    double frac = rint((a / ldexp(1.0, e) - 1.0) * 1024.0);
+    if (frac >= 1024.0) {        /* rounded up to the next binade */
+        frac = 0.0;
+        e += 1;
+    }
+    if (e + 15 >= 31)
+        return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)frac);
+}
+
+/* bfloat16 is the upper half of a binary32: widening is exact. */
+double oracle_bf16_value(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* fmt=4: grouped int4 ([colibri #457] sections 3, 11)                       */
+/*   w: O rows of rb = (I+1)/2 bytes; element i of row o sits in byte i/2,   */
+/*      the low nibble for even i, the high nibble for odd i; the stored     */
+/*      nibble n means the integer n - 8.                                    */
+/*   scales: f32 [O, ng], ng = ceil(I/gs); element i uses scale[o*ng + i/gs] */
+/*   y[s,o] = sum_i (n(o,i) - 8) * scale[o, i/gs] * x[s,i]                   */
+/* The scale multiplies every term (per group, before summing across         */
+/* groups); it is never applied once to the finished row sum.                */
+/* ------------------------------------------------------------------------ */
+
+static int i4g_value(const uint8_t *w, size_t rb, int o, int i)
+{
+    uint8_t byte = w[(size_t)o * rb + (size_t)(i / 2)];
+    int nib = (i % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+    return nib - 8;
+}
+
+/* y and mag are double [S, O].  mag[s,o] = sum_i |term_i| is the magnitude
+ * that the relative tolerance is measured against ([colibri #457] section 5:
+ * per-element |delta| / sum |x_i * (n-8) * scale|).                         */
+void oracle_qgemv_i4g(double *y, double *mag, const float *x, const uint8_t *w,
+                      const float *scales, int S, int I, int O, int gs)
+{
+    size_t rb = ((size_t)I + 1) / 2;
+    size_t ng = ((size_t)I + (size_t)gs - 1) / (size_t)gs;
+    for (int s = 0; s < S; ++s) {
+        for (int o = 0; o < O; ++o) {
+            double acc = 0.0, m = 0.0;
+            for (int i = 0; i < I; ++i) {
+                double q = (double)i4g_value(w, rb, o, i);
+                double sc = (double)scales[(size_t)o * ng + (size_t)(i / gs)];
+                double t = q * sc * (double)x[(size_t)s * I + i];
+                acc += t;
+                m += fabs(t);
+            }
+            y[(size_t)s * O + o] = acc;
+            mag[(size_t)s * O + o] = m;
+        }
+    }
+}
+
+/* Batched prefill for fmt=4: the same sum with bf16 activations X[M, I]
+ * ([colibri #457] section 4: the large-batch GEMM path computes the same
+ * grouped product as the GEMV).                                             */
+void oracle_qgemm_i4g(double *Y, double *mag, const uint16_t *X, const uint8_t *w,
+                      const float *scales, int M, int I, int O, int gs)
+{
+    size_t rb = ((size_t)I + 1) / 2;
+    size_t ng = ((size_t)I + (size_t)gs - 1) / (size_t)gs;
+    for (int s = 0; s < M; ++s) {
+        for (int o = 0; o < O; ++o) {
+            double acc = 0.0, m = 0.0;
+            for (int i = 0; i < I; ++i) {
+                double q = (double)i4g_value(w, rb, o, i);
+                double sc = (double)scales[(size_t)o * ng + (size_t)(i / gs)];
+                double t = q * sc * oracle_bf16_value(X[(size_t)s * I + i]);
+                acc += t;
+                m += fabs(t);
+            }
+            Y[(size_t)s * O + o] = acc;
+            mag[(size_t)s * O + o] = m;
+        }
+    }
+}
+
+/* Symmetric per-group int4 quantizer used to build fmt=4 weights.
+ *   scale_g = max_{i in g} |w_i| / 7          (binary32 division)
+ *   q_i     = clamp(rint(w_i / scale_g), -8, 7), stored as q_i + 8
+ *   an all-zero group gets scale 0 and every nibble 8 (value 0).
+ * An odd I leaves the high nibble of each row's last byte unused; it is
+ * written as 8 (value 0).  The rounding is binary32 round-to-nearest-even
+ * on both the division and rint, so any implementation taking the same
+ * binary32 steps produces identical bytes.                                  */
+void oracle_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs)
+{
+    size_t rb = ((size_t)I + 1) / 2;
+    size_t ng = ((size_t)I + (size_t)gs - 1) / (size_t)gs;
+    for (int o = 0; o < O; ++o) {
+        memset(wq + (size_t)o * rb, 0x88, rb);
+        for (size_t g = 0; g < ng; ++g) {
+            int i0 = (int)(g * (size_t)gs);
+            int i1 = i0 + gs < I ? i0 + gs : I;
+            float amax = 0.0f;
+            for (int i = i0; i < i1; ++i) {
+                float a = fabsf(w[(size_t)o * I + i]);
+                if (a > amax)
+                    amax = a;
+            }
+            volatile float sc = amax / 7.0f;
+            scales[(size_t)o * ng + g] = sc;
+            for (int i = i0; i < i1; ++i) {
+                int q = 0;
+                if (sc != 0.0f) {
+                    volatile float r = w[(size_t)o * I + i] / sc;
+                    float qr = rintf(r);
+                    if (qr < -8.0f) qr = -8.0f;
+                    if (qr > 7.0f) qr = 7.0f;
+                    q = (int)qr;
+                }
+                uint8_t nib = (uint8_t)(q + 8);
+                uint8_t *byte = wq + (size_t)o * rb + (size_t)(i / 2);
+                if (i % 2 == 0)
+                    *byte = (uint8_t)((*byte & 0xF0) | nib);
+                else
+                    *byte = (uint8_t)((*byte & 0x0F) | (nib << 4));
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* fmt=7: FP8-e4m3, 128x128 block scales ([colibri #528] Design)             */
+/*   w: O*I e4m3 codes, row-major [O, I]                                     */
+/*   scale_inv: f32, one per 128x128 block, ceil(O/128) x ceil(I/128),       */
+/*              row-major block order                                        */
+/*   W[o,i] = e4m3(w[o*I+i]) * scale_inv[(o/128)*ceil(I/128) + i/128]        */
+/*   (multiply, not divide); partial edge blocks use the same indexing.      */
+/*   A NaN weight makes its output row NaN through the sum.                  */
+/* ------------------------------------------------------------------------ */
+void oracle_qgemv_fp8b128(double *y, double *mag, const uint16_t *x, const uint8_t *w,
+                          const float *scale_inv, int S, int I, int O)
+{
+    size_t nbi = ((size_t)I + 127) / 128;
+    for (int s = 0; s < S; ++s) {
+        for (int o = 0; o < O; ++o) {
+            double acc = 0.0, m = 0.0;
+            for (int i = 0; i < I; ++i) {
+                double wv = oracle_e4m3_value(w[(size_t)o * I + i]);
+                double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];
+                double t = wv * sc * oracle_bf16_value(x[(size_t)s * I + i]);
+                acc += t;
+                m += fabs(t);
+            }
+            y[(size_t)s * O + o] = acc;
+            mag[(size_t)s * O + o] = m;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* MQ4-V2 (qt=44) ([hipfire MQ4V2] sections 2 and 4)                         */
+/*   136 bytes per 256 weights, little-endian:                               */
+/*     [0,4)   dword hA: low 16 bits fp16 scale, high 16 bits fp16 zero,     */
+/*             for weights 0..127 of the block (half 0)                      */
+/*     [4,8)   dword hB: the same for weights 128..255 (half 1)              */
+/*     [8,136) 128 bytes of nibbles; weight j of the block sits in payload   */
+/*             byte j/2, low nibble for even j                               */
+/*   w_j = q_j * scale[h] + zero[h], q_j in 0..15,                           */
+/*   h = 1 when the weight's payload byte offset is >= 64 (j >= 128).        */
+/*   Row o holds I/256 blocks back to back; I must be a multiple of 256.     */
+/* ------------------------------------------------------------------------ */
+
+static uint32_t le32(const uint8_t *p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) |
+           ((uint32_t)p[3] << 24);
+}
+
+double oracle_mq4v2_weight(const uint8_t *block, int j)
+{
+    int byte_off = j / 2;                    /* offset within the payload */
+    int h = byte_off >= 64 ? 1 : 0;
+    uint32_t hd = le32(block + 4 * h);
+    double sc = oracle_f16_value((uint16_t)(hd & 0xFFFFu));
+    double z = oracle_f16_value((uint16_t)(hd >> 16));
+    uint8_t byte = block[8 + byte_off];
+    int q = (j % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+    return (double)q * sc + z;
+}
+
+void oracle_qgemv_mq4v2(double *y, double *mag, const uint16_t *x, const uint8_t *blocks,
+                        int S, int I, int O)
+{
+    size_t nb = (size_t)I / 256;
+    for (int s = 0; s < S; ++s) {
+        for (int o = 0; o < O; ++o) {
+            double acc = 0.0, m = 0.0;
+            for (size_t b = 0; b < nb; ++b) {
+                const uint8_t *blk = blocks + ((size_t)o * nb + b) * 136;
+                for (int j = 0; j < 256; ++j) {
+                    double t = oracle_mq4v2_weight(blk, j) *
+                               oracle_bf16_value(x[(size_t)s * I + b * 256 + (size_t)j]);
+                    acc += t;
+                    m += fabs(t);
+                }
+            }
+            y[(size_t)s * O + o] = acc;
+            mag[(size_t)s * O + o] = m;
+        }
+    }
+}
+
+/* Encoder ([hipfire MQ4V2] section 3).  Per 128-weight half:
+ *   lo = min, hi = max, step = (hi - lo) / 15       (binary32)
+ *   scale = f16(step), zero = f16(lo)               (stored)
+ *   st = f32(scale), z = f32(zero)                  (round-tripped)
+ *   q = clamp(rint((w - z) / st), 0, 15)            (binary32)
+ * A constant half (hi == lo) stores scale 0, zero f16(lo) and q = 0.
+ * Reading taken where the page is silent: a half whose rounded step is 0
+ * (step below half the smallest fp16 subnormal) is treated like a constant
+ * half (q = 0) instead of dividing by zero.                                 */
+void oracle_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I)
+{
+    size_t nb = (size_t)I / 256;
+    for (int o = 0; o < O; ++o) {
+        for (size_t b = 0; b < nb; ++b) {
+            uint8_t *blk = blocks + ((size_t)o * nb + b) * 136;
+            const float *src = w + (size_t)o * I + b * 256;
+            memset(blk, 0, 136);
+            for (int h = 0; h < 2; ++h) {
+                const float *hw = src + 128 * h;
+                float lo = hw[0], hi = hw[0];
+                for (int j = 1; j < 128; ++j) {
+                    if (hw[j] < lo) lo = hw[j];
+                    if (hw[j] > hi) hi = hw[j];
+                }
+                volatile float diff = hi - lo;
+                volatile float step = diff / 15.0f;
+                uint16_t sc16 = (hi == lo) ? (uint16_t)0 : oracle_f16_from_f32(step);
+                uint16_t z16 = oracle_f16_from_f32(lo);
+                float st = (float)oracle_f16_value(sc16);
+                float z = (float)oracle_f16_value(z16);
+                uint32_t hd = (uint32_t)sc16 | ((uint32_t)z16 << 16);
+                blk[4 * h + 0] = (uint8_t)(hd & 0xFF);
+                blk[4 * h + 1] = (uint8_t)((hd >> 8) & 0xFF);
+                blk[4 * h + 2] = (uint8_t)((hd >> 16) & 0xFF);
+                blk[4 * h + 3] = (uint8_t)((hd >> 24) & 0xFF);
+                for (int j = 0; j < 128; ++j) {
+                    int q = 0;
+                    if (st != 0.0f) {
+                        volatile float d = hw[j] - z;
+                        volatile float r = d / st;
+                        float qr = rintf(r);
+                        if (qr < 0.0f) qr = 0.0f;
+                        if (qr > 15.0f) qr = 15.0f;
+                        q = (int)qr;
+                    }
+                    int jj = 128 * h + j;
+                    uint8_t *byte = blk + 8 + jj / 2;
+                    if (jj % 2 == 0)
+                        *byte = (uint8_t)((*byte & 0xF0) | q);
+                    else
+                        *byte = (uint8_t)((*byte & 0x0F) | (q << 4));
+                }
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Seeded sign-FWHT over 256-element blocks ([hipfire MQ4V2] sections 1, 1d, */
+/* 3: the MQ line rotates every 256-block with a signed Walsh-Hadamard       */
+/* transform before quantizing; the rotated activation is consumed by the    */
+/* GEMV).  Reading: v <- H_256 (d . v) / 16 with H_256 the Sylvester         */
+/* Hadamard matrix in natural order and d in {+1,-1}^256 a sign vector       */
+/* passed in by the caller.  H/16 is orthonormal, so applying the transform  */
+/* to both a weight row and the activation preserves every dot product.     */
+/* The butterfly is the fast Walsh-Hadamard algorithm itself, in double.     */
+/* ------------------------------------------------------------------------ */
+void oracle_fwht256(float *out, const float *in, const int8_t *signs, size_t nblocks)
+{
+    double v[256];
+    for (size_t b = 0; b < nblocks; ++b) {
+        for (int j = 0; j < 256; ++j)
+            v[j] = (double)signs[j] * (double)in[b * 256 + (size_t)j];
+        for (int len = 1; len < 256; len <<= 1) {
+            for (int base = 0; base < 256; base += 2 * len) {
+                for (int j = base; j < base + len; ++j) {
+                    double a = v[j], c = v[j + len];
+                    v[j] = a + c;
+                    v[j + len] = a - c;
+                }
+            }
+        }
+        for (int j = 0; j < 256; ++j)
+            out[b * 256 + (size_t)j] = (float)(v[j] / 16.0);
+    }
+}
+
+/* Inverse of oracle_fwht256: H/16 is symmetric and orthonormal, so the
+ * inverse applies the same transform and then the same signs again.         */
+void oracle_ifwht256(float *out, const float *in, const int8_t *signs, size_t nblocks)
+{
+    double v[256];
+    for (size_t b = 0; b < nblocks; ++b) {
+        for (int j = 0; j < 256; ++j)
+            v[j] = (double)in[b * 256 + (size_t)j];
+        for (int len = 1; len < 256; len <<= 1) {
+            for (int base = 0; base < 256; base += 2 * len) {
+                for (int j = base; j < base + len; ++j) {
+                    double a = v[j], c = v[j + len];
+                    v[j] = a + c;
+                    v[j + len] = a - c;
+                }
+            }
+        }
+        for (int j = 0; j < 256; ++j)
+            out[b * 256 + (size_t)j] = (float)((double)signs[j] * v[j] / 16.0);
+    }
+}
