@@ -1,0 +1,180 @@
+/*
+ * qgemv.h -- C ABI of libqgemv: dequantize-fused weight-only quantized GEMV
+ * (decode, a handful of tokens) and dequant-GEMM (batched prefill) for three
+ * packed weight formats, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources of each format's definition (page title, section):
+ *   fmt=4  grouped int4     colibri PR #457 "metal: grouped-int4 (fmt=4) GEMV
+ *                           support + two latent fmt=4 fixes", sections 3, 4, 11
+ *   fmt=7  FP8-e4m3 b128    colibri PR #528 "fmt=7: fp8-e4m3-b128 passthrough
+ *                           weight format", section "Design"
+ *   MQ4-V2 (qt=44)          hipfire docs "MQ4 V2", sections 2, 3, 4
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All data pointers are DEVICE pointers owned by the caller.  The library
+ *   allocates no device memory, keeps no global device state and never frees
+ *   anything.  The only host-side state is a per-device cache of the SM count.
+ * - Calls are asynchronous on `stream` (0 = legacy default stream).  No call
+ *   synchronises the host.  Outputs are fully overwritten, never accumulated.
+ * - Activations x are row-major [S, I]; outputs y are row-major f32 [S, O]
+ *   (y[s*O + o]).  bf16 activations are passed as their raw 16-bit patterns.
+ * - Every argument is validated on the host BEFORE any pointer is touched or
+ *   any kernel is launched.  A refused call returns a negative qg_status and
+ *   launches nothing; qg_last_error() names the failed condition.  There is
+ *   no CPU fallback and no silent format conversion: a shape or alignment the
+ *   fast kernels cannot take runs a general (slower) kernel of the same
+ *   format, which is still exact to the same tolerance.
+ * - Accumulation is f32.  Results match the exact (f64) value of the
+ *   definition within 1e-3 * sum_i |w_i * x_i| per output element; NaN
+ *   weights or activations propagate to their output element.
+ * - Workspace: a call that splits the reduction dimension across thread
+ *   blocks needs a caller-provided scratch buffer of qg_workspace_bytes()
+ *   bytes (256-byte aligned).  When that function returns 0, ws may be NULL.
+ *   Passing a smaller workspace than required returns QG_EWORKSPACE.
+ *   Two calls in flight at the same time must not share a workspace.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so that this header does not
+ * require the CUDA headers. */
+typedef struct CUstream_st *qg_stream_t;
+
+typedef enum {
+    QG_OK = 0,
+    QG_EINVAL = -1,      /* NULL pointer, S/M/I/O < 1, or a size overflows  */
+    QG_EGS = -2,         /* fmt=4 group size odd or < 2                      */
+    QG_ESHAPE = -3,      /* MQ4-V2 with I % 256 != 0                         */
+    QG_EALIGN = -4,      /* pointer misaligned for its element type          */
+    QG_EWORKSPACE = -5,  /* workspace NULL or smaller than required          */
+    QG_ECUDA = -6        /* CUDA runtime error (no device, launch failure)   */
+} qg_status;
+
+/* Static name of a status code ("QG_EGS: ..."). Never NULL. */
+const char *qg_strerror(int status);
+
+/* Detail of the last refusal or CUDA error on the calling host thread
+ * (which argument, which condition, or the CUDA error string).  The pointer
+ * stays valid until the next call on the same thread. */
+const char *qg_last_error(void);
+
+/* Format ids for qg_workspace_bytes. */
+enum { QG_FMT_I4G = 4, QG_FMT_FP8B128 = 7, QG_FMT_MQ4V2 = 44 };
+
+/* Bytes of workspace that the GEMV entry point of format `fmt` needs for
+ * this shape on the current device (0 when the call does not split the
+ * reduction).  Returns 0 for invalid arguments (the call itself then
+ * refuses).  `gs` is only read for fmt=4. */
+size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs);
+
+/* ------------------------------------------------------------------------ */
+/* fmt=4 grouped int4, decode GEMV                                          */
+/* colibri PR #457, section 3 (per-group scale folded into the sum) and     */
+/* section 11 (packed layout shared with the CUDA tier).                    */
+/*                                                                          */
+/*   w      uint8 [O, (I+1)/2]: element i of row o is in byte i/2 of the    */
+/*          row, low nibble for even i, high nibble for odd i; the stored   */
+/*          nibble n means the integer n - 8.  For odd I the last high      */
+/*          nibble of each row is never read.                               */
+/*   scales f32 [O, ceil(I/gs)]: element i uses scales[o*ceil(I/gs) + i/gs] */
+/*   x      f32 [S, I]                                                      */
+/*   y      f32 [S, O]:  y[s,o] = sum_i (n(o,i) - 8) * scales[o, i/gs] * x[s,i] */
+/*   gs     any even group size >= 2 (16..256 are the loader's values)      */
+/*   S      any >= 1 (the weights are streamed once per group of up to 8    */
+/*          activation rows)                                                */
+/* Alignment: x, y, scales 4-byte aligned.  The fastest path also wants     */
+/* w and x 16-byte aligned, I % 32 == 0 and gs % 32 == 0.                   */
+/* ------------------------------------------------------------------------ */
+int qgemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales,
+              int S, int I, int O, int gs, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* fmt=7 FP8-e4m3 with 128x128 block scales, decode GEMV                    */
+/* colibri PR #528, section "Design".                                       */
+/*                                                                          */
+/*   w         uint8 [O, I]: raw OCP E4M3-FN codes (bias 7; the only NaN    */
+/*             codes are 0x7F and 0xFF; no infinities; subnormals valid)    */
+/*   scale_inv f32 [ceil(O/128), ceil(I/128)], row-major block order:       */
+/*             W[o,i] = e4m3(w[o*I+i]) * scale_inv[(o/128)*ceil(I/128) + i/128] */
+/*             (multiply, not divide; partial edge blocks indexed the same) */
+/*   x         bf16 bits [S, I]                                             */
+/*   y         f32 [S, O] = x . W^T; a NaN weight makes its row NaN         */
+/* Alignment: x 2-byte, y and scale_inv 4-byte aligned.  The fastest path   */
+/* also wants w and x 16-byte aligned and I % 16 == 0.                      */
+/* ------------------------------------------------------------------------ */
+int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv,
+                  int S, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* MQ4-V2 (hipfire qt=44), decode GEMV                                      */
+/* hipfire "MQ4 V2", section 2 (layout) and section 4 (decoder).            */
+/*                                                                          */
+/*   blocks uint8 [O, I/256, 136]: per 256 weights, little-endian           */
+/*          [0,4)   fp16 scale (low 16 bits) and fp16 zero (high 16 bits)   */
+/*                  of weights 0..127                                       */
+/*          [4,8)   the same for weights 128..255                           */
+/*          [8,136) nibbles: weight j in payload byte j/2, low nibble for   */
+/*                  even j                                                  */
+/*          w_j = q_j * scale[h] + zero[h], h = (j >= 128)                  */
+/*   x      bf16 bits [S, I];  y f32 [S, O]                                 */
+/*   I      multiple of 256 (else QG_ESHAPE)                                */
+/* Alignment: blocks 8-byte, x 2-byte, y 4-byte aligned.  The fastest path  */
+/* also wants x 16-byte aligned.                                            */
+/* ------------------------------------------------------------------------ */
+int qgemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks,
+                int S, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* fmt=4 batched prefill dequant-GEMM on the tensor cores                   */
+/* colibri PR #457, section 4 (the large-batch GEMM path takes the same     */
+/* grouped layout as the GEMV).                                             */
+/*                                                                          */
+/*   Y[M, O] f32 = X[M, I] (bf16 bits) . W^T, W as in qgemv_i4g.  The       */
+/*   weight tile is dequantized to bf16 ((n-8)*scale rounded to nearest     */
+/*   even) in shared memory and contracted with f32 accumulation.           */
+/*   Any M >= 1.  The tensor-core path needs I % 64 == 0, gs % 64 == 0 and  */
+/*   16-byte aligned X and w; other shapes run a general kernel.            */
+/* ------------------------------------------------------------------------ */
+int qgemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales,
+              int M, int I, int O, int gs, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Weight preparation on the device (not on the decode path)                */
+/* ------------------------------------------------------------------------ */
+
+/* Symmetric per-group int4 quantizer producing fmt=4 (the reading used for
+ * the grouped-int4 checkpoints): scale_g = max|w| / 7 (binary32 division),
+ * q = clamp(rint(w / scale_g), -8, 7) stored as q + 8; an all-zero group
+ * stores scale 0 and nibbles 8; for odd I the unused last high nibble is 8.
+ *   w  f32 [O, I] (device);  wq uint8 [O, (I+1)/2];  scales f32 [O, ceil(I/gs)] */
+int qg_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs,
+                    qg_stream_t stream);
+
+/* MQ4-V2 encoder, hipfire "MQ4 V2" section 3: per 128-weight half,
+ * step = (max - min) / 15 in binary32, scale = fp16(step), zero = fp16(min),
+ * q = clamp(rint((w - f32(zero)) / f32(scale)), 0, 15) against the
+ * round-tripped header; a constant half (or one whose fp16 step rounds to 0)
+ * stores scale 0 and q = 0.
+ *   w f32 [O, I] (device), I % 256 == 0;  blocks uint8 [O, I/256, 136] */
+int qg_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, qg_stream_t stream);
+
+/* Signed Walsh-Hadamard rotation of 256-element blocks (hipfire "MQ4 V2"
+ * sections 1 and 3: the MQ line rotates weights and activations with the
+ * same seeded sign-FWHT): out_b = H_256 (signs . in_b) / 16, H_256 the
+ * Sylvester Hadamard matrix in natural order, signs int8 +-1 [256].
+ *   in, out f32 [n_blocks, 256] (device; may alias) */
+int qg_fwht256(float *out, const float *in, const int8_t *signs, size_t n_blocks,
+               qg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QGEMV_H */

@@ -1,0 +1,99 @@
+"""The C ABI on the host (no GPU): the library loads, exports every function
+that include/qgemv.h declares, and refuses bad arguments before touching any
+pointer (poison pointers that would fault if dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemv.h")
+
+
+@pytest.fixture(scope="module")
+def qg():
+    from weight_only_quantized_i4g_gb300 import _build
+    _build.build()
+    import weight_only_quantized_i4g_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(q[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_header_lists_the_entry_points():
+    names = declared_functions()
+    for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qg_workspace_bytes",
+                 "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256"]:
+        assert must in names, names
+
+
+def test_library_exports_every_declared_symbol(qg):
+    lib = ctypes.CDLL(qg.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(qg.EXPORTED)
+
+
+def test_strerror(qg):
+    for code in range(0, -7, -1):
+        assert qg.strerror(code).startswith("QG_")
+    assert "unknown" in qg.strerror(-99)
+
+
+POISON = 0xDEADBEE0     # 16-byte aligned, never mapped: a dereference would fault
+
+
+def test_i4g_refusals(qg):
+    P = POISON
+    assert qg.qgemv_i4g(P, P, P, P, 1, 512, 256, 3, stream=0) == qg.QG_EGS
+    assert "gs = 3" in qg.last_error()
+    assert qg.qgemv_i4g(P, P, P, P, 1, 512, 256, 0, stream=0) == qg.QG_EGS
+    assert qg.qgemv_i4g(P, P, P, P, 0, 512, 256, 64, stream=0) == qg.QG_EINVAL
+    assert qg.qgemv_i4g(P, P, P, P, 1, 0, 256, 64, stream=0) == qg.QG_EINVAL
+    assert qg.qgemv_i4g(P, P, P, P, 1, 512, -5, 64, stream=0) == qg.QG_EINVAL
+    assert qg.qgemv_i4g(P, P, 0, P, 1, 512, 256, 64, stream=0) == qg.QG_EINVAL
+    assert qg.qgemv_i4g(P + 2, P, P, P, 1, 512, 256, 64, stream=0) == qg.QG_EALIGN
+    assert qg.qgemv_i4g(P, P, P, P + 1, 1, 512, 256, 64, stream=0) == qg.QG_EALIGN
+    assert qg.qgemv_i4g(P, P, P, P, 1, 512, 256, 64, ws=P + 16, stream=0) == qg.QG_EALIGN
+
+
+def test_fp8_refusals(qg):
+    P = POISON
+    assert qg.qgemv_fp8b128(P, P, P, P, 1, 0, 1, stream=0) == qg.QG_EINVAL
+    assert qg.qgemv_fp8b128(P, P + 1, P, P, 1, 16, 1, stream=0) == qg.QG_EALIGN
+    assert qg.qgemv_fp8b128(0, P, P, P, 1, 16, 1, stream=0) == qg.QG_EINVAL
+
+
+def test_mq4_refusals(qg):
+    P = POISON
+    assert qg.qgemv_mq4v2(P, P, P, 1, 300, 4, stream=0) == qg.QG_ESHAPE
+    assert "300" in qg.last_error()
+    assert qg.qgemv_mq4v2(P, P, P + 4, 1, 256, 4, stream=0) == qg.QG_EALIGN
+    assert qg.qgemv_mq4v2(P, P, P, 1, 256, 0, stream=0) == qg.QG_EINVAL
+
+
+def test_gemm_and_prep_refusals(qg):
+    P = POISON
+    assert qg.qgemm_i4g(P, P, P, P, 0, 64, 64, 64, stream=0) == qg.QG_EINVAL
+    assert qg.qgemm_i4g(P, P, P, P, 4, 64, 64, 7, stream=0) == qg.QG_EGS
+    assert qg.qg_quantize_i4g(P, P, P, 4, 64, 5, stream=0) == qg.QG_EGS
+    assert qg.qg_encode_mq4v2(P, P, 4, 100, stream=0) == qg.QG_ESHAPE
+    assert qg.qg_fwht256(P, P, P, 0, stream=0) == qg.QG_EINVAL
+
+
+def test_workspace_query_is_pure(qg):
+    # no split for the decode shapes of the workloads
+    assert qg.qg_workspace_bytes(qg.QG_FMT_I4G, 1, 7168, 2048, 64) == 0
+    assert qg.qg_workspace_bytes(qg.QG_FMT_FP8B128, 1, 16384, 7168) == 0
+    assert qg.qg_workspace_bytes(qg.QG_FMT_MQ4V2, 1, 17408, 5120) == 0
+    # a short-O / long-I shape splits the reduction and needs splits*S*O floats
+    n = qg.qg_workspace_bytes(qg.QG_FMT_I4G, 1, 16384, 64, 64)
+    assert n > 0 and n % (64 * 4) == 0
+    # invalid arguments -> 0
+    assert qg.qg_workspace_bytes(qg.QG_FMT_MQ4V2, 1, 300, 4) == 0
+    assert qg.qg_workspace_bytes(99, 1, 256, 4) == 0

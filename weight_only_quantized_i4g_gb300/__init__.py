@@ -1,0 +1,126 @@
+"""Python binding of libqgemv (weight-only quantized GEMV / GEMM for GB300).
+
+Argument marshalling only: each function takes the same arguments as the C
+entry point of the same name in ``include/qgemv.h`` -- device pointers given
+as ``torch.Tensor`` (its ``data_ptr()``) or plain integers, sizes as ints, a
+CUDA stream as a ``torch.cuda.Stream``, a raw handle or None (the current
+torch stream) -- and returns the C status code.  ``check(rc)`` turns a
+non-zero status into ``QGError``.  Every computation runs in the CUDA library;
+importing this package fails if the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqgemv.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        "libqgemv.so is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+        "(or `python weight_only_quantized_i4g_gb300/_build.py`)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+QG_OK, QG_EINVAL, QG_EGS, QG_ESHAPE, QG_EALIGN, QG_EWORKSPACE, QG_ECUDA = 0, -1, -2, -3, -4, -5, -6
+QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_MQ4V2 = 4, 7, 44
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_Z = ctypes.c_size_t
+
+_SIGNATURES = {
+    "qg_strerror": ([_I], ctypes.c_char_p),
+    "qg_last_error": ([], ctypes.c_char_p),
+    "qg_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
+    "qgemv_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemv_fp8b128": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemv_mq4v2": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemm_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "qg_quantize_i4g": ([_P, _P, _P, _I, _I, _I, _P], _I),
+    "qg_encode_mq4v2": ([_P, _P, _I, _I, _P], _I),
+    "qg_fwht256": ([_P, _P, _P, _Z, _P], _I),
+}
+for _name, (_args, _res) in _SIGNATURES.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+EXPORTED = tuple(_SIGNATURES)
+
+
+class QGError(RuntimeError):
+    def __init__(self, status: int):
+        self.status = status
+        super().__init__(f"{strerror(status)} -- {last_error()}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return torch.cuda.current_stream().cuda_stream
+        except ImportError:
+            pass
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def strerror(status: int) -> str:
+    return _lib.qg_strerror(status).decode()
+
+
+def last_error() -> str:
+    return _lib.qg_last_error().decode()
+
+
+def check(rc: int) -> None:
+    if rc != QG_OK:
+        raise QGError(rc)
+
+
+def qg_workspace_bytes(fmt: int, S: int, I: int, O: int, gs: int = 0) -> int:
+    return _lib.qg_workspace_bytes(fmt, S, I, O, gs)
+
+
+def qgemv_i4g(y, x, w, scales, S, I, O, gs, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemv_i4g(_ptr(y), _ptr(x), _ptr(w), _ptr(scales), S, I, O, gs, _ptr(ws), ws_bytes,
+                          _stream(stream))
+
+
+def qgemv_fp8b128(y, x, w, scale_inv, S, I, O, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemv_fp8b128(_ptr(y), _ptr(x), _ptr(w), _ptr(scale_inv), S, I, O, _ptr(ws), ws_bytes,
+                              _stream(stream))
+
+
+def qgemv_mq4v2(y, x, blocks, S, I, O, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemv_mq4v2(_ptr(y), _ptr(x), _ptr(blocks), S, I, O, _ptr(ws), ws_bytes, _stream(stream))
+
+
+def qgemm_i4g(Y, X, w, scales, M, I, O, gs, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemm_i4g(_ptr(Y), _ptr(X), _ptr(w), _ptr(scales), M, I, O, gs, _ptr(ws), ws_bytes,
+                          _stream(stream))
+
+
+def qg_quantize_i4g(wq, scales, w, O, I, gs, stream=None) -> int:
+    return _lib.qg_quantize_i4g(_ptr(wq), _ptr(scales), _ptr(w), O, I, gs, _stream(stream))
+
+
+def qg_encode_mq4v2(blocks, w, O, I, stream=None) -> int:
+    return _lib.qg_encode_mq4v2(_ptr(blocks), _ptr(w), O, I, _stream(stream))
+
+
+def qg_fwht256(out, inp, signs, n_blocks, stream=None) -> int:
+    return _lib.qg_fwht256(_ptr(out), _ptr(inp), _ptr(signs), n_blocks, _stream(stream))

@@ -1,0 +1,166 @@
+// abi.cu -- the extern "C" entry points of libqgemv (declared in
+// include/qgemv.h).  Every argument is checked here, on the host, before any
+// pointer is dereferenced or any kernel is enqueued; a refused call returns a
+// negative status and records which condition failed (qg_last_error).
+#include <limits.h>
+#include <stdint.h>
+
+#include "../../include/qgemv.h"
+#include "launch.h"
+
+namespace qg {
+const char *error_detail();
+int run_gemm_i4g_general(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I,
+                         int O, int gs, cudaStream_t st);
+int run_gemm_i4g_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I, int O,
+                    int gs, cudaStream_t st, bool *taken);
+}  // namespace qg
+
+using namespace qg;
+
+namespace {
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+#define QG_REFUSE(code, ...)              \
+    do {                                  \
+        set_error_detail(__VA_ARGS__);    \
+        return (code);                    \
+    } while (0)
+
+// Common checks of the shape arguments.
+int check_dims(const char *fn, const char *sname, int S, int I, int O) {
+    if (S < 1) QG_REFUSE(kEInval, "%s: %s = %d, must be >= 1", fn, sname, S);
+    if (I < 1) QG_REFUSE(kEInval, "%s: I = %d, must be >= 1", fn, I);
+    if (O < 1) QG_REFUSE(kEInval, "%s: O = %d, must be >= 1", fn, O);
+    return kOk;
+}
+
+int check_gs(const char *fn, int gs) {
+    if (gs < 2 || (gs & 1)) QG_REFUSE(kEGs, "%s: gs = %d, must be even and >= 2", fn, gs);
+    return kOk;
+}
+
+cudaStream_t as_stream(qg_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+const char *qg_strerror(int status) {
+    switch (status) {
+        case QG_OK: return "QG_OK: success";
+        case QG_EINVAL: return "QG_EINVAL: null pointer, non-positive size or size overflow";
+        case QG_EGS: return "QG_EGS: group size must be even and >= 2";
+        case QG_ESHAPE: return "QG_ESHAPE: shape not supported by the format (MQ4-V2 needs I % 256 == 0)";
+        case QG_EALIGN: return "QG_EALIGN: pointer misaligned for its element type";
+        case QG_EWORKSPACE: return "QG_EWORKSPACE: workspace missing or smaller than qg_workspace_bytes()";
+        case QG_ECUDA: return "QG_ECUDA: CUDA runtime error";
+        default: return "unknown qg_status";
+    }
+}
+
+const char *qg_last_error(void) { return error_detail(); }
+
+size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs) {
+    if (S < 1 || I < 1 || O < 1) return 0;
+    switch (fmt) {
+        case QG_FMT_I4G: return (gs >= 2 && !(gs & 1)) ? ws_i4g(S, I, O, gs) : 0;
+        case QG_FMT_FP8B128: return ws_fp8b128(S, I, O);
+        case QG_FMT_MQ4V2: return (I % 256 == 0) ? ws_mq4v2(S, I, O) : 0;
+        default: return 0;
+    }
+}
+
+int qgemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O, int gs,
+              void *ws, size_t ws_bytes, qg_stream_t stream) {
+    const char *fn = "qgemv_i4g";
+    int rc = check_dims(fn, "S", S, I, O);
+    if (rc) return rc;
+    if ((rc = check_gs(fn, gs))) return rc;
+    if (!y || !x || !w || !scales) QG_REFUSE(kEInval, "%s: y, x, w and scales must be non-NULL", fn);
+    if (!aligned(y, 4) || !aligned(x, 4) || !aligned(scales, 4))
+        QG_REFUSE(kEAlign, "%s: y, x and scales must be 4-byte aligned", fn);
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    cudaGetLastError();
+    return run_gemv_i4g(y, x, w, scales, S, I, O, gs, ws, ws_bytes, as_stream(stream));
+}
+
+int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S, int I, int O,
+                  void *ws, size_t ws_bytes, qg_stream_t stream) {
+    const char *fn = "qgemv_fp8b128";
+    int rc = check_dims(fn, "S", S, I, O);
+    if (rc) return rc;
+    if (!y || !x || !w || !scale_inv) QG_REFUSE(kEInval, "%s: y, x, w and scale_inv must be non-NULL", fn);
+    if (!aligned(y, 4) || !aligned(x, 2) || !aligned(scale_inv, 4))
+        QG_REFUSE(kEAlign, "%s: y and scale_inv must be 4-byte and x 2-byte aligned", fn);
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    cudaGetLastError();
+    return run_gemv_fp8b128(y, x, w, scale_inv, S, I, O, ws, ws_bytes, as_stream(stream));
+}
+
+int qgemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+                size_t ws_bytes, qg_stream_t stream) {
+    const char *fn = "qgemv_mq4v2";
+    int rc = check_dims(fn, "S", S, I, O);
+    if (rc) return rc;
+    if (I % 256) QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 256", fn, I);
+    if (!y || !x || !blocks) QG_REFUSE(kEInval, "%s: y, x and blocks must be non-NULL", fn);
+    if (!aligned(y, 4) || !aligned(x, 2) || !aligned(blocks, 8))
+        QG_REFUSE(kEAlign, "%s: y must be 4-byte, x 2-byte and blocks 8-byte aligned", fn);
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    cudaGetLastError();
+    return run_gemv_mq4v2(y, x, blocks, S, I, O, ws, ws_bytes, as_stream(stream));
+}
+
+int qgemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I, int O, int gs,
+              void *ws, size_t ws_bytes, qg_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    const char *fn = "qgemm_i4g";
+    int rc = check_dims(fn, "M", M, I, O);
+    if (rc) return rc;
+    if ((rc = check_gs(fn, gs))) return rc;
+    if (!Y || !X || !w || !scales) QG_REFUSE(kEInval, "%s: Y, X, w and scales must be non-NULL", fn);
+    if (!aligned(Y, 4) || !aligned(X, 2) || !aligned(scales, 4))
+        QG_REFUSE(kEAlign, "%s: Y and scales must be 4-byte and X 2-byte aligned", fn);
+    cudaGetLastError();
+    bool taken = false;
+    rc = run_gemm_i4g_tc(Y, X, w, scales, M, I, O, gs, as_stream(stream), &taken);
+    if (taken) return rc;
+    return run_gemm_i4g_general(Y, X, w, scales, M, I, O, gs, as_stream(stream));
+}
+
+int qg_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs, qg_stream_t stream) {
+    const char *fn = "qg_quantize_i4g";
+    int rc = check_dims(fn, "O", 1, I, O);
+    if (rc) return rc;
+    if ((rc = check_gs(fn, gs))) return rc;
+    if (!wq || !scales || !w) QG_REFUSE(kEInval, "%s: wq, scales and w must be non-NULL", fn);
+    if (!aligned(scales, 4) || !aligned(w, 4)) QG_REFUSE(kEAlign, "%s: scales and w must be 4-byte aligned", fn);
+    cudaGetLastError();
+    return run_quantize_i4g(wq, scales, w, O, I, gs, as_stream(stream));
+}
+
+int qg_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, qg_stream_t stream) {
+    const char *fn = "qg_encode_mq4v2";
+    int rc = check_dims(fn, "O", 1, I, O);
+    if (rc) return rc;
+    if (I % 256) QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 256", fn, I);
+    if (!blocks || !w) QG_REFUSE(kEInval, "%s: blocks and w must be non-NULL", fn);
+    if (!aligned(w, 4)) QG_REFUSE(kEAlign, "%s: w must be 4-byte aligned", fn);
+    cudaGetLastError();
+    return run_encode_mq4v2(blocks, w, O, I, as_stream(stream));
+}
+
+int qg_fwht256(float *out, const float *in, const int8_t *signs, size_t n_blocks, qg_stream_t stream) {
+    const char *fn = "qg_fwht256";
+    if (n_blocks < 1) QG_REFUSE(kEInval, "%s: n_blocks must be >= 1", fn);
+    if (n_blocks > ((size_t)1 << 40)) QG_REFUSE(kEInval, "%s: n_blocks too large", fn);
+    if (!out || !in || !signs) QG_REFUSE(kEInval, "%s: out, in and signs must be non-NULL", fn);
+    if (!aligned(out, 4) || !aligned(in, 4)) QG_REFUSE(kEAlign, "%s: out and in must be 4-byte aligned", fn);
+    cudaGetLastError();
+    return run_fwht256(out, in, signs, n_blocks, as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,215 @@
+// gemv_fp8b128.cu -- fmt=7 FP8-e4m3 decode GEMV with 128x128 f32 block scales.
+//
+// Format (colibri PR #528, "Design"): O*I raw OCP E4M3-FN codes, row-major;
+// scale_inv f32 [ceil(O/128), ceil(I/128)] in row-major block order;
+//     W[o,i] = e4m3(code) * scale_inv[o/128, i/128]   (multiply, not divide)
+// The only NaN codes are 0x7F and 0xFF; a NaN weight propagates to its row.
+//
+// Decode: the hardware e4m3x2 -> f16x2 conversion (exact for every code:
+// each E4M3-FN value, subnormals included, is an f16 value, and the NaN codes
+// convert to NaN), then f16 -> f32 (exact).  A unit (4*NW codes, NW <= 4)
+// lies inside one 128-column block, so the block scale multiplies the unit's
+// partial sum.
+#include "gemv_cs.cuh"
+#include "launch.h"
+
+namespace qg {
+
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_codes));
+    float a, b;
+    asm("{.reg .f16 lo, hi; mov.b32 {lo, hi}, %2; cvt.f32.f16 %0, lo; cvt.f32.f16 %1, hi;}"
+        : "=f"(a), "=f"(b) : "r"(h2));
+    return make_float2(a, b);
+}
+
+struct FmtFp8B128 {
+    static constexpr int kElemsPerWord = 4;
+    struct Params {
+        const uint16_t *x;
+        const uint8_t *w;
+        const float *scale_inv;
+        int I, O, nbi;
+    };
+    struct ThreadConst { int ib; };  // 128-column block of the thread's unit
+    typedef float Aux;
+
+    __device__ static ThreadConst thread_const(const Params &, int u, int XU) {
+        return ThreadConst{(u * XU) >> 7};
+    }
+    __device__ static const void *unit_ptr(const Params &p, int o, int u, int XU) {
+        return p.w + (size_t)o * p.I + (size_t)u * XU;
+    }
+    __device__ static Aux unit_aux(const Params &p, int o, int, ThreadConst tc) {
+        return ld_nc_f32(p.scale_inv + (size_t)(o >> 7) * p.nbi + tc.ib);
+    }
+    __device__ static Aux zero_aux() { return 0.f; }
+
+    // xs: natural element order, f32
+    template <int XU>
+    __device__ static void load_x(const Params &p, int s, int u, float (&xs)[XU], float &xsum) {
+        xsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < XU; ++k)
+            xs[k] = u >= 0 ? bf16_bits_to_f32(p.x[(size_t)s * p.I + (size_t)u * XU + k]) : 0.f;
+    }
+
+    template <int S, int NW, int XU>
+    __device__ static void accumulate(const Words<NW> &wd, Aux sc, const float (&xs)[S][XU],
+                                      const float (&)[S], float *part) {
+        float2 d[NW * 2];
+#pragma unroll
+        for (int wq = 0; wq < NW; ++wq) {
+            d[2 * wq] = e4m3x2_to_f32x2(wd.w[wq]);
+            d[2 * wq + 1] = e4m3x2_to_f32x2(wd.w[wq] >> 16);
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < NW * 2; ++i)
+                acc = __ffma2_rn(d[i], make_float2(xs[s][2 * i], xs[s][2 * i + 1]), acc);
+            part[s] = fmaf(sc, acc.x + acc.y, part[s]);
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// General kernel: any shape and alignment.  One warp per row.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+    return e4m3x2_to_f32x2((uint32_t)c).x;
+}
+
+template <int S>
+__global__ void __launch_bounds__(256)
+gemv_fp8_general_kernel(float *__restrict__ y, const uint16_t *__restrict__ x, const uint8_t *__restrict__ w,
+                        const float *__restrict__ scale_inv, int I, int O) {
+    const int lane = threadIdx.x & 31;
+    const int nbi = (I + 127) / 128;
+    for (int o = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); o < O;
+         o += gridDim.x * (blockDim.x >> 5)) {
+        float acc[S];
+#pragma unroll
+        for (int s = 0; s < S; ++s) acc[s] = 0.f;
+        const uint8_t *wr = w + (size_t)o * I;
+        const float *sr = scale_inv + (size_t)(o >> 7) * nbi;
+        for (int i = lane; i < I; i += 32) {
+            const float wv = e4m3_to_f32(wr[i]) * sr[i >> 7];
+#pragma unroll
+            for (int s = 0; s < S; ++s) acc[s] = fmaf(wv, bf16_bits_to_f32(x[(size_t)s * I + i]), acc[s]);
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const float t = warp_sum(acc[s]);
+            if (lane == 0) y[(size_t)s * O + o] = t;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dispatch
+// ---------------------------------------------------------------------------
+namespace {
+
+int fp8_nw(int S) { return S <= 4 ? 4 : 2; }       // activation registers 4*NW*S <= 64
+int fp8_rb(int S, int U) { return S <= 2 ? (U == 1 ? 8 : 4) : 4; }
+
+bool fp8_fast_ok(const uint16_t *x, const uint8_t *w, int I, int S) {
+    const int nw = fp8_nw(S);
+    return (I % (4 * nw) == 0) && ((uintptr_t)w % (4 * nw) == 0) && ((uintptr_t)x % 2 == 0);
+}
+
+CsPlan fp8_plan(int S, int I, int O, int *U_out) {
+    const int nw = fp8_nw(S);
+    const int units = I / (4 * nw);
+    // up to three units per thread at S = 1 (at S > 1 more than one spills
+    // registers); longer rows split across blocks
+    const int U = S == 1 ? (units > 2 * kCsMaxThreads ? 3 : units > kCsMaxThreads ? 2 : 1) : 1;
+    *U_out = U;
+    const int regs = 40 + 4 * nw * S * U + fp8_rb(S, U) * U * (nw + 1) + 2 * fp8_rb(S, U) * S;
+    return cs_plan(units, O, U, fp8_rb(S, U), regs);
+}
+
+template <int S, int NW, int U>
+void launch_cs_fp8(const FmtFp8B128::Params &p, float *out, const CsPlan &pl, int units, cudaStream_t st) {
+    constexpr int RB = S <= 2 ? (U == 1 ? 8 : 4) : 4;
+    dim3 grid(pl.grid_x, pl.splits);
+    gemv_cs_kernel<FmtFp8B128, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
+                                                                         pl.nrowb);
+}
+
+template <int S>
+void launch_cs_fp8_s(const FmtFp8B128::Params &p, float *out, const CsPlan &pl, int units, int U,
+                     cudaStream_t st) {
+    constexpr int NW = S <= 4 ? 4 : 2;
+    if constexpr (S == 1) {
+        if (U == 2) {
+            launch_cs_fp8<S, NW, 2>(p, out, pl, units, st);
+            return;
+        }
+        if (U == 3) {
+            launch_cs_fp8<S, NW, 3>(p, out, pl, units, st);
+            return;
+        }
+    }
+    (void)U;
+    launch_cs_fp8<S, NW, 1>(p, out, pl, units, st);
+}
+
+int gemv_fp8_chunk(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S, int I,
+                   int O, void *ws, size_t ws_bytes, cudaStream_t st) {
+    if (!fp8_fast_ok(x, w, I, S)) {
+        const int blocks_needed = (O + 7) / 8;
+        const int cap = num_sms() * 16;
+        const int grid = blocks_needed < cap ? blocks_needed : cap;
+        switch (S) {
+#define QG_CASE(SS) case SS: gemv_fp8_general_kernel<SS><<<grid, 256, 0, st>>>(y, x, w, scale_inv, I, O); break;
+            QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+        }
+        return check_launch("qgemv_fp8b128 (general kernel)");
+    }
+    int U = 1;
+    const CsPlan pl = fp8_plan(S, I, O, &U);
+    const int units = I / (4 * fp8_nw(S));
+    const size_t need = cs_ws_bytes(pl, S, O);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) {
+        set_error_detail("qgemv_fp8b128: this shape splits the reduction and needs %zu bytes of "
+                         "workspace (got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
+        return kEWorkspace;
+    }
+    FmtFp8B128::Params p;
+    p.x = x; p.w = w; p.scale_inv = scale_inv; p.I = I; p.O = O; p.nbi = (I + 127) / 128;
+    float *out = pl.splits > 1 ? static_cast<float *>(ws) : y;
+    switch (S) {
+#define QG_CASE(SS) case SS: launch_cs_fp8_s<SS>(p, out, pl, units, U, st); break;
+        QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+    }
+    if (pl.splits > 1) launch_splitk_reduce(y, static_cast<float *>(ws), pl.splits, S, O, st);
+    return check_launch("qgemv_fp8b128");
+}
+
+}  // namespace
+
+size_t ws_fp8b128(int S, int I, int O) {
+    const int s = S < 8 ? S : 8;
+    if (I % (4 * fp8_nw(s)) != 0) return 0;
+    int U = 1;
+    return cs_ws_bytes(fp8_plan(s, I, O, &U), s, O);
+}
+
+int run_gemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S, int I,
+                     int O, void *ws, size_t ws_bytes, cudaStream_t st) {
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        const int sc = S - s0 < 8 ? S - s0 : 8;
+        const int rc = gemv_fp8_chunk(y + (size_t)s0 * O, x + (size_t)s0 * I, w, scale_inv, sc, I, O, ws,
+                                      ws_bytes, st);
+        if (rc != kOk) return rc;
+    }
+    return kOk;
+}
+
+}  // namespace qg

@@ -1,0 +1,231 @@
+// gemv_i4g.cu -- fmt=4 grouped-int4 decode GEMV.
+//
+// Format (colibri PR #457, sections 3 and 11): row-major packed nibbles, row o
+// is (I+1)/2 bytes; element i is in byte i/2, low nibble for even i; the
+// stored nibble n means n - 8; f32 scales [O, ceil(I/gs)], one per gs
+// consecutive elements of a row, applied to every term of its group:
+//     y[s,o] = sum_i (n(o,i) - 8) * scale[o, i/gs] * x[s,i]
+//
+// Fast path (column-stationary, gemv_cs.cuh): a thread's unit is 4*NW bytes =
+// 8*NW consecutive elements inside one group (gs % (8*NW) == 0), so one scale
+// multiplies the unit's partial sum.  Decode: for a 32-bit word holding 8
+// nibbles, OR-ing the masked nibble into the bit pattern of 2^23 gives the
+// float 2^23 + n*16^p exactly (p = nibble position within a 16-bit half);
+// subtracting 2^23 + 8*16^p (exact) leaves (n - 8)*16^p, and the matching
+// activation is pre-scaled by 16^-p (exact).  Two elements at a time with
+// packed f32x2 add and fma.
+#include "gemv_cs.cuh"
+#include "launch.h"
+
+namespace qg {
+
+struct FmtI4G {
+    static constexpr int kElemsPerWord = 8;
+    struct Params {
+        const float *x;
+        const uint8_t *w;
+        const float *scales;
+        int I, O, gs, ng;
+        size_t rb;
+    };
+    struct ThreadConst { int g; };   // group of the thread's unit
+    typedef float Aux;               // the row's scale for that group
+
+    __device__ static ThreadConst thread_const(const Params &p, int u, int XU) {
+        return ThreadConst{(u * XU) / p.gs};
+    }
+    __device__ static const void *unit_ptr(const Params &p, int o, int u, int XU) {
+        return p.w + (size_t)o * p.rb + (size_t)u * (XU / 2);
+    }
+    __device__ static Aux unit_aux(const Params &p, int o, int /*u*/, ThreadConst tc) {
+        return ld_nc_f32(p.scales + (size_t)o * p.ng + tc.g);
+    }
+    __device__ static Aux zero_aux() { return 0.f; }
+
+    // xs layout: pair i = 4*w + q holds elements (8w + q, 8w + q + 4), both
+    // scaled by 16^-q, at xs[2i], xs[2i+1].
+    template <int XU>
+    __device__ static void load_x(const Params &p, int s, int u, float (&xs)[XU], float &xsum) {
+        xsum = 0.f;
+#pragma unroll
+        for (int wq = 0; wq < XU / 8; ++wq) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float sc = q == 0 ? 1.f : q == 1 ? 0.0625f : q == 2 ? 0.00390625f : 0.000244140625f;
+                float a = 0.f, b = 0.f;
+                if (u >= 0) {
+                    const float *xp = p.x + (size_t)s * p.I + (size_t)u * XU + 8 * wq;
+                    a = xp[q] * sc;
+                    b = xp[q + 4] * sc;
+                }
+                xs[2 * (4 * wq + q)] = a;
+                xs[2 * (4 * wq + q) + 1] = b;
+            }
+        }
+    }
+
+    template <int S, int NW, int XU>
+    __device__ static void accumulate(const Words<NW> &wd, Aux sc, const float (&xs)[S][XU],
+                                      const float (&)[S], float *part) {
+        constexpr uint32_t kMagic = 0x4B000000u;   // 2^23
+        float2 d[NW * 4];
+#pragma unroll
+        for (int wq = 0; wq < NW; ++wq) {
+            const uint32_t lo = wd.w[wq];
+            const uint32_t hi = lo >> 16;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t m = 0xFu << (4 * q);
+                const float c = -(8388608.f + 8.f * (float)(1u << (4 * q)));
+                float2 f = make_float2(__uint_as_float((lo & m) | kMagic), __uint_as_float((hi & m) | kMagic));
+                d[4 * wq + q] = __fadd2_rn(f, make_float2(c, c));
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < NW * 4; ++i)
+                acc = __ffma2_rn(d[i], make_float2(xs[s][2 * i], xs[s][2 * i + 1]), acc);
+            part[s] = fmaf(sc, acc.x + acc.y, part[s]);
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// General kernel: any I, any even gs, any alignment.  One warp per row; lanes
+// walk the elements; byte loads.
+// ---------------------------------------------------------------------------
+template <int S>
+__global__ void __launch_bounds__(256)
+gemv_i4g_general_kernel(float *__restrict__ y, const float *__restrict__ x, const uint8_t *__restrict__ w,
+                        const float *__restrict__ scales, int I, int O, int gs) {
+    const int lane = threadIdx.x & 31;
+    const size_t rb = ((size_t)I + 1) / 2;
+    const int ng = (I + gs - 1) / gs;
+    for (int o = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); o < O;
+         o += gridDim.x * (blockDim.x >> 5)) {
+        float acc[S];
+#pragma unroll
+        for (int s = 0; s < S; ++s) acc[s] = 0.f;
+        const uint8_t *wr = w + (size_t)o * rb;
+        const float *sr = scales + (size_t)o * ng;
+        for (int i = lane; i < I; i += 32) {
+            const uint8_t b = wr[i >> 1];
+            const int q = (int)((i & 1) ? (b >> 4) : (b & 0xF)) - 8;
+            const float wv = (float)q * sr[i / gs];
+#pragma unroll
+            for (int s = 0; s < S; ++s) acc[s] = fmaf(wv, x[(size_t)s * I + i], acc[s]);
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const float t = warp_sum(acc[s]);
+            if (lane == 0) y[(size_t)s * O + o] = t;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dispatch
+// ---------------------------------------------------------------------------
+namespace {
+
+// words per unit for S tokens: keep the activation registers (8*NW*S) <= 64
+int i4g_nw(int S) { return S <= 2 ? 4 : S <= 4 ? 2 : 1; }
+int i4g_rb(int S, int U) { return S <= 2 ? (U == 1 ? 8 : 4) : 4; }
+
+bool i4g_fast_ok(const float *x, const uint8_t *w, int I, int gs, int S) {
+    const int nw = i4g_nw(S);
+    const int ue = 8 * nw;                       // elements per unit
+    return (I % ue == 0) && (gs % ue == 0) && ((uintptr_t)w % (4 * nw) == 0) &&
+           ((uintptr_t)x % 4 == 0);
+}
+
+CsPlan i4g_plan(int S, int I, int O, int *U_out) {
+    const int nw = i4g_nw(S);
+    const int units = I / (8 * nw);
+    // up to two units per thread at S = 1 (more, or more than one at S > 1,
+    // spills registers); longer rows split across blocks
+    const int U = (S == 1 && units > kCsMaxThreads) ? 2 : 1;
+    *U_out = U;
+    const int regs = 40 + 8 * nw * S * U + i4g_rb(S, U) * U * (nw + 1) + 2 * i4g_rb(S, U) * S;
+    return cs_plan(units, O, U, i4g_rb(S, U), regs);
+}
+
+template <int S, int NW, int U>
+void launch_cs_i4g(const FmtI4G::Params &p, float *out, const CsPlan &pl, int units, cudaStream_t st) {
+    constexpr int RB = S <= 2 ? (U == 1 ? 8 : 4) : 4;
+    dim3 grid(pl.grid_x, pl.splits);
+    gemv_cs_kernel<FmtI4G, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
+                                                                     pl.nrowb);
+}
+
+template <int S>
+void launch_cs_i4g_s(const FmtI4G::Params &p, float *out, const CsPlan &pl, int units, int U, cudaStream_t st) {
+    constexpr int NW = S <= 2 ? 4 : S <= 4 ? 2 : 1;
+    if constexpr (S == 1) {
+        if (U == 2) {
+            launch_cs_i4g<S, NW, 2>(p, out, pl, units, st);
+            return;
+        }
+    }
+    (void)U;
+    launch_cs_i4g<S, NW, 1>(p, out, pl, units, st);
+}
+
+int gemv_i4g_chunk(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,
+                   int gs, void *ws, size_t ws_bytes, cudaStream_t st) {
+    if (!i4g_fast_ok(x, w, I, gs, S)) {
+        const int blocks_needed = (O + 7) / 8;
+        const int cap = num_sms() * 16;
+        const int grid = blocks_needed < cap ? blocks_needed : cap;
+        switch (S) {
+#define QG_CASE(SS) case SS: gemv_i4g_general_kernel<SS><<<grid, 256, 0, st>>>(y, x, w, scales, I, O, gs); break;
+            QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+        }
+        return check_launch("qgemv_i4g (general kernel)");
+    }
+    int U = 1;
+    const CsPlan pl = i4g_plan(S, I, O, &U);
+    const int units = I / (8 * i4g_nw(S));
+    const size_t need = cs_ws_bytes(pl, S, O);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) {
+        set_error_detail("qgemv_i4g: this shape splits the reduction and needs %zu bytes of workspace "
+                         "(got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
+        return kEWorkspace;
+    }
+    FmtI4G::Params p;
+    p.x = x; p.w = w; p.scales = scales; p.I = I; p.O = O; p.gs = gs;
+    p.ng = (I + gs - 1) / gs; p.rb = ((size_t)I + 1) / 2;
+    float *out = pl.splits > 1 ? static_cast<float *>(ws) : y;
+    switch (S) {
+#define QG_CASE(SS) case SS: launch_cs_i4g_s<SS>(p, out, pl, units, U, st); break;
+        QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+    }
+    if (pl.splits > 1) launch_splitk_reduce(y, static_cast<float *>(ws), pl.splits, S, O, st);
+    return check_launch("qgemv_i4g");
+}
+
+}  // namespace
+
+size_t ws_i4g(int S, int I, int O, int gs) {
+    const int s = S < 8 ? S : 8;
+    if (I % (8 * i4g_nw(s)) != 0 || gs % (8 * i4g_nw(s)) != 0) return 0;  // general kernel: none
+    int U = 1;
+    return cs_ws_bytes(i4g_plan(s, I, O, &U), s, O);
+}
+
+int run_gemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,
+                 int gs, void *ws, size_t ws_bytes, cudaStream_t st) {
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        const int sc = S - s0 < 8 ? S - s0 : 8;
+        const int rc = gemv_i4g_chunk(y + (size_t)s0 * O, x + (size_t)s0 * I, w, scales, sc, I, O, gs, ws,
+                                      ws_bytes, st);
+        if (rc != kOk) return rc;
+    }
+    return kOk;
+}
+
+}  // namespace qg

@@ -1,0 +1,185 @@
+// gemv_mq4v2.cu -- MQ4-V2 (hipfire qt=44) decode GEMV.
+//
+// Format (hipfire "MQ4 V2", sections 2 and 4): 136 bytes per 256 weights,
+// little-endian: dword [0,4) = fp16 scale (low half) | fp16 zero (high half)
+// of weights 0..127, dword [4,8) the same for weights 128..255, then 128
+// payload bytes, weight j in payload byte j/2 (low nibble for even j):
+//     w_j = q_j * scale[h] + zero[h],   h = (payload byte offset >= 64)
+//
+// Fast path (column-stationary): a unit is 4*NW payload bytes (8*NW weights)
+// inside one half, so one header dword serves the unit; the half is derived
+// from the unit's payload byte offset, never from a lane id.  The sum is
+// folded as scale * sum(q*x) + zero * sum(x); the activations' sum over the
+// unit is computed once per thread.  Nibble decode as for fmt=4 (the float
+// 2^23 + q*16^p minus 2^23).
+#include "gemv_cs.cuh"
+#include "launch.h"
+
+namespace qg {
+
+struct FmtMq4v2 {
+    static constexpr int kElemsPerWord = 8;
+    struct Params {
+        const uint16_t *x;
+        const uint8_t *blocks;
+        int I, O;
+        size_t rowbytes;
+    };
+    struct ThreadConst { int uoff; int hoff; };   // byte offsets of the unit and its header in a row
+    typedef uint32_t Aux;                          // the header dword of the unit's half
+
+    __device__ static ThreadConst thread_const(const Params &, int u, int XU) {
+        const int ub = XU / 2;                     // payload bytes per unit
+        const int upb = 128 / ub;                  // units per block
+        const int b = u / upb, k = u - (u / upb) * upb;
+        const int poff = ub * k;                   // payload byte offset of the unit
+        return ThreadConst{136 * b + 8 + poff, 136 * b + (poff >= 64 ? 4 : 0)};
+    }
+    __device__ static const void *unit_ptr(const Params &p, int o, int u, int XU) {
+        return p.blocks + (size_t)o * p.rowbytes + thread_const(p, u, XU).uoff;
+    }
+    __device__ static Aux unit_aux(const Params &p, int o, int, ThreadConst tc) {
+        return ld_nc_u32(p.blocks + (size_t)o * p.rowbytes + tc.hoff);
+    }
+    __device__ static Aux zero_aux() { return 0u; }
+
+    template <int XU>
+    __device__ static void load_x(const Params &p, int s, int u, float (&xs)[XU], float &xsum) {
+        float sum = 0.f;
+#pragma unroll
+        for (int wq = 0; wq < XU / 8; ++wq) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float sc = q == 0 ? 1.f : q == 1 ? 0.0625f : q == 2 ? 0.00390625f : 0.000244140625f;
+                float a = 0.f, b = 0.f;
+                if (u >= 0) {
+                    const uint16_t *xp = p.x + (size_t)s * p.I + (size_t)u * XU + 8 * wq;
+                    a = bf16_bits_to_f32(xp[q]);
+                    b = bf16_bits_to_f32(xp[q + 4]);
+                }
+                sum += a + b;
+                xs[2 * (4 * wq + q)] = a * sc;
+                xs[2 * (4 * wq + q) + 1] = b * sc;
+            }
+        }
+        xsum = sum;
+    }
+
+    template <int S, int NW, int XU>
+    __device__ static void accumulate(const Words<NW> &wd, Aux hd, const float (&xs)[S][XU],
+                                      const float (&xsum)[S], float *part) {
+        constexpr uint32_t kMagic = 0x4B000000u;
+        float2 d[NW * 4];
+#pragma unroll
+        for (int wq = 0; wq < NW; ++wq) {
+            const uint32_t lo = wd.w[wq];
+            const uint32_t hi = lo >> 16;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t m = 0xFu << (4 * q);
+                float2 f = make_float2(__uint_as_float((lo & m) | kMagic), __uint_as_float((hi & m) | kMagic));
+                d[4 * wq + q] = __fadd2_rn(f, make_float2(-8388608.f, -8388608.f));
+            }
+        }
+        const float scale = f16_bits_to_f32((uint16_t)(hd & 0xFFFFu));
+        const float zero = f16_bits_to_f32((uint16_t)(hd >> 16));
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < NW * 4; ++i)
+                acc = __ffma2_rn(d[i], make_float2(xs[s][2 * i], xs[s][2 * i + 1]), acc);
+            part[s] = fmaf(scale, acc.x + acc.y, fmaf(zero, xsum[s], part[s]));
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// dispatch
+// ---------------------------------------------------------------------------
+namespace {
+
+int mq4_nw(int S) { return S <= 4 ? 2 : 1; }      // activation registers 8*NW*S <= 64
+int mq4_rb(int S, int U) { return S <= 2 ? (U == 1 ? 8 : 4) : 4; }
+
+CsPlan mq4_plan(int S, int I, int O, int *U_out) {
+    const int nw = mq4_nw(S);
+    const int units = I / (8 * nw);
+    // up to three units per thread at S = 1 (at S > 1 more than one spills
+    // registers); longer rows split across blocks
+    const int U = S == 1 ? (units > 2 * kCsMaxThreads ? 3 : units > kCsMaxThreads ? 2 : 1) : 1;
+    *U_out = U;
+    const int regs = 40 + 8 * nw * S * U + S * U + mq4_rb(S, U) * U * (nw + 1) + 2 * mq4_rb(S, U) * S;
+    return cs_plan(units, O, U, mq4_rb(S, U), regs);
+}
+
+template <int S, int NW, int U>
+void launch_cs_mq4(const FmtMq4v2::Params &p, float *out, const CsPlan &pl, int units, cudaStream_t st) {
+    constexpr int RB = S <= 2 ? (U == 1 ? 8 : 4) : 4;
+    dim3 grid(pl.grid_x, pl.splits);
+    gemv_cs_kernel<FmtMq4v2, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
+                                                                       pl.nrowb);
+}
+
+template <int S>
+void launch_cs_mq4_s(const FmtMq4v2::Params &p, float *out, const CsPlan &pl, int units, int U,
+                     cudaStream_t st) {
+    constexpr int NW = S <= 4 ? 2 : 1;
+    if constexpr (S == 1) {
+        if (U == 2) {
+            launch_cs_mq4<S, NW, 2>(p, out, pl, units, st);
+            return;
+        }
+        if (U == 3) {
+            launch_cs_mq4<S, NW, 3>(p, out, pl, units, st);
+            return;
+        }
+    }
+    (void)U;
+    launch_cs_mq4<S, NW, 1>(p, out, pl, units, st);
+}
+
+int gemv_mq4_chunk(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+                   size_t ws_bytes, cudaStream_t st) {
+    // the ABI guarantees 8-byte aligned blocks and 2-byte aligned x, which is
+    // all the fast path needs, so MQ4-V2 has no general fallback kernel
+    int U = 1;
+    const CsPlan pl = mq4_plan(S, I, O, &U);
+    const int units = I / (8 * mq4_nw(S));
+    const size_t need = cs_ws_bytes(pl, S, O);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) {
+        set_error_detail("qgemv_mq4v2: this shape splits the reduction and needs %zu bytes of workspace "
+                         "(got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
+        return kEWorkspace;
+    }
+    FmtMq4v2::Params p;
+    p.x = x; p.blocks = blocks; p.I = I; p.O = O; p.rowbytes = (size_t)(I / 256) * 136;
+    float *out = pl.splits > 1 ? static_cast<float *>(ws) : y;
+    switch (S) {
+#define QG_CASE(SS) case SS: launch_cs_mq4_s<SS>(p, out, pl, units, U, st); break;
+        QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+    }
+    if (pl.splits > 1) launch_splitk_reduce(y, static_cast<float *>(ws), pl.splits, S, O, st);
+    return check_launch("qgemv_mq4v2");
+}
+
+}  // namespace
+
+size_t ws_mq4v2(int S, int I, int O) {
+    const int s = S < 8 ? S : 8;
+    int U = 1;
+    return cs_ws_bytes(mq4_plan(s, I, O, &U), s, O);
+}
+
+int run_gemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+                   size_t ws_bytes, cudaStream_t st) {
+    for (int s0 = 0; s0 < S; s0 += 8) {
+        const int sc = S - s0 < 8 ? S - s0 : 8;
+        const int rc = gemv_mq4_chunk(y + (size_t)s0 * O, x + (size_t)s0 * I, blocks, sc, I, O, ws, ws_bytes, st);
+        if (rc != kOk) return rc;
+    }
+    return kOk;
+}
+
+}  // namespace qg

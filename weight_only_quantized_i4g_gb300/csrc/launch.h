@@ -1,0 +1,38 @@
+// launch.h -- internal interface between the C ABI (abi.cu) and the kernels.
+// Arguments reaching these functions have been validated by abi.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qg {
+
+// Status codes mirror qg_status in include/qgemv.h.
+enum { kOk = 0, kEInval = -1, kEGs = -2, kEShape = -3, kEAlign = -4, kEWorkspace = -5, kECuda = -6 };
+
+// Records a refusal / error detail for qg_last_error() (thread-local).
+void set_error_detail(const char *fmt, ...);
+
+// Reports launch errors of the kernels just enqueued.
+int check_launch(const char *what);
+
+size_t ws_i4g(int S, int I, int O, int gs);
+size_t ws_fp8b128(int S, int I, int O);
+size_t ws_mq4v2(int S, int I, int O);
+
+int run_gemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,
+                 int gs, void *ws, size_t ws_bytes, cudaStream_t st);
+int run_gemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S,
+                     int I, int O, void *ws, size_t ws_bytes, cudaStream_t st);
+int run_gemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+                   size_t ws_bytes, cudaStream_t st);
+
+int run_gemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I,
+                 int O, int gs, void *ws, size_t ws_bytes, cudaStream_t st);
+
+int run_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs, cudaStream_t st);
+int run_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, cudaStream_t st);
+int run_fwht256(float *out, const float *in, const int8_t *signs, size_t nblocks, cudaStream_t st);
+
+}  // namespace qg
