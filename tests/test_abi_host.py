@@ -13,8 +13,12 @@ HEADER = os.path.join(ROOT, "include", "qgemv.h")
 
 @pytest.fixture(scope="module")
 def qg():
-    from weight_only_quantized_i4g_gb300 import _build
-    _build.build()
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "qgemv_build", os.path.join(ROOT, "weight_only_quantized_i4g_gb300", "_build.py"))
+    build_script = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(build_script)
+    build_script.build()
     import weight_only_quantized_i4g_gb300 as m
     return m
 
