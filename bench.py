@@ -61,10 +61,6 @@ def weight_bytes(fmt, O, I):
     return O * (I // 256) * 136
 
 
-def step_bytes():
-    return sum(weight_bytes(f, O, I) for _, f, O, I, _ in SHAPES)
-
-
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -218,9 +214,9 @@ def build_device_call(qg, torch, fmt, O, I, raw, dev, stream):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
-def build_oracle_inputs(orc, raws):
+def build_oracle_inputs(orc, raws, shapes):
     inputs = []
-    for (name, fmt, O, I, _), raw in zip(SHAPES, raws):
+    for (name, fmt, O, I, _), raw in zip(shapes, raws):
         if fmt == "i4g":
             wq, sc = orc.quantize_i4g(raw["w"], O, I, GS)
             inputs.append((fmt, O, I, (raw["x"], wq, sc)))
@@ -258,10 +254,10 @@ def oracle_pass(orc, inputs, frac, pool, nthreads):
     return done
 
 
-def cpu_oracle_timing(raws, steps, warmup, frac):
+def cpu_oracle_timing(raws, shapes, steps, warmup, frac):
     import oracle
     orc = oracle.Oracle()
-    inputs = build_oracle_inputs(orc, raws)
+    inputs = build_oracle_inputs(orc, raws, shapes)
     nthreads = os.cpu_count() or 1
     with ThreadPoolExecutor(nthreads) as pool:
         for _ in range(warmup):
@@ -281,10 +277,11 @@ def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    raws = [make_raw(*s) for s in SHAPES]
+    shapes = selected_shapes(args)
+    raws = [make_raw(*s) for s in shapes]
     # bound the CPU work: about 40 full passes' worth over the whole run
     frac = min(1.0, 40.0 / max(1, args.steps + args.warmup))
-    gbs, dt, cores = cpu_oracle_timing(raws, args.steps, args.warmup, frac)
+    gbs, dt, cores = cpu_oracle_timing(raws, shapes, args.steps, args.warmup, frac)
     sample = (f"each step: the first {frac:.3g} of the rows of all six matrices (fp8 in whole "
               f"128-row blocks), batch 1, split by rows across {cores} host threads")
     line = {
@@ -315,18 +312,19 @@ def ours_arm(args):
     stream = torch.cuda.Stream(device=dev)
     hbm_peak, peak_kind = load_peaks()
 
-    raws = [make_raw(*s) for s in SHAPES]
+    shapes = selected_shapes(args)
+    raws = [make_raw(*s) for s in shapes]
     calls = []
     with torch.cuda.stream(stream):
-        for (name, fmt, O, I, tag), raw in zip(SHAPES, raws):
+        for (name, fmt, O, I, tag), raw in zip(shapes, raws):
             call, x, y, keep = build_device_call(qg, torch, fmt, O, I, raw, dev, stream)
             calls.append({"name": name, "fmt": fmt, "O": O, "I": I, "call": call, "x": x, "y": y,
                           "keep": keep, "bytes": weight_bytes(fmt, O, I)})
     stream.synchronize()
     for c in calls:
         c["xp"], c["yp"] = c["x"].data_ptr(), c["y"].data_ptr()
-    dom = next(i for i, c in enumerate(calls) if c["name"] == DOMINANT)
-    nbytes = step_bytes()
+    dom = next((i for i, c in enumerate(calls) if c["name"] == DOMINANT), 0)
+    nbytes = sum(c["bytes"] for c in calls)
 
     def step(ev_pair=None):
         for i, c in enumerate(calls):
@@ -411,7 +409,7 @@ def ours_arm(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, dt, cores = cpu_oracle_timing(raws, 1, 0, 1.0)
+        gbs, dt, cores = cpu_oracle_timing(raws, shapes, 1, 0, 1.0)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"one full step (all six matrices, batch 1) split by rows across {cores} "
                          f"host threads, {dt:.1f} s"}
@@ -422,7 +420,8 @@ def ours_arm(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": 1, "gs": GS,
+            "config": {"workload": WORKLOAD if len(shapes) == len(SHAPES) else
+                       "subset: " + ", ".join(c["name"] for c in calls), "batch": 1, "gs": GS,
                        "bytes_per_step": nbytes,
                        "pct_hbm_peak": round(100 * value / world / hbm_peak, 2),
                        "hbm_peak_gbs": hbm_peak, "hbm_peak_kind": peak_kind,
@@ -451,7 +450,6 @@ def per_format_breakdown(qg, torch, calls, stream, hbm_peak):
     """Kernel-only time per call of each shape: a CUDA graph of back-to-back
     calls cycling through enough copies of the weights (>= 3x L2) that every
     call reads from HBM; mean over the graph, best of 3 replays."""
-    import ctypes
     out = {}
     l2 = 129 * 2 ** 20
     for c in calls:
@@ -471,18 +469,21 @@ def per_format_breakdown(qg, torch, calls, stream, hbm_peak):
             for r in range(reps):
                 ps = ptrsets[r % len(ptrsets)]
                 if fmt == "i4g":
-                    lib.qgemv_i4g(c["yp"], c["xp"], ps[0], ps[1], 1, I, O, GS, None, 0, st)
+                    rc = lib.qgemv_i4g(c["yp"], c["xp"], ps[0], ps[1], 1, I, O, GS, None, 0, st)
                 elif fmt == "fp8":
-                    lib.qgemv_fp8b128(c["yp"], c["xp"], ps[0], ps[1], 1, I, O, None, 0, st)
+                    rc = lib.qgemv_fp8b128(c["yp"], c["xp"], ps[0], ps[1], 1, I, O, None, 0, st)
                 else:
-                    lib.qgemv_mq4v2(c["yp"], c["xp"], ps[0], 1, I, O, None, 0, st)
+                    rc = lib.qgemv_mq4v2(c["yp"], c["xp"], ps[0], 1, I, O, None, 0, st)
+                if rc:
+                    raise qg.QGError(rc)
         best = None
         for _ in range(4):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
+            with torch.cuda.stream(stream):         # replay runs on the current stream
+                a.record(stream)
+                g.replay()
+                b.record(stream)
             b.synchronize()
             t = a.elapsed_time(b) / reps
             best = t if best is None else min(best, t)
@@ -490,8 +491,17 @@ def per_format_breakdown(qg, torch, calls, stream, hbm_peak):
         gbs = c["bytes"] / (best * 1e-3) / 1e9
         out[c["name"]] = {"us_per_call": round(best * 1e3, 3), "weight_gbs": round(gbs, 1),
                           "pct_hbm_peak": round(100 * gbs / hbm_peak, 1), "weight_copies": copies}
-        _ = ctypes
     return out
+
+
+def selected_shapes(args):
+    if not args.only:
+        return SHAPES
+    names = args.only.split(",")
+    unknown = set(names) - {s[0] for s in SHAPES}
+    if unknown:
+        raise SystemExit(f"--only: unknown shape(s) {sorted(unknown)}")
+    return [s for s in SHAPES if s[0] in names]
 
 
 def main():
@@ -502,6 +512,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-breakdown", dest="breakdown", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="comma-separated subset of the shapes (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -163,7 +163,8 @@ int qg_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, in
  * q = clamp(rint((w - f32(zero)) / f32(scale)), 0, 15) against the
  * round-tripped header; a constant half (or one whose fp16 step rounds to 0)
  * stores scale 0 and q = 0.
- *   w f32 [O, I] (device), I % 256 == 0;  blocks uint8 [O, I/256, 136] */
+ *   w f32 [O, I] (device, 4-byte aligned), I % 256 == 0;
+ *   blocks uint8 [O, I/256, 136] (device, 8-byte aligned) */
 int qg_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, qg_stream_t stream);
 
 /* Signed Walsh-Hadamard rotation of 256-element blocks (hipfire "MQ4 V2"

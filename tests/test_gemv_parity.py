@@ -134,7 +134,9 @@ def run_fp8(qg, x, codes, scales, S, I, O):
 
 def test_fp8_all_256_codes_through_the_kernel(qg):
     """Row r holds code r in column 0 (zeros elsewhere), x = e_0, scale 1:
-    y[r] must be the E4M3-FN value of code r, bit for bit (NaN for 0x7F/0xFF)."""
+    y[r] must be the E4M3-FN value of code r, bit for bit (NaN for 0x7F/0xFF).
+    The sign of a zero cannot survive a sum that starts at +0 (0 + -0 = +0),
+    so both zero codes must read +0."""
     O, I, S = 256, 16, 1
     codes = np.zeros((O, I), np.uint8)
     codes[:, 0] = np.arange(256, dtype=np.uint8)
@@ -147,6 +149,7 @@ def test_fp8_all_256_codes_through_the_kernel(qg):
     nan = np.isnan(ref)
     assert np.array_equal(np.isnan(y), nan)
     assert set(np.nonzero(nan)[0].tolist()) == {0x7F, 0xFF}
+    ref = np.where(ref == 0.0, 0.0, ref)          # -0 -> +0
     assert np.array_equal(y[~nan].astype(np.float32).view(np.uint32),
                           ref[~nan].astype(np.float32).view(np.uint32))
 

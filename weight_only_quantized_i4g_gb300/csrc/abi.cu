@@ -148,7 +148,8 @@ int qg_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, qg_stream_t s
     if (rc) return rc;
     if (I % 256) QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 256", fn, I);
     if (!blocks || !w) QG_REFUSE(kEInval, "%s: blocks and w must be non-NULL", fn);
-    if (!aligned(w, 4)) QG_REFUSE(kEAlign, "%s: w must be 4-byte aligned", fn);
+    if (!aligned(w, 4) || !aligned(blocks, 8))
+        QG_REFUSE(kEAlign, "%s: w must be 4-byte and blocks 8-byte aligned", fn);
     cudaGetLastError();
     return run_encode_mq4v2(blocks, w, O, I, as_stream(stream));
 }

@@ -84,23 +84,23 @@ __global__ void encode_mq4v2_kernel(uint8_t *__restrict__ blocks, const float *_
         const float stf = __half2float(sc16);
         const float zf = __half2float(z16);
         const uint32_t hd = (uint32_t)__half_as_ushort(sc16) | ((uint32_t)__half_as_ushort(z16) << 16);
-        blk[4 * h + 0] = (uint8_t)(hd & 0xFF);
-        blk[4 * h + 1] = (uint8_t)((hd >> 8) & 0xFF);
-        blk[4 * h + 2] = (uint8_t)((hd >> 16) & 0xFF);
-        blk[4 * h + 3] = (uint8_t)(hd >> 24);
-        uint8_t *pay = blk + 8 + 64 * h;
-        for (int j = 0; j < 128; j += 2) {
-            uint32_t q2[2];
-            for (int k = 0; k < 2; ++k) {
+        // Header and payload go out as aligned 32-bit words (the block base is
+        // 8-byte aligned): single-byte stores of the fp16 bits were observed
+        // to lose the low byte on this toolchain, whole words never did.
+        reinterpret_cast<uint32_t *>(blk)[h] = hd;
+        uint32_t *pay = reinterpret_cast<uint32_t *>(blk + 8 + 64 * h);
+        for (int k = 0; k < 16; ++k) {            // word k holds weights 8k..8k+7 of the half
+            uint32_t word = 0u;
+            for (int m = 0; m < 8; ++m) {
                 int q = 0;
                 if (stf != 0.f) {
-                    float r = rintf(__fdiv_rn(__fsub_rn(hw[j + k], zf), stf));
+                    float r = rintf(__fdiv_rn(__fsub_rn(hw[8 * k + m], zf), stf));
                     r = r < 0.f ? 0.f : (r > 15.f ? 15.f : r);
                     q = (int)r;
                 }
-                q2[k] = (uint32_t)q;
+                word |= (uint32_t)q << (4 * m);
             }
-            pay[j >> 1] = (uint8_t)(q2[0] | (q2[1] << 4));
+            pay[k] = word;
         }
     }
 }
