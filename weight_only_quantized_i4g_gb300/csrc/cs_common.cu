@@ -6,9 +6,54 @@
 #include <mutex>
 
 #include "gemv_cs.cuh"
+#include "gemv_tma.cuh"
 #include "launch.h"
+#include "pipeline.cuh"
 
 namespace qg {
+
+// One error word per device: kernels that give up waiting set it; the host
+// reads and clears it with qg_device_status().
+__device__ int g_device_error = 0;
+
+int *device_error_word() {
+    static std::mutex mu;
+    static int *cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        cache[dev] = static_cast<int *>(p);
+    }
+    return cache[dev];
+}
+
+int read_device_error(int *status) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess) {
+        set_error_detail("qg_device_status: %s", cudaGetErrorString(e));
+        return kECuda;
+    }
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+        if (e != cudaSuccess) {
+            set_error_detail("qg_device_status: %s", cudaGetErrorString(e));
+            return kECuda;
+        }
+    }
+    *status = v;
+    return kOk;
+}
 
 // ---------------------------------------------------------------------------
 // error detail (thread-local, read by qg_last_error)
@@ -92,6 +137,62 @@ CsPlan cs_plan(int units, int O, int u, int rb, int regs_per_thread) {
     const long resident = (long)nsm * per_sm / (splits > 0 ? splits : 1);
     pl.grid_x = pl.nrowb < resident ? pl.nrowb : (int)(resident > 0 ? resident : 1);
     return pl;
+}
+
+// ---------------------------------------------------------------------------
+// plan of the staged (TMA) kernel
+// ---------------------------------------------------------------------------
+bool tma_plan(const TmaGeom &g, int O, int RB, int NV, int U_max, TmaPlan *pl) {
+    const int max_thr = kTmaMaxConsumerWarps * 32;
+    int U = 1, splits = 1;
+    if (g.units > max_thr) {
+        if (g.units <= max_thr * U_max) {
+            U = cdiv(g.units, max_thr);
+        } else {
+            U = U_max;
+            splits = cdiv(g.units, max_thr * U);
+        }
+    }
+    int ups = cdiv(g.units, splits);
+    if (splits > 1) {
+        ups = round_up(ups, g.granule);
+        splits = cdiv(g.units, ups);
+    }
+    if (cdiv(ups, U) > max_thr) return false;
+    const uint32_t seg = splits == 1 ? g.rowbytes : (uint32_t)(ups / g.granule) * g.granule_bytes;
+    if (seg % 16 != 0 || g.rowbytes % 16 != 0 || g.arowbytes % 4 != 0) return false;
+    const int nc = cdiv(cdiv(ups, U), 32);
+    const uint32_t stage_w = (uint32_t)round_up((int)(RB * seg), 128);
+    const uint32_t stage_a = (uint32_t)round_up((int)(RB * g.arowbytes), 128);
+    const uint32_t red_stage = (uint32_t)(nc * NV * 4);
+    const uint32_t per_slot = stage_w + stage_a + red_stage + 16;
+    // aim for about 16 consumer warps per SM, up to 8 blocks; then as many
+    // ring slots (2..6) as that share of the 228 KB of shared memory holds
+    int nst = 0;
+    int target = 16 / nc;
+    if (target < 1) target = 1;
+    if (target > 8) target = 8;
+    for (; target >= 1; --target) {
+        long budget = 233472L / target - 1024;
+        if (budget > 232448) budget = 232448;
+        nst = (int)(budget / per_slot);
+        if (nst > 6) nst = 6;
+        if (nst >= 2) break;
+    }
+    if (nst < 2) return false;
+    pl->units = g.units;
+    pl->U = U;
+    pl->nc = nc;
+    pl->splits = splits;
+    pl->units_per_split = ups;
+    pl->nrowb = cdiv(O, RB);
+    pl->nst = nst;
+    pl->L.stage_w = stage_w;
+    pl->L.stage_a = stage_a;
+    pl->L.red_off = (uint32_t)nst * (stage_w + stage_a);
+    pl->L.bar_off = (uint32_t)round_up((int)(pl->L.red_off + nst * red_stage), 16);
+    pl->L.total = pl->L.bar_off + 16u * (uint32_t)nst;
+    return true;
 }
 
 // ---------------------------------------------------------------------------

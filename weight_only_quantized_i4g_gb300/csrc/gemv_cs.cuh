@@ -29,6 +29,12 @@ namespace qg {
 
 constexpr int kCsMaxThreads = 512;
 
+inline int next_pow2(int x) {
+    int p = 1;
+    while (p < x) p <<= 1;
+    return p;
+}
+
 template <int X> struct NextPow2 {
     static constexpr int value = X <= 1 ? 1 : X <= 2 ? 2 : X <= 4 ? 4 : X <= 8 ? 8 : X <= 16 ? 16 : 32;
 };

@@ -6,21 +6,29 @@
 // consecutive elements of a row, applied to every term of its group:
 //     y[s,o] = sum_i (n(o,i) - 8) * scale[o, i/gs] * x[s,i]
 //
-// Fast path (column-stationary, gemv_cs.cuh): a thread's unit is 4*NW bytes =
-// 8*NW consecutive elements inside one group (gs % (8*NW) == 0), so one scale
-// multiplies the unit's partial sum.  Decode: for a 32-bit word holding 8
-// nibbles, OR-ing the masked nibble into the bit pattern of 2^23 gives the
-// float 2^23 + n*16^p exactly (p = nibble position within a 16-bit half);
-// subtracting 2^23 + 8*16^p (exact) leaves (n - 8)*16^p, and the matching
-// activation is pre-scaled by 16^-p (exact).  Two elements at a time with
-// packed f32x2 add and fma.
+// A thread's unit is 4*NW bytes = 8*NW consecutive elements inside one group
+// (gs % (8*NW) == 0), so one scale multiplies the unit's partial sum.
+// Decode: for a 32-bit word of 8 nibbles, OR-ing a masked nibble into the bit
+// pattern of 2^23 gives the float 2^23 + n*16^p exactly (p = position of the
+// nibble in its 16-bit half); subtracting 2^23 + 8*16^p (exact) leaves
+// (n - 8)*16^p, and the matching activation is pre-scaled by 16^-p (exact).
+// Two elements at a time with packed f32x2 add and fma.
+//
+// Paths, fastest first:
+//   staged   gemv_tma.cuh: bulk copies of whole rows (and their scales) into
+//            a shared-memory ring; needs 16-byte aligned w, x and scales,
+//            I % 32 == 0, gs a multiple of the unit and ceil(I/gs) % 4 == 0
+//   direct   gemv_cs.cuh: the same decode with 16-, 8- or 4-byte global loads
+//   general  any shape and alignment, byte loads
 #include "gemv_cs.cuh"
+#include "gemv_tma.cuh"
 #include "launch.h"
 
 namespace qg {
 
 struct FmtI4G {
     static constexpr int kElemsPerWord = 8;
+    static constexpr int kPairsPerWord = 4;
     struct Params {
         const float *x;
         const uint8_t *w;
@@ -28,6 +36,7 @@ struct FmtI4G {
         int I, O, gs, ng;
         size_t rb;
     };
+    // ---- direct (column-stationary) kernel ---------------------------------
     struct ThreadConst { int g; };   // group of the thread's unit
     typedef float Aux;               // the row's scale for that group
 
@@ -90,6 +99,62 @@ struct FmtI4G {
             part[s] = fmaf(sc, acc.x + acc.y, part[s]);
         }
     }
+
+    // ---- staged (TMA) kernel -------------------------------------------------
+    struct TConst { uint32_t uoff; uint32_t goff; };   // unit byte offset, scale byte offset
+    struct StageConst {};
+
+    __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.rb; }
+    __device__ static uint32_t aux_row_bytes(const Params &p) { return (uint32_t)p.ng * 4u; }
+    __device__ static uint32_t seg_byte(const Params &, int u, int XU) { return (uint32_t)(u * (XU / 2)); }
+    __device__ static const void *w_src(const Params &p, int o, uint32_t col) {
+        return p.w + (size_t)o * p.rb + col;
+    }
+    __device__ static const void *a_src(const Params &p, int o) { return p.scales + (size_t)o * p.ng; }
+    __device__ static TConst tconst(const Params &p, int u, int XU, uint32_t seg_col) {
+        return TConst{(uint32_t)(u * (XU / 2)) - seg_col, 4u * (uint32_t)((u * XU) / p.gs)};
+    }
+    __device__ static StageConst stage_const(const Params &, int, TConst) { return StageConst{}; }
+    __device__ static float aux(const uint8_t *, const uint8_t *row_a, TConst tc, StageConst) {
+        return lds_f32(row_a + tc.goff);
+    }
+
+    // xp[4*wq + q] = {x[8wq + q], x[8wq + q + 4]} * 16^-q  (16-byte vector loads)
+    template <int XU, int NP>
+    __device__ static void load_x(const Params &p, int s, int u, uint64_t (&xp)[NP], float &xsum) {
+        xsum = 0.f;
+#pragma unroll
+        for (int wq = 0; wq < XU / 8; ++wq) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (u >= 0) {
+                const float4 *src = reinterpret_cast<const float4 *>(p.x + (size_t)s * p.I + (size_t)u * XU + 8 * wq);
+                a = __ldg(src);
+                b = __ldg(src + 1);
+            }
+            xp[4 * wq + 0] = pack2(a.x, b.x);
+            xp[4 * wq + 1] = pack2(a.y * 0.0625f, b.y * 0.0625f);
+            xp[4 * wq + 2] = pack2(a.z * 0.00390625f, b.z * 0.00390625f);
+            xp[4 * wq + 3] = pack2(a.w * 0.000244140625f, b.w * 0.000244140625f);
+        }
+    }
+
+    template <int S, int NW, int NP>
+    __device__ static void accumulate(const Words<NW> &wd, float sc, const uint64_t (&xp)[S][NP],
+                                      const float (&)[S], float *part) {
+        uint64_t d[NW][4];
+#pragma unroll
+        for (int wq = 0; wq < NW; ++wq) decode_nibbles<true>(wd.w[wq], d[wq]);
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            uint64_t acc = 0ull;
+#pragma unroll
+            for (int wq = 0; wq < NW; ++wq)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) ffma2(acc, d[wq][q], xp[s][4 * wq + q]);
+            const float2 a = unpack2(acc);
+            part[s] = fmaf(sc, a.x + a.y, part[s]);
+        }
+    }
 };
 
 // ---------------------------------------------------------------------------
@@ -133,12 +198,31 @@ namespace {
 // words per unit for S tokens: keep the activation registers (8*NW*S) <= 64
 int i4g_nw(int S) { return S <= 2 ? 4 : S <= 4 ? 2 : 1; }
 int i4g_rb(int S, int U) { return S <= 2 ? (U == 1 ? 8 : 4) : 4; }
+constexpr int kTmaRb(int S) { return S <= 2 ? 8 : 4; }
 
 bool i4g_fast_ok(const float *x, const uint8_t *w, int I, int gs, int S) {
     const int nw = i4g_nw(S);
     const int ue = 8 * nw;                       // elements per unit
     return (I % ue == 0) && (gs % ue == 0) && ((uintptr_t)w % (4 * nw) == 0) &&
            ((uintptr_t)x % 4 == 0);
+}
+
+bool i4g_tma_ok(const float *x, const uint8_t *w, const float *scales, int I, int gs, int S) {
+    const int ng = (I + gs - 1) / gs;
+    return i4g_fast_ok(x, w, I, gs, S) && (I % 32 == 0) && (ng % 4 == 0) && ((uintptr_t)w % 16 == 0) &&
+           ((uintptr_t)x % 16 == 0) && ((uintptr_t)scales % 16 == 0);
+}
+
+bool i4g_tma_plan(int S, int I, int O, int gs, TmaPlan *pl) {
+    const int nw = i4g_nw(S);
+    TmaGeom g;
+    g.units = I / (8 * nw);
+    g.granule = 4 / nw;                          // 16 bytes of weights
+    g.rowbytes = (uint32_t)(I / 2);
+    g.granule_bytes = 16;
+    g.arowbytes = (uint32_t)((I + gs - 1) / gs) * 4u;
+    const int rb = kTmaRb(S);
+    return tma_plan(g, O, rb, next_pow2(rb * S), S == 1 ? 2 : 1, pl);
 }
 
 CsPlan i4g_plan(int S, int I, int O, int *U_out) {
@@ -173,8 +257,43 @@ void launch_cs_i4g_s(const FmtI4G::Params &p, float *out, const CsPlan &pl, int 
     launch_cs_i4g<S, NW, 1>(p, out, pl, units, st);
 }
 
+template <int S>
+void launch_tma_i4g_s(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+    constexpr int NW = S <= 2 ? 4 : S <= 4 ? 2 : 1;
+    constexpr int RB = kTmaRb(S);
+    if constexpr (S == 1) {
+        if (pl.U == 2) {
+            launch_tma<FmtI4G, S, NW, 2, RB>(p, out, pl, st);
+            return;
+        }
+    }
+    launch_tma<FmtI4G, S, NW, 1, RB>(p, out, pl, st);
+}
+
 int gemv_i4g_chunk(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,
                    int gs, void *ws, size_t ws_bytes, cudaStream_t st) {
+    FmtI4G::Params p;
+    p.x = x; p.w = w; p.scales = scales; p.I = I; p.O = O; p.gs = gs;
+    p.ng = (I + gs - 1) / gs; p.rb = ((size_t)I + 1) / 2;
+
+    TmaPlan tp;
+    if (i4g_tma_ok(x, w, scales, I, gs, S) && i4g_tma_plan(S, I, O, gs, &tp)) {
+        const size_t need = tp.splits > 1 ? (size_t)tp.splits * S * O * sizeof(float) : 0;
+        if (need > 0 && (ws == nullptr || ws_bytes < need)) {
+            set_error_detail("qgemv_i4g: this shape splits the reduction and needs %zu bytes of workspace "
+                             "(got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
+            return kEWorkspace;
+        }
+        float *out = tp.splits > 1 ? static_cast<float *>(ws) : y;
+        switch (S) {
+#define QG_CASE(SS) case SS: launch_tma_i4g_s<SS>(p, out, tp, st); break;
+            QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+        }
+        if (tp.splits > 1) launch_splitk_reduce(y, static_cast<float *>(ws), tp.splits, S, O, st);
+        return check_launch("qgemv_i4g");
+    }
+
     if (!i4g_fast_ok(x, w, I, gs, S)) {
         const int blocks_needed = (O + 7) / 8;
         const int cap = num_sms() * 16;
@@ -195,9 +314,6 @@ int gemv_i4g_chunk(float *y, const float *x, const uint8_t *w, const float *scal
                          "(got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
         return kEWorkspace;
     }
-    FmtI4G::Params p;
-    p.x = x; p.w = w; p.scales = scales; p.I = I; p.O = O; p.gs = gs;
-    p.ng = (I + gs - 1) / gs; p.rb = ((size_t)I + 1) / 2;
     float *out = pl.splits > 1 ? static_cast<float *>(ws) : y;
     switch (S) {
 #define QG_CASE(SS) case SS: launch_cs_i4g_s<SS>(p, out, pl, units, U, st); break;
@@ -213,8 +329,14 @@ int gemv_i4g_chunk(float *y, const float *x, const uint8_t *w, const float *scal
 size_t ws_i4g(int S, int I, int O, int gs) {
     const int s = S < 8 ? S : 8;
     if (I % (8 * i4g_nw(s)) != 0 || gs % (8 * i4g_nw(s)) != 0) return 0;  // general kernel: none
+    // the larger of the staged and the direct plan (the pointers decide the path)
+    size_t need = 0;
+    TmaPlan tp;
+    if (I % 32 == 0 && ((I + gs - 1) / gs) % 4 == 0 && i4g_tma_plan(s, I, O, gs, &tp) && tp.splits > 1)
+        need = (size_t)tp.splits * s * O * sizeof(float);
     int U = 1;
-    return cs_ws_bytes(i4g_plan(s, I, O, &U), s, O);
+    const size_t cs = cs_ws_bytes(i4g_plan(s, I, O, &U), s, O);
+    return need > cs ? need : cs;
 }
 
 int run_gemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,

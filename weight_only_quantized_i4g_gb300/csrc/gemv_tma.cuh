@@ -1,0 +1,349 @@
+// gemv_tma.cuh -- warp-specialized decode GEMV: bulk-copy (TMA) streaming of
+// weight rows through a shared-memory ring, decode from shared memory.
+//
+// Block = 1 producer warp + nc consumer warps.  The block walks row batches
+// rb = blockIdx.x, blockIdx.x + gridDim.x, ... of RB rows each.
+//   producer  lane 0 fills up to nst ring slots ahead with 1-D bulk copies of
+//             the batch's rows (one copy for whole rows, one per row for a
+//             column split), completion counted on the slot's `full`
+//             mbarrier; when the consumers release a slot (`empty` mbarrier)
+//             the warp adds the consumers' per-warp partial sums of that
+//             batch, writes the outputs and refills the slot.
+//   consumers every thread owns U fixed column units (NW 32-bit words of
+//             packed weights each) and holds the matching activations in
+//             registers, loaded once with 16-byte vector loads and already in
+//             the form the decode needs.  Per batch it reads its units from
+//             shared memory, decodes, multiplies, reduces across the warp
+//             with a reduce-scatter butterfly and leaves one partial per
+//             (row, token) per warp in shared memory.
+// Every wait is bounded; a wait that gives up raises the device error word
+// and the warp leaves (the producer first lets its copies in flight land).
+//
+// A format F supplies:
+//   kElemsPerWord, kPairsPerWord     elements / f32 pairs per 32-bit word
+//   Params, TConst, StageConst
+//   row_bytes(p), aux_row_bytes(p)   staged bytes per row (weights, side data)
+//   w_src(p, o, col_byte), a_src(p, o)
+//   seg_byte(p, u, XU)               byte offset in a row where unit u's segment starts
+//   tconst(p, u, XU, seg_col)        per-unit offsets inside the staged segment
+//   stage_const(p, o0, tc)           per-batch side data read from global
+//   aux(sw_row, sa_row, tc, sc)      per-(row, unit) side data
+//   load_x<XU, NP>(p, s, u, xp, xsum)
+//   accumulate<S, NW, NP>(words, aux, xp, xsum, part)
+#pragma once
+
+#include "common.cuh"
+#include "gemv_cs.cuh"
+#include "pipeline.cuh"
+
+namespace qg {
+
+constexpr int kTmaMaxConsumerWarps = 16;
+
+template <int NW>
+__device__ __forceinline__ Words<NW> lds_words(const uint8_t *p);
+template <>
+__device__ __forceinline__ Words<4> lds_words<4>(const uint8_t *p) {
+    Words<4> r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]) : "r"(smem_addr(p)));
+    return r;
+}
+template <>
+__device__ __forceinline__ Words<2> lds_words<2>(const uint8_t *p) {
+    Words<2> r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "r"(smem_addr(p)));
+    return r;
+}
+template <>
+__device__ __forceinline__ Words<1> lds_words<1>(const uint8_t *p) {
+    Words<1> r;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r.w[0]) : "r"(smem_addr(p)));
+    return r;
+}
+
+__device__ __forceinline__ float lds_f32(const uint8_t *p) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_addr(p)));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(const uint8_t *p) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Packed f32x2 helpers (sm_100 family)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+    return make_float2(a, b);
+}
+__device__ __forceinline__ void ffma2(uint64_t &acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// Eight nibbles of one word -> four f32 pairs d[q] = {n(q)*16^q, n(q+4)*16^q} - c_q
+// where n(e) is the nibble of element e (bits 4e..4e+3).  OR-ing the masked
+// nibble into the pattern of 2^23 gives 2^23 + n*16^q exactly; subtracting
+// c_q = 2^23 + bias*16^q (bias 8 for signed nibbles, 0 for unsigned) is exact.
+template <bool kSigned>
+__device__ __forceinline__ void decode_nibbles(uint32_t w, uint64_t (&d)[4]) {
+    // -(2^23 + bias*16^q) as f32 bit patterns, twice
+    constexpr uint64_t c0 = kSigned ? 0xCB000008CB000008ull : 0xCB000000CB000000ull;
+    constexpr uint64_t c1 = kSigned ? 0xCB000080CB000080ull : 0xCB000000CB000000ull;
+    constexpr uint64_t c2 = kSigned ? 0xCB000800CB000800ull : 0xCB000000CB000000ull;
+    constexpr uint64_t c3 = kSigned ? 0xCB008000CB008000ull : 0xCB000000CB000000ull;
+    const uint32_t hi = w >> 16;
+    uint64_t f0, f1, f2, f3;
+    asm("{.reg .b32 a, b;\n\t"
+        "lop3.b32 a, %1, 0x0000000F, 0x4B000000, 0xEA;\n\t"
+        "lop3.b32 b, %2, 0x0000000F, 0x4B000000, 0xEA;\n\t"
+        "mov.b64 %0, {a, b};}" : "=l"(f0) : "r"(w), "r"(hi));
+    asm("{.reg .b32 a, b;\n\t"
+        "lop3.b32 a, %1, 0x000000F0, 0x4B000000, 0xEA;\n\t"
+        "lop3.b32 b, %2, 0x000000F0, 0x4B000000, 0xEA;\n\t"
+        "mov.b64 %0, {a, b};}" : "=l"(f1) : "r"(w), "r"(hi));
+    asm("{.reg .b32 a, b;\n\t"
+        "lop3.b32 a, %1, 0x00000F00, 0x4B000000, 0xEA;\n\t"
+        "lop3.b32 b, %2, 0x00000F00, 0x4B000000, 0xEA;\n\t"
+        "mov.b64 %0, {a, b};}" : "=l"(f2) : "r"(w), "r"(hi));
+    asm("{.reg .b32 a, b;\n\t"
+        "lop3.b32 a, %1, 0x0000F000, 0x4B000000, 0xEA;\n\t"
+        "lop3.b32 b, %2, 0x0000F000, 0x4B000000, 0xEA;\n\t"
+        "mov.b64 %0, {a, b};}" : "=l"(f3) : "r"(w), "r"(hi));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d[0]) : "l"(f0), "l"(c0));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d[1]) : "l"(f1), "l"(c1));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d[2]) : "l"(f2), "l"(c2));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d[3]) : "l"(f3), "l"(c3));
+}
+
+// Two e4m3 codes (low 16 bits of `two`) -> f32 pair (exact; NaN codes -> NaN)
+__device__ __forceinline__ uint64_t decode_e4m3x2(uint32_t two) {
+    uint64_t r;
+    asm("{.reg .b16 lo, hi;\n\t"
+        ".reg .b32 h2;\n\t"
+        ".reg .f16 fl, fh;\n\t"
+        ".reg .f32 a, b;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h2, lo;\n\t"
+        "mov.b32 {fl, fh}, h2;\n\t"
+        "cvt.f32.f16 a, fl;\n\t"
+        "cvt.f32.f16 b, fh;\n\t"
+        "mov.b64 %0, {a, b};}" : "=l"(r) : "r"(two));
+    return r;
+}
+
+struct TmaLayout {
+    uint32_t stage_w;    // bytes per ring slot, weights
+    uint32_t stage_a;    // bytes per ring slot, side data
+    uint32_t red_off;    // offset of the partial-sum area
+    uint32_t bar_off;    // offset of the mbarriers
+    uint32_t total;      // dynamic shared memory bytes
+};
+
+template <class F, int S, int NW, int U, int RB>
+__global__ void __launch_bounds__(32 * (kTmaMaxConsumerWarps + 1))
+gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, int units_per_split,
+                int nrowb, int nst, TmaLayout L, int *err)
+{
+    constexpr int XU = NW * F::kElemsPerWord;
+    constexpr int NP = NW * F::kPairsPerWord;
+    constexpr int NV = NextPow2<RB * S>::value;
+    static_assert(RB * S <= 32, "RB * S must be <= 32");
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nc = (blockDim.x >> 5) - 1;
+    uint8_t *stage_w = smem;
+    uint8_t *stage_a = smem + (size_t)nst * L.stage_w;
+    float *red = reinterpret_cast<float *>(smem + L.red_off);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
+    uint64_t *empty = full + nst;
+
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], (uint32_t)nc);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    const int G = gridDim.x, b = blockIdx.x;
+    const int split = blockIdx.y, nsplit = gridDim.y;
+    const int n_my = b < nrowb ? (nrowb - b + G - 1) / G : 0;
+    const uint32_t rowbytes = F::row_bytes(p);
+    const uint32_t arowbytes = F::aux_row_bytes(p);
+    const int ubeg = split * units_per_split;
+    const int uend = min(units, ubeg + units_per_split);
+    // bytes of one row staged by this block (the whole row, or this split's segment)
+    const uint32_t seg_col = nsplit == 1 ? 0u : F::seg_byte(p, ubeg, XU);
+    const uint32_t seg_bytes = nsplit == 1 ? rowbytes : F::seg_byte(p, uend, XU) - seg_col;
+
+    if (warp == 0) {
+        // ------------------------------- producer -------------------------------
+        auto issue = [&](int k) {
+            const int slot = k % nst;
+            const int o0 = (b + k * G) * RB;
+            const int rows = min(RB, p.O - o0);
+            const uint32_t wb = (uint32_t)rows * seg_bytes, ab = (uint32_t)rows * arowbytes;
+            mbar_arrive_expect_tx(&full[slot], wb + ab);
+            uint8_t *dw = stage_w + (size_t)slot * L.stage_w;
+            if (nsplit == 1) {
+                bulk_copy_g2s(dw, F::w_src(p, o0, 0u), wb, &full[slot]);
+            } else {
+                for (int r = 0; r < rows; ++r)
+                    bulk_copy_g2s(dw + (size_t)r * seg_bytes, F::w_src(p, o0 + r, seg_col), seg_bytes, &full[slot]);
+            }
+            if (ab) bulk_copy_g2s(stage_a + (size_t)slot * L.stage_a, F::a_src(p, o0), ab, &full[slot]);
+        };
+        if (lane == 0)
+            for (int k = 0; k < min(nst, n_my); ++k) issue(k);
+        __syncwarp();
+        for (int k = 0; k < n_my; ++k) {
+            const int slot = k % nst;
+            if (!mbar_wait(&empty[slot], (uint32_t)(k / nst) & 1u)) {
+                if (lane == 0) {
+                    raise_device_error(err, kErrTimeout);
+                    for (int j = k; j < min(k + nst, n_my); ++j)
+                        (void)mbar_wait(&full[j % nst], (uint32_t)(j / nst) & 1u);
+                }
+                return;
+            }
+            const int o0 = (b + k * G) * RB;
+            if (lane < RB * S) {
+                const int r = lane / S, s = lane - (lane / S) * S;
+                const float *rs = red + (size_t)slot * nc * NV + lane;
+                float acc = 0.f;
+                for (int w = 0; w < nc; ++w) acc += rs[(size_t)w * NV];
+                if (o0 + r < p.O) out[((size_t)split * S + s) * p.O + o0 + r] = acc;
+            }
+            __syncwarp();
+            if (lane == 0 && k + nst < n_my) issue(k + nst);
+        }
+        return;
+    }
+
+    // ------------------------------- consumers ----------------------------------
+    const int cw = warp - 1;
+    const int ct = tid - 32;
+    const int ncth = nc * 32;
+    int uidx[U];
+    bool uok[U];
+    typename F::TConst tc[U];
+    uint64_t xp[U][S][NP];
+    float xsum[U][S];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+        uidx[j] = ubeg + ct + j * ncth;
+        uok[j] = uidx[j] < uend;
+        tc[j] = F::tconst(p, uok[j] ? uidx[j] : ubeg, XU, seg_col);
+#pragma unroll
+        for (int s = 0; s < S; ++s) F::template load_x<XU, NP>(p, s, uok[j] ? uidx[j] : -1, xp[j][s], xsum[j][s]);
+    }
+    typename F::StageConst scur[U], snext[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) scur[j] = F::stage_const(p, b * RB, tc[j]);
+
+    for (int k = 0; k < n_my; ++k) {
+        const int slot = k % nst;
+        const int o0 = (b + k * G) * RB;
+#pragma unroll
+        for (int j = 0; j < U; ++j) snext[j] = F::stage_const(p, (b + (k + 1) * G) * RB, tc[j]);
+        if (!mbar_wait(&full[slot], (uint32_t)(k / nst) & 1u)) {
+            if (lane == 0) raise_device_error(err, kErrTimeout);
+            return;
+        }
+        const int rows = min(RB, p.O - o0);
+        const uint8_t *sw = stage_w + (size_t)slot * L.stage_w;
+        const uint8_t *sa = stage_a + (size_t)slot * L.stage_a;
+        float part[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) part[v] = 0.f;
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            if (r < rows) {
+#pragma unroll
+                for (int j = 0; j < U; ++j) {
+                    if (uok[j]) {
+                        const uint8_t *row_w = sw + (size_t)r * seg_bytes;
+                        const Words<NW> wd = lds_words<NW>(row_w + tc[j].uoff);
+                        const auto ax = F::aux(row_w, sa + (size_t)r * arowbytes, tc[j], scur[j]);
+                        F::template accumulate<S, NW, NP>(wd, ax, xp[j], xsum[j], &part[r * S]);
+                    }
+                }
+            }
+        }
+        const float tot = warp_reduce_scatter<NV>(part, lane);
+        if ((lane & ((32 / NV) - 1)) == 0)
+            red[((size_t)slot * nc + cw) * NV + reduce_scatter_index<NV>(lane)] = tot;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+#pragma unroll
+        for (int j = 0; j < U; ++j) scur[j] = snext[j];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: plan and launch
+// ---------------------------------------------------------------------------
+struct TmaPlan {
+    int units;            // units per row
+    int U;                // units per consumer thread
+    int nc;               // consumer warps
+    int splits;           // column splits (grid.y)
+    int units_per_split;
+    int nrowb;            // row batches
+    int nst;              // ring slots
+    TmaLayout L;
+};
+
+// Row geometry handed to the planner by a format.
+struct TmaGeom {
+    int units;                // units per row
+    int granule;              // a column split covers a multiple of this many units
+    uint32_t rowbytes;        // staged bytes of a whole row
+    uint32_t granule_bytes;   // staged bytes of one granule
+    uint32_t arowbytes;       // staged side-data bytes per row
+};
+
+bool tma_plan(const TmaGeom &g, int O, int RB, int NV, int U_max, TmaPlan *pl);
+
+// Device address of this device's error word (cached per device).
+int *device_error_word();
+
+// Launch gemv_tma_kernel<F, S, NW, U, RB> with plan `pl`.
+template <class F, int S, int NW, int U, int RB>
+void launch_tma(const typename F::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+    auto kern = gemv_tma_kernel<F, S, NW, U, RB>;
+    static int attr_set_mask = 0;   // one bit per device ordinal (< 31)
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 31 && !(__atomic_load_n(&attr_set_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+        __atomic_fetch_or(&attr_set_mask, 1 << dev, __ATOMIC_ACQ_REL);
+    }
+    const int threads = 32 * (pl.nc + 1);
+    int per_sm = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, pl.L.total) != cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+    }
+    long resident = (long)num_sms() * per_sm / pl.splits;
+    if (resident < 1) resident = 1;
+    const int grid_x = pl.nrowb < resident ? pl.nrowb : (int)resident;
+    dim3 grid(grid_x, pl.splits);
+    kern<<<grid, threads, pl.L.total, st>>>(p, out, pl.units, pl.units_per_split, pl.nrowb, pl.nst, pl.L,
+                                            device_error_word());
+}
+
+}  // namespace qg

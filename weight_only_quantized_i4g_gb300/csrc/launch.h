@@ -17,6 +17,9 @@ void set_error_detail(const char *fmt, ...);
 // Reports launch errors of the kernels just enqueued.
 int check_launch(const char *what);
 
+// Reads and clears this device's kernel error word (0 or a qg status).
+int read_device_error(int *status);
+
 size_t ws_i4g(int S, int I, int O, int gs);
 size_t ws_fp8b128(int S, int I, int O);
 size_t ws_mq4v2(int S, int I, int O);
