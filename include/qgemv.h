@@ -13,8 +13,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - All data pointers are DEVICE pointers owned by the caller.  The library
- *   allocates no device memory, keeps no global device state and never frees
- *   anything.  The only host-side state is a per-device cache of the SM count.
+ *   allocates no device memory and never frees anything.  Its only state is
+ *   one 4-byte error word per device (see qg_device_status) and host-side
+ *   per-device caches (SM count, that word's address, kernel attributes).
  * - Calls are asynchronous on `stream` (0 = legacy default stream).  No call
  *   synchronises the host.  Outputs are fully overwritten, never accumulated.
  * - Activations x are row-major [S, I]; outputs y are row-major f32 [S, O]
@@ -55,7 +56,8 @@ typedef enum {
     QG_ESHAPE = -3,      /* MQ4-V2 with I % 256 != 0                         */
     QG_EALIGN = -4,      /* pointer misaligned for its element type          */
     QG_EWORKSPACE = -5,  /* workspace NULL or smaller than required          */
-    QG_ECUDA = -6        /* CUDA runtime error (no device, launch failure)   */
+    QG_ECUDA = -6,       /* CUDA runtime error (no device, launch failure)   */
+    QG_ETIMEOUT = -7     /* a kernel gave up waiting (see qg_device_status)  */
 } qg_status;
 
 /* Static name of a status code ("QG_EGS: ..."). Never NULL. */
@@ -65,6 +67,15 @@ const char *qg_strerror(int status);
  * (which argument, which condition, or the CUDA error string).  The pointer
  * stays valid until the next call on the same thread. */
 const char *qg_last_error(void);
+
+/* Kernel-side status of the current device.  Kernels that stage weights
+ * through shared memory wait on hardware barriers; every such wait is bounded
+ * and, if it ever gives up (which no valid call does), the kernel stops early
+ * and records QG_ETIMEOUT in a per-device error word instead of hanging the
+ * GPU.  This call synchronizes the device, stores that word (QG_OK when
+ * clean) in *status and clears it.  Returns QG_OK, QG_EINVAL for a NULL
+ * status, or QG_ECUDA. */
+int qg_device_status(int *status);
 
 /* Format ids for qg_workspace_bytes. */
 enum { QG_FMT_I4G = 4, QG_FMT_FP8B128 = 7, QG_FMT_MQ4V2 = 44 };

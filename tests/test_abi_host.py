@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_lists_the_entry_points():
     names = declared_functions()
-    for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qg_workspace_bytes",
+    for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qg_workspace_bytes", "qg_device_status",
                  "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256"]:
         assert must in names, names
 
@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(qg):
 
 
 def test_strerror(qg):
-    for code in range(0, -7, -1):
+    for code in range(0, -8, -1):
         assert qg.strerror(code).startswith("QG_")
     assert "unknown" in qg.strerror(-99)
 

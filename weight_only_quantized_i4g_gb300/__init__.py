@@ -23,7 +23,8 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-QG_OK, QG_EINVAL, QG_EGS, QG_ESHAPE, QG_EALIGN, QG_EWORKSPACE, QG_ECUDA = 0, -1, -2, -3, -4, -5, -6
+QG_OK, QG_EINVAL, QG_EGS, QG_ESHAPE, QG_EALIGN, QG_EWORKSPACE, QG_ECUDA, QG_ETIMEOUT = (
+    0, -1, -2, -3, -4, -5, -6, -7)
 QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_MQ4V2 = 4, 7, 44
 
 _P = ctypes.c_void_p
@@ -34,6 +35,7 @@ _SIGNATURES = {
     "qg_strerror": ([_I], ctypes.c_char_p),
     "qg_last_error": ([], ctypes.c_char_p),
     "qg_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
+    "qg_device_status": ([ctypes.POINTER(_I)], _I),
     "qgemv_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_fp8b128": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_mq4v2": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
@@ -89,6 +91,13 @@ def last_error() -> str:
 def check(rc: int) -> None:
     if rc != QG_OK:
         raise QGError(rc)
+
+
+def qg_device_status() -> tuple[int, int]:
+    """(return code, device status) of the current device; clears the status."""
+    st = _I(0)
+    rc = _lib.qg_device_status(ctypes.byref(st))
+    return rc, st.value
 
 
 def qg_workspace_bytes(fmt: int, S: int, I: int, O: int, gs: int = 0) -> int:

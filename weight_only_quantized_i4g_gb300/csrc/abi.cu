@@ -56,11 +56,22 @@ const char *qg_strerror(int status) {
         case QG_EALIGN: return "QG_EALIGN: pointer misaligned for its element type";
         case QG_EWORKSPACE: return "QG_EWORKSPACE: workspace missing or smaller than qg_workspace_bytes()";
         case QG_ECUDA: return "QG_ECUDA: CUDA runtime error";
+        case QG_ETIMEOUT: return "QG_ETIMEOUT: a kernel gave up waiting on a barrier";
         default: return "unknown qg_status";
     }
 }
 
 const char *qg_last_error(void) { return error_detail(); }
+
+int qg_device_status(int *status) {
+    if (!status) QG_REFUSE(kEInval, "qg_device_status: status must be non-NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        set_error_detail("qg_device_status: %s", cudaGetErrorString(e));
+        return kECuda;
+    }
+    return read_device_error(status);
+}
 
 size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs) {
     if (S < 1 || I < 1 || O < 1) return 0;

@@ -180,6 +180,7 @@ bool tma_plan(const TmaGeom &g, int O, int RB, int NV, int U_max, TmaPlan *pl) {
         if (nst >= 2) break;
     }
     if (nst < 2) return false;
+    pl->rb = RB;
     pl->units = g.units;
     pl->U = U;
     pl->nc = nc;

@@ -10,7 +10,11 @@
 // convert to NaN), then f16 -> f32 (exact).  A unit (4*NW codes, NW <= 4)
 // lies inside one 128-column block, so the block scale multiplies the unit's
 // partial sum.
+//
+// Paths, fastest first: staged (gemv_tma.cuh; 16-byte aligned w and x,
+// I % 16 == 0), direct (gemv_cs.cuh; 16- or 8-byte global loads), general.
 #include "gemv_cs.cuh"
+#include "gemv_tma.cuh"
 #include "launch.h"
 
 namespace qg {
@@ -26,6 +30,7 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
 
 struct FmtFp8B128 {
     static constexpr int kElemsPerWord = 4;
+    static constexpr int kPairsPerWord = 2;
     struct Params {
         const uint16_t *x;
         const uint8_t *w;
@@ -71,6 +76,60 @@ struct FmtFp8B128 {
             for (int i = 0; i < NW * 2; ++i)
                 acc = __ffma2_rn(d[i], make_float2(xs[s][2 * i], xs[s][2 * i + 1]), acc);
             part[s] = fmaf(sc, acc.x + acc.y, part[s]);
+        }
+    }
+
+    // ---- staged (TMA) kernel -------------------------------------------------
+    struct TConst { uint32_t uoff; int ib; };   // unit byte offset, 128-column block
+    struct StageConst { float sc; };            // the batch's block scale for that column block
+
+    __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.I; }
+    __device__ static uint32_t aux_row_bytes(const Params &) { return 0u; }
+    __device__ static uint32_t seg_byte(const Params &, int u, int XU) { return (uint32_t)(u * XU); }
+    __device__ static const void *w_src(const Params &p, int o, uint32_t col) {
+        return p.w + (size_t)o * p.I + col;
+    }
+    __device__ static const void *a_src(const Params &, int) { return nullptr; }
+    __device__ static TConst tconst(const Params &, int u, int XU, uint32_t seg_col) {
+        return TConst{(uint32_t)(u * XU) - seg_col, (u * XU) >> 7};
+    }
+    // rows of a batch share one 128-row block (the batch size divides 128)
+    __device__ static StageConst stage_const(const Params &p, int o0, TConst tc) {
+        return StageConst{o0 < p.O ? ld_nc_f32(p.scale_inv + (size_t)(o0 >> 7) * p.nbi + tc.ib) : 0.f};
+    }
+    __device__ static float aux(const uint8_t *, const uint8_t *, TConst, StageConst sc) { return sc.sc; }
+
+    // xp[i] = {x[2i], x[2i+1]} of the unit, widened from bf16 (16-byte vector loads)
+    template <int XU, int NP>
+    __device__ static void load_x(const Params &p, int s, int u, uint64_t (&xp)[NP], float &xsum) {
+        xsum = 0.f;
+#pragma unroll
+        for (int v = 0; v < XU / 8; ++v) {
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (u >= 0) q = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)s * p.I + (size_t)u * XU) + v);
+            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                xp[4 * v + i] = pack2(__uint_as_float(wv[i] << 16), __uint_as_float(wv[i] & 0xFFFF0000u));
+        }
+    }
+
+    template <int S, int NW, int NP>
+    __device__ static void accumulate(const Words<NW> &wd, float sc, const uint64_t (&xp)[S][NP],
+                                      const float (&)[S], float *part) {
+        uint64_t d[NW * 2];
+#pragma unroll
+        for (int wq = 0; wq < NW; ++wq) {
+            d[2 * wq] = decode_e4m3x2(wd.w[wq]);
+            d[2 * wq + 1] = decode_e4m3x2(wd.w[wq] >> 16);
+        }
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            uint64_t acc = 0ull;
+#pragma unroll
+            for (int i = 0; i < NW * 2; ++i) ffma2(acc, d[i], xp[s][i]);
+            const float2 a = unpack2(acc);
+            part[s] = fmaf(sc, a.x + a.y, part[s]);
         }
     }
 };
@@ -121,6 +180,24 @@ bool fp8_fast_ok(const uint16_t *x, const uint8_t *w, int I, int S) {
     return (I % (4 * nw) == 0) && ((uintptr_t)w % (4 * nw) == 0) && ((uintptr_t)x % 2 == 0);
 }
 
+
+bool fp8_tma_ok(const uint16_t *x, const uint8_t *w, int I, int S) {
+    return fp8_fast_ok(x, w, I, S) && (I % 16 == 0) && ((uintptr_t)w % 16 == 0) && ((uintptr_t)x % 16 == 0);
+}
+
+bool fp8_tma_plan(int S, int I, int O, TmaPlan *pl) {
+    const int nw = fp8_nw(S);
+    TmaGeom g;
+    g.units = I / (4 * nw);
+    g.granule = 4 / nw;                          // 16 bytes of weights
+    g.rowbytes = (uint32_t)I;
+    g.granule_bytes = 16;
+    g.arowbytes = 0;
+    const int umax = S == 1 ? 3 : 1;
+    if (S <= 2 && tma_plan(g, O, 8, next_pow2(8 * S), umax, pl)) return true;
+    return tma_plan(g, O, 4, next_pow2(4 * S), umax, pl);     // rows too long for 8-row slots
+}
+
 CsPlan fp8_plan(int S, int I, int O, int *U_out) {
     const int nw = fp8_nw(S);
     const int units = I / (4 * nw);
@@ -158,8 +235,56 @@ void launch_cs_fp8_s(const FmtFp8B128::Params &p, float *out, const CsPlan &pl, 
     launch_cs_fp8<S, NW, 1>(p, out, pl, units, st);
 }
 
+template <int S, int RB>
+void launch_tma_fp8_u(const FmtFp8B128::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+    constexpr int NW = S <= 4 ? 4 : 2;
+    if constexpr (S == 1) {
+        if (pl.U == 2) {
+            launch_tma<FmtFp8B128, S, NW, 2, RB>(p, out, pl, st);
+            return;
+        }
+        if (pl.U == 3) {
+            launch_tma<FmtFp8B128, S, NW, 3, RB>(p, out, pl, st);
+            return;
+        }
+    }
+    launch_tma<FmtFp8B128, S, NW, 1, RB>(p, out, pl, st);
+}
+
+template <int S>
+void launch_tma_fp8_s(const FmtFp8B128::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+    if constexpr (S <= 2) {
+        if (pl.rb == 8) {
+            launch_tma_fp8_u<S, 8>(p, out, pl, st);
+            return;
+        }
+    }
+    launch_tma_fp8_u<S, 4>(p, out, pl, st);
+}
+
 int gemv_fp8_chunk(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S, int I,
                    int O, void *ws, size_t ws_bytes, cudaStream_t st) {
+    FmtFp8B128::Params p;
+    p.x = x; p.w = w; p.scale_inv = scale_inv; p.I = I; p.O = O; p.nbi = (I + 127) / 128;
+
+    TmaPlan tp;
+    if (fp8_tma_ok(x, w, I, S) && fp8_tma_plan(S, I, O, &tp)) {
+        const size_t need = tp.splits > 1 ? (size_t)tp.splits * S * O * sizeof(float) : 0;
+        if (need > 0 && (ws == nullptr || ws_bytes < need)) {
+            set_error_detail("qgemv_fp8b128: this shape splits the reduction and needs %zu bytes of "
+                             "workspace (got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
+            return kEWorkspace;
+        }
+        float *out = tp.splits > 1 ? static_cast<float *>(ws) : y;
+        switch (S) {
+#define QG_CASE(SS) case SS: launch_tma_fp8_s<SS>(p, out, tp, st); break;
+            QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+        }
+        if (tp.splits > 1) launch_splitk_reduce(y, static_cast<float *>(ws), tp.splits, S, O, st);
+        return check_launch("qgemv_fp8b128");
+    }
+
     if (!fp8_fast_ok(x, w, I, S)) {
         const int blocks_needed = (O + 7) / 8;
         const int cap = num_sms() * 16;
@@ -180,8 +305,6 @@ int gemv_fp8_chunk(float *y, const uint16_t *x, const uint8_t *w, const float *s
                          "workspace (got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
         return kEWorkspace;
     }
-    FmtFp8B128::Params p;
-    p.x = x; p.w = w; p.scale_inv = scale_inv; p.I = I; p.O = O; p.nbi = (I + 127) / 128;
     float *out = pl.splits > 1 ? static_cast<float *>(ws) : y;
     switch (S) {
 #define QG_CASE(SS) case SS: launch_cs_fp8_s<SS>(p, out, pl, units, U, st); break;
@@ -197,8 +320,13 @@ int gemv_fp8_chunk(float *y, const uint16_t *x, const uint8_t *w, const float *s
 size_t ws_fp8b128(int S, int I, int O) {
     const int s = S < 8 ? S : 8;
     if (I % (4 * fp8_nw(s)) != 0) return 0;
+    // the larger of the staged and the direct plan (the pointers decide the path)
+    size_t need = 0;
+    TmaPlan tp;
+    if (I % 16 == 0 && fp8_tma_plan(s, I, O, &tp) && tp.splits > 1) need = (size_t)tp.splits * s * O * sizeof(float);
     int U = 1;
-    return cs_ws_bytes(fp8_plan(s, I, O, &U), s, O);
+    const size_t cs = cs_ws_bytes(fp8_plan(s, I, O, &U), s, O);
+    return need > cs ? need : cs;
 }
 
 int run_gemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S, int I,

@@ -198,7 +198,6 @@ namespace {
 // words per unit for S tokens: keep the activation registers (8*NW*S) <= 64
 int i4g_nw(int S) { return S <= 2 ? 4 : S <= 4 ? 2 : 1; }
 int i4g_rb(int S, int U) { return S <= 2 ? (U == 1 ? 8 : 4) : 4; }
-constexpr int kTmaRb(int S) { return S <= 2 ? 8 : 4; }
 
 bool i4g_fast_ok(const float *x, const uint8_t *w, int I, int gs, int S) {
     const int nw = i4g_nw(S);
@@ -221,8 +220,9 @@ bool i4g_tma_plan(int S, int I, int O, int gs, TmaPlan *pl) {
     g.rowbytes = (uint32_t)(I / 2);
     g.granule_bytes = 16;
     g.arowbytes = (uint32_t)((I + gs - 1) / gs) * 4u;
-    const int rb = kTmaRb(S);
-    return tma_plan(g, O, rb, next_pow2(rb * S), S == 1 ? 2 : 1, pl);
+    const int umax = S == 1 ? 2 : 1;
+    if (S <= 2 && tma_plan(g, O, 8, next_pow2(8 * S), umax, pl)) return true;
+    return tma_plan(g, O, 4, next_pow2(4 * S), umax, pl);     // rows too long for 8-row slots
 }
 
 CsPlan i4g_plan(int S, int I, int O, int *U_out) {
@@ -257,10 +257,9 @@ void launch_cs_i4g_s(const FmtI4G::Params &p, float *out, const CsPlan &pl, int 
     launch_cs_i4g<S, NW, 1>(p, out, pl, units, st);
 }
 
-template <int S>
-void launch_tma_i4g_s(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+template <int S, int RB>
+void launch_tma_i4g_u(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
     constexpr int NW = S <= 2 ? 4 : S <= 4 ? 2 : 1;
-    constexpr int RB = kTmaRb(S);
     if constexpr (S == 1) {
         if (pl.U == 2) {
             launch_tma<FmtI4G, S, NW, 2, RB>(p, out, pl, st);
@@ -268,6 +267,17 @@ void launch_tma_i4g_s(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cu
         }
     }
     launch_tma<FmtI4G, S, NW, 1, RB>(p, out, pl, st);
+}
+
+template <int S>
+void launch_tma_i4g_s(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+    if constexpr (S <= 2) {
+        if (pl.rb == 8) {
+            launch_tma_i4g_u<S, 8>(p, out, pl, st);
+            return;
+        }
+    }
+    launch_tma_i4g_u<S, 4>(p, out, pl, st);
 }
 
 int gemv_i4g_chunk(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,

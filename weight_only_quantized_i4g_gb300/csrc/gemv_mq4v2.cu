@@ -12,13 +12,18 @@
 // folded as scale * sum(q*x) + zero * sum(x); the activations' sum over the
 // unit is computed once per thread.  Nibble decode as for fmt=4 (the float
 // 2^23 + q*16^p minus 2^23).
+//
+// Paths: staged (gemv_tma.cuh) when the rows are a whole number of 16-byte
+// lines (I/256 even) and blocks and x are 16-byte aligned; direct otherwise.
 #include "gemv_cs.cuh"
+#include "gemv_tma.cuh"
 #include "launch.h"
 
 namespace qg {
 
 struct FmtMq4v2 {
     static constexpr int kElemsPerWord = 8;
+    static constexpr int kPairsPerWord = 4;
     struct Params {
         const uint16_t *x;
         const uint8_t *blocks;
@@ -92,6 +97,75 @@ struct FmtMq4v2 {
             part[s] = fmaf(scale, acc.x + acc.y, fmaf(zero, xsum[s], part[s]));
         }
     }
+
+    // ---- staged (TMA) kernel -------------------------------------------------
+    struct TConst { uint32_t uoff; uint32_t hoff; };   // unit and header byte offsets in the segment
+    struct StageConst {};
+
+    __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.rowbytes; }
+    __device__ static uint32_t aux_row_bytes(const Params &) { return 0u; }
+    // a segment starts at a block boundary (splits cover whole blocks)
+    __device__ static uint32_t seg_byte(const Params &, int u, int XU) {
+        return 136u * (uint32_t)(u / (128 / (XU / 2)));
+    }
+    __device__ static const void *w_src(const Params &p, int o, uint32_t col) {
+        return p.blocks + (size_t)o * p.rowbytes + col;
+    }
+    __device__ static const void *a_src(const Params &, int) { return nullptr; }
+    __device__ static TConst tconst(const Params &p, int u, int XU, uint32_t seg_col) {
+        const ThreadConst t = thread_const(p, u, XU);
+        return TConst{(uint32_t)t.uoff - seg_col, (uint32_t)t.hoff - seg_col};
+    }
+    __device__ static StageConst stage_const(const Params &, int, TConst) { return StageConst{}; }
+    __device__ static uint32_t aux(const uint8_t *row_w, const uint8_t *, TConst tc, StageConst) {
+        return lds_u32(row_w + tc.hoff);
+    }
+
+    // xp[4*wq + q] = {x[8wq + q], x[8wq + q + 4]} * 16^-q, xsum = sum of the
+    // unit's activations (16-byte vector loads of bf16)
+    template <int XU, int NP>
+    __device__ static void load_x(const Params &p, int s, int u, uint64_t (&xp)[NP], float &xsum) {
+        float sum = 0.f;
+#pragma unroll
+        for (int wq = 0; wq < XU / 8; ++wq) {
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (u >= 0) q = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)s * p.I + (size_t)u * XU) + wq);
+            float e[8];
+            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                e[2 * i] = __uint_as_float(wv[i] << 16);
+                e[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sum += e[i];
+            xp[4 * wq + 0] = pack2(e[0], e[4]);
+            xp[4 * wq + 1] = pack2(e[1] * 0.0625f, e[5] * 0.0625f);
+            xp[4 * wq + 2] = pack2(e[2] * 0.00390625f, e[6] * 0.00390625f);
+            xp[4 * wq + 3] = pack2(e[3] * 0.000244140625f, e[7] * 0.000244140625f);
+        }
+        xsum = sum;
+    }
+
+    template <int S, int NW, int NP>
+    __device__ static void accumulate(const Words<NW> &wd, uint32_t hd, const uint64_t (&xp)[S][NP],
+                                      const float (&xsum)[S], float *part) {
+        uint64_t d[NW][4];
+#pragma unroll
+        for (int wq = 0; wq < NW; ++wq) decode_nibbles<false>(wd.w[wq], d[wq]);
+        const float scale = f16_bits_to_f32((uint16_t)(hd & 0xFFFFu));
+        const float zero = f16_bits_to_f32((uint16_t)(hd >> 16));
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            uint64_t acc = 0ull;
+#pragma unroll
+            for (int wq = 0; wq < NW; ++wq)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) ffma2(acc, d[wq][q], xp[s][4 * wq + q]);
+            const float2 a = unpack2(acc);
+            part[s] = fmaf(scale, a.x + a.y, fmaf(zero, xsum[s], part[s]));
+        }
+    }
 };
 
 // ---------------------------------------------------------------------------
@@ -101,6 +175,25 @@ namespace {
 
 int mq4_nw(int S) { return S <= 4 ? 2 : 1; }      // activation registers 8*NW*S <= 64
 int mq4_rb(int S, int U) { return S <= 2 ? (U == 1 ? 8 : 4) : 4; }
+
+
+bool mq4_tma_ok(const uint16_t *x, const uint8_t *blocks, int I) {
+    return ((I / 256) % 2 == 0) && ((uintptr_t)blocks % 16 == 0) && ((uintptr_t)x % 16 == 0);
+}
+
+bool mq4_tma_plan(int S, int I, int O, TmaPlan *pl) {
+    const int nw = mq4_nw(S);
+    const int upb = 128 / (4 * nw);              // units per 256-weight block
+    TmaGeom g;
+    g.units = I / (8 * nw);
+    g.granule = 2 * upb;                         // two blocks = 272 bytes = 17 lines of 16
+    g.rowbytes = (uint32_t)((I / 256) * 136);
+    g.granule_bytes = 272;
+    g.arowbytes = 0;
+    const int umax = S == 1 ? 3 : 1;
+    if (S <= 2 && tma_plan(g, O, 8, next_pow2(8 * S), umax, pl)) return true;
+    return tma_plan(g, O, 4, next_pow2(4 * S), umax, pl);     // rows too long for 8-row slots
+}
 
 CsPlan mq4_plan(int S, int I, int O, int *U_out) {
     const int nw = mq4_nw(S);
@@ -139,8 +232,56 @@ void launch_cs_mq4_s(const FmtMq4v2::Params &p, float *out, const CsPlan &pl, in
     launch_cs_mq4<S, NW, 1>(p, out, pl, units, st);
 }
 
+template <int S, int RB>
+void launch_tma_mq4_u(const FmtMq4v2::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+    constexpr int NW = S <= 4 ? 2 : 1;
+    if constexpr (S == 1) {
+        if (pl.U == 2) {
+            launch_tma<FmtMq4v2, S, NW, 2, RB>(p, out, pl, st);
+            return;
+        }
+        if (pl.U == 3) {
+            launch_tma<FmtMq4v2, S, NW, 3, RB>(p, out, pl, st);
+            return;
+        }
+    }
+    launch_tma<FmtMq4v2, S, NW, 1, RB>(p, out, pl, st);
+}
+
+template <int S>
+void launch_tma_mq4_s(const FmtMq4v2::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+    if constexpr (S <= 2) {
+        if (pl.rb == 8) {
+            launch_tma_mq4_u<S, 8>(p, out, pl, st);
+            return;
+        }
+    }
+    launch_tma_mq4_u<S, 4>(p, out, pl, st);
+}
+
 int gemv_mq4_chunk(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
                    size_t ws_bytes, cudaStream_t st) {
+    FmtMq4v2::Params p;
+    p.x = x; p.blocks = blocks; p.I = I; p.O = O; p.rowbytes = (size_t)(I / 256) * 136;
+
+    TmaPlan tp;
+    if (mq4_tma_ok(x, blocks, I) && mq4_tma_plan(S, I, O, &tp)) {
+        const size_t need = tp.splits > 1 ? (size_t)tp.splits * S * O * sizeof(float) : 0;
+        if (need > 0 && (ws == nullptr || ws_bytes < need)) {
+            set_error_detail("qgemv_mq4v2: this shape splits the reduction and needs %zu bytes of workspace "
+                             "(got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
+            return kEWorkspace;
+        }
+        float *out = tp.splits > 1 ? static_cast<float *>(ws) : y;
+        switch (S) {
+#define QG_CASE(SS) case SS: launch_tma_mq4_s<SS>(p, out, tp, st); break;
+            QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+        }
+        if (tp.splits > 1) launch_splitk_reduce(y, static_cast<float *>(ws), tp.splits, S, O, st);
+        return check_launch("qgemv_mq4v2");
+    }
+
     // the ABI guarantees 8-byte aligned blocks and 2-byte aligned x, which is
     // all the fast path needs, so MQ4-V2 has no general fallback kernel
     int U = 1;
@@ -152,8 +293,6 @@ int gemv_mq4_chunk(float *y, const uint16_t *x, const uint8_t *blocks, int S, in
                          "(got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
         return kEWorkspace;
     }
-    FmtMq4v2::Params p;
-    p.x = x; p.blocks = blocks; p.I = I; p.O = O; p.rowbytes = (size_t)(I / 256) * 136;
     float *out = pl.splits > 1 ? static_cast<float *>(ws) : y;
     switch (S) {
 #define QG_CASE(SS) case SS: launch_cs_mq4_s<SS>(p, out, pl, units, U, st); break;
@@ -168,8 +307,14 @@ int gemv_mq4_chunk(float *y, const uint16_t *x, const uint8_t *blocks, int S, in
 
 size_t ws_mq4v2(int S, int I, int O) {
     const int s = S < 8 ? S : 8;
+    // the larger of the staged and the direct plan (the pointers decide the path)
+    size_t need = 0;
+    TmaPlan tp;
+    if ((I / 256) % 2 == 0 && mq4_tma_plan(s, I, O, &tp) && tp.splits > 1)
+        need = (size_t)tp.splits * s * O * sizeof(float);
     int U = 1;
-    return cs_ws_bytes(mq4_plan(s, I, O, &U), s, O);
+    const size_t cs = cs_ws_bytes(mq4_plan(s, I, O, &U), s, O);
+    return need > cs ? need : cs;
 }
 
 int run_gemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,

@@ -38,7 +38,9 @@
 
 namespace qg {
 
-constexpr int kTmaMaxConsumerWarps = 16;
+// 15 consumer warps + the producer = 16 warps, four per SM sub-partition, which
+// leaves up to 128 registers per thread for a single resident block.
+constexpr int kTmaMaxConsumerWarps = 15;
 
 template <int NW>
 __device__ __forceinline__ Words<NW> lds_words(const uint8_t *p);
@@ -150,7 +152,7 @@ struct TmaLayout {
 };
 
 template <class F, int S, int NW, int U, int RB>
-__global__ void __launch_bounds__(32 * (kTmaMaxConsumerWarps + 1))
+__global__ void __launch_bounds__(32 * (kTmaMaxConsumerWarps + 1), 1)
 gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, int units_per_split,
                 int nrowb, int nst, TmaLayout L, int *err)
 {
@@ -296,6 +298,7 @@ gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, 
 // Host side: plan and launch
 // ---------------------------------------------------------------------------
 struct TmaPlan {
+    int rb;               // rows per batch
     int units;            // units per row
     int U;                // units per consumer thread
     int nc;               // consumer warps
