@@ -285,3 +285,12 @@ def test_mq4_equal_halves_constant(qg):
     y = run_mq4(qg, synth.bf16_bits(x), blocks, S, I, O)
     want = (3 * 0.125 - 0.5) * float(x.sum())
     assert np.all(y == want), (y, want)
+
+
+def test_device_status_clean_after_staged_calls(qg):
+    """No staged-kernel barrier wait gave up in any call above (or in this one)."""
+    O, I, S, gs = 2048, 7168, 1, 64
+    x, wq, sc = i4g_inputs(O, I, S, gs, tag=99)
+    run_i4g(qg, x, wq, sc, S, I, O, gs)
+    rc, status = qg.qg_device_status()
+    assert rc == qg.QG_OK and status == qg.QG_OK, (rc, status, qg.last_error())
