@@ -107,6 +107,24 @@ size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs);
 int qgemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales,
               int S, int I, int O, int gs, void *ws, size_t ws_bytes, qg_stream_t stream);
 
+/* qgemv_i4g for callers that cannot allocate device memory.  The pages have
+ * no counterpart: this is a library convenience.  Same arguments, layout,
+ * results and errors as qgemv_i4g, minus the workspace: a shape whose
+ * reduction is split across thread blocks takes its scratch from a fixed
+ * 4 MiB array inside the library instead of a caller buffer.  Meant for
+ * engines whose device memory is planned once at start-up by their own
+ * allocator, and for host code that must not call cudaMalloc on the decode
+ * path (it can wait for the whole device).  Shapes needing more than 4 MiB
+ * of scratch (qg_workspace_bytes(QG_FMT_I4G, ...) > 4 MiB) are refused with
+ * QG_EWORKSPACE.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call on a device shares the array and leaves its contents
+ * behind; calls whose kernels may run at the same time (different streams or
+ * host threads) race on it and must be ordered by the caller.  Allocates
+ * nothing; every GPU that loads the library holds the 4 MiB until exit. */
+int qgemv_i4g_noalloc(float *y, const float *x, const uint8_t *w, const float *scales,
+                      int S, int I, int O, int gs, qg_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* fmt=7 FP8-e4m3 with 128x128 block scales, decode GEMV                    */
 /* colibri PR #528, section "Design".                                       */

@@ -66,6 +66,17 @@ def test_i4g_refusals(qg):
     assert qg.qgemv_i4g(P, P, P, P, 1, 512, 256, 64, ws=P + 16, stream=0) == qg.QG_EALIGN
 
 
+def test_i4g_noalloc_refusals(qg):
+    P = POISON
+    assert qg.qgemv_i4g_noalloc(P, P, P, P, 1, 512, 256, 3, stream=0) == qg.QG_EGS
+    assert qg.qgemv_i4g_noalloc(P, P, 0, P, 1, 512, 256, 64, stream=0) == qg.QG_EINVAL
+    assert qg.qgemv_i4g_noalloc(P + 2, P, P, P, 1, 512, 256, 64, stream=0) == qg.QG_EALIGN
+    # a shape whose split-reduction scratch exceeds the fixed 4 MiB
+    assert qg.qg_workspace_bytes(qg.QG_FMT_I4G, 8, 65536, 16384, 64) > (4 << 20)
+    assert qg.qgemv_i4g_noalloc(P, P, P, P, 8, 65536, 16384, 64, stream=0) == qg.QG_EWORKSPACE
+    assert "4194304" in qg.last_error()
+
+
 def test_fp8_refusals(qg):
     P = POISON
     assert qg.qgemv_fp8b128(P, P, P, P, 1, 0, 1, stream=0) == qg.QG_EINVAL

@@ -37,6 +37,7 @@ _SIGNATURES = {
     "qg_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
     "qg_device_status": ([ctypes.POINTER(_I)], _I),
     "qgemv_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemv_i4g_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "qgemv_fp8b128": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_mq4v2": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
@@ -107,6 +108,10 @@ def qg_workspace_bytes(fmt: int, S: int, I: int, O: int, gs: int = 0) -> int:
 def qgemv_i4g(y, x, w, scales, S, I, O, gs, ws=None, ws_bytes=0, stream=None) -> int:
     return _lib.qgemv_i4g(_ptr(y), _ptr(x), _ptr(w), _ptr(scales), S, I, O, gs, _ptr(ws), ws_bytes,
                           _stream(stream))
+
+
+def qgemv_i4g_noalloc(y, x, w, scales, S, I, O, gs, stream=None) -> int:
+    return _lib.qgemv_i4g_noalloc(_ptr(y), _ptr(x), _ptr(w), _ptr(scales), S, I, O, gs, _stream(stream))
 
 
 def qgemv_fp8b128(y, x, w, scale_inv, S, I, O, ws=None, ws_bytes=0, stream=None) -> int:
