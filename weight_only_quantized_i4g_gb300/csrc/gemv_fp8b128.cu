@@ -114,9 +114,14 @@ struct FmtFp8B128 {
         }
     }
 
+    __device__ static float zero_staged_aux() { return 0.f; }
+    struct ThreadScale {};
+    template <int U, int S, int NP>
+    __device__ static ThreadScale prepare_x(uint64_t (&)[U][S][NP], float (&)[U][S]) { return ThreadScale{}; }
+
     template <int S, int NW, int NP>
     __device__ static void accumulate(const Words<NW> &wd, float sc, const uint64_t (&xp)[S][NP],
-                                      const float (&)[S], float *part) {
+                                      const float (&)[S], ThreadScale, float *part) {
         uint64_t d[NW * 2];
 #pragma unroll
         for (int wq = 0; wq < NW; ++wq) {

@@ -119,40 +119,99 @@ struct FmtI4G {
         return lds_f32(row_a + tc.goff);
     }
 
-    // xp[4*wq + q] = {x[8wq + q], x[8wq + q + 4]} * 16^-q  (16-byte vector loads)
+    __device__ static float zero_staged_aux() { return 0.f; }
+
+    // Activation pairs in the order nibbles_as_denormals produces weights:
+    // for a word pair (2i, 2i+1) of the unit, xp[8i+q] = {x[16i+q], x[16i+8+q]}
+    // and xp[8i+4+q] = {x[16i+4+q], x[16i+12+q]}; for a single-word unit
+    // (NW = 1) xp[q] = {x[q], x[q+4]}.  Raw values here; prepare_x scales.
+    // xsum = the unit's activation sum (the -8 offset of the nibbles).
     template <int XU, int NP>
     __device__ static void load_x(const Params &p, int s, int u, uint64_t (&xp)[NP], float &xsum) {
-        xsum = 0.f;
+        float e[XU];
 #pragma unroll
-        for (int wq = 0; wq < XU / 8; ++wq) {
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-            if (u >= 0) {
-                const float4 *src = reinterpret_cast<const float4 *>(p.x + (size_t)s * p.I + (size_t)u * XU + 8 * wq);
-                a = __ldg(src);
-                b = __ldg(src + 1);
-            }
-            xp[4 * wq + 0] = pack2(a.x, b.x);
-            xp[4 * wq + 1] = pack2(a.y * 0.0625f, b.y * 0.0625f);
-            xp[4 * wq + 2] = pack2(a.z * 0.00390625f, b.z * 0.00390625f);
-            xp[4 * wq + 3] = pack2(a.w * 0.000244140625f, b.w * 0.000244140625f);
+        for (int v = 0; v < XU / 4; ++v) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (u >= 0) a = __ldg(reinterpret_cast<const float4 *>(p.x + (size_t)s * p.I + (size_t)u * XU) + v);
+            e[4 * v] = a.x; e[4 * v + 1] = a.y; e[4 * v + 2] = a.z; e[4 * v + 3] = a.w;
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < XU; ++k) sum += e[k];
+        xsum = sum;
+        if constexpr (XU == 8) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xp[q] = pack2(e[q], e[q + 4]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < XU / 16; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    xp[8 * i + q] = pack2(e[16 * i + q], e[16 * i + 8 + q]);
+                    xp[8 * i + 4 + q] = pack2(e[16 * i + 4 + q], e[16 * i + 12 + q]);
+                }
         }
     }
 
+    // Choose c with |x| < 2^(c-23) over the thread's activations, scale pair p
+    // by 2^(149 - 4*(p%4) - c) (finite for every finite x) and keep 2^c as two
+    // factors, each representable.
+    struct ThreadScale { float p1, p2; };
+    template <int U, int S, int NP>
+    __device__ static ThreadScale prepare_x(uint64_t (&xp)[U][S][NP], float (&)[U][S]) {
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const float2 v = unpack2(xp[j][s][i]);
+                    m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
+                }
+        const int c = exponent_bound(m) + 23;
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const float2 v = unpack2(xp[j][s][i]);
+                    const int k = 149 - 4 * (i % 4) - c;
+                    xp[j][s][i] = pack2(ldexpf(v.x, k), ldexpf(v.y, k));
+                }
+        return ThreadScale{ldexpf(1.f, c >> 1), ldexpf(1.f, c - (c >> 1))};
+    }
+
+    // sum (n - 8) * x over the unit = 2^c * sum(n * x * 2^-c) - 8 * xsum
     template <int S, int NW, int NP>
     __device__ static void accumulate(const Words<NW> &wd, float sc, const uint64_t (&xp)[S][NP],
-                                      const float (&)[S], float *part) {
-        uint64_t d[NW][4];
+                                      const float (&xsum)[S], ThreadScale ts, float *part) {
+        uint64_t d[NP];
+        if constexpr (NW == 1) {
+            const uint64_t ab = pack2(__uint_as_float(wd.w[0]), __uint_as_float(wd.w[0] >> 16));
 #pragma unroll
-        for (int wq = 0; wq < NW; ++wq) decode_nibbles<true>(wd.w[wq], d[wq]);
+            for (int q = 0; q < 4; ++q) d[q] = ab & ((uint64_t)(0xFu << (4 * q)) * 0x0000000100000001ull);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NW / 2; ++i) {
+                uint64_t di[8];
+                nibbles_as_denormals(((uint64_t)wd.w[2 * i + 1] << 32) | wd.w[2 * i], di);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) d[8 * i + k] = di[k];
+            }
+        }
 #pragma unroll
         for (int s = 0; s < S; ++s) {
-            uint64_t acc = 0ull;
+            uint64_t a0 = 0ull, a1 = 0ull;
 #pragma unroll
-            for (int wq = 0; wq < NW; ++wq)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) ffma2(acc, d[wq][q], xp[s][4 * wq + q]);
-            const float2 a = unpack2(acc);
-            part[s] = fmaf(sc, a.x + a.y, part[s]);
+            for (int i = 0; i < NP; i += 2) {
+                ffma2(a0, d[i], xp[s][i]);
+                if (i + 1 < NP) ffma2(a1, d[i + 1], xp[s][i + 1]);
+            }
+            const float2 u0 = unpack2(a0), u1 = unpack2(a1);
+            const float t = fmaf((u0.x + u0.y + (u1.x + u1.y)) * ts.p1, ts.p2, -8.f * xsum[s]);
+            part[s] = fmaf(sc, t, part[s]);
         }
     }
 };

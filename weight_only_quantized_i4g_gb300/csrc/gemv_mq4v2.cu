@@ -121,49 +121,99 @@ struct FmtMq4v2 {
         return lds_u32(row_w + tc.hoff);
     }
 
-    // xp[4*wq + q] = {x[8wq + q], x[8wq + q + 4]} * 16^-q, xsum = sum of the
-    // unit's activations (16-byte vector loads of bf16)
+    __device__ static uint32_t zero_staged_aux() { return 0u; }
+
+    // Activation pairs in the order nibbles_as_denormals produces weights
+    // (see FmtI4G::load_x), raw; xsum = the unit's activation sum.
     template <int XU, int NP>
     __device__ static void load_x(const Params &p, int s, int u, uint64_t (&xp)[NP], float &xsum) {
-        float sum = 0.f;
+        float e[XU];
 #pragma unroll
-        for (int wq = 0; wq < XU / 8; ++wq) {
+        for (int v = 0; v < XU / 8; ++v) {
             uint4 q = make_uint4(0u, 0u, 0u, 0u);
-            if (u >= 0) q = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)s * p.I + (size_t)u * XU) + wq);
-            float e[8];
+            if (u >= 0) q = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)s * p.I + (size_t)u * XU) + v);
             const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                e[2 * i] = __uint_as_float(wv[i] << 16);
-                e[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+                e[8 * v + 2 * i] = __uint_as_float(wv[i] << 16);
+                e[8 * v + 2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sum += e[i];
-            xp[4 * wq + 0] = pack2(e[0], e[4]);
-            xp[4 * wq + 1] = pack2(e[1] * 0.0625f, e[5] * 0.0625f);
-            xp[4 * wq + 2] = pack2(e[2] * 0.00390625f, e[6] * 0.00390625f);
-            xp[4 * wq + 3] = pack2(e[3] * 0.000244140625f, e[7] * 0.000244140625f);
         }
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < XU; ++k) sum += e[k];
         xsum = sum;
+        if constexpr (XU == 8) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xp[q] = pack2(e[q], e[q + 4]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < XU / 16; ++i)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    xp[8 * i + q] = pack2(e[16 * i + q], e[16 * i + 8 + q]);
+                    xp[8 * i + 4 + q] = pack2(e[16 * i + 4 + q], e[16 * i + 12 + q]);
+                }
+        }
     }
 
+    struct ThreadScale { float p1, p2; };
+    template <int U, int S, int NP>
+    __device__ static ThreadScale prepare_x(uint64_t (&xp)[U][S][NP], float (&)[U][S]) {
+        float m = 0.f;
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const float2 v = unpack2(xp[j][s][i]);
+                    m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
+                }
+        const int c = exponent_bound(m) + 23;
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const float2 v = unpack2(xp[j][s][i]);
+                    const int k = 149 - 4 * (i % 4) - c;
+                    xp[j][s][i] = pack2(ldexpf(v.x, k), ldexpf(v.y, k));
+                }
+        return ThreadScale{ldexpf(1.f, c >> 1), ldexpf(1.f, c - (c >> 1))};
+    }
+
+    // sum (q*scale + zero) * x = scale * 2^c * sum(q * x * 2^-c) + zero * xsum
     template <int S, int NW, int NP>
     __device__ static void accumulate(const Words<NW> &wd, uint32_t hd, const uint64_t (&xp)[S][NP],
-                                      const float (&xsum)[S], float *part) {
-        uint64_t d[NW][4];
+                                      const float (&xsum)[S], ThreadScale ts, float *part) {
+        uint64_t d[NP];
+        if constexpr (NW == 1) {
+            const uint64_t ab = pack2(__uint_as_float(wd.w[0]), __uint_as_float(wd.w[0] >> 16));
 #pragma unroll
-        for (int wq = 0; wq < NW; ++wq) decode_nibbles<false>(wd.w[wq], d[wq]);
-        const float scale = f16_bits_to_f32((uint16_t)(hd & 0xFFFFu));
+            for (int q = 0; q < 4; ++q) d[q] = ab & ((uint64_t)(0xFu << (4 * q)) * 0x0000000100000001ull);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NW / 2; ++i) {
+                uint64_t di[8];
+                nibbles_as_denormals(((uint64_t)wd.w[2 * i + 1] << 32) | wd.w[2 * i], di);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) d[8 * i + k] = di[k];
+            }
+        }
+        const float scale = f16_bits_to_f32((uint16_t)(hd & 0xFFFFu)) * ts.p1;
         const float zero = f16_bits_to_f32((uint16_t)(hd >> 16));
 #pragma unroll
         for (int s = 0; s < S; ++s) {
-            uint64_t acc = 0ull;
+            uint64_t a0 = 0ull, a1 = 0ull;
 #pragma unroll
-            for (int wq = 0; wq < NW; ++wq)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) ffma2(acc, d[wq][q], xp[s][4 * wq + q]);
-            const float2 a = unpack2(acc);
-            part[s] = fmaf(scale, a.x + a.y, fmaf(zero, xsum[s], part[s]));
+            for (int i = 0; i < NP; i += 2) {
+                ffma2(a0, d[i], xp[s][i]);
+                if (i + 1 < NP) ffma2(a1, d[i + 1], xp[s][i + 1]);
+            }
+            const float2 u0 = unpack2(a0), u1 = unpack2(a1);
+            part[s] = fmaf(scale, (u0.x + u0.y + (u1.x + u1.y)) * ts.p2, fmaf(zero, xsum[s], part[s]));
         }
     }
 };

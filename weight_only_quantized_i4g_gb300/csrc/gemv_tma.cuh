@@ -28,8 +28,10 @@
 //   tconst(p, u, XU, seg_col)        per-unit offsets inside the staged segment
 //   stage_const(p, o0, tc)           per-batch side data read from global
 //   aux(sw_row, sa_row, tc, sc)      per-(row, unit) side data
-//   load_x<XU, NP>(p, s, u, xp, xsum)
-//   accumulate<S, NW, NP>(words, aux, xp, xsum, part)
+//   load_x<XU, NP>(p, s, u, xp, xsum)  raw activations in decode order, their sum
+//   prepare_x<U, S, NP>(xp, xsum)     per-thread scaling of the activations -> ThreadScale
+//   zero_staged_aux()                 side data of an absent (row, unit): contributes 0
+//   accumulate<S, NW, NP>(words, aux, xp, xsum, ts, part)
 #pragma once
 
 #include "common.cuh"
@@ -125,6 +127,36 @@ __device__ __forceinline__ void decode_nibbles(uint32_t w, uint64_t (&d)[4]) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d[1]) : "l"(f1), "l"(c1));
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d[2]) : "l"(f2), "l"(c2));
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d[3]) : "l"(f3), "l"(c3));
+}
+
+// Nibbles read as denormal floats.  For a 32-bit pair {a, b} (two words of
+// packed nibbles in one 64-bit register pair), AND-ing with a nibble mask
+// leaves, in each half, the bit pattern n*16^q, which as a binary32 is the
+// denormal n*16^q*2^-149 exactly.  d[q] holds nibble q of a and of b,
+// d[4+q] nibble q+4 of a and of b (from the halves shifted down by 16).
+// Multiplying by an activation pre-scaled by 2^(149-4q-c) gives n*x*2^-c in
+// one fma with no subtraction; c is chosen per thread so every pre-scaled
+// activation is finite and every product of a nonzero nibble is normal.
+__device__ __forceinline__ void nibbles_as_denormals(uint64_t ab, uint64_t (&d)[8]) {
+    uint64_t hab;
+    asm("{.reg .b32 a, b, c, e;\n\t"
+        "mov.b64 {a, b}, %1;\n\t"
+        "shr.b32 c, a, 16;\n\t"
+        "shr.b32 e, b, 16;\n\t"
+        "mov.b64 %0, {c, e};}" : "=l"(hab) : "l"(ab));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint64_t m = (uint64_t)(0xFu << (4 * q)) * 0x0000000100000001ull;
+        d[q] = ab & m;
+        d[4 + q] = hab & m;
+    }
+}
+
+// Exponent e with |v| < 2^e for the largest |v| seen (v finite): the binary32
+// exponent field of the maximum, unbiased, plus one (denormals give -126).
+__device__ __forceinline__ int exponent_bound(float vmax_abs) {
+    const int field = (int)((__float_as_uint(vmax_abs) >> 23) & 0xFF);
+    return (field == 0 ? 1 : field) - 126;
 }
 
 // Two e4m3 codes (low 16 bits of `two`) -> f32 pair (exact; NaN codes -> NaN)
@@ -251,6 +283,7 @@ gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, 
 #pragma unroll
         for (int s = 0; s < S; ++s) F::template load_x<XU, NP>(p, s, uok[j] ? uidx[j] : -1, xp[j][s], xsum[j][s]);
     }
+    const typename F::ThreadScale ts = F::template prepare_x<U, S, NP>(xp, xsum);
     typename F::StageConst scur[U], snext[U];
 #pragma unroll
     for (int j = 0; j < U; ++j) scur[j] = F::stage_const(p, b * RB, tc[j]);
@@ -270,19 +303,36 @@ gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, 
         float part[NV];
 #pragma unroll
         for (int v = 0; v < NV; ++v) part[v] = 0.f;
+        // rows in sub-batches of RS: the sub-batch's shared-memory reads first,
+        // then its arithmetic (RS * U words stay live)
+        constexpr int RS = (S <= 2 ? 4 : 2) / U >= 1 ? (S <= 2 ? 4 : 2) / U : 1;
 #pragma unroll
-        for (int r = 0; r < RB; ++r) {
-            if (r < rows) {
+        for (int r0 = 0; r0 < RB; r0 += RS) {
+            Words<NW> wd[RS][U];
+            decltype(F::aux(sw, sa, tc[0], scur[0])) ax[RS][U];
+#pragma unroll
+            for (int rr = 0; rr < RS; ++rr) {
+                const int r = r0 + rr;
 #pragma unroll
                 for (int j = 0; j < U; ++j) {
-                    if (uok[j]) {
+                    if (r < RB && r < rows && uok[j]) {
                         const uint8_t *row_w = sw + (size_t)r * seg_bytes;
-                        const Words<NW> wd = lds_words<NW>(row_w + tc[j].uoff);
-                        const auto ax = F::aux(row_w, sa + (size_t)r * arowbytes, tc[j], scur[j]);
-                        F::template accumulate<S, NW, NP>(wd, ax, xp[j], xsum[j], &part[r * S]);
+                        wd[rr][j] = lds_words<NW>(row_w + tc[j].uoff);
+                        ax[rr][j] = F::aux(row_w, sa + (size_t)r * arowbytes, tc[j], scur[j]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < NW; ++k) wd[rr][j].w[k] = 0u;
+                        ax[rr][j] = F::zero_staged_aux();
                     }
                 }
             }
+#pragma unroll
+            for (int rr = 0; rr < RS; ++rr)
+                if (r0 + rr < RB)
+#pragma unroll
+                    for (int j = 0; j < U; ++j)
+                        F::template accumulate<S, NW, NP>(wd[rr][j], ax[rr][j], xp[j], xsum[j], ts,
+                                                          &part[(r0 + rr) * S]);
         }
         const float tot = warp_reduce_scatter<NV>(part, lane);
         if ((lane & ((32 / NV) - 1)) == 0)
