@@ -180,6 +180,7 @@ bool tma_plan(const TmaGeom &g, int O, int RB, int NV, int U_max, TmaPlan *pl) {
         if (nst >= 2) break;
     }
     if (nst < 2) return false;
+    pl->per_sm = target;
     pl->rb = RB;
     pl->units = g.units;
     pl->U = U;
@@ -194,6 +195,23 @@ bool tma_plan(const TmaGeom &g, int O, int RB, int NV, int U_max, TmaPlan *pl) {
     pl->L.bar_off = (uint32_t)round_up((int)(pl->L.red_off + nst * red_stage), 16);
     pl->L.total = pl->L.bar_off + 16u * (uint32_t)nst;
     return true;
+}
+
+bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl) {
+    const int cands[3] = {8, 4, 2};
+    bool have = false;
+    for (int i = 0; i < 3; ++i) {
+        const int rb = cands[i];
+        if (S > 2 && rb == 8) continue;
+        TmaPlan t;
+        if (!tma_plan(g, O, rb, next_pow2(rb * S), U_max, &t)) continue;
+        if (rb == 2 && t.U > 1) continue;
+        *pl = t;
+        have = true;
+        const long resident = (long)num_sms() * t.per_sm;
+        if ((long)t.nrowb * t.splits >= 3 * resident) return true;
+    }
+    return have;
 }
 
 // ---------------------------------------------------------------------------

@@ -97,7 +97,9 @@ struct FmtFp8B128 {
     __device__ static StageConst stage_const(const Params &p, int o0, TConst tc) {
         return StageConst{o0 < p.O ? ld_nc_f32(p.scale_inv + (size_t)(o0 >> 7) * p.nbi + tc.ib) : 0.f};
     }
-    __device__ static float aux(const uint8_t *, const uint8_t *, TConst, StageConst sc) { return sc.sc; }
+    template <int NW>
+    __device__ static Words<NW> lds_unit(uint32_t a) { return lds_at<NW, true>(a); }
+    __device__ static float aux(uint32_t, uint32_t, TConst, StageConst sc) { return sc.sc; }
 
     // xp[i] = {x[2i], x[2i+1]} of the unit, widened from bf16 (16-byte vector loads)
     template <int XU, int NP>
@@ -114,7 +116,6 @@ struct FmtFp8B128 {
         }
     }
 
-    __device__ static float zero_staged_aux() { return 0.f; }
     struct ThreadScale {};
     template <int U, int S, int NP>
     __device__ static ThreadScale prepare_x(uint64_t (&)[U][S][NP], float (&)[U][S]) { return ThreadScale{}; }
@@ -130,9 +131,9 @@ struct FmtFp8B128 {
         }
 #pragma unroll
         for (int s = 0; s < S; ++s) {
-            uint64_t acc = 0ull;
+            uint64_t acc = fmul2(d[0], xp[s][0]);
 #pragma unroll
-            for (int i = 0; i < NW * 2; ++i) ffma2(acc, d[i], xp[s][i]);
+            for (int i = 1; i < NW * 2; ++i) ffma2(acc, d[i], xp[s][i]);
             const float2 a = unpack2(acc);
             part[s] = fmaf(sc, a.x + a.y, part[s]);
         }
@@ -198,9 +199,7 @@ bool fp8_tma_plan(int S, int I, int O, TmaPlan *pl) {
     g.rowbytes = (uint32_t)I;
     g.granule_bytes = 16;
     g.arowbytes = 0;
-    const int umax = S == 1 ? 3 : 1;
-    if (S <= 2 && tma_plan(g, O, 8, next_pow2(8 * S), umax, pl)) return true;
-    return tma_plan(g, O, 4, next_pow2(4 * S), umax, pl);     // rows too long for 8-row slots
+    return tma_plan_rows(g, S, O, S == 1 ? 3 : 1, pl);
 }
 
 CsPlan fp8_plan(int S, int I, int O, int *U_out) {
@@ -263,6 +262,10 @@ void launch_tma_fp8_s(const FmtFp8B128::Params &p, float *out, const TmaPlan &pl
             launch_tma_fp8_u<S, 8>(p, out, pl, st);
             return;
         }
+    }
+    if (pl.rb == 2) {
+        launch_tma<FmtFp8B128, S, (S <= 4 ? 4 : 2), 1, 2>(p, out, pl, st);
+        return;
     }
     launch_tma_fp8_u<S, 4>(p, out, pl, st);
 }

@@ -115,11 +115,12 @@ struct FmtI4G {
         return TConst{(uint32_t)(u * (XU / 2)) - seg_col, 4u * (uint32_t)((u * XU) / p.gs)};
     }
     __device__ static StageConst stage_const(const Params &, int, TConst) { return StageConst{}; }
-    __device__ static float aux(const uint8_t *, const uint8_t *row_a, TConst tc, StageConst) {
-        return lds_f32(row_a + tc.goff);
+    template <int NW>
+    __device__ static Words<NW> lds_unit(uint32_t a) { return lds_at<NW, true>(a); }
+    __device__ static float aux(uint32_t, uint32_t row_a, TConst tc, StageConst) {
+        return lds_f32_at(row_a + tc.goff);
     }
 
-    __device__ static float zero_staged_aux() { return 0.f; }
 
     // Activation pairs in the order nibbles_as_denormals produces weights:
     // for a word pair (2i, 2i+1) of the unit, xp[8i+q] = {x[16i+q], x[16i+8+q]}
@@ -153,34 +154,10 @@ struct FmtI4G {
         }
     }
 
-    // Choose c with |x| < 2^(c-23) over the thread's activations, scale pair p
-    // by 2^(149 - 4*(p%4) - c) (finite for every finite x) and keep 2^c as two
-    // factors, each representable.
-    struct ThreadScale { float p1, p2; };
+    typedef Pow2Pair ThreadScale;
     template <int U, int S, int NP>
     __device__ static ThreadScale prepare_x(uint64_t (&xp)[U][S][NP], float (&)[U][S]) {
-        float m = 0.f;
-#pragma unroll
-        for (int j = 0; j < U; ++j)
-#pragma unroll
-            for (int s = 0; s < S; ++s)
-#pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    const float2 v = unpack2(xp[j][s][i]);
-                    m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
-                }
-        const int c = exponent_bound(m) + 23;
-#pragma unroll
-        for (int j = 0; j < U; ++j)
-#pragma unroll
-            for (int s = 0; s < S; ++s)
-#pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    const float2 v = unpack2(xp[j][s][i]);
-                    const int k = 149 - 4 * (i % 4) - c;
-                    xp[j][s][i] = pack2(ldexpf(v.x, k), ldexpf(v.y, k));
-                }
-        return ThreadScale{ldexpf(1.f, c >> 1), ldexpf(1.f, c - (c >> 1))};
+        return prescale_for_denormals<U, S, NP>(xp);
     }
 
     // sum (n - 8) * x over the unit = 2^c * sum(n * x * 2^-c) - 8 * xsum
@@ -203,14 +180,11 @@ struct FmtI4G {
         }
 #pragma unroll
         for (int s = 0; s < S; ++s) {
-            uint64_t a0 = 0ull, a1 = 0ull;
+            uint64_t acc = fmul2(d[0], xp[s][0]);
 #pragma unroll
-            for (int i = 0; i < NP; i += 2) {
-                ffma2(a0, d[i], xp[s][i]);
-                if (i + 1 < NP) ffma2(a1, d[i + 1], xp[s][i + 1]);
-            }
-            const float2 u0 = unpack2(a0), u1 = unpack2(a1);
-            const float t = fmaf((u0.x + u0.y + (u1.x + u1.y)) * ts.p1, ts.p2, -8.f * xsum[s]);
+            for (int i = 1; i < NP; ++i) ffma2(acc, d[i], xp[s][i]);
+            const float2 u = unpack2(acc);
+            const float t = fmaf((u.x + u.y) * ts.p1, ts.p2, -8.f * xsum[s]);
             part[s] = fmaf(sc, t, part[s]);
         }
     }
@@ -279,9 +253,7 @@ bool i4g_tma_plan(int S, int I, int O, int gs, TmaPlan *pl) {
     g.rowbytes = (uint32_t)(I / 2);
     g.granule_bytes = 16;
     g.arowbytes = (uint32_t)((I + gs - 1) / gs) * 4u;
-    const int umax = S == 1 ? 2 : 1;
-    if (S <= 2 && tma_plan(g, O, 8, next_pow2(8 * S), umax, pl)) return true;
-    return tma_plan(g, O, 4, next_pow2(4 * S), umax, pl);     // rows too long for 8-row slots
+    return tma_plan_rows(g, S, O, S == 1 ? 2 : 1, pl);
 }
 
 CsPlan i4g_plan(int S, int I, int O, int *U_out) {
@@ -335,6 +307,10 @@ void launch_tma_i4g_s(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cu
             launch_tma_i4g_u<S, 8>(p, out, pl, st);
             return;
         }
+    }
+    if (pl.rb == 2) {
+        launch_tma<FmtI4G, S, (S <= 2 ? 4 : S <= 4 ? 2 : 1), 1, 2>(p, out, pl, st);
+        return;
     }
     launch_tma_i4g_u<S, 4>(p, out, pl, st);
 }

@@ -117,11 +117,12 @@ struct FmtMq4v2 {
         return TConst{(uint32_t)t.uoff - seg_col, (uint32_t)t.hoff - seg_col};
     }
     __device__ static StageConst stage_const(const Params &, int, TConst) { return StageConst{}; }
-    __device__ static uint32_t aux(const uint8_t *row_w, const uint8_t *, TConst tc, StageConst) {
-        return lds_u32(row_w + tc.hoff);
+    template <int NW>
+    __device__ static Words<NW> lds_unit(uint32_t a) { return lds_at<NW, false>(a); }  // 8-byte aligned units
+    __device__ static uint32_t aux(uint32_t row_w, uint32_t, TConst tc, StageConst) {
+        return lds_u32_at(row_w + tc.hoff);
     }
 
-    __device__ static uint32_t zero_staged_aux() { return 0u; }
 
     // Activation pairs in the order nibbles_as_denormals produces weights
     // (see FmtI4G::load_x), raw; xsum = the unit's activation sum.
@@ -157,31 +158,10 @@ struct FmtMq4v2 {
         }
     }
 
-    struct ThreadScale { float p1, p2; };
+    typedef Pow2Pair ThreadScale;
     template <int U, int S, int NP>
     __device__ static ThreadScale prepare_x(uint64_t (&xp)[U][S][NP], float (&)[U][S]) {
-        float m = 0.f;
-#pragma unroll
-        for (int j = 0; j < U; ++j)
-#pragma unroll
-            for (int s = 0; s < S; ++s)
-#pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    const float2 v = unpack2(xp[j][s][i]);
-                    m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
-                }
-        const int c = exponent_bound(m) + 23;
-#pragma unroll
-        for (int j = 0; j < U; ++j)
-#pragma unroll
-            for (int s = 0; s < S; ++s)
-#pragma unroll
-                for (int i = 0; i < NP; ++i) {
-                    const float2 v = unpack2(xp[j][s][i]);
-                    const int k = 149 - 4 * (i % 4) - c;
-                    xp[j][s][i] = pack2(ldexpf(v.x, k), ldexpf(v.y, k));
-                }
-        return ThreadScale{ldexpf(1.f, c >> 1), ldexpf(1.f, c - (c >> 1))};
+        return prescale_for_denormals<U, S, NP>(xp);
     }
 
     // sum (q*scale + zero) * x = scale * 2^c * sum(q * x * 2^-c) + zero * xsum
@@ -206,14 +186,11 @@ struct FmtMq4v2 {
         const float zero = f16_bits_to_f32((uint16_t)(hd >> 16));
 #pragma unroll
         for (int s = 0; s < S; ++s) {
-            uint64_t a0 = 0ull, a1 = 0ull;
+            uint64_t acc = fmul2(d[0], xp[s][0]);
 #pragma unroll
-            for (int i = 0; i < NP; i += 2) {
-                ffma2(a0, d[i], xp[s][i]);
-                if (i + 1 < NP) ffma2(a1, d[i + 1], xp[s][i + 1]);
-            }
-            const float2 u0 = unpack2(a0), u1 = unpack2(a1);
-            part[s] = fmaf(scale, (u0.x + u0.y + (u1.x + u1.y)) * ts.p2, fmaf(zero, xsum[s], part[s]));
+            for (int i = 1; i < NP; ++i) ffma2(acc, d[i], xp[s][i]);
+            const float2 u = unpack2(acc);
+            part[s] = fmaf(scale, (u.x + u.y) * ts.p2, fmaf(zero, xsum[s], part[s]));
         }
     }
 };
@@ -231,8 +208,11 @@ bool mq4_tma_ok(const uint16_t *x, const uint8_t *blocks, int I) {
     return ((I / 256) % 2 == 0) && ((uintptr_t)blocks % 16 == 0) && ((uintptr_t)x % 16 == 0);
 }
 
+// staged path: 32-weight units (two 8-byte shared loads) at S <= 2
+int mq4_nw_tma(int S) { return S <= 2 ? 4 : S <= 4 ? 2 : 1; }
+
 bool mq4_tma_plan(int S, int I, int O, TmaPlan *pl) {
-    const int nw = mq4_nw(S);
+    const int nw = mq4_nw_tma(S);
     const int upb = 128 / (4 * nw);              // units per 256-weight block
     TmaGeom g;
     g.units = I / (8 * nw);
@@ -240,9 +220,7 @@ bool mq4_tma_plan(int S, int I, int O, TmaPlan *pl) {
     g.rowbytes = (uint32_t)((I / 256) * 136);
     g.granule_bytes = 272;
     g.arowbytes = 0;
-    const int umax = S == 1 ? 3 : 1;
-    if (S <= 2 && tma_plan(g, O, 8, next_pow2(8 * S), umax, pl)) return true;
-    return tma_plan(g, O, 4, next_pow2(4 * S), umax, pl);     // rows too long for 8-row slots
+    return tma_plan_rows(g, S, O, S == 1 ? 3 : 1, pl);
 }
 
 CsPlan mq4_plan(int S, int I, int O, int *U_out) {
@@ -284,7 +262,7 @@ void launch_cs_mq4_s(const FmtMq4v2::Params &p, float *out, const CsPlan &pl, in
 
 template <int S, int RB>
 void launch_tma_mq4_u(const FmtMq4v2::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
-    constexpr int NW = S <= 4 ? 2 : 1;
+    constexpr int NW = S <= 2 ? 4 : S <= 4 ? 2 : 1;
     if constexpr (S == 1) {
         if (pl.U == 2) {
             launch_tma<FmtMq4v2, S, NW, 2, RB>(p, out, pl, st);
@@ -305,6 +283,10 @@ void launch_tma_mq4_s(const FmtMq4v2::Params &p, float *out, const TmaPlan &pl, 
             launch_tma_mq4_u<S, 8>(p, out, pl, st);
             return;
         }
+    }
+    if (pl.rb == 2) {
+        launch_tma<FmtMq4v2, S, (S <= 2 ? 4 : S <= 4 ? 2 : 1), 1, 2>(p, out, pl, st);
+        return;
     }
     launch_tma_mq4_u<S, 4>(p, out, pl, st);
 }

@@ -66,6 +66,37 @@ __device__ __forceinline__ Words<1> lds_words<1>(const uint8_t *p) {
     return r;
 }
 
+// Loads at 32-bit shared addresses (the stage ring is addressed that way).
+template <int NW, bool kAlign16>
+__device__ __forceinline__ Words<NW> lds_at(uint32_t a) {
+    Words<NW> r;
+    if constexpr (NW == 4 && kAlign16) {
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]) : "r"(a));
+    } else if constexpr (NW == 4) {
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%4];\n\tld.shared.v2.u32 {%2,%3}, [%4+8];"
+                     : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]) : "r"(a));
+    } else if constexpr (NW == 2) {
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.w[0]), "=r"(r.w[1]) : "r"(a));
+    } else {
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r.w[0]) : "r"(a));
+    }
+    return r;
+}
+__device__ __forceinline__ float lds_f32_at(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u32_at(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// 2^k as a binary32, k in [-126, 127]
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
+
 __device__ __forceinline__ float lds_f32(const uint8_t *p) {
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_addr(p)));
@@ -92,6 +123,47 @@ __device__ __forceinline__ float2 unpack2(uint64_t v) {
 }
 __device__ __forceinline__ void ffma2(uint64_t &acc, uint64_t a, uint64_t b) {
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// Scale every activation pair p of the thread by 2^(149 - 4*(p%4) - c), c
+// chosen from the largest |x| it holds so the results are finite (see
+// nibbles_as_denormals); returns 2^c as two representable factors.  Both
+// multiplications are by powers of two, so they are exact.
+struct Pow2Pair { float p1, p2; };
+template <int U, int S, int NP>
+__device__ __forceinline__ Pow2Pair prescale_for_denormals(uint64_t (&xp)[U][S][NP]) {
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                const float2 v = unpack2(xp[j][s][i]);
+                m = fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
+            }
+    const int field = (int)((__float_as_uint(m) >> 23) & 0xFF);
+    const int c = (field == 0 ? 1 : field) - 126 + 23;       // |x| < 2^(c - 23); c in [-102, 152]
+    uint64_t f1[4], f2[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int kq = 149 - 4 * q - c;                      // in [-15, 251]
+        const float a = pow2i(kq >> 1), b = pow2i(kq - (kq >> 1));
+        f1[q] = pack2(a, a);
+        f2[q] = pack2(b, b);
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+#pragma unroll
+            for (int i = 0; i < NP; ++i) xp[j][s][i] = fmul2(fmul2(xp[j][s][i], f1[i % 4]), f2[i % 4]);
+    return Pow2Pair{pow2i(c >> 1), pow2i(c - (c >> 1))};
 }
 
 // Eight nibbles of one word -> four f32 pairs d[q] = {n(q)*16^q, n(q+4)*16^q} - c_q
@@ -150,13 +222,6 @@ __device__ __forceinline__ void nibbles_as_denormals(uint64_t ab, uint64_t (&d)[
         d[q] = ab & m;
         d[4 + q] = hab & m;
     }
-}
-
-// Exponent e with |v| < 2^e for the largest |v| seen (v finite): the binary32
-// exponent field of the maximum, unbiased, plus one (denormals give -126).
-__device__ __forceinline__ int exponent_bound(float vmax_abs) {
-    const int field = (int)((__float_as_uint(vmax_abs) >> 23) & 0xFF);
-    return (field == 0 ? 1 : field) - 126;
 }
 
 // Two e4m3 codes (low 16 bits of `two`) -> f32 pair (exact; NaN codes -> NaN)
@@ -272,7 +337,7 @@ gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, 
     const int ncth = nc * 32;
     int uidx[U];
     bool uok[U];
-    typename F::TConst tc[U];
+    typename F::TConst tc[U];   // a thread past the last unit takes unit ubeg (zero activations)
     uint64_t xp[U][S][NP];
     float xsum[U][S];
 #pragma unroll
@@ -287,52 +352,47 @@ gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, 
     typename F::StageConst scur[U], snext[U];
 #pragma unroll
     for (int j = 0; j < U; ++j) scur[j] = F::stage_const(p, b * RB, tc[j]);
+    const uint32_t sw0 = smem_addr(stage_w), sa0 = smem_addr(stage_a);
 
     for (int k = 0; k < n_my; ++k) {
         const int slot = k % nst;
-        const int o0 = (b + k * G) * RB;
 #pragma unroll
         for (int j = 0; j < U; ++j) snext[j] = F::stage_const(p, (b + (k + 1) * G) * RB, tc[j]);
         if (!mbar_wait(&full[slot], (uint32_t)(k / nst) & 1u)) {
             if (lane == 0) raise_device_error(err, kErrTimeout);
             return;
         }
-        const int rows = min(RB, p.O - o0);
-        const uint8_t *sw = stage_w + (size_t)slot * L.stage_w;
-        const uint8_t *sa = stage_a + (size_t)slot * L.stage_a;
+        const uint32_t swb = sw0 + (uint32_t)slot * L.stage_w;
+        const uint32_t sab = sa0 + (uint32_t)slot * L.stage_a;
         float part[NV];
 #pragma unroll
         for (int v = 0; v < NV; ++v) part[v] = 0.f;
-        // rows in sub-batches of RS: the sub-batch's shared-memory reads first,
-        // then its arithmetic (RS * U words stay live)
+        // Rows in sub-batches of RS: the sub-batch's shared-memory reads first,
+        // then its arithmetic.  No predicates: a thread without a unit of its
+        // own reads unit ubeg of the same row with zero activations (adds 0),
+        // and rows past the end of the matrix (last batch) read stale slot
+        // bytes whose partial sums are never written out.
         constexpr int RS = (S <= 2 ? 4 : 2) / U >= 1 ? (S <= 2 ? 4 : 2) / U : 1;
 #pragma unroll
         for (int r0 = 0; r0 < RB; r0 += RS) {
             Words<NW> wd[RS][U];
-            decltype(F::aux(sw, sa, tc[0], scur[0])) ax[RS][U];
+            typename F::Aux ax[RS][U];
 #pragma unroll
             for (int rr = 0; rr < RS; ++rr) {
-                const int r = r0 + rr;
+                const uint32_t rw = swb + (uint32_t)(r0 + rr) * seg_bytes;
+                const uint32_t ra = sab + (uint32_t)(r0 + rr) * arowbytes;
 #pragma unroll
                 for (int j = 0; j < U; ++j) {
-                    if (r < RB && r < rows && uok[j]) {
-                        const uint8_t *row_w = sw + (size_t)r * seg_bytes;
-                        wd[rr][j] = lds_words<NW>(row_w + tc[j].uoff);
-                        ax[rr][j] = F::aux(row_w, sa + (size_t)r * arowbytes, tc[j], scur[j]);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < NW; ++k) wd[rr][j].w[k] = 0u;
-                        ax[rr][j] = F::zero_staged_aux();
-                    }
+                    wd[rr][j] = F::template lds_unit<NW>(rw + tc[j].uoff);
+                    ax[rr][j] = F::aux(rw, ra, tc[j], scur[j]);
                 }
             }
 #pragma unroll
             for (int rr = 0; rr < RS; ++rr)
-                if (r0 + rr < RB)
 #pragma unroll
-                    for (int j = 0; j < U; ++j)
-                        F::template accumulate<S, NW, NP>(wd[rr][j], ax[rr][j], xp[j], xsum[j], ts,
-                                                          &part[(r0 + rr) * S]);
+                for (int j = 0; j < U; ++j)
+                    F::template accumulate<S, NW, NP>(wd[rr][j], ax[rr][j], xp[j], xsum[j], ts,
+                                                      &part[(r0 + rr) * S]);
         }
         const float tot = warp_reduce_scatter<NV>(part, lane);
         if ((lane & ((32 / NV) - 1)) == 0)
@@ -356,6 +416,7 @@ struct TmaPlan {
     int units_per_split;
     int nrowb;            // row batches
     int nst;              // ring slots
+    int per_sm;           // blocks per SM the ring was sized for
     TmaLayout L;
 };
 
@@ -369,6 +430,11 @@ struct TmaGeom {
 };
 
 bool tma_plan(const TmaGeom &g, int O, int RB, int NV, int U_max, TmaPlan *pl);
+
+// Plan with the largest batch (8, 4 or 2 rows; only 4 or 2 when S > 2, only 8
+// or 4 when a thread owns several units) that still gives every resident
+// block about three batches to overlap; short matrices get 2-row batches.
+bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl);
 
 // Device address of this device's error word (cached per device).
 int *device_error_word();
