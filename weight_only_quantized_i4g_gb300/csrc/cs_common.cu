@@ -142,10 +142,11 @@ CsPlan cs_plan(int units, int O, int u, int rb, int regs_per_thread) {
 // ---------------------------------------------------------------------------
 // plan of the staged (TMA) kernel
 // ---------------------------------------------------------------------------
-bool tma_plan(const TmaGeom &g, int O, int RB, int NV, int U_max, TmaPlan *pl) {
-    const int max_thr = kTmaMaxConsumerWarps * 32;
+bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl) {
     int U = 1, splits = 1;
+    int max_thr = tma_max_consumer_warps(S, 1) * 32;
     if (g.units > max_thr) {
+        max_thr = tma_max_consumer_warps(S, 2) * 32;
         if (g.units <= max_thr * U_max) {
             U = cdiv(g.units, max_thr);
         } else {
@@ -204,7 +205,7 @@ bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl) {
         const int rb = cands[i];
         if (S > 2 && rb == 8) continue;
         TmaPlan t;
-        if (!tma_plan(g, O, rb, next_pow2(rb * S), U_max, &t)) continue;
+        if (!tma_plan(g, S, O, rb, next_pow2(rb * S), U_max, &t)) continue;
         if (rb == 2 && t.U > 1) continue;
         *pl = t;
         have = true;

@@ -40,9 +40,11 @@
 
 namespace qg {
 
-// 15 consumer warps + the producer = 16 warps, four per SM sub-partition, which
-// leaves up to 128 registers per thread for a single resident block.
-constexpr int kTmaMaxConsumerWarps = 15;
+// Consumer warps per block.  15 + the producer = 16 warps, four per SM
+// sub-partition, leaves up to 128 registers per thread; the lighter
+// one-unit, one-token variants (<= 96 registers) take 17 + 1.
+constexpr int kTmaMaxConsumerWarps = 17;
+__host__ __device__ constexpr int tma_max_consumer_warps(int S, int U) { return (U == 1 && S == 1) ? 17 : 15; }
 
 template <int NW>
 __device__ __forceinline__ Words<NW> lds_words(const uint8_t *p);
@@ -249,7 +251,7 @@ struct TmaLayout {
 };
 
 template <class F, int S, int NW, int U, int RB>
-__global__ void __launch_bounds__(32 * (kTmaMaxConsumerWarps + 1), 1)
+__global__ void __launch_bounds__(32 * (tma_max_consumer_warps(S, U) + 1), 1)
 gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, int units_per_split,
                 int nrowb, int nst, TmaLayout L, int *err)
 {
@@ -429,7 +431,7 @@ struct TmaGeom {
     uint32_t arowbytes;       // staged side-data bytes per row
 };
 
-bool tma_plan(const TmaGeom &g, int O, int RB, int NV, int U_max, TmaPlan *pl);
+bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl);
 
 // Plan with the largest batch (8, 4 or 2 rows; only 4 or 2 when S > 2, only 8
 // or 4 when a thread owns several units) that still gives every resident
