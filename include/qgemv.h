@@ -86,6 +86,14 @@ enum { QG_FMT_I4G = 4, QG_FMT_FP8B128 = 7, QG_FMT_MQ4V2 = 44 };
  * refuses).  `gs` is only read for fmt=4. */
 size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs);
 
+/* Bytes of workspace that the batched-prefill GEMM entry point of format
+ * `fmt` (qgemm_i4g for QG_FMT_I4G) needs for an M x I x O call on the
+ * current device: tile counters plus two f32 partial-sum slots of 256 x 256
+ * per thread block, for tiles whose K range is shared by several blocks.
+ * 0 when the shape runs the general kernel (no workspace) or the arguments
+ * are invalid. */
+size_t qg_gemm_workspace_bytes(int fmt, int M, int I, int O, int gs);
+
 /* ------------------------------------------------------------------------ */
 /* fmt=4 grouped int4, decode GEMV                                          */
 /* colibri PR #457, section 3 (per-group scale folded into the sum) and     */
@@ -169,8 +177,13 @@ int qgemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks,
 /*   Y[M, O] f32 = X[M, I] (bf16 bits) . W^T, W as in qgemv_i4g.  The       */
 /*   weight tile is dequantized to bf16 ((n-8)*scale rounded to nearest     */
 /*   even) in shared memory and contracted with f32 accumulation.           */
-/*   Any M >= 1.  The tensor-core path needs I % 64 == 0, gs % 64 == 0 and  */
-/*   16-byte aligned X and w; other shapes run a general kernel.            */
+/*   Any M >= 1.  The tensor-core path takes I % 64 == 0, gs % 32 == 0 and  */
+/*   16-byte aligned X and w, and needs a 256-byte aligned workspace of     */
+/*   qg_gemm_workspace_bytes(QG_FMT_I4G, M, I, O, gs) bytes (QG_EWORKSPACE  */
+/*   otherwise); other shapes run a general CUDA-core kernel and ignore ws. */
+/*   The work is split evenly over one thread block per SM; a tile shared   */
+/*   by several blocks is summed in a fixed order, so repeated calls give   */
+/*   identical results.                                                     */
 /* ------------------------------------------------------------------------ */
 int qgemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales,
               int M, int I, int O, int gs, void *ws, size_t ws_bytes, qg_stream_t stream);

@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_lists_the_entry_points():
     names = declared_functions()
-    for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qg_workspace_bytes", "qg_device_status",
+    for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qg_workspace_bytes", "qg_gemm_workspace_bytes", "qg_device_status",
                  "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256"]:
         assert must in names, names
 

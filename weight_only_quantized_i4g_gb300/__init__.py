@@ -35,6 +35,7 @@ _SIGNATURES = {
     "qg_strerror": ([_I], ctypes.c_char_p),
     "qg_last_error": ([], ctypes.c_char_p),
     "qg_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
+    "qg_gemm_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
     "qg_device_status": ([ctypes.POINTER(_I)], _I),
     "qgemv_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_i4g_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
@@ -103,6 +104,10 @@ def qg_device_status() -> tuple[int, int]:
 
 def qg_workspace_bytes(fmt: int, S: int, I: int, O: int, gs: int = 0) -> int:
     return _lib.qg_workspace_bytes(fmt, S, I, O, gs)
+
+
+def qg_gemm_workspace_bytes(fmt: int, M: int, I: int, O: int, gs: int = 0) -> int:
+    return _lib.qg_gemm_workspace_bytes(fmt, M, I, O, gs)
 
 
 def qgemv_i4g(y, x, w, scales, S, I, O, gs, ws=None, ws_bytes=0, stream=None) -> int:

@@ -13,7 +13,8 @@ const char *error_detail();
 int run_gemm_i4g_general(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I,
                          int O, int gs, cudaStream_t st);
 int run_gemm_i4g_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I, int O,
-                    int gs, cudaStream_t st, bool *taken);
+                    int gs, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken);
+size_t ws_gemm_i4g(int M, int I, int O, int gs);
 }  // namespace qg
 
 using namespace qg;
@@ -83,6 +84,14 @@ size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs) {
     }
 }
 
+size_t qg_gemm_workspace_bytes(int fmt, int M, int I, int O, int gs) {
+    if (M < 1 || I < 1 || O < 1) return 0;
+    switch (fmt) {
+        case QG_FMT_I4G: return (gs >= 2 && !(gs & 1)) ? ws_gemm_i4g(M, I, O, gs) : 0;
+        default: return 0;
+    }
+}
+
 int qgemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O, int gs,
               void *ws, size_t ws_bytes, qg_stream_t stream) {
     const char *fn = "qgemv_i4g";
@@ -126,8 +135,6 @@ int qgemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I
 
 int qgemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I, int O, int gs,
               void *ws, size_t ws_bytes, qg_stream_t stream) {
-    (void)ws;
-    (void)ws_bytes;
     const char *fn = "qgemm_i4g";
     int rc = check_dims(fn, "M", M, I, O);
     if (rc) return rc;
@@ -135,9 +142,10 @@ int qgemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales
     if (!Y || !X || !w || !scales) QG_REFUSE(kEInval, "%s: Y, X, w and scales must be non-NULL", fn);
     if (!aligned(Y, 4) || !aligned(X, 2) || !aligned(scales, 4))
         QG_REFUSE(kEAlign, "%s: Y and scales must be 4-byte and X 2-byte aligned", fn);
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
     cudaGetLastError();
     bool taken = false;
-    rc = run_gemm_i4g_tc(Y, X, w, scales, M, I, O, gs, as_stream(stream), &taken);
+    rc = run_gemm_i4g_tc(Y, X, w, scales, M, I, O, gs, ws, ws_bytes, as_stream(stream), &taken);
     if (taken) return rc;
     return run_gemm_i4g_general(Y, X, w, scales, M, I, O, gs, as_stream(stream));
 }

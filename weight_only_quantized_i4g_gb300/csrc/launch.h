@@ -31,8 +31,6 @@ int run_gemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float 
 int run_gemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
                    size_t ws_bytes, cudaStream_t st);
 
-int run_gemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I,
-                 int O, int gs, void *ws, size_t ws_bytes, cudaStream_t st);
 
 int run_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs, cudaStream_t st);
 int run_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, cudaStream_t st);

@@ -50,6 +50,63 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     return false;
 }
 
+// As mbar_wait, but also gives up early once *abort is set (checked every
+// 256 tries), and sets *abort itself when it runs out of tries, so that one
+// timed-out wait ends the other waits of the block quickly.  Polls without
+// sleeping: for the waits on a pipeline's critical path.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+    const uint32_t a = smem_addr(bar);
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((it & 255u) == 255u && *abort) return false;
+    }
+    *abort = 1u;
+    return false;
+}
+
+// mbar_wait_or_abort for a whole warp: lane 0 alone polls the barrier and the
+// other lanes wait at __syncwarp (polls from every lane of several warps
+// crowd the SM's barrier unit and slow every other barrier operation,
+// including the transaction counts of bulk copies).  Returns the result on
+// every lane; the warp must be converged.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait_or_abort(bar, parity, abort);
+    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// As mbar_wait_or_abort, for long waits off the critical path (a warp that
+// waits for a whole tile): between tries the thread sleeps kBackoffNs, so it
+// takes almost no issue slots from the warps that work meanwhile.
+constexpr uint32_t kBackoffNs = 256;
+constexpr uint32_t kBackoffLimit = 1u << 24;   // ~4 s of 256 ns sleeps
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+    const uint32_t a = smem_addr(bar);
+    for (uint32_t it = 0; it < kBackoffLimit; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((it & 15u) == 15u && *abort) return false;
+        __nanosleep(kBackoffNs);
+    }
+    *abort = 1u;
+    return false;
+}
+
 // 1-D bulk copy of `bytes` (multiple of 16) from global `src` (16-byte
 // aligned) to shared `dst` (16-byte aligned); completion is counted on `bar`.
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
