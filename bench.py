@@ -10,6 +10,11 @@ every call streams its weights from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+The batched-prefill dequant-GEMM (fmt=4, M=512 tokens, 7168x7168 and
+2048x7168) is measured after the step loop and reported in the same line as
+a fraction of the measured bf16 tensor peak ("prefill"): it is compute-bound
+and has its own metric, so it is not folded into the GEMV bytes.
+
 Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs the
 same step on its own GPU (replicas: the GEMVs need no exchange) and the
 value is the bytes of all ranks over the slowest rank's time.
@@ -70,10 +75,25 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """Dense bf16 TFLOP/s: the measured burst figure (a kernel timed alone)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured (burst)"
+    except Exception:  # noqa: BLE001
+        return 1900.0, "fallback"
+
+
+# Sources of the dominant kernel (the staged fmt=7 GEMV); the committed DRAM
+# traffic figure is valid only for the build these hash to.
+DOMINANT_SOURCES = ("gemv_tma.cuh", "gemv_fp8b128.cu", "common.cuh", "pipeline.cuh")
+
+
 def source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "weight_only_quantized_i4g_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in DOMINANT_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -406,6 +426,7 @@ def ours_arm(args):
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
 
     per_format = per_format_breakdown(qg, torch, calls, stream, hbm_peak) if args.breakdown else None
+    prefill = prefill_measure(qg, torch, dev, stream) if args.prefill else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -439,11 +460,70 @@ def ours_arm(args):
             "gpu_launches": len(calls) * args.steps,
             "clocks": clocks,
             "per_format": per_format,
+            "prefill": prefill,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+PREFILL_M, PREFILL_I = 512, 7168
+PREFILL_O = (7168, 2048)
+
+
+def prefill_measure(qg, torch, dev, stream, reps=20):
+    """The fmt=4 batched-prefill GEMM of the workload's prefill config:
+    Y[512, O] = X[512, 7168] . W^T for O = 7168 and 2048, gs = 64.  Weights
+    N(0, 0.02) quantized on the device by qg_quantize_i4g, X N(0, 1) in
+    bf16, both from seeded generators.  Each call is timed alone with CUDA
+    events on its stream after a 256 MiB write that flushes L2; median of
+    `reps`.  Returns TFLOP/s (2*M*I*O per call) and the fraction of the
+    measured dense bf16 peak."""
+    peak, kind = load_tensor_peak()
+    M, I = PREFILL_M, PREFILL_I
+    out = {"workload": f"fmt4 int4-g64 prefill GEMM, M={M}, I={I}, O in {list(PREFILL_O)}, "
+                       f"bf16 activations, f32 out",
+           "bound": "tensor", "peak": peak, "unit": "TFLOP/s", "peak_kind": kind, "calls": {}}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    launches = 0
+    with torch.cuda.stream(stream):
+        for O in PREFILL_O:
+            g = torch.Generator(device=dev)
+            g.manual_seed(4000 + O)
+            w = torch.randn(O, I, generator=g, device=dev) * 0.02
+            wq = torch.empty(O * I // 2, dtype=torch.uint8, device=dev)
+            sc = torch.empty(O * (I // GS), dtype=torch.float32, device=dev)
+            qg.check(qg.qg_quantize_i4g(wq, sc, w, O, I, GS, stream=stream))
+            del w
+            g.manual_seed(5000 + O)
+            X = torch.randn(M, I, generator=g, device=dev).to(torch.bfloat16).view(torch.int16)
+            Y = torch.empty(M * O, dtype=torch.float32, device=dev)
+            n = qg.qg_gemm_workspace_bytes(qg.QG_FMT_I4G, M, I, O, GS)
+            ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+            for _ in range(3):
+                qg.check(qg.qgemm_i4g(Y, X, wq, sc, M, I, O, GS, ws, n, stream=stream))
+            ts = []
+            for _ in range(reps):
+                flush.fill_(1)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                qg.check(qg.qgemm_i4g(Y, X, wq, sc, M, I, O, GS, ws, n, stream=stream))
+                b.record(stream)
+                b.synchronize()
+                ts.append(a.elapsed_time(b))
+                launches += 1
+            t = statistics.median(ts) * 1e-3
+            tf = 2.0 * M * I * O / t / 1e12
+            out["calls"][f"{M}x{O}x{I}"] = {"us": round(t * 1e6, 2), "tflops": round(tf, 1),
+                                             "frac": round(tf / peak, 4)}
+    tot_flop = sum(2.0 * M * I * O for O in PREFILL_O)
+    tot_t = sum(c["us"] for c in out["calls"].values()) * 1e-6
+    out["achieved"] = round(tot_flop / tot_t / 1e12, 1)
+    out["frac"] = round(out["achieved"] / peak, 4)
+    out["launches_timed"] = launches
+    return out
 
 
 def per_format_breakdown(qg, torch, calls, stream, hbm_peak):
@@ -512,6 +592,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-breakdown", dest="breakdown", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false",
+                    help="skip the prefill GEMM measurement")
     ap.add_argument("--only", default="", help="comma-separated subset of the shapes (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:

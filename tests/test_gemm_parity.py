@@ -41,12 +41,14 @@ def run_gemm(qg, X, wq, sc, M, I, O, gs, ws=None):
     return host(Y, M, O)
 
 
-# Shapes with I % 64 == 0 and gs % 32 == 0 take the tensor-core kernel: one
-# or two token halves, ragged M and O tails, gs 32/64/96/128/256, tiles whose
-# K range is split over many blocks (few tiles) and whole tiles.
+# Shapes with I % 64 == 0 and gs % 32 == 0 take the tensor-core kernel:
+# ragged M and O tails, gs 32/64/96/128/256, a last K step of 64 (I % 128 ==
+# 64), tiles whose K range is split over many blocks (few tiles) and whole
+# tiles.
 TC_SHAPES = [(1, 64, 1, 64), (64, 6144, 2048, 64), (70, 512, 130, 32), (128, 1024, 256, 128),
              (257, 2048, 384, 64), (129, 768, 33, 96), (300, 4096, 520, 256), (16, 128, 4, 64),
-             (512, 1024, 1024, 64), (200, 8192, 16, 64)]
+             (512, 1024, 1024, 64), (200, 8192, 16, 64), (33, 320, 200, 64), (7, 192, 130, 32),
+             (96, 448, 64, 32)]
 
 
 @pytest.mark.parametrize("M,I,O,gs", TC_SHAPES + [(5, 200, 33, 64), (3, 201, 7, 64), (40, 96, 24, 48)])

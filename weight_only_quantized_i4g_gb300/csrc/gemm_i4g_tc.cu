@@ -8,19 +8,24 @@
 // shared memory and contracted with f32 accumulation.)
 //
 // One persistent thread block per SM, warp-specialized.  Output tile: 128
-// outputs (the weight rows, MMA M) by BT tokens (MMA N), K in steps of 64.
-//   warp 0      TMA producer: per K step the BT x 64 bf16 tile of X
-//               (128-byte swizzle) into a shared-memory ring (operand B);
+// outputs (the weight rows, MMA M) by BT tokens (MMA N), K in steps of 128.
+//   warp 0      TMA producer: per K step the BT x 128 bf16 tile of X (two
+//               128-byte-swizzled boxes of 64) into a shared-memory ring
+//               (operand B);
 //   warp 1      allocates tensor memory and issues the MMAs from one thread:
-//               per K step 4 instructions of M=128, N=BT, K=16 with operand
+//               per K step 8 instructions of M=128, N=BT, K=16 with operand
 //               A read from tensor memory;
 //   warps 2-5   epilogue: accumulator -> registers -> Y (or a partial slot);
 //   warps 6-13  load the packed weights of the tile straight from global
 //               memory (16-byte loads, three K steps ahead in registers),
 //               dequantize them and store the bf16 rows into a ring of A
 //               tiles in tensor memory (tcgen05.st): warp w covers the 32
-//               lanes (weight rows) its position allows and one 32-wide half
+//               lanes (weight rows) its position allows and one 64-wide half
 //               of the K step.
+// One barrier per stage counts both the X bytes and the eight dequantizing
+// warps, and one commit per step frees the stage: the MMA thread's waits and
+// commits cost ~200 cycles each, so they are kept to one of each per 1024
+// cycles of tensor-core work.
 // Keeping the dequantized weights as operand A in tensor memory means each
 // of them serves BT = 256 tokens, and shared memory carries only X: the
 // dequantization work per MAC is half that of a 128-token tile, and no
@@ -45,7 +50,8 @@ int *device_error_word();
 namespace tc {
 
 constexpr int kMmaM = 128;        // rows of one MMA (weight rows = outputs)
-constexpr int kBK = 64;           // K per stage: one 128-byte row of bf16
+constexpr int kBK = 128;          // K per stage: two 128-byte rows of bf16
+constexpr int kBKBox = 64;        // K of one 128-byte-swizzled box
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi = 2, kNumEpiWarps = 4, kWarpDeq = 6, kNumDeqWarps = 8;
 constexpr int kThreads = 32 * (kWarpDeq + kNumDeqWarps);
 constexpr uint32_t kSmemBudget = 227 * 1024;
@@ -88,13 +94,16 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b_desc), "r"(accumulate), "r"(idesc));
 }
 
-// 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+// 32 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -224,24 +233,23 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned *p) {
 template <int BT>
 struct Cfg {
     static_assert(BT % 32 == 0 && BT >= 32 && BT <= 256, "N of one MMA, whole 32-token chunks");
-    static constexpr int kBO = kMmaM;                       // outputs per tile
-    static constexpr uint32_t kXBytes = BT * kBK * 2;       // operand B stage: BT tokens x 64 bf16
-    static constexpr int kAStages = 4;                      // operand A stages in tensor memory
-    static constexpr uint32_t kACols = kBK / 2;             // 64 bf16 per row = 32 columns
+    static constexpr uint32_t kBoxBytes = BT * kBKBox * 2;  // one 64-wide box of X
+    static constexpr uint32_t kXBytes = 2 * kBoxBytes;      // operand B stage: BT tokens x 128 bf16
+    static constexpr uint32_t kACols = kBK / 2;             // 128 bf16 per row = 64 columns
     static constexpr uint32_t kACol0 = 256;                 // A ring after the accumulator
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kStagesMax = 8;
-    static constexpr int kNumBarsFor(int st) { return 2 * st + 2 * kAStages + 2; }
+    static constexpr int kAStagesMax = (int)((kTmemCols - kACol0) / kACols);   // 4
+    static constexpr int kNumBarsFor(int st) { return 2 * st + 2; }
     static constexpr uint32_t kFixed = 1024 + 16;           // alignment slack + tmem / flag words
-    static constexpr int kStagesFit = (int)((kSmemBudget - kFixed - 8 * kNumBarsFor(kStagesMax)) / kXBytes);
-    static constexpr int kStages = kStagesFit > kStagesMax ? kStagesMax : kStagesFit;
+    static constexpr int kStagesFit = (int)((kSmemBudget - kFixed - 8 * kNumBarsFor(kAStagesMax)) / kXBytes);
+    static constexpr int kStages = kStagesFit > kAStagesMax ? kAStagesMax : kStagesFit;
     static constexpr int kNumBars = kNumBarsFor(kStages);
     static constexpr uint32_t kSmemBytes = kFixed + kStages * kXBytes + 8 * kNumBars;
     static constexpr int kSlotFloats = kMmaM * BT;          // one partial slot
     static constexpr uint32_t kIdesc = idesc_bf16(BT);
-    static_assert(kStages >= 3, "at least three X stages");
-    static_assert(kXBytes % 1024 == 0, "swizzled tiles must stay 1024-byte aligned");
-    static_assert(kACol0 >= (uint32_t)BT && kACol0 + kAStages * kACols <= kTmemCols, "tensor memory map");
+    static_assert(kStages >= 3, "at least three stages");
+    static_assert(kBoxBytes % 1024 == 0, "swizzled tiles must stay 1024-byte aligned");
+    static_assert(kACol0 >= (uint32_t)BT && kACol0 + kStages * kACols <= kTmemCols, "tensor memory map");
 };
 
 struct Args {
@@ -251,6 +259,7 @@ struct Args {
     unsigned *counters;   // one per output tile, zero at launch
     float *partials;      // 2 slots per block
     int M, O, gs, ng, MB, Kt;
+    int tail_half;        // the last K step of every tile is 64 wide (I % 128 == 64)
     long long rowbytes;   // I / 2
     long long U;          // (tile, K step) units
     int *err;
@@ -278,9 +287,8 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
     unsigned char *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
     const uint32_t sbase = smem_addr(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kXBytes);
-    uint64_t *xfull = bars, *xempty = bars + C::kStages;
-    uint64_t *aready = bars + 2 * C::kStages, *aempty = aready + C::kAStages;
-    uint64_t *acc_full = aempty + C::kAStages, *acc_empty = acc_full + 1;
+    uint64_t *full = bars, *empty = bars + C::kStages;   // per stage: X bytes + dequantized A / MMA done
+    uint64_t *acc_full = empty + C::kStages, *acc_empty = acc_full + 1;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + C::kNumBars);
     volatile uint32_t *flag = tmem_slot + 1;    // epilogue broadcast: this block finishes the tile
     volatile uint32_t *abort = tmem_slot + 2;   // set by the first wait that times out
@@ -288,12 +296,8 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&xfull[s], 1);
-            mbar_init(&xempty[s], 1);
-        }
-        for (int s = 0; s < C::kAStages; ++s) {
-            mbar_init(&aready[s], kNumDeqWarps);
-            mbar_init(&aempty[s], 1);
+            mbar_init(&full[s], 1 + kNumDeqWarps);
+            mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kNumEpiWarps);
@@ -326,16 +330,18 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
                 const int m0 = (int)(g.t % a.MB) * BT;
                 for (int k = g.ks; k < g.ke; ++k, ++it) {
                     const uint32_t s = it % C::kStages, r = it / C::kStages;
-                    if (r > 0 && !mbar_wait_or_abort(&xempty[s], (r & 1) ^ 1, abort))
+                    const bool half = a.tail_half && k == Kt - 1;
+                    if (r > 0 && !mbar_wait_or_abort(&empty[s], (r & 1) ^ 1, abort))
                         raise_device_error(a.err, kErrTimeout);
-                    mbar_arrive_expect_tx(&xfull[s], C::kXBytes);
-                    tma_load_2d(sbase + s * C::kXBytes, &tmX, k * kBK, m0, &xfull[s]);
+                    mbar_arrive_expect_tx(&full[s], half ? C::kBoxBytes : C::kXBytes);
+                    tma_load_2d(sbase + s * C::kXBytes, &tmX, k * kBK, m0, &full[s]);
+                    if (!half) tma_load_2d(sbase + s * C::kXBytes + C::kBoxBytes, &tmX, k * kBK + kBKBox, m0, &full[s]);
                 }
                 u = g.t * Kt + g.ke;
             }
             // Every copy issued must have landed before the block exits.
             for (uint32_t j = it > (uint32_t)C::kStages ? it - C::kStages : 0; j < it; ++j)
-                if (!mbar_wait(&xfull[j % C::kStages], (j / C::kStages) & 1)) raise_device_error(a.err, kErrTimeout);
+                if (!mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1)) raise_device_error(a.err, kErrTimeout);
         }
     } else if (warp == kWarpMma) {
         if (lane == 0) {
@@ -347,18 +353,17 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
                 tc_fence_after();
                 for (int k = g.ks; k < g.ke; ++k, ++it) {
                     const uint32_t s = it % C::kStages, r = it / C::kStages;
-                    const uint32_t sa = it % C::kAStages, ra = it / C::kAStages;
-                    if (!mbar_wait_or_abort(&xfull[s], r & 1, abort)) raise_device_error(a.err, kErrTimeout);
-                    if (!mbar_wait_or_abort(&aready[sa], ra & 1, abort)) raise_device_error(a.err, kErrTimeout);
+                    const int nk = (a.tail_half && k == Kt - 1) ? kBKBox / 16 : kBK / 16;
+                    if (!mbar_wait_or_abort(&full[s], r & 1, abort)) raise_device_error(a.err, kErrTimeout);
                     tc_fence_after();
                     const uint32_t xa = sbase + s * C::kXBytes;
-                    const uint32_t at = tmem + C::kACol0 + sa * C::kACols;
+                    const uint32_t at = tmem + C::kACol0 + s * C::kACols;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16_ts(tmem, at + kk * 8, sw128_desc(xa + kk * 32), C::kIdesc,
-                                    (k > g.ks || kk > 0) ? 1u : 0u);
-                    mma_commit(&xempty[s]);
-                    mma_commit(&aempty[sa]);
+                        if (kk < nk)
+                            mma_bf16_ts(tmem, at + kk * 8, sw128_desc(xa + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32),
+                                        C::kIdesc, (k > g.ks || kk > 0) ? 1u : 0u);
+                    mma_commit(&empty[s]);
                 }
                 mma_commit(acc_full);
                 u = g.t * Kt + g.ke;
@@ -484,39 +489,42 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
     } else {
         // Dequantize.  Warp w may write tensor-memory lanes 32*(w % 4) ..
         // +31 (weight rows of the tile); the two warps of a lane quarter
-        // split each K step into halves kh = 0, 1 of 32 weights (16 bytes).
+        // split each K step into halves kh = 0, 1 of 64 weights (32 bytes).
         const int q = warp & 3, kh = (warp - kWarpDeq) >> 2;
         const int R = q * 32 + lane;
         const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + C::kACol0 + kh * (C::kACols / 2);
         struct Fetch {
-            uint4 q;
-            float s;
+            uint4 q[2];
+            float s[2];
         };
         // Fetch state: the next unit to load, this row's pointers, and the
-        // scale group of this thread's 32-weight half, advanced without
-        // divisions (one division per tile change).
+        // scale group of this thread's first 32-weight quarter, advanced
+        // without divisions (one division per tile change).
         long long pu = ub, pt = ub / Kt;
         int pk = (int)(ub - pt * Kt);
-        const int gq = a.gs / 32;   // 32-weight halves per scale group
+        const int gq = a.gs / 32;   // 32-weight quarters per scale group
         const uint8_t *wrow = nullptr;
         const float *srow = nullptr;
         int gi = 0, gr = 0;
         auto set_tile = [&]() {
             const int o = (int)(pt / a.MB) * kMmaM + R;
-            wrow = o < a.O ? a.w + (size_t)o * a.rowbytes + kh * 16 : nullptr;
+            wrow = o < a.O ? a.w + (size_t)o * a.rowbytes + kh * 32 : nullptr;
             srow = o < a.O ? a.scales + (size_t)o * a.ng : nullptr;
-            const int hi = 2 * pk + kh;
-            gi = hi / gq;
-            gr = hi - gi * gq;
+            const int u0 = 4 * pk + 2 * kh;
+            gi = u0 / gq;
+            gr = u0 - gi * gq;
         };
         if (pu < ue) set_tile();
         auto fetch = [&](Fetch &f) {
-            f.q = make_uint4(0u, 0u, 0u, 0u);
-            f.s = 0.f;
+            f.q[0] = f.q[1] = make_uint4(0u, 0u, 0u, 0u);
+            f.s[0] = f.s[1] = 0.f;
             if (pu < ue) {
-                if (wrow) {
-                    f.q = ldg_w16(wrow + pk * 32);
-                    f.s = __ldg(srow + gi);
+                // The 64-wide last step of a row with I % 128 == 64 has no second half.
+                if (wrow && !(kh == 1 && a.tail_half && pk == Kt - 1)) {
+                    f.q[0] = ldg_w16(wrow + pk * 64);
+                    f.q[1] = ldg_w16(wrow + pk * 64 + 16);
+                    f.s[0] = __ldg(srow + gi);
+                    f.s[1] = __ldg(srow + gi + (gr + 1 >= gq ? 1 : 0));
                 }
                 ++pu;
                 if (++pk == Kt) {
@@ -524,7 +532,7 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
                     ++pt;
                     if (pu < ue) set_tile();
                 } else {
-                    gr += 2;
+                    gr += 4;
                     while (gr >= gq) {
                         gr -= gq;
                         ++gi;
@@ -534,24 +542,27 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         };
         uint32_t it = 0;
         auto step = [&](const Fetch &cur) {
-            const uint32_t sa = it % C::kAStages, ra = it / C::kAStages;
-            if (ra > 0 && !mbar_wait_warp(&aempty[sa], (ra & 1) ^ 1, abort) && lane == 0)
+            const uint32_t s = it % C::kStages, r = it / C::kStages;
+            if (r > 0 && !mbar_wait_warp(&empty[s], (r & 1) ^ 1, abort) && lane == 0)
                 raise_device_error(a.err, kErrTimeout);
             tc_fence_after();
-            const ScalePairs sp = scale_pairs(cur.s);
-            const uint32_t wv[4] = {cur.q.x, cur.q.y, cur.q.z, cur.q.w};
-            uint32_t col[16];
+            uint32_t col[32];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t o4[4];
-                dequant_word(wv[j], sp, o4);
+            for (int i = 0; i < 2; ++i) {
+                const ScalePairs sp = scale_pairs(cur.s[i]);
+                const uint32_t wv[4] = {cur.q[i].x, cur.q[i].y, cur.q[i].z, cur.q[i].w};
 #pragma unroll
-                for (int p = 0; p < 4; ++p) col[4 * j + p] = o4[p];
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t o4[4];
+                    dequant_word(wv[j], sp, o4);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) col[16 * i + 4 * j + p] = o4[p];
+                }
             }
-            tmem_st16(ta + sa * C::kACols, col);
+            tmem_st32(ta + s * C::kACols, col);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&aready[sa]);
+            if (lane == 0) mbar_arrive(&full[s]);
             ++it;
         };
         // Three register buffers used in rotation with fixed names, so a
@@ -618,7 +629,7 @@ Plan make_plan(int tile, int M, int I, int O, int nsm) {
     p.bt = kTileBT[tile];
     p.MB = (M + p.bt - 1) / p.bt;
     p.NB = (O + kMmaM - 1) / kMmaM;
-    p.Kt = I / kBK;
+    p.Kt = (I + kBK - 1) / kBK;
     p.T = (long long)p.MB * p.NB;
     p.U = p.T * p.Kt;
     // One tile per block when the tiles fit in one wave; otherwise an even
@@ -629,31 +640,38 @@ Plan make_plan(int tile, int M, int I, int O, int nsm) {
     return p;
 }
 
-// Estimated SM cycles of the busiest block: K steps x the step time of the
-// tile (tensor cores at ~2900 MAC/clk/SM, X through TMA at ~46 B/clk/SM,
-// dequantization of 128 x 64 weights at ~550 clk) plus the split-tile
-// traffic (partial slots written and read at ~40 B/clk/SM).
+// Estimated cycles of the busiest block, from measurements on GB300: a
+// 128-wide K step costs ~2300 cycles with 256 tokens per tile and ~2150 with
+// fewer (the dequantization of 128 x 128 weights bounds it), and a tile whose
+// K range is split over blocks costs ~14000 cycles per contributor for the
+// partial sums (written, then read back by the block that finishes it).
 double plan_cost(const Plan &p) {
-    const double mma = 128.0 * p.bt * kBK / 2900.0;
-    const double tma = p.bt * 128.0 / 46.0;
-    const double deq = 550.0;
-    const double step = std::max(mma, std::max(tma, deq)) + 40.0;
+    const double step = p.bt == 256 ? 2300.0 : 2150.0;
     const double steps = (double)((p.U + p.P - 1) / p.P);
     const bool split = (p.U / p.P) % p.Kt != 0 || p.U % p.P != 0;
-    const double slot = (double)kMmaM * p.bt * 4.0;
-    return steps * step + (split ? 3.0 * slot / 40.0 : 0.0);
+    const double contributors = (double)p.Kt / std::max(1.0, (double)(p.U / p.P)) + 1.0;
+    return steps * step + (split ? 14000.0 * contributors : 0.0);
 }
 
+// Both launch shapes for every token width: one whole tile per block when
+// the tiles fit in one wave, and the stream-K split over all SMs.
 Plan choose_plan(int M, int I, int O) {
     const int nsm = num_sms();
     Plan best = make_plan(0, M, I, O, nsm);
     double best_cost = plan_cost(best);
-    for (int t = 1; t < kNumTiles; ++t) {
-        const Plan p = make_plan(t, M, I, O, nsm);
-        const double c = plan_cost(p);
-        if (c < best_cost) {
-            best = p;
-            best_cost = c;
+    for (int t = 0; t < kNumTiles; ++t) {
+        for (int mode = 0; mode < 2; ++mode) {
+            Plan p = make_plan(t, M, I, O, nsm);
+            if (mode == 1) {
+                if (p.T >= nsm) continue;   // already the split over all SMs
+                p.P = (int)std::min<long long>(nsm, p.U);
+                p.ws_bytes = p.counter_bytes + (size_t)2 * p.P * kMmaM * p.bt * sizeof(float);
+            }
+            const double c = plan_cost(p);
+            if (c < best_cost) {
+                best = p;
+                best_cost = c;
+            }
         }
     }
     return best;
@@ -683,7 +701,7 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, const uint8_t *w, co
     CUtensorMap tmX;
     const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)I * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)p.bt};
+    const cuuint32_t box[2] = {(cuuint32_t)kBKBox, (cuuint32_t)p.bt};
     const cuuint32_t es[2] = {1, 1};
     CUresult r = encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -704,6 +722,7 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, const uint8_t *w, co
     args.ng = (I + gs - 1) / gs;
     args.MB = p.MB;
     args.Kt = p.Kt;
+    args.tail_half = (I % kBK) != 0 ? 1 : 0;
     args.rowbytes = I / 2;
     args.U = p.U;
     args.err = device_error_word();
@@ -718,15 +737,15 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, const uint8_t *w, co
 
 }  // namespace tc
 
-// Shapes the tensor-core kernel takes: K in whole 64-steps, every 32-weight
+// Shapes the tensor-core kernel takes: K in whole 64-steps (a last step of 64), every 32-weight
 // half step inside one scale group, a 16-byte aligned w (its rows then start
 // on 16-byte boundaries too) and a TMA-aligned X.
 bool gemm_i4g_tc_ok(const uint16_t *X, const uint8_t *w, int I, int gs) {
-    return I % tc::kBK == 0 && gs % 32 == 0 && (uintptr_t)X % 16 == 0 && (uintptr_t)w % 16 == 0;
+    return I % tc::kBKBox == 0 && gs % 32 == 0 && (uintptr_t)X % 16 == 0 && (uintptr_t)w % 16 == 0;
 }
 
 size_t ws_gemm_i4g(int M, int I, int O, int gs) {
-    if (I % tc::kBK != 0 || gs % 32 != 0) return 0;
+    if (I % tc::kBKBox != 0 || gs % 32 != 0) return 0;
     return tc::choose_plan(M, I, O).ws_bytes;
 }
 
