@@ -3,6 +3,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "gemv_cs.cuh"
@@ -200,18 +201,36 @@ bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan
 
 bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl) {
     const int cands[3] = {8, 4, 2};
-    bool have = false;
+    bool have = false, have_bal = false;
+    TmaPlan last, bal;
+    double bal_eff = 0.0;
     for (int i = 0; i < 3; ++i) {
         const int rb = cands[i];
         if (S > 2 && rb == 8) continue;
         TmaPlan t;
         if (!tma_plan(g, S, O, rb, next_pow2(rb * S), U_max, &t)) continue;
         if (rb == 2 && t.U > 1) continue;
-        *pl = t;
+        last = t;
         have = true;
-        const long resident = (long)num_sms() * t.per_sm;
-        if ((long)t.nrowb * t.splits >= 3 * resident) return true;
+        // Batches per resident block: at least three to overlap, and an even
+        // last wave (a block with one batch more than the mean sets the time).
+        const double resident = (double)num_sms() * t.per_sm;
+        const double waves = (double)t.nrowb * t.splits / resident;
+        if (waves >= 3.0) {
+            const double eff = waves / std::ceil(waves);
+            if (eff >= 0.92) {
+                *pl = t;
+                return true;
+            }
+            if (!have_bal || eff > bal_eff) {
+                bal = t;
+                bal_eff = eff;
+                have_bal = true;
+            }
+        }
     }
+    if (have_bal) *pl = bal;
+    else if (have) *pl = last;
     return have;
 }
 
@@ -220,6 +239,8 @@ bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl) {
 // ---------------------------------------------------------------------------
 __global__ void splitk_reduce_kernel(float *__restrict__ y, const float *__restrict__ ws, int splits,
                                      size_t n) {
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();   // ws is the previous kernel's output
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         float acc = 0.f;
         for (int k = 0; k < splits; ++k) acc += ws[(size_t)k * n + i];
@@ -233,7 +254,18 @@ void launch_splitk_reduce(float *y, const float *ws, int splits, int S, int O, c
     const int cap = num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(y, ws, splits, n);
+    // Launched as a programmatic dependent of the GEMV that fills ws: it
+    // starts early and waits in the kernel (griddep_wait) for that GEMV.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, y, ws, splits, n);
 }
 
 }  // namespace qg

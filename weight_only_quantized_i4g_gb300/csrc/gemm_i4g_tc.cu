@@ -543,8 +543,7 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         uint32_t it = 0;
         auto step = [&](const Fetch &cur) {
             const uint32_t s = it % C::kStages, r = it / C::kStages;
-            if (r > 0 && !mbar_wait_warp(&empty[s], (r & 1) ^ 1, abort) && lane == 0)
-                raise_device_error(a.err, kErrTimeout);
+            if (r > 0 && !mbar_wait_or_abort(&empty[s], (r & 1) ^ 1, abort)) raise_device_error(a.err, kErrTimeout);
             tc_fence_after();
             uint32_t col[32];
 #pragma unroll

@@ -270,6 +270,7 @@ gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, 
     uint64_t *empty = full + nst;
 
     if (tid == 0) {
+        griddep_launch_dependents();
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], (uint32_t)nc);
@@ -306,9 +307,12 @@ gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, 
             }
             if (ab) bulk_copy_g2s(stage_a + (size_t)slot * L.stage_a, F::a_src(p, o0), ab, &full[slot]);
         };
+        // The weights do not depend on the previous kernel on the stream: the
+        // first batches stream in before the wait that guards the outputs.
         if (lane == 0)
             for (int k = 0; k < min(nst, n_my); ++k) issue(k);
         __syncwarp();
+        griddep_wait();
         for (int k = 0; k < n_my; ++k) {
             const int slot = k % nst;
             if (!mbar_wait(&empty[slot], (uint32_t)(k / nst) & 1u)) {
@@ -334,6 +338,7 @@ gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, 
     }
 
     // ------------------------------- consumers ----------------------------------
+    griddep_wait();   // x may be the previous kernel's output
     const int cw = warp - 1;
     const int ct = tid - 32;
     const int ncth = nc * 32;
@@ -434,8 +439,10 @@ struct TmaGeom {
 bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl);
 
 // Plan with the largest batch (8, 4 or 2 rows; only 4 or 2 when S > 2, only 8
-// or 4 when a thread owns several units) that still gives every resident
-// block about three batches to overlap; short matrices get 2-row batches.
+// or 4 when a thread owns several units) that gives every resident block at
+// least three batches to overlap with an even last wave (mean batches per
+// block >= 92% of the maximum), else the most even of those; short matrices
+// get 2-row batches.
 bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl);
 
 // Device address of this device's error word (cached per device).
@@ -462,9 +469,20 @@ void launch_tma(const typename F::Params &p, float *out, const TmaPlan &pl, cuda
     long resident = (long)num_sms() * per_sm / pl.splits;
     if (resident < 1) resident = 1;
     const int grid_x = pl.nrowb < resident ? pl.nrowb : (int)resident;
-    dim3 grid(grid_x, pl.splits);
-    kern<<<grid, threads, pl.L.total, st>>>(p, out, pl.units, pl.units_per_split, pl.nrowb, pl.nst, pl.L,
-                                            device_error_word());
+    // Programmatic dependent launch: the kernel may start while the previous
+    // kernel on the stream finishes (see griddep_wait).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_x, pl.splits);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = pl.L.total;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kern, p, out, pl.units, pl.units_per_split, pl.nrowb, pl.nst, pl.L,
+                       device_error_word());
 }
 
 }  // namespace qg

@@ -72,17 +72,6 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parit
     return false;
 }
 
-// mbar_wait_or_abort for a whole warp: lane 0 alone polls the barrier and the
-// other lanes wait at __syncwarp (polls from every lane of several warps
-// crowd the SM's barrier unit and slow every other barrier operation,
-// including the transaction counts of bulk copies).  Returns the result on
-// every lane; the warp must be converged.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait_or_abort(bar, parity, abort);
-    return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-}
-
 // As mbar_wait_or_abort, for long waits off the critical path (a warp that
 // waits for a whole tile): between tries the thread sleeps kBackoffNs, so it
 // takes almost no issue slots from the warps that work meanwhile.
@@ -115,6 +104,19 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream is still
+// running; it must execute griddep_wait() before it reads anything that
+// kernel wrote or writes anything that kernel reads (the wait returns once
+// the previous grid has completed and its memory is visible).  Work that
+// depends on neither (streaming the weights into shared memory) can be
+// issued before the wait.  griddep_launch_dependents() lets the next such
+// kernel start early.  Both are no-ops for a kernel launched normally.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Record a kernel-side failure (a wait that gave up) in the device error word
