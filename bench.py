@@ -54,6 +54,7 @@ SHAPES = [
     ("mq4v2_17408x5120", "mq4", 17408, 5120, 3),
 ]
 DOMINANT = "fmt7_24576x7168"
+DOM_EVERY = 16      # timed steps per sample of the dominant call's duration
 GS = 64
 
 
@@ -368,8 +369,12 @@ def ours_arm(args):
             step()
     barrier()
 
+    # The dominant call is bracketed by CUDA events on every DOM_EVERY-th
+    # timed step: an event between two calls stops the next call from
+    # starting early (programmatic dependent launch), so recording them on
+    # every step would slow the very step being measured.
     dom_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)]
+                  for _ in range(0, args.steps, DOM_EVERY)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
@@ -378,7 +383,7 @@ def ours_arm(args):
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for k in range(args.steps):
-            step(dom_events[k])
+            step(dom_events[k // DOM_EVERY] if k % DOM_EVERY == 0 else None)
         t_end.record(stream)
     barrier()
     clocks = sampler.stop()
@@ -426,6 +431,8 @@ def ours_arm(args):
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
 
     per_format = per_format_breakdown(qg, torch, calls, stream, hbm_peak) if args.breakdown else None
+    if per_format is not None:
+        per_format.update(batched_breakdown(qg, torch, calls, stream, hbm_peak, dev))
     prefill = prefill_measure(qg, torch, dev, stream) if args.prefill else None
 
     cpu = None
@@ -453,6 +460,7 @@ def ours_arm(args):
                          "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                          "traffic": load_traffic(), "algorithmic_bytes": dom_bytes,
                          "avg_launch_us": round(dom_ms * 1e3, 3),
+                         "launches_sampled": len(dom_events),
                          "peak_kind": f"{peak_kind} (copy bandwidth)"},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -571,6 +579,65 @@ def per_format_breakdown(qg, torch, calls, stream, hbm_peak):
         gbs = c["bytes"] / (best * 1e-3) / 1e9
         out[c["name"]] = {"us_per_call": round(best * 1e3, 3), "weight_gbs": round(gbs, 1),
                           "pct_hbm_peak": round(100 * gbs / hbm_peak, 1), "weight_copies": copies}
+    return out
+
+
+BATCHED = {"i4g": 4, "mq4": 8}     # the configs' batched decode cases: fmt4 at batch 4, MQ4-V2 at 8
+
+
+def batched_breakdown(qg, torch, calls, stream, hbm_peak, dev):
+    """Kernel-only time per call of the batched decode cases (fmt=4 batch 4,
+    MQ4-V2 batch 8, on the same two shapes each): as per_format_breakdown,
+    a CUDA graph of back-to-back calls cycling through >= 3x L2 of weight
+    copies; x ~ N(0, 1) (f32 for fmt=4, bf16 for MQ4-V2), seeded."""
+    out = {}
+    l2 = 129 * 2 ** 20
+    lib = qg._lib
+    st = stream.cuda_stream
+    for c in calls:
+        fmt = next((f for f in BATCHED if c["name"].startswith({"i4g": "fmt4", "mq4": "mq4"}[f])), None)
+        if fmt is None:
+            continue
+        S = BATCHED[fmt]
+        O, I = c["O"], c["I"]
+        g = torch.Generator(device=dev)
+        g.manual_seed(2000 + S)
+        xs = torch.randn(S, I, generator=g, device=dev)
+        x = xs if fmt == "i4g" else xs.to(torch.bfloat16).view(torch.int16)
+        y = torch.empty(S * O, dtype=torch.float32, device=dev)
+        n = qg.qg_workspace_bytes(4 if fmt == "i4g" else 44, S, I, O, GS)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        copies = min(64, max(1, -(-3 * l2 // c["bytes"])))
+        wcopies = [c["keep"]] + [tuple(t.clone() for t in c["keep"]) for _ in range(copies - 1)]
+        reps = max(copies, 60)
+        gr = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(gr, stream=stream):
+            for r in range(reps):
+                ps = wcopies[r % len(wcopies)]
+                if fmt == "i4g":
+                    rc = lib.qgemv_i4g(y.data_ptr(), x.data_ptr(), ps[0].data_ptr(), ps[1].data_ptr(), S, I, O, GS,
+                                       ws.data_ptr() if n else None, n, st)
+                else:
+                    rc = lib.qgemv_mq4v2(y.data_ptr(), x.data_ptr(), ps[0].data_ptr(), S, I, O,
+                                         ws.data_ptr() if n else None, n, st)
+                if rc:
+                    raise qg.QGError(rc)
+        best = None
+        for _ in range(4):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                gr.replay()
+                b.record(stream)
+            b.synchronize()
+            t = a.elapsed_time(b) / reps
+            best = t if best is None else min(best, t)
+        del gr, wcopies
+        gbs = c["bytes"] / (best * 1e-3) / 1e9
+        out[f"{c['name']}_batch{S}"] = {"us_per_call": round(best * 1e3, 3), "weight_gbs": round(gbs, 1),
+                                        "pct_hbm_peak": round(100 * gbs / hbm_peak, 1), "batch": S}
     return out
 
 
