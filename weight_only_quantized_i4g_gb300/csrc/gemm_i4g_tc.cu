@@ -16,13 +16,14 @@
 //               per K step 8 instructions of M=128, N=BT, K=16 with operand
 //               A read from tensor memory;
 //   warps 2-5   epilogue: accumulator -> registers -> Y (or a partial slot);
-//   warps 6-13  load the packed weights of the tile straight from global
+//   warps 6-21  load the packed weights of the tile straight from global
 //               memory (16-byte loads, three K steps ahead in registers),
 //               dequantize them and store the bf16 rows into a ring of A
 //               tiles in tensor memory (tcgen05.st): warp w covers the 32
-//               lanes (weight rows) its position allows and one 64-wide half
-//               of the K step.
-// One barrier per stage counts both the X bytes and the eight dequantizing
+//               lanes (weight rows) its position allows and one 32-wide
+//               quarter of the K step (four dequantizing warps per
+//               sub-partition hide each other's latency).
+// One barrier per stage counts both the X bytes and the sixteen dequantizing
 // warps, and one commit per step frees the stage: the MMA thread's waits and
 // commits cost ~200 cycles each, so they are kept to one of each per 1024
 // cycles of tensor-core work.
@@ -52,7 +53,7 @@ namespace tc {
 constexpr int kMmaM = 128;        // rows of one MMA (weight rows = outputs)
 constexpr int kBK = 128;          // K per stage: two 128-byte rows of bf16
 constexpr int kBKBox = 64;        // K of one 128-byte-swizzled box
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi = 2, kNumEpiWarps = 4, kWarpDeq = 6, kNumDeqWarps = 8;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi = 2, kNumEpiWarps = 4, kWarpDeq = 6, kNumDeqWarps = 16;
 constexpr int kThreads = 32 * (kWarpDeq + kNumDeqWarps);
 constexpr uint32_t kSmemBudget = 227 * 1024;
 constexpr int kPrefetch = 3;      // K steps of packed weights in flight per dequantizing thread
@@ -94,6 +95,17 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b_desc), "r"(accumulate), "r"(idesc));
 }
 
+// 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // 32 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
@@ -121,6 +133,38 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "[%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
         : "memory");
+}
+
+// As tma_load_2d, written to the same offset in the shared memory of every
+// block of the cluster in `mask`, each of whose barrier at `bar`'s offset
+// counts the bytes.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                                      uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "h"(mask)
+        : "memory");
+}
+
+// As mma_commit, arriving on the barrier at `bar`'s offset in every block of
+// the cluster in `mask`.
+__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_addr(bar)),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
 
 // 32 consecutive f32 columns of this warp's 32 tensor-memory lanes.
@@ -260,10 +304,26 @@ struct Args {
     float *partials;      // 2 slots per block
     int M, O, gs, ng, MB, Kt;
     int tail_half;        // the last K step of every tile is 64 wide (I % 128 == 64)
+    int cluster;          // pairs of blocks share X by multicast (one whole tile per block)
     long long rowbytes;   // I / 2
     long long U;          // (tile, K step) units
     int *err;
 };
+
+// Token block and output tile of tile index t.  Normally t = nb * MB + mb;
+// with clusters of two blocks the pair (2j, 2j+1) takes token block j % MB
+// and the neighbouring output tiles 2 (j / MB) and 2 (j / MB) + 1, so both
+// blocks stream the same X.
+__device__ __forceinline__ void tile_coords(long long t, int MB, int cluster, int &mb, int &nb) {
+    if (cluster) {
+        const long long j = t >> 1;
+        mb = (int)(j % MB);
+        nb = (int)(2 * (j / MB) + (t & 1));
+    } else {
+        mb = (int)(t % MB);
+        nb = (int)(t / MB);
+    }
+}
 
 // Segment of a block's range that starts at unit u: tile t, K steps [ks, ke).
 struct Seg {
@@ -276,6 +336,160 @@ __device__ __forceinline__ Seg segment_at(long long u, long long ue, int Kt) {
     g.ks = (int)(u - g.t * Kt);
     g.ke = (int)min(ue - g.t * Kt, (long long)Kt);
     return g;
+}
+
+// Epilogue of one segment (tile t, K steps [ks, ke)) of this block's range,
+// run by the four epilogue warps (one per tensor-memory lane quarter): wait
+// for the accumulator, then either store it to Y (the whole K range is this
+// block's) or go through the partial slots.  `et` numbers the 128
+// participating threads.
+template <int BT>
+__device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, const uint32_t seg, const uint32_t tmem,
+                                              const int q, const int lane, const int et, const long long cta,
+                                              const long long U, const long long P, const int Kt,
+                                              uint64_t *acc_full, uint64_t *acc_empty, volatile uint32_t *flag,
+                                              volatile uint32_t *abort, const int nslots) {
+    using C = Cfg<BT>;
+    const int row = q * 32 + lane;          // accumulator row = weight row within the tile
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    int mb, nb;
+    tile_coords(g.t, a.MB, a.cluster, mb, nb);
+    const int m0 = mb * BT, o = nb * kMmaM + row;
+    {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_backoff(acc_full, seg & 1, abort);
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) raise_device_error(a.err, kErrTimeout);
+    }
+    tc_fence_after();
+    auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+    };
+    // Column j of the accumulator is token m0 + j; lanes hold 32
+    // consecutive outputs, so each store of a warp is 128 bytes.
+    auto store_chunk = [&](int c, const float (&v)[16]) {
+        if (o < a.O) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int m = m0 + c * 16 + j;
+                if (m < a.M) a.Y[(size_t)m * a.O + o] = v[j];
+            }
+        }
+    };
+    if (g.ks == 0 && g.ke == Kt) {
+        // The whole K range is ours: straight to Y.  With nslots > 1 the
+        // dequantizing warps of this lane quarter take chunks 1, 2, ... of
+        // every nslots (store_tile_slice).
+#pragma unroll 1
+        for (int c = 0; c < BT / 16; c += nslots) {
+            uint32_t r[16];
+            tmem_ld16(tq + c * 16, r);
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+            store_chunk(c, v);
+        }
+        release();
+    } else {
+        const long long cf = sk::first_contributor(g.t, Kt, U, P);
+        const long long cl = sk::last_contributor(g.t, Kt, U, P);
+        const unsigned nc = (unsigned)(cl - cf + 1);
+        // Are all other contributors done already?  Then this block
+        // finishes the tile from its own accumulator and their slots.
+        if (et == 0) *flag = (ld_acquire_u32(&a.counters[g.t]) + 1 == nc) ? 1u : 0u;
+        named_sync(1, 32 * kNumEpiWarps);
+        const bool last_now = *flag != 0;
+        named_sync(1, 32 * kNumEpiWarps);
+        bool finish = last_now;
+        if (!last_now) {
+            // Park the partial sums ([token / 4][row] float4s), then count in.
+            float *mine = a.partials + (size_t)sk::partial_slot(cta, g.t, Kt, U, P) * C::kSlotFloats;
+#pragma unroll 1
+            for (int c = 0; c < BT / 16; ++c) {
+                uint32_t r[16];
+                tmem_ld16(tq + c * 16, r);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    stcg_f4(mine + ((size_t)(c * 4 + j) * kMmaM + row) * 4, r[4 * j], r[4 * j + 1],
+                            r[4 * j + 2], r[4 * j + 3]);
+            }
+            release();
+            __threadfence();
+            named_sync(1, 32 * kNumEpiWarps);
+            if (et == 0) *flag = (atomicAdd(&a.counters[g.t], 1u) + 1 == nc) ? 1u : 0u;
+            named_sync(1, 32 * kNumEpiWarps);
+            finish = *flag != 0;
+            if (finish) __threadfence();
+        }
+        if (finish) {
+            // Sum the contributors in order (the same order whichever
+            // block finishes), 16 tokens at a time, then store.
+            const long long slot_cf = sk::partial_slot(cf, g.t, Kt, U, P);
+#pragma unroll 1
+            for (int c = 0; c < BT / 16; ++c) {
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                for (long long cc = cf; cc <= cl; ++cc) {
+                    if (last_now && cc == cta) {   // warp-uniform
+                        uint32_t own[16];
+                        tmem_ld16(tq + c * 16, own);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(own[j]);
+                        continue;
+                    }
+                    // Every contributor after the first starts its range
+                    // inside this tile, so its slot is 2 * cc.
+                    const long long slot = cc == cf ? slot_cf : 2 * cc;
+                    const float *src = a.partials + (size_t)slot * C::kSlotFloats +
+                                       ((size_t)(c * 4) * kMmaM + row) * 4;
+                    float4 p[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) p[j] = ldcg_f4(src + (size_t)j * kMmaM * 4);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        v[4 * j] += p[j].x;
+                        v[4 * j + 1] += p[j].y;
+                        v[4 * j + 2] += p[j].z;
+                        v[4 * j + 3] += p[j].w;
+                    }
+                }
+                store_chunk(c, v);
+            }
+        }
+        if (last_now) release();
+    }
+}
+
+// The part of a whole tile's store that a dequantizing warp takes once its
+// block has no K steps left: chunks slot, slot + nslots, ... of its lane
+// quarter, after the accumulator is complete.
+template <int BT>
+__device__ __forceinline__ void store_tile_slice(const Args &a, const Seg g, const uint32_t tmem, const int q,
+                                                 const int lane, const int slot, const int nslots,
+                                                 uint64_t *acc_full, volatile uint32_t *abort) {
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait_backoff(acc_full, 0u, abort);
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) raise_device_error(a.err, kErrTimeout);
+    tc_fence_after();
+    int mb, nb;
+    tile_coords(g.t, a.MB, a.cluster, mb, nb);
+    const int o = nb * kMmaM + q * 32 + lane, m0 = mb * BT;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+    for (int c = slot; c < BT / 16; c += nslots) {
+        uint32_t r[16];
+        tmem_ld16(tq + c * 16, r);
+        if (o < a.O) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int m = m0 + c * 16 + j;
+                if (m < a.M) a.Y[(size_t)m * a.O + o] = __uint_as_float(r[j]);
+            }
+        }
+    }
+    tc_fence_before();
 }
 
 template <int BT>
@@ -295,9 +509,10 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        griddep_launch_dependents();
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1 + kNumDeqWarps);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], a.cluster ? 2 : 1);   // with a cluster: both blocks' MMAs
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kNumEpiWarps);
@@ -317,31 +532,61 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // With a cluster, the peer's copies and commits reach this block's
+    // barriers: both blocks initialize theirs first.
+    if (a.cluster) cluster_sync();
+    const uint32_t crank = a.cluster ? cluster_rank() : 0u;
 
     const long long P = gridDim.x, cta = blockIdx.x, U = a.U;
     const long long ub = sk::range_begin(cta, U, P), ue = sk::range_begin(cta + 1, U, P);
     const int Kt = a.Kt;
+    // A range that is exactly one whole tile: the dequantizing warps, idle
+    // after its last K step, help store it (5 warps per lane quarter).
+    const bool whole_only = ub % Kt == 0 && ue - ub == Kt;
+    constexpr int kEpiSlots = 1 + kNumDeqWarps / 4;
 
     if (warp == kWarpTma) {
+        // X may be the previous kernel's output (programmatic dependent
+        // launch): wait for it.  The packed weights, which nothing on the
+        // stream writes while this library's kernels overlap, stream in
+        // meanwhile.
+        griddep_wait();
         if (lane == 0) {
             uint32_t it = 0;
             for (long long u = ub; u < ue;) {
                 const Seg g = segment_at(u, ue, Kt);
-                const int m0 = (int)(g.t % a.MB) * BT;
+                int mb, nb;
+                tile_coords(g.t, a.MB, a.cluster, mb, nb);
+                const int m0 = mb * BT;
                 for (int k = g.ks; k < g.ke; ++k, ++it) {
                     const uint32_t s = it % C::kStages, r = it / C::kStages;
                     const bool half = a.tail_half && k == Kt - 1;
                     if (r > 0 && !mbar_wait_or_abort(&empty[s], (r & 1) ^ 1, abort))
                         raise_device_error(a.err, kErrTimeout);
                     mbar_arrive_expect_tx(&full[s], half ? C::kBoxBytes : C::kXBytes);
-                    tma_load_2d(sbase + s * C::kXBytes, &tmX, k * kBK, m0, &full[s]);
-                    if (!half) tma_load_2d(sbase + s * C::kXBytes + C::kBoxBytes, &tmX, k * kBK + kBKBox, m0, &full[s]);
+                    const uint32_t st = sbase + s * C::kXBytes;
+                    if (a.cluster) {
+                        // This block's half of the tokens, into both blocks.
+                        const uint32_t off = crank * (uint32_t)(BT / 2) * 128u;
+                        const int mr = m0 + (int)crank * (BT / 2);
+                        tma_load_2d_multicast(st + off, &tmX, k * kBK, mr, &full[s], 0x3);
+                        if (!half)
+                            tma_load_2d_multicast(st + C::kBoxBytes + off, &tmX, k * kBK + kBKBox, mr, &full[s], 0x3);
+                    } else {
+                        tma_load_2d(st, &tmX, k * kBK, m0, &full[s]);
+                        if (!half) tma_load_2d(st + C::kBoxBytes, &tmX, k * kBK + kBKBox, m0, &full[s]);
+                    }
                 }
                 u = g.t * Kt + g.ke;
             }
-            // Every copy issued must have landed before the block exits.
-            for (uint32_t j = it > (uint32_t)C::kStages ? it - C::kStages : 0; j < it; ++j)
+            // Every copy issued must have landed before the block exits, and
+            // with a cluster every commit of the peer's MMAs must have
+            // arrived here too.
+            for (uint32_t j = it > (uint32_t)C::kStages ? it - C::kStages : 0; j < it; ++j) {
                 if (!mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1)) raise_device_error(a.err, kErrTimeout);
+                if (a.cluster && !mbar_wait(&empty[j % C::kStages], (j / C::kStages) & 1))
+                    raise_device_error(a.err, kErrTimeout);
+            }
         }
     } else if (warp == kWarpMma) {
         if (lane == 0) {
@@ -363,143 +608,41 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
                         if (kk < nk)
                             mma_bf16_ts(tmem, at + kk * 8, sw128_desc(xa + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32),
                                         C::kIdesc, (k > g.ks || kk > 0) ? 1u : 0u);
-                    mma_commit(&empty[s]);
+                    if (a.cluster)
+                        mma_commit_multicast(&empty[s], 0x3);   // frees the stage in both blocks
+                    else
+                        mma_commit(&empty[s]);
                 }
                 mma_commit(acc_full);
                 u = g.t * Kt + g.ke;
             }
         }
     } else if (warp < kWarpEpi + kNumEpiWarps) {
-        const int q = warp & 3;                 // tensor-memory lane quarter of this warp
-        const int row = q * 32 + lane;          // accumulator row = weight row within the tile
-        const int et = threadIdx.x - 32 * kWarpEpi;
-        const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+        // Epilogue of every segment of the range, in order (Y, the
+        // counters and the partial slots only after the previous kernel).
+        griddep_wait();
         uint32_t seg = 0;
         for (long long u = ub; u < ue; ++seg) {
             const Seg g = segment_at(u, ue, Kt);
-            const int m0 = (int)(g.t % a.MB) * BT, o = (int)(g.t / a.MB) * kMmaM + row;
-            {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_backoff(acc_full, seg & 1, abort);
-                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) raise_device_error(a.err, kErrTimeout);
-            }
-            tc_fence_after();
-            auto release = [&]() {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
-            };
-            // Column j of the accumulator is token m0 + j; lanes hold 32
-            // consecutive outputs, so each store of a warp is 128 bytes.
-            auto store_chunk = [&](int c, const float (&v)[32]) {
-                if (o < a.O) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int m = m0 + c * 32 + j;
-                        if (m < a.M) a.Y[(size_t)m * a.O + o] = v[j];
-                    }
-                }
-            };
-            if (g.ks == 0 && g.ke == Kt) {
-                // The whole K range is ours: straight to Y.
-#pragma unroll 1
-                for (int c = 0; c < BT / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tq + c * 32, r);
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    store_chunk(c, v);
-                }
-                release();
-            } else {
-                const long long cf = sk::first_contributor(g.t, Kt, U, P);
-                const long long cl = sk::last_contributor(g.t, Kt, U, P);
-                const unsigned nc = (unsigned)(cl - cf + 1);
-                // Are all other contributors done already?  Then this block
-                // finishes the tile from its own accumulator and their slots.
-                if (et == 0) *flag = (ld_acquire_u32(&a.counters[g.t]) + 1 == nc) ? 1u : 0u;
-                named_sync(1, 32 * kNumEpiWarps);
-                const bool last_now = *flag != 0;
-                named_sync(1, 32 * kNumEpiWarps);
-                bool finish = last_now;
-                if (!last_now) {
-                    // Park the partial sums ([token / 4][row] float4s), then count in.
-                    float *mine = a.partials + (size_t)sk::partial_slot(cta, g.t, Kt, U, P) * C::kSlotFloats;
-#pragma unroll 1
-                    for (int c = 0; c < BT / 16; ++c) {
-                        uint32_t r[16];
-                        tmem_ld16(tq + c * 16, r);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            stcg_f4(mine + ((size_t)(c * 4 + j) * kMmaM + row) * 4, r[4 * j], r[4 * j + 1],
-                                    r[4 * j + 2], r[4 * j + 3]);
-                    }
-                    release();
-                    __threadfence();
-                    named_sync(1, 32 * kNumEpiWarps);
-                    if (et == 0) *flag = (atomicAdd(&a.counters[g.t], 1u) + 1 == nc) ? 1u : 0u;
-                    named_sync(1, 32 * kNumEpiWarps);
-                    finish = *flag != 0;
-                    if (finish) __threadfence();
-                }
-                if (finish) {
-                    // Sum the contributors in order (the same order whichever
-                    // block finishes), 32 tokens at a time, then store.
-                    const long long slot_cf = sk::partial_slot(cf, g.t, Kt, U, P);
-#pragma unroll 1
-                    for (int c = 0; c < BT / 32; ++c) {
-                        float v[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                        for (long long cc = cf; cc <= cl; ++cc) {
-                            if (last_now && cc == cta) {   // warp-uniform
-                                uint32_t own[32];
-                                tmem_ld32(tq + c * 32, own);
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] += __uint_as_float(own[j]);
-                                continue;
-                            }
-                            // Every contributor after the first starts its range
-                            // inside this tile, so its slot is 2 * cc.
-                            const long long slot = cc == cf ? slot_cf : 2 * cc;
-                            const float *src = a.partials + (size_t)slot * C::kSlotFloats +
-                                               ((size_t)(c * 8) * kMmaM + row) * 4;
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                float4 p[4];
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) p[j] = ldcg_f4(src + (size_t)(4 * h + j) * kMmaM * 4);
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) {
-                                    v[16 * h + 4 * j] += p[j].x;
-                                    v[16 * h + 4 * j + 1] += p[j].y;
-                                    v[16 * h + 4 * j + 2] += p[j].z;
-                                    v[16 * h + 4 * j + 3] += p[j].w;
-                                }
-                            }
-                        }
-                        store_chunk(c, v);
-                    }
-                }
-                if (last_now) release();
-            }
+            epilogue_segment<BT>(a, g, seg, tmem, warp & 3, lane, threadIdx.x - 32 * kWarpEpi, cta, U, P, Kt,
+                                 acc_full, acc_empty, flag, abort, whole_only ? kEpiSlots : 1);
             u = g.t * Kt + g.ke;
         }
     } else {
         // Dequantize.  Warp w may write tensor-memory lanes 32*(w % 4) ..
-        // +31 (weight rows of the tile); the two warps of a lane quarter
-        // split each K step into halves kh = 0, 1 of 64 weights (32 bytes).
-        const int q = warp & 3, kh = (warp - kWarpDeq) >> 2;
+        // +31 (weight rows of the tile); the four warps of a lane quarter
+        // split each K step into quarters kq = 0..3 of 32 weights (16 bytes),
+        // so every sub-partition holds four dequantizing warps.
+        const int q = warp & 3, kq = (warp - kWarpDeq) >> 2;
         const int R = q * 32 + lane;
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + C::kACol0 + kh * (C::kACols / 2);
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + C::kACol0 + kq * (C::kACols / 4);
         struct Fetch {
-            uint4 q[2];
-            float s[2];
+            uint4 q;
+            float s;
         };
         // Fetch state: the next unit to load, this row's pointers, and the
-        // scale group of this thread's first 32-weight quarter, advanced
-        // without divisions (one division per tile change).
+        // scale group of this thread's 32-weight quarter, advanced without
+        // divisions (one division per tile change).
         long long pu = ub, pt = ub / Kt;
         int pk = (int)(ub - pt * Kt);
         const int gq = a.gs / 32;   // 32-weight quarters per scale group
@@ -507,24 +650,24 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         const float *srow = nullptr;
         int gi = 0, gr = 0;
         auto set_tile = [&]() {
-            const int o = (int)(pt / a.MB) * kMmaM + R;
-            wrow = o < a.O ? a.w + (size_t)o * a.rowbytes + kh * 32 : nullptr;
+            int mb, nb;
+            tile_coords(pt, a.MB, a.cluster, mb, nb);
+            const int o = nb * kMmaM + R;
+            wrow = o < a.O ? a.w + (size_t)o * a.rowbytes + kq * 16 : nullptr;
             srow = o < a.O ? a.scales + (size_t)o * a.ng : nullptr;
-            const int u0 = 4 * pk + 2 * kh;
+            const int u0 = 4 * pk + kq;
             gi = u0 / gq;
             gr = u0 - gi * gq;
         };
         if (pu < ue) set_tile();
         auto fetch = [&](Fetch &f) {
-            f.q[0] = f.q[1] = make_uint4(0u, 0u, 0u, 0u);
-            f.s[0] = f.s[1] = 0.f;
+            f.q = make_uint4(0u, 0u, 0u, 0u);
+            f.s = 0.f;
             if (pu < ue) {
-                // The 64-wide last step of a row with I % 128 == 64 has no second half.
-                if (wrow && !(kh == 1 && a.tail_half && pk == Kt - 1)) {
-                    f.q[0] = ldg_w16(wrow + pk * 64);
-                    f.q[1] = ldg_w16(wrow + pk * 64 + 16);
-                    f.s[0] = __ldg(srow + gi);
-                    f.s[1] = __ldg(srow + gi + (gr + 1 >= gq ? 1 : 0));
+                // The 64-wide last step of a row with I % 128 == 64 has no upper half.
+                if (wrow && !(kq >= 2 && a.tail_half && pk == Kt - 1)) {
+                    f.q = ldg_w16(wrow + pk * 64);
+                    f.s = __ldg(srow + gi);
                 }
                 ++pu;
                 if (++pk == Kt) {
@@ -545,20 +688,17 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
             const uint32_t s = it % C::kStages, r = it / C::kStages;
             if (r > 0 && !mbar_wait_or_abort(&empty[s], (r & 1) ^ 1, abort)) raise_device_error(a.err, kErrTimeout);
             tc_fence_after();
-            uint32_t col[32];
+            uint32_t col[16];
+            const ScalePairs sp = scale_pairs(cur.s);
+            const uint32_t wv[4] = {cur.q.x, cur.q.y, cur.q.z, cur.q.w};
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const ScalePairs sp = scale_pairs(cur.s[i]);
-                const uint32_t wv[4] = {cur.q[i].x, cur.q[i].y, cur.q[i].z, cur.q[i].w};
+            for (int j = 0; j < 4; ++j) {
+                uint32_t o4[4];
+                dequant_word(wv[j], sp, o4);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t o4[4];
-                    dequant_word(wv[j], sp, o4);
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) col[16 * i + 4 * j + p] = o4[p];
-                }
+                for (int p = 0; p < 4; ++p) col[4 * j + p] = o4[p];
             }
-            tmem_st32(ta + s * C::kACols, col);
+            tmem_st16(ta + s * C::kACols, col);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[s]);
@@ -582,10 +722,15 @@ gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
             fetch(f2);
             ++u;
         }
+        if (whole_only) {
+            griddep_wait();
+            store_tile_slice<BT>(a, segment_at(ub, ue, Kt), tmem, q, lane, 1 + kq, kEpiSlots, acc_full, abort);
+        }
     }
 
     tc_fence_before();
     __syncthreads();
+    if (a.cluster) cluster_sync();   // the peer no longer writes into this block
     if (warp == kWarpMma) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols)
@@ -618,6 +763,7 @@ constexpr int kTileBT[kNumTiles] = {256, 128, 64};
 
 struct Plan {
     int tile, bt, MB, NB, Kt, P;
+    int cluster;          // whole tiles in pairs sharing X by multicast
     long long T, U;
     size_t counter_bytes, ws_bytes;
 };
@@ -634,6 +780,11 @@ Plan make_plan(int tile, int M, int I, int O, int nsm) {
     // One tile per block when the tiles fit in one wave; otherwise an even
     // split of the units over all SMs.
     p.P = (int)std::min<long long>(p.T <= nsm ? p.T : nsm, p.U);
+    // Pairs of whole tiles sharing X by multicast (cluster = 1) measured no
+    // faster on GB300: the bytes each SM receives per K step, not the copies
+    // it issues, bound the step, and multicast leaves those unchanged.  The
+    // planner does not pick it.
+    p.cluster = 0;
     p.counter_bytes = ((size_t)p.T * sizeof(unsigned) + 255) & ~(size_t)255;
     p.ws_bytes = p.counter_bytes + (size_t)2 * p.P * kMmaM * p.bt * sizeof(float);
     return p;
@@ -645,7 +796,7 @@ Plan make_plan(int tile, int M, int I, int O, int nsm) {
 // K range is split over blocks costs ~14000 cycles per contributor for the
 // partial sums (written, then read back by the block that finishes it).
 double plan_cost(const Plan &p) {
-    const double step = p.bt == 256 ? 2300.0 : 2150.0;
+    const double step = (p.bt == 256 ? 2300.0 : 2150.0) * (p.cluster ? 0.75 : 1.0);
     const double steps = (double)((p.U + p.P - 1) / p.P);
     const bool split = (p.U / p.P) % p.Kt != 0 || p.U % p.P != 0;
     const double contributors = (double)p.Kt / std::max(1.0, (double)(p.U / p.P)) + 1.0;
@@ -664,6 +815,7 @@ Plan choose_plan(int M, int I, int O) {
             if (mode == 1) {
                 if (p.T >= nsm) continue;   // already the split over all SMs
                 p.P = (int)std::min<long long>(nsm, p.U);
+                p.cluster = 0;
                 p.ws_bytes = p.counter_bytes + (size_t)2 * p.P * kMmaM * p.bt * sizeof(float);
             }
             const double c = plan_cost(p);
@@ -686,7 +838,21 @@ int launch_tile(const Plan &p, const CUtensorMap &tmX, const Args &args, cudaStr
         cudaFuncSetAttribute(gemm_i4g_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::kSmemBytes);
     });
-    gemm_i4g_tc_kernel<BT><<<p.P, kThreads, C::kSmemBytes, st>>>(tmX, args);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.P);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.cluster ? 2 : 1;
+    cudaLaunchKernelEx(&cfg, gemm_i4g_tc_kernel<BT>, tmX, args);
     return check_launch("qgemm_i4g (tensor-core kernel)");
 }
 
@@ -700,7 +866,7 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, const uint8_t *w, co
     CUtensorMap tmX;
     const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)I * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBKBox, (cuuint32_t)p.bt};
+    const cuuint32_t box[2] = {(cuuint32_t)kBKBox, (cuuint32_t)(p.cluster ? p.bt / 2 : p.bt)};
     const cuuint32_t es[2] = {1, 1};
     CUresult r = encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -722,10 +888,13 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, const uint8_t *w, co
     args.MB = p.MB;
     args.Kt = p.Kt;
     args.tail_half = (I % kBK) != 0 ? 1 : 0;
+    args.cluster = p.cluster;
     args.rowbytes = I / 2;
     args.U = p.U;
     args.err = device_error_word();
-    if (cudaMemsetAsync(ws, 0, (size_t)p.T * sizeof(unsigned), st) != cudaSuccess)
+    // Tile counters are only read when a tile's K range is split over blocks.
+    const bool split = !(p.U % p.P == 0 && (p.U / p.P) % p.Kt == 0);
+    if (split && cudaMemsetAsync(ws, 0, (size_t)p.T * sizeof(unsigned), st) != cudaSuccess)
         return check_launch("qgemm_i4g (counter reset)");
     switch (p.tile) {
         case kT256: return launch_tile<256>(p, tmX, args, st);
