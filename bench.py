@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -480,14 +481,74 @@ PREFILL_M, PREFILL_I = 512, 7168
 PREFILL_O = (7168, 2048)
 
 
-def prefill_measure(qg, torch, dev, stream, reps=20):
+def _time_alone(fn, flush, stream, reps, torch):
+    """Median device time (s) of fn() on `stream`, each call after a write
+    that flushes L2, bracketed by CUDA events on the same stream."""
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts) * 1e-3
+
+
+def _prefill_inputs(qg, torch, dev, stream, fmt, O, I, M):
+    """Seeded device inputs of one prefill GEMM shape: the decode workloads'
+    weight recipes (fmt=4 quantized N(0, 0.02); fmt=7 uniform e4m3 codes
+    without the NaN codes and log-uniform [1e-4, 1e-2] block scales; MQ4-V2
+    N(0, 0.02) rotated by the seeded sign-FWHT and encoded) and bf16 N(0, 1)
+    activations (rotated for MQ4-V2).  Returns the launch closure's args."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(4000 + O + 7 * I)
+    if fmt == "i4g":
+        w = torch.randn(O, I, generator=g, device=dev) * 0.02
+        wq = torch.empty(O * I // 2, dtype=torch.uint8, device=dev)
+        sc = torch.empty(O * (I // GS), dtype=torch.float32, device=dev)
+        qg.check(qg.qg_quantize_i4g(wq, sc, w, O, I, GS, stream=stream))
+        del w
+        weights = (wq, sc)
+    elif fmt == "fp8":
+        codes = torch.randint(0, 254, (O * I,), generator=g, device=dev, dtype=torch.int32)
+        codes = (codes + (codes >= 0x7F).to(torch.int32)).to(torch.uint8)   # skip 0x7F; 0xFF unreachable
+        nbo, nbi = -(-O // 128), -(-I // 128)
+        u = torch.rand(nbo * nbi, generator=g, device=dev, dtype=torch.float64)
+        sc = torch.exp(math.log(1e-4) + u * (math.log(1e-2) - math.log(1e-4))).to(torch.float32)
+        weights = (codes, sc)
+    else:
+        signs = (torch.randint(0, 2, (256,), generator=g, device=dev, dtype=torch.int32) * 2 - 1).to(torch.int8)
+        w = torch.randn(O, I, generator=g, device=dev) * 0.02
+        qg.check(qg.qg_fwht256(w, w, signs, O * I // 256, stream=stream))
+        blocks = torch.empty(O * (I // 256) * 136, dtype=torch.uint8, device=dev)
+        qg.check(qg.qg_encode_mq4v2(blocks, w, O, I, stream=stream))
+        del w
+        weights = (blocks, signs)
+    g.manual_seed(5000 + O + 7 * I)
+    x = torch.randn(M, I, generator=g, device=dev)
+    if fmt == "mq4":
+        qg.check(qg.qg_fwht256(x, x, weights[1], M * I // 256, stream=stream))
+    X = x.to(torch.bfloat16).view(torch.int16)
+    return weights, X
+
+
+PREFILL_OTHER = (("fp8", 7168, 16384), ("fp8", 24576, 7168), ("mq4", 5120, 17408), ("mq4", 17408, 5120))
+FMT_ID = {"i4g": 4, "fp8": 7, "mq4": 44}
+
+
+def prefill_measure(qg, torch, dev, stream, reps=20, other=True):
     """The fmt=4 batched-prefill GEMM of the workload's prefill config:
-    Y[512, O] = X[512, 7168] . W^T for O = 7168 and 2048, gs = 64.  Weights
-    N(0, 0.02) quantized on the device by qg_quantize_i4g, X N(0, 1) in
-    bf16, both from seeded generators.  Each call is timed alone with CUDA
-    events on its stream after a 256 MiB write that flushes L2; median of
-    `reps`.  Returns TFLOP/s (2*M*I*O per call) and the fraction of the
-    measured dense bf16 peak."""
+    Y[512, O] = X[512, 7168] . W^T for O = 7168 and 2048, gs = 64, plus the
+    fmt=7 and MQ4-V2 prefill GEMMs at M = 512 on their decode shapes
+    ("other_formats").  Weights and activations from seeded generators on
+    the device.  Each call is timed alone with CUDA events on its stream
+    after a 256 MiB write that flushes L2; median of `reps`.  Returns TFLOP/s
+    (2*M*I*O per call) and the fraction of the measured dense bf16 peak."""
     peak, kind = load_tensor_peak()
     M, I = PREFILL_M, PREFILL_I
     out = {"workload": f"fmt4 int4-g64 prefill GEMM, M={M}, I={I}, O in {list(PREFILL_O)}, "
@@ -495,37 +556,29 @@ def prefill_measure(qg, torch, dev, stream, reps=20):
            "bound": "tensor", "peak": peak, "unit": "TFLOP/s", "peak_kind": kind, "calls": {}}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     launches = 0
+
+    def run_one(fmt, O, I):
+        nonlocal launches
+        weights, X = _prefill_inputs(qg, torch, dev, stream, fmt, O, I, M)
+        Y = torch.empty(M * O, dtype=torch.float32, device=dev)
+        n = qg.qg_gemm_workspace_bytes(FMT_ID[fmt], M, I, O, GS if fmt == "i4g" else 0)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        if fmt == "i4g":
+            fn = lambda: qg.check(qg.qgemm_i4g(Y, X, weights[0], weights[1], M, I, O, GS, ws, n, stream=stream))
+        elif fmt == "fp8":
+            fn = lambda: qg.check(qg.qgemm_fp8b128(Y, X, weights[0], weights[1], M, I, O, ws, n, stream=stream))
+        else:
+            fn = lambda: qg.check(qg.qgemm_mq4v2(Y, X, weights[0], M, I, O, ws, n, stream=stream))
+        t = _time_alone(fn, flush, stream, reps, torch)
+        launches += reps
+        tf = 2.0 * M * I * O / t / 1e12
+        return {"us": round(t * 1e6, 2), "tflops": round(tf, 1), "frac": round(tf / peak, 4)}
+
     with torch.cuda.stream(stream):
         for O in PREFILL_O:
-            g = torch.Generator(device=dev)
-            g.manual_seed(4000 + O)
-            w = torch.randn(O, I, generator=g, device=dev) * 0.02
-            wq = torch.empty(O * I // 2, dtype=torch.uint8, device=dev)
-            sc = torch.empty(O * (I // GS), dtype=torch.float32, device=dev)
-            qg.check(qg.qg_quantize_i4g(wq, sc, w, O, I, GS, stream=stream))
-            del w
-            g.manual_seed(5000 + O)
-            X = torch.randn(M, I, generator=g, device=dev).to(torch.bfloat16).view(torch.int16)
-            Y = torch.empty(M * O, dtype=torch.float32, device=dev)
-            n = qg.qg_gemm_workspace_bytes(qg.QG_FMT_I4G, M, I, O, GS)
-            ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
-            for _ in range(3):
-                qg.check(qg.qgemm_i4g(Y, X, wq, sc, M, I, O, GS, ws, n, stream=stream))
-            ts = []
-            for _ in range(reps):
-                flush.fill_(1)
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                qg.check(qg.qgemm_i4g(Y, X, wq, sc, M, I, O, GS, ws, n, stream=stream))
-                b.record(stream)
-                b.synchronize()
-                ts.append(a.elapsed_time(b))
-                launches += 1
-            t = statistics.median(ts) * 1e-3
-            tf = 2.0 * M * I * O / t / 1e12
-            out["calls"][f"{M}x{O}x{I}"] = {"us": round(t * 1e6, 2), "tflops": round(tf, 1),
-                                             "frac": round(tf / peak, 4)}
+            out["calls"][f"{M}x{O}x{I}"] = run_one("i4g", O, I)
+        if other:
+            out["other_formats"] = {f"{fmt} {M}x{O}x{I2}": run_one(fmt, O, I2) for fmt, O, I2 in PREFILL_OTHER}
     tot_flop = sum(2.0 * M * I * O for O in PREFILL_O)
     tot_t = sum(c["us"] for c in out["calls"].values()) * 1e-6
     out["achieved"] = round(tot_flop / tot_t / 1e12, 1)

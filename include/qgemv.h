@@ -87,11 +87,12 @@ enum { QG_FMT_I4G = 4, QG_FMT_FP8B128 = 7, QG_FMT_MQ4V2 = 44 };
 size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs);
 
 /* Bytes of workspace that the batched-prefill GEMM entry point of format
- * `fmt` (qgemm_i4g for QG_FMT_I4G) needs for an M x I x O call on the
- * current device: tile counters plus two f32 partial-sum slots of 256 x 256
- * per thread block, for tiles whose K range is shared by several blocks.
- * 0 when the shape runs the general kernel (no workspace) or the arguments
- * are invalid. */
+ * `fmt` (qgemm_i4g, qgemm_fp8b128, qgemm_mq4v2) needs for an M x I x O call
+ * on the current device: the fp16 copy of X (2*M*I bytes), one exponent per
+ * token row and per weight row, tile counters, and, when tiles' K ranges
+ * are shared by several blocks, two f32 partial-sum slots of up to
+ * 128 x 256 per thread block.  0 when the shape runs the general kernel (no
+ * workspace) or the arguments are invalid.  `gs` is only read for fmt=4. */
 size_t qg_gemm_workspace_bytes(int fmt, int M, int I, int O, int gs);
 
 /* ------------------------------------------------------------------------ */
@@ -174,19 +175,64 @@ int qgemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks,
 /* colibri PR #457, section 4 (the large-batch GEMM path takes the same     */
 /* grouped layout as the GEMV).                                             */
 /*                                                                          */
-/*   Y[M, O] f32 = X[M, I] (bf16 bits) . W^T, W as in qgemv_i4g.  The       */
-/*   weight tile is dequantized to bf16 ((n-8)*scale rounded to nearest     */
-/*   even) in shared memory and contracted with f32 accumulation.           */
+/*   Y[M, O] f32 = X[M, I] (bf16 bits) . W^T, W as in qgemv_i4g.  The      */
+/*   tensor-core path contracts fp16 operands with f32 accumulation: each   */
+/*   weight (n-8)*scale is formed in f32 and rounded to 11 significant bits */
+/*   (nearest even), X is exact; powers of two per weight row and per token */
+/*   row keep both in fp16's range and are undone exactly at the store.     */
+/*   Every output is within 2^-11 (plus f32 summation error) of             */
+/*   sum_i |w_i x_i|, for elements of X within 2^29 of their row's largest  */
+/*   finite |x| and weights within 2^29 of their row's bound                */
+/*   (8 max_g |scale_g|).                                                   */
 /*   Any M >= 1.  The tensor-core path takes I % 64 == 0, gs % 32 == 0 and  */
 /*   16-byte aligned X and w, and needs a 256-byte aligned workspace of     */
 /*   qg_gemm_workspace_bytes(QG_FMT_I4G, M, I, O, gs) bytes (QG_EWORKSPACE  */
-/*   otherwise); other shapes run a general CUDA-core kernel and ignore ws. */
+/*   otherwise: it holds the fp16 copy of X, 2*M*I bytes, plus per-row      */
+/*   exponents and the split-tile scratch); other shapes run a general      */
+/*   CUDA-core kernel with f32 weights and ignore ws.                       */
 /*   The work is split evenly over one thread block per SM; a tile shared   */
 /*   by several blocks is summed in a fixed order, so repeated calls give   */
 /*   identical results.                                                     */
 /* ------------------------------------------------------------------------ */
 int qgemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales,
               int M, int I, int O, int gs, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* fmt=7 batched prefill dequant-GEMM on the tensor cores                   */
+/* colibri PR #528, section "Design" (the same block-scaled product as the  */
+/* GEMV, over M tokens).                                                    */
+/*                                                                          */
+/*   Y[M, O] f32 = X[M, I] (bf16 bits) . W^T, w and scale_inv as in         */
+/*   qgemv_fp8b128.  Each weight e4m3(code) * scale is formed in f32 and    */
+/*   rounded to fp16 as in qgemm_i4g (row bound 448 max_k |scale_inv|).     */
+/*   A NaN code makes its output column Y[:, o] NaN.                        */
+/*   Any M >= 1.  The tensor-core path takes I % 64 == 0 and 16-byte        */
+/*   aligned X and w, and needs a 256-byte aligned workspace of             */
+/*   qg_gemm_workspace_bytes(QG_FMT_FP8B128, M, I, O, 0) bytes              */
+/*   (QG_EWORKSPACE otherwise); other shapes run a general CUDA-core kernel */
+/*   and ignore ws.  Deterministic like qgemm_i4g.                          */
+/* ------------------------------------------------------------------------ */
+int qgemm_fp8b128(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv,
+                  int M, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* MQ4-V2 batched prefill dequant-GEMM on the tensor cores                  */
+/* hipfire "MQ4 V2", sections 2 and 4 (the same decoder as the GEMV, over   */
+/* M tokens).                                                               */
+/*                                                                          */
+/*   Y[M, O] f32 = X[M, I] (bf16 bits) . W^T, blocks as in qgemv_mq4v2.     */
+/*   Each weight q * scale + zero is formed in f32 with one rounding (fused */
+/*   multiply-add) and rounded to fp16 as in qgemm_i4g (row bound           */
+/*   max_h |zero_h| + 15 |scale_h|); f32 accumulation.                      */
+/*   I % 256 == 0 (else QG_ESHAPE); blocks 8-byte, X 2-byte, Y 4-byte       */
+/*   aligned.  A 16-byte aligned X takes the tensor-core path, which needs  */
+/*   a 256-byte aligned workspace of                                        */
+/*   qg_gemm_workspace_bytes(QG_FMT_MQ4V2, M, I, O, 0) bytes (QG_EWORKSPACE */
+/*   otherwise); other X run a general CUDA-core kernel and ignore ws.      */
+/*   Deterministic like qgemm_i4g.                                          */
+/* ------------------------------------------------------------------------ */
+int qgemm_mq4v2(float *Y, const uint16_t *X, const uint8_t *blocks,
+                int M, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Weight preparation on the device (not on the decode path)                */

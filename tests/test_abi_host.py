@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_lists_the_entry_points():
     names = declared_functions()
-    for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qg_workspace_bytes", "qg_gemm_workspace_bytes", "qg_device_status",
+    for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qgemm_fp8b128", "qgemm_mq4v2",
+                 "qg_workspace_bytes", "qg_gemm_workspace_bytes", "qg_device_status",
                  "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256"]:
         assert must in names, names
 
@@ -96,6 +97,14 @@ def test_gemm_and_prep_refusals(qg):
     P = POISON
     assert qg.qgemm_i4g(P, P, P, P, 0, 64, 64, 64, stream=0) == qg.QG_EINVAL
     assert qg.qgemm_i4g(P, P, P, P, 4, 64, 64, 7, stream=0) == qg.QG_EGS
+    assert qg.qgemm_fp8b128(P, P, P, P, 4, 0, 64, stream=0) == qg.QG_EINVAL
+    assert qg.qgemm_fp8b128(P, P, 0, P, 4, 64, 64, stream=0) == qg.QG_EINVAL
+    assert qg.qgemm_fp8b128(P, P + 1, P, P, 4, 64, 64, stream=0) == qg.QG_EALIGN
+    assert qg.qgemm_fp8b128(P, P, P, P + 2, 4, 64, 64, stream=0) == qg.QG_EALIGN
+    assert qg.qgemm_mq4v2(P, P, P, 4, 300, 64, stream=0) == qg.QG_ESHAPE
+    assert qg.qgemm_mq4v2(P, P, P + 4, 4, 256, 64, stream=0) == qg.QG_EALIGN
+    assert qg.qgemm_mq4v2(P, P, P, 4, 256, 64, ws=P + 16, stream=0) == qg.QG_EALIGN
+    assert qg.qgemm_mq4v2(P, P, P, 4, 256, 0, stream=0) == qg.QG_EINVAL
     assert qg.qg_quantize_i4g(P, P, P, 4, 64, 5, stream=0) == qg.QG_EGS
     assert qg.qg_encode_mq4v2(P, P, 4, 100, stream=0) == qg.QG_ESHAPE
     assert qg.qg_fwht256(P, P, P, 0, stream=0) == qg.QG_EINVAL
@@ -112,3 +121,15 @@ def test_workspace_query_is_pure(qg):
     # invalid arguments -> 0
     assert qg.qg_workspace_bytes(qg.QG_FMT_MQ4V2, 1, 300, 4) == 0
     assert qg.qg_workspace_bytes(99, 1, 256, 4) == 0
+
+
+def test_gemm_workspace_query(qg):
+    # tensor-core shapes of every format: counters + partial slots, 256-byte multiple
+    for fmt, gs in ((qg.QG_FMT_I4G, 64), (qg.QG_FMT_FP8B128, 0), (qg.QG_FMT_MQ4V2, 0)):
+        n = qg.qg_gemm_workspace_bytes(fmt, 512, 7168, 2048, gs)
+        assert n > 0 and n % 256 == 0, (fmt, n)
+    # shapes that run the general kernel need none
+    assert qg.qg_gemm_workspace_bytes(qg.QG_FMT_I4G, 64, 1000, 256, 64) == 0
+    assert qg.qg_gemm_workspace_bytes(qg.QG_FMT_FP8B128, 64, 1000, 256) == 0
+    assert qg.qg_gemm_workspace_bytes(qg.QG_FMT_MQ4V2, 64, 300, 256) == 0
+    assert qg.qg_gemm_workspace_bytes(qg.QG_FMT_MQ4V2, 0, 256, 256) == 0

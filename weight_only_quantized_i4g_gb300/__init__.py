@@ -42,6 +42,8 @@ _SIGNATURES = {
     "qgemv_fp8b128": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_mq4v2": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemm_fp8b128": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemm_mq4v2": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qg_quantize_i4g": ([_P, _P, _P, _I, _I, _I, _P], _I),
     "qg_encode_mq4v2": ([_P, _P, _I, _I, _P], _I),
     "qg_fwht256": ([_P, _P, _P, _Z, _P], _I),
@@ -131,6 +133,15 @@ def qgemv_mq4v2(y, x, blocks, S, I, O, ws=None, ws_bytes=0, stream=None) -> int:
 def qgemm_i4g(Y, X, w, scales, M, I, O, gs, ws=None, ws_bytes=0, stream=None) -> int:
     return _lib.qgemm_i4g(_ptr(Y), _ptr(X), _ptr(w), _ptr(scales), M, I, O, gs, _ptr(ws), ws_bytes,
                           _stream(stream))
+
+
+def qgemm_fp8b128(Y, X, w, scale_inv, M, I, O, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemm_fp8b128(_ptr(Y), _ptr(X), _ptr(w), _ptr(scale_inv), M, I, O, _ptr(ws), ws_bytes,
+                              _stream(stream))
+
+
+def qgemm_mq4v2(Y, X, blocks, M, I, O, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemm_mq4v2(_ptr(Y), _ptr(X), _ptr(blocks), M, I, O, _ptr(ws), ws_bytes, _stream(stream))
 
 
 def qg_quantize_i4g(wq, scales, w, O, I, gs, stream=None) -> int:

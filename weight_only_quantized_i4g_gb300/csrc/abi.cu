@@ -15,6 +15,16 @@ int run_gemm_i4g_general(float *Y, const uint16_t *X, const uint8_t *w, const fl
 int run_gemm_i4g_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I, int O,
                     int gs, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken);
 size_t ws_gemm_i4g(int M, int I, int O, int gs);
+int run_gemm_fp8b128_general(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv, int M,
+                             int I, int O, cudaStream_t st);
+int run_gemm_fp8b128_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv, int M, int I,
+                        int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken);
+size_t ws_gemm_fp8b128(int M, int I, int O);
+int run_gemm_mq4v2_general(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O,
+                           cudaStream_t st);
+int run_gemm_mq4v2_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
+                      size_t ws_bytes, cudaStream_t st, bool *taken);
+size_t ws_gemm_mq4v2(int M, int I, int O);
 }  // namespace qg
 
 using namespace qg;
@@ -88,6 +98,8 @@ size_t qg_gemm_workspace_bytes(int fmt, int M, int I, int O, int gs) {
     if (M < 1 || I < 1 || O < 1) return 0;
     switch (fmt) {
         case QG_FMT_I4G: return (gs >= 2 && !(gs & 1)) ? ws_gemm_i4g(M, I, O, gs) : 0;
+        case QG_FMT_FP8B128: return ws_gemm_fp8b128(M, I, O);
+        case QG_FMT_MQ4V2: return ws_gemm_mq4v2(M, I, O);
         default: return 0;
     }
 }
@@ -148,6 +160,39 @@ int qgemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales
     rc = run_gemm_i4g_tc(Y, X, w, scales, M, I, O, gs, ws, ws_bytes, as_stream(stream), &taken);
     if (taken) return rc;
     return run_gemm_i4g_general(Y, X, w, scales, M, I, O, gs, as_stream(stream));
+}
+
+int qgemm_fp8b128(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv, int M, int I, int O,
+                  void *ws, size_t ws_bytes, qg_stream_t stream) {
+    const char *fn = "qgemm_fp8b128";
+    int rc = check_dims(fn, "M", M, I, O);
+    if (rc) return rc;
+    if (!Y || !X || !w || !scale_inv) QG_REFUSE(kEInval, "%s: Y, X, w and scale_inv must be non-NULL", fn);
+    if (!aligned(Y, 4) || !aligned(X, 2) || !aligned(scale_inv, 4))
+        QG_REFUSE(kEAlign, "%s: Y and scale_inv must be 4-byte and X 2-byte aligned", fn);
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    cudaGetLastError();
+    bool taken = false;
+    rc = run_gemm_fp8b128_tc(Y, X, w, scale_inv, M, I, O, ws, ws_bytes, as_stream(stream), &taken);
+    if (taken) return rc;
+    return run_gemm_fp8b128_general(Y, X, w, scale_inv, M, I, O, as_stream(stream));
+}
+
+int qgemm_mq4v2(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
+                size_t ws_bytes, qg_stream_t stream) {
+    const char *fn = "qgemm_mq4v2";
+    int rc = check_dims(fn, "M", M, I, O);
+    if (rc) return rc;
+    if (I % 256) QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 256", fn, I);
+    if (!Y || !X || !blocks) QG_REFUSE(kEInval, "%s: Y, X and blocks must be non-NULL", fn);
+    if (!aligned(Y, 4) || !aligned(X, 2) || !aligned(blocks, 8))
+        QG_REFUSE(kEAlign, "%s: Y must be 4-byte, X 2-byte and blocks 8-byte aligned", fn);
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    cudaGetLastError();
+    bool taken = false;
+    rc = run_gemm_mq4v2_tc(Y, X, blocks, M, I, O, ws, ws_bytes, as_stream(stream), &taken);
+    if (taken) return rc;
+    return run_gemm_mq4v2_general(Y, X, blocks, M, I, O, as_stream(stream));
 }
 
 int qg_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs, qg_stream_t stream) {

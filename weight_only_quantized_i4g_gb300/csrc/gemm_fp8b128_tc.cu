@@ -1,0 +1,128 @@
+// gemm_fp8b128_tc.cu -- fmt=7 (FP8-e4m3, 128x128 block scales) batched-prefill
+// dequant-GEMM on the tensor cores: the format policy of the kernel in
+// gemm_tc.cuh.
+//
+// colibri PR #528 "fmt=7: fp8-e4m3-b128 passthrough weight format", section
+// "Design": W[o, i] = e4m3(code) * scale_inv[o/128, i/128] (a multiply), and
+// Y[m, o] = sum_i X[m, i] * W[o, i].  Here each weight is formed in f32 (the
+// e4m3 value is exact in f16 and f32; one rounding of the product), scaled by
+// the row's power of two and rounded to fp16 for the MMA.  A NaN code stays
+// NaN and makes its output column NaN through the MMA.  Row bound:
+// |w| <= 448 max_k |scale_inv[o/128, k]|.
+//
+// One dequantizing thread takes 32 codes of its row per K step (two 16-byte
+// loads).  A 128-row tile lies inside one block row of scale_inv and a K
+// step inside one block column, so the thread needs one scale per step.
+#include "gemm_tc.cuh"
+
+namespace qg {
+namespace tc {
+namespace {
+
+// Two e4m3 codes (the low and high byte of `two`) -> f16x2 of code * s,
+// low byte in the low half.
+__device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint16_t two, uint64_t s2) {
+    uint32_t r;
+    asm("{\n\t.reg .b32 h2;\n\t.reg .f16 fl, fh;\n\t.reg .f32 a, b;\n\t.reg .b64 t;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h2, %1;\n\t"
+        "mov.b32 {fl, fh}, h2;\n\t"
+        "cvt.f32.f16 a, fl;\n\t"
+        "cvt.f32.f16 b, fh;\n\t"
+        "mov.b64 t, {a, b};\n\t"
+        "mul.rn.f32x2 t, t, %2;\n\t"
+        "mov.b64 {a, b}, t;\n\t"
+        "cvt.rn.f16x2.f32 %0, b, a;\n\t}"
+        : "=r"(r)
+        : "h"(two), "l"(s2));
+    return r;
+}
+
+struct PolicyFp8B128 {
+    static constexpr const char *kName = "qgemm_fp8b128 (tensor-core kernel)";
+    // Scaled scales: f32 [ceil(O/128), nbi], scale_inv times 2^E of the block
+    // row (every row of a 128-row block shares the bound, hence E).
+    static size_t sc_bytes(int I, int O) { return (size_t)((O + 127) / 128) * ((I + 127) / 128) * sizeof(float); }
+    static __device__ __forceinline__ void prep_row(const Args &a, int o, int lane) {
+        const float *src = a.scales + (size_t)(o >> 7) * a.nbi;
+        float b = 0.f;
+        for (int k = lane; k < a.nbi; k += 32) b = fmaxf(b, fabsf(__ldg(src + k)));
+        const int e = range_exponent(448.f * warp_max(b));   // |e4m3| <= 448
+        if ((o & 127) == 0) {
+            const float p2 = exp2_int(e);
+            float *dst = static_cast<float *>(a.sc) + (size_t)(o >> 7) * a.nbi;
+            for (int k = lane; k < a.nbi; k += 32) dst[k] = __ldg(src + k) * p2;
+        }
+        if (lane == 0) a.wexp[o] = e;
+    }
+    struct Fetch {
+        uint4 q0, q1;
+        float s;
+    };
+    struct Row {
+        const uint8_t *w;
+        const float *s;
+    };
+    static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int, Row &r) {
+        const bool in = o < a.O;
+        r.w = in ? a.w + (size_t)o * (size_t)a.rowbytes + kq * 32 : nullptr;
+        r.s = in ? static_cast<const float *>(a.sc) + (size_t)(o >> 7) * a.nbi : nullptr;
+    }
+    static __device__ __forceinline__ void clear(Fetch &f) {
+        f.q0 = make_uint4(0u, 0u, 0u, 0u);
+        f.q1 = f.q0;
+        f.s = 0.f;
+    }
+    static __device__ __forceinline__ void fetch(const Args &, Row &r, int pk, int, bool skip, Fetch &f) {
+        if (r.w && !skip) {
+            const uint8_t *p = r.w + (size_t)pk * kBK;
+            f.q0 = ldg_w16(p);
+            f.q1 = ldg_w16(p + 16);
+            f.s = __ldg(r.s + pk);
+        }
+    }
+    static __device__ __forceinline__ void dequant(const Fetch &f, uint32_t (&col)[16]) {
+        const uint64_t s2 = f32_pair(f.s, f.s);
+        const uint32_t wv[8] = {f.q0.x, f.q0.y, f.q0.z, f.q0.w, f.q1.x, f.q1.y, f.q1.z, f.q1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            col[2 * j] = e4m3x2_scaled_f16x2((uint16_t)wv[j], s2);
+            col[2 * j + 1] = e4m3x2_scaled_f16x2((uint16_t)(wv[j] >> 16), s2);
+        }
+    }
+};
+
+}  // namespace
+}  // namespace tc
+
+// Shapes the tensor-core kernel takes: K in whole 64-steps (a last step of
+// 64), 16-byte aligned w (rows of I bytes then start on 16-byte boundaries)
+// and a TMA-aligned X.
+static bool gemm_fp8b128_tc_ok(const uint16_t *X, const uint8_t *w, int I) {
+    return I % tc::kBKBox == 0 && (uintptr_t)X % 16 == 0 && (uintptr_t)w % 16 == 0;
+}
+
+size_t ws_gemm_fp8b128(int M, int I, int O) {
+    if (I % tc::kBKBox != 0) return 0;
+    return tc::choose_plan(M, I, O, tc::PolicyFp8B128::sc_bytes(I, O)).ws_bytes;
+}
+
+int run_gemm_fp8b128_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv, int M, int I,
+                        int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken) {
+    *taken = false;
+    if (!gemm_fp8b128_tc_ok(X, w, I)) return kOk;
+    *taken = true;
+    const tc::Plan p = tc::choose_plan(M, I, O, tc::PolicyFp8B128::sc_bytes(I, O));
+    if (ws == nullptr || ws_bytes < p.ws_bytes) {
+        set_error_detail("qgemm_fp8b128: this shape needs a workspace of %zu bytes (got %zu)", p.ws_bytes,
+                         ws == nullptr ? (size_t)0 : ws_bytes);
+        return kEWorkspace;
+    }
+    tc::Args args{};
+    args.w = w;
+    args.scales = scale_inv;
+    args.nbi = (I + tc::kBK - 1) / tc::kBK;
+    args.rowbytes = I;
+    return tc::launch_plan<tc::PolicyFp8B128>(p, Y, X, args, M, I, O, ws, st);
+}
+
+}  // namespace qg

@@ -1,920 +1,102 @@
-// gemm_i4g_tc.cu -- fmt=4 batched-prefill dequant-GEMM on the 5th-generation
-// tensor cores (tcgen05 MMA, accumulators in tensor memory).
+// gemm_i4g_tc.cu -- fmt=4 (grouped int4) batched-prefill dequant-GEMM on the
+// tensor cores: the format policy of the kernel in gemm_tc.cuh.
 //
-//   Y[m, o] = sum_i X[m, i] * bf16((n(o, i) - 8) * scale[o, i / gs])
+// colibri PR #457 "metal: grouped-int4 (fmt=4) GEMV support + two latent
+// fmt=4 fixes", section 4: the large-batch path computes the same grouped
+// product as the GEMV, Y[m, o] = sum_i (n(o,i) - 8) * scale[o, i/gs] * X[m, i];
+// here each weight (n - 8) * scale is rounded once to f32 and, scaled by the
+// row's power of two, to fp16 for the MMA.  Row bound: |w| <= 8 max_g |scale_g|.
 //
-// (colibri PR #457, section 4: the large-batch path multiplies the same
-// grouped-int4 weights as the GEMV; the weight tile is dequantized to bf16 in
-// shared memory and contracted with f32 accumulation.)
-//
-// One persistent thread block per SM, warp-specialized.  Output tile: 128
-// outputs (the weight rows, MMA M) by BT tokens (MMA N), K in steps of 128.
-//   warp 0      TMA producer: per K step the BT x 128 bf16 tile of X (two
-//               128-byte-swizzled boxes of 64) into a shared-memory ring
-//               (operand B);
-//   warp 1      allocates tensor memory and issues the MMAs from one thread:
-//               per K step 8 instructions of M=128, N=BT, K=16 with operand
-//               A read from tensor memory;
-//   warps 2-5   epilogue: accumulator -> registers -> Y (or a partial slot);
-//   warps 6-21  load the packed weights of the tile straight from global
-//               memory (16-byte loads, three K steps ahead in registers),
-//               dequantize them and store the bf16 rows into a ring of A
-//               tiles in tensor memory (tcgen05.st): warp w covers the 32
-//               lanes (weight rows) its position allows and one 32-wide
-//               quarter of the K step (four dequantizing warps per
-//               sub-partition hide each other's latency).
-// One barrier per stage counts both the X bytes and the sixteen dequantizing
-// warps, and one commit per step frees the stage: the MMA thread's waits and
-// commits cost ~200 cycles each, so they are kept to one of each per 1024
-// cycles of tensor-core work.
-// Keeping the dequantized weights as operand A in tensor memory means each
-// of them serves BT = 256 tokens, and shared memory carries only X: the
-// dequantization work per MAC is half that of a 128-token tile, and no
-// shared-memory bandwidth goes to writing and re-reading bf16 weights.
-// The (tile, K step) units are split evenly over the blocks ("stream-K",
-// streamk.h); a tile shared by several blocks is summed in contributor order
-// by the block that arrives last at the tile's counter.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
-#include "common.cuh"
-#include "launch.h"
-#include "pipeline.cuh"
-#include "streamk.h"
+// Layout (section 11): row o holds (I+1)/2 bytes, weight i in byte i/2 (low
+// nibble for even i); scales f32 [O, ceil(I/gs)].  One dequantizing thread
+// takes 32 weights of its row per K step: one 16-byte load and one scale
+// (gs % 32 == 0 keeps the 32 weights inside one group).
+#include "gemm_tc.cuh"
 
 namespace qg {
-int num_sms();
-int *device_error_word();
-
 namespace tc {
+namespace {
 
-constexpr int kMmaM = 128;        // rows of one MMA (weight rows = outputs)
-constexpr int kBK = 128;          // K per stage: two 128-byte rows of bf16
-constexpr int kBKBox = 64;        // K of one 128-byte-swizzled box
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi = 2, kNumEpiWarps = 4, kWarpDeq = 6, kNumDeqWarps = 16;
-constexpr int kThreads = 32 * (kWarpDeq + kNumDeqWarps);
-constexpr uint32_t kSmemBudget = 227 * 1024;
-constexpr int kPrefetch = 3;      // K steps of packed weights in flight per dequantizing thread
-
-// Instruction descriptor of tcgen05.mma kind::f16: f32 accumulator, bf16 A
-// and B, both K-major, M = 128, N = n.
-constexpr uint32_t idesc_bf16(int n) {
-    return (1u << 4)                          // D format f32
-           | (1u << 7)                        // A format bf16
-           | (1u << 10)                       // B format bf16
-           | ((uint32_t)(n >> 3) << 17)       // N / 8
-           | ((uint32_t)(kMmaM >> 4) << 24);  // M / 16
-}
-
-// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
-// layout (8-row groups of 128-byte rows, 1024 bytes apart).  Advancing K by
-// 16 bf16 inside the 128-byte row moves the start address by 32 bytes.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
-    d |= (uint64_t)1 << 16;                      // leading offset (unused with this swizzle)
-    d |= (uint64_t)(1024 >> 4) << 32;            // stride offset between 8-row groups
-    d |= (uint64_t)1 << 46;                      // descriptor version
-    d |= (uint64_t)2 << 61;                      // 128-byte swizzle
-    return d;
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D (tensor memory) (+)= A (tensor memory, 128 rows x 16 bf16 in 8
-// columns) x B (shared memory, descriptor)^T.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %3, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(accumulate), "r"(idesc));
-}
-
-// 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// 32 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// Arrive on `bar` once every MMA issued so far by this thread has completed.
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_addr(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// As tma_load_2d, written to the same offset in the shared memory of every
-// block of the cluster in `mask`, each of whose barrier at `bar`'s offset
-// counts the bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                                      uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "h"(mask)
-        : "memory");
-}
-
-// As mma_commit, arriving on the barrier at `bar`'s offset in every block of
-// the cluster in `mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_addr(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// 32 consecutive f32 columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-          "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// 16 consecutive f32 columns of this warp's 32 tensor-memory lanes.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_sync(int id, int threads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
-// Two weights -> one bf16x2 word.  `lo` / `hi` carry a nibble n at bit 4p
-// (p <= 4, inside the 23-bit mantissa) under the exponent of 2^23, i.e. the
-// f32 value 2^23 + n*16^p; adding -(2^23 + 8*16^p) leaves (n - 8)*16^p
-// exactly, and the product with scale*16^-p is (n - 8)*scale rounded once
-// to f32, then to bf16 (round to nearest even).
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t lo, uint32_t hi, uint64_t neg_bias, uint64_t scale2) {
-    uint32_t r;
-    asm("{\n\t.reg .b64 t;\n\t.reg .f32 a, b;\n\t"
-        "mov.b64 t, {%1, %2};\n\t"
-        "add.rn.f32x2 t, t, %3;\n\t"
-        "mul.rn.f32x2 t, t, %4;\n\t"
-        "mov.b64 {a, b}, t;\n\t"
-        "cvt.rn.bf16x2.f32 %0, b, a;\n\t}"
-        : "=r"(r)
-        : "r"(lo), "r"(hi), "l"(neg_bias), "l"(scale2));
-    return r;
-}
-
-// Scale pairs for the nibble positions dequant_word uses, lane 0 = the even
-// weight: (p0, p1), (p2, p3), (p4, p2), (p3, p4), each scale * 16^-p.
-struct ScalePairs {
-    uint64_t v[4];
-};
-__device__ __forceinline__ uint64_t f32_pair(float lo, float hi) {
-    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
-}
-__device__ __forceinline__ ScalePairs scale_pairs(float s) {
-    const float s1 = s * 0.0625f, s2 = s * 0.00390625f, s3 = s * 0.000244140625f, s4 = s * 0.0000152587890625f;
-    ScalePairs p;
-    p.v[0] = f32_pair(s, s1);
-    p.v[1] = f32_pair(s2, s3);
-    p.v[2] = f32_pair(s4, s2);
-    p.v[3] = f32_pair(s3, s4);
-    return p;
-}
-
-// Eight weights (nibble j of `w` = weight j) -> four bf16x2 words, weight
-// 2i in the low half of word i.  Nibbles 0-4 are masked in place; nibbles
-// 5-7 after one shift by 12 (positions 2-4).
-__device__ __forceinline__ void dequant_word(uint32_t w, const ScalePairs &sp, uint32_t (&o)[4]) {
-    constexpr uint32_t M = 0x4B000000u;   // 2^23
-    // -(2^23 + 8*16^p) for p = 0..4: 0xCB000008, 0xCB000080, 0xCB000800, 0xCB008000, 0xCB080000
-    constexpr uint64_t kB01 = 0xCB000080CB000008ull, kB23 = 0xCB008000CB000800ull;
-    constexpr uint64_t kB42 = 0xCB000800CB080000ull, kB34 = 0xCB080000CB008000ull;
-    const uint32_t v = w >> 12;
-    o[0] = dequant_pair((w & 0xFu) | M, (w & 0xF0u) | M, kB01, sp.v[0]);
-    o[1] = dequant_pair((w & 0xF00u) | M, (w & 0xF000u) | M, kB23, sp.v[1]);
-    o[2] = dequant_pair((w & 0xF0000u) | M, (v & 0xF00u) | M, kB42, sp.v[2]);
-    o[3] = dequant_pair((v & 0xF000u) | M, (v & 0xF0000u) | M, kB34, sp.v[3]);
-}
-
-__device__ __forceinline__ uint4 ldg_w16(const uint8_t *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ float4 ldcg_f4(const float *p) {
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ void stcg_f4(float *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.global.cg.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Tile of 128 weight rows (outputs) by BT tokens, and the shared / tensor
-// memory that follows from it.
-template <int BT>
-struct Cfg {
-    static_assert(BT % 32 == 0 && BT >= 32 && BT <= 256, "N of one MMA, whole 32-token chunks");
-    static constexpr uint32_t kBoxBytes = BT * kBKBox * 2;  // one 64-wide box of X
-    static constexpr uint32_t kXBytes = 2 * kBoxBytes;      // operand B stage: BT tokens x 128 bf16
-    static constexpr uint32_t kACols = kBK / 2;             // 128 bf16 per row = 64 columns
-    static constexpr uint32_t kACol0 = 256;                 // A ring after the accumulator
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr int kAStagesMax = (int)((kTmemCols - kACol0) / kACols);   // 4
-    static constexpr int kNumBarsFor(int st) { return 2 * st + 2; }
-    static constexpr uint32_t kFixed = 1024 + 16;           // alignment slack + tmem / flag words
-    static constexpr int kStagesFit = (int)((kSmemBudget - kFixed - 8 * kNumBarsFor(kAStagesMax)) / kXBytes);
-    static constexpr int kStages = kStagesFit > kAStagesMax ? kAStagesMax : kStagesFit;
-    static constexpr int kNumBars = kNumBarsFor(kStages);
-    static constexpr uint32_t kSmemBytes = kFixed + kStages * kXBytes + 8 * kNumBars;
-    static constexpr int kSlotFloats = kMmaM * BT;          // one partial slot
-    static constexpr uint32_t kIdesc = idesc_bf16(BT);
-    static_assert(kStages >= 3, "at least three stages");
-    static_assert(kBoxBytes % 1024 == 0, "swizzled tiles must stay 1024-byte aligned");
-    static_assert(kACol0 >= (uint32_t)BT && kACol0 + kStages * kACols <= kTmemCols, "tensor memory map");
-};
-
-struct Args {
-    float *Y;
-    const uint8_t *w;
-    const float *scales;
-    unsigned *counters;   // one per output tile, zero at launch
-    float *partials;      // 2 slots per block
-    int M, O, gs, ng, MB, Kt;
-    int tail_half;        // the last K step of every tile is 64 wide (I % 128 == 64)
-    int cluster;          // pairs of blocks share X by multicast (one whole tile per block)
-    long long rowbytes;   // I / 2
-    long long U;          // (tile, K step) units
-    int *err;
-};
-
-// Token block and output tile of tile index t.  Normally t = nb * MB + mb;
-// with clusters of two blocks the pair (2j, 2j+1) takes token block j % MB
-// and the neighbouring output tiles 2 (j / MB) and 2 (j / MB) + 1, so both
-// blocks stream the same X.
-__device__ __forceinline__ void tile_coords(long long t, int MB, int cluster, int &mb, int &nb) {
-    if (cluster) {
-        const long long j = t >> 1;
-        mb = (int)(j % MB);
-        nb = (int)(2 * (j / MB) + (t & 1));
-    } else {
-        mb = (int)(t % MB);
-        nb = (int)(t / MB);
+struct PolicyI4G {
+    static constexpr const char *kName = "qgemm_i4g (tensor-core kernel)";
+    // Scaled scales: f32 [O, ng], scale[o, g] * 2^E[o].
+    static size_t sc_bytes(int I, int O, int gs) { return (size_t)O * ((I + gs - 1) / gs) * sizeof(float); }
+    static __device__ __forceinline__ void prep_row(const Args &a, int o, int lane) {
+        const float *src = a.scales + (size_t)o * a.ng;
+        float b = 0.f;
+        for (int g = lane; g < a.ng; g += 32) b = fmaxf(b, fabsf(__ldg(src + g)));
+        const int e = range_exponent(8.f * warp_max(b));   // |n - 8| <= 8
+        const float p2 = exp2_int(e);
+        float *dst = static_cast<float *>(a.sc) + (size_t)o * a.ng;
+        for (int g = lane; g < a.ng; g += 32) dst[g] = __ldg(src + g) * p2;
+        if (lane == 0) a.wexp[o] = e;
     }
-}
-
-// Segment of a block's range that starts at unit u: tile t, K steps [ks, ke).
-struct Seg {
-    long long t;
-    int ks, ke;
-};
-__device__ __forceinline__ Seg segment_at(long long u, long long ue, int Kt) {
-    Seg g;
-    g.t = u / Kt;
-    g.ks = (int)(u - g.t * Kt);
-    g.ke = (int)min(ue - g.t * Kt, (long long)Kt);
-    return g;
-}
-
-// Epilogue of one segment (tile t, K steps [ks, ke)) of this block's range,
-// run by the four epilogue warps (one per tensor-memory lane quarter): wait
-// for the accumulator, then either store it to Y (the whole K range is this
-// block's) or go through the partial slots.  `et` numbers the 128
-// participating threads.
-template <int BT>
-__device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, const uint32_t seg, const uint32_t tmem,
-                                              const int q, const int lane, const int et, const long long cta,
-                                              const long long U, const long long P, const int Kt,
-                                              uint64_t *acc_full, uint64_t *acc_empty, volatile uint32_t *flag,
-                                              volatile uint32_t *abort, const int nslots) {
-    using C = Cfg<BT>;
-    const int row = q * 32 + lane;          // accumulator row = weight row within the tile
-    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-    int mb, nb;
-    tile_coords(g.t, a.MB, a.cluster, mb, nb);
-    const int m0 = mb * BT, o = nb * kMmaM + row;
-    {
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait_backoff(acc_full, seg & 1, abort);
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) raise_device_error(a.err, kErrTimeout);
-    }
-    tc_fence_after();
-    auto release = [&]() {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acc_empty);
+    struct Fetch {
+        uint4 q;
+        float s;
     };
-    // Column j of the accumulator is token m0 + j; lanes hold 32
-    // consecutive outputs, so each store of a warp is 128 bytes.
-    auto store_chunk = [&](int c, const float (&v)[16]) {
-        if (o < a.O) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int m = m0 + c * 16 + j;
-                if (m < a.M) a.Y[(size_t)m * a.O + o] = v[j];
-            }
-        }
+    // Row pointers and the scale group of this thread's 32-weight quarter,
+    // advanced without divisions (one division per tile change).
+    struct Row {
+        const uint8_t *w;
+        const float *s;
+        int gi, gr;
     };
-    if (g.ks == 0 && g.ke == Kt) {
-        // The whole K range is ours: straight to Y.  With nslots > 1 the
-        // dequantizing warps of this lane quarter take chunks 1, 2, ... of
-        // every nslots (store_tile_slice).
-#pragma unroll 1
-        for (int c = 0; c < BT / 16; c += nslots) {
-            uint32_t r[16];
-            tmem_ld16(tq + c * 16, r);
-            float v[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-            store_chunk(c, v);
-        }
-        release();
-    } else {
-        const long long cf = sk::first_contributor(g.t, Kt, U, P);
-        const long long cl = sk::last_contributor(g.t, Kt, U, P);
-        const unsigned nc = (unsigned)(cl - cf + 1);
-        // Are all other contributors done already?  Then this block
-        // finishes the tile from its own accumulator and their slots.
-        if (et == 0) *flag = (ld_acquire_u32(&a.counters[g.t]) + 1 == nc) ? 1u : 0u;
-        named_sync(1, 32 * kNumEpiWarps);
-        const bool last_now = *flag != 0;
-        named_sync(1, 32 * kNumEpiWarps);
-        bool finish = last_now;
-        if (!last_now) {
-            // Park the partial sums ([token / 4][row] float4s), then count in.
-            float *mine = a.partials + (size_t)sk::partial_slot(cta, g.t, Kt, U, P) * C::kSlotFloats;
-#pragma unroll 1
-            for (int c = 0; c < BT / 16; ++c) {
-                uint32_t r[16];
-                tmem_ld16(tq + c * 16, r);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    stcg_f4(mine + ((size_t)(c * 4 + j) * kMmaM + row) * 4, r[4 * j], r[4 * j + 1],
-                            r[4 * j + 2], r[4 * j + 3]);
-            }
-            release();
-            __threadfence();
-            named_sync(1, 32 * kNumEpiWarps);
-            if (et == 0) *flag = (atomicAdd(&a.counters[g.t], 1u) + 1 == nc) ? 1u : 0u;
-            named_sync(1, 32 * kNumEpiWarps);
-            finish = *flag != 0;
-            if (finish) __threadfence();
-        }
-        if (finish) {
-            // Sum the contributors in order (the same order whichever
-            // block finishes), 16 tokens at a time, then store.
-            const long long slot_cf = sk::partial_slot(cf, g.t, Kt, U, P);
-#pragma unroll 1
-            for (int c = 0; c < BT / 16; ++c) {
-                float v[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                for (long long cc = cf; cc <= cl; ++cc) {
-                    if (last_now && cc == cta) {   // warp-uniform
-                        uint32_t own[16];
-                        tmem_ld16(tq + c * 16, own);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] += __uint_as_float(own[j]);
-                        continue;
-                    }
-                    // Every contributor after the first starts its range
-                    // inside this tile, so its slot is 2 * cc.
-                    const long long slot = cc == cf ? slot_cf : 2 * cc;
-                    const float *src = a.partials + (size_t)slot * C::kSlotFloats +
-                                       ((size_t)(c * 4) * kMmaM + row) * 4;
-                    float4 p[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) p[j] = ldcg_f4(src + (size_t)j * kMmaM * 4);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        v[4 * j] += p[j].x;
-                        v[4 * j + 1] += p[j].y;
-                        v[4 * j + 2] += p[j].z;
-                        v[4 * j + 3] += p[j].w;
-                    }
-                }
-                store_chunk(c, v);
-            }
-        }
-        if (last_now) release();
+    static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int pk, Row &r) {
+        const bool in = o < a.O;
+        r.w = in ? a.w + (size_t)o * (size_t)(a.rowbytes) + kq * 16 : nullptr;
+        r.s = in ? static_cast<const float *>(a.sc) + (size_t)o * a.ng : nullptr;
+        const int gq = a.gs / 32, u0 = 4 * pk + kq;
+        r.gi = u0 / gq;
+        r.gr = u0 - r.gi * gq;
     }
-}
-
-// The part of a whole tile's store that a dequantizing warp takes once its
-// block has no K steps left: chunks slot, slot + nslots, ... of its lane
-// quarter, after the accumulator is complete.
-template <int BT>
-__device__ __forceinline__ void store_tile_slice(const Args &a, const Seg g, const uint32_t tmem, const int q,
-                                                 const int lane, const int slot, const int nslots,
-                                                 uint64_t *acc_full, volatile uint32_t *abort) {
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait_backoff(acc_full, 0u, abort);
-    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) raise_device_error(a.err, kErrTimeout);
-    tc_fence_after();
-    int mb, nb;
-    tile_coords(g.t, a.MB, a.cluster, mb, nb);
-    const int o = nb * kMmaM + q * 32 + lane, m0 = mb * BT;
-    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-    for (int c = slot; c < BT / 16; c += nslots) {
-        uint32_t r[16];
-        tmem_ld16(tq + c * 16, r);
-        if (o < a.O) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int m = m0 + c * 16 + j;
-                if (m < a.M) a.Y[(size_t)m * a.O + o] = __uint_as_float(r[j]);
-            }
+    static __device__ __forceinline__ void clear(Fetch &f) {
+        f.q = make_uint4(0u, 0u, 0u, 0u);
+        f.s = 0.f;
+    }
+    static __device__ __forceinline__ void fetch(const Args &a, Row &r, int pk, int, bool skip, Fetch &f) {
+        if (r.w && !skip) {
+            f.q = ldg_w16(r.w + pk * 64);
+            f.s = __ldg(r.s + r.gi);
+        }
+        const int gq = a.gs >> 5;
+        r.gr += 4;
+        while (r.gr >= gq) {
+            r.gr -= gq;
+            ++r.gi;
         }
     }
-    tc_fence_before();
-}
-
-template <int BT>
-__global__ void __launch_bounds__(kThreads, 1)
-gemm_i4g_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
-    using C = Cfg<BT>;
-    extern __shared__ unsigned char smem_raw[];
-    const uint32_t raw_base = smem_addr(smem_raw);
-    unsigned char *smem = smem_raw + ((1024u - (raw_base & 1023u)) & 1023u);
-    const uint32_t sbase = smem_addr(smem);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kXBytes);
-    uint64_t *full = bars, *empty = bars + C::kStages;   // per stage: X bytes + dequantized A / MMA done
-    uint64_t *acc_full = empty + C::kStages, *acc_empty = acc_full + 1;
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + C::kNumBars);
-    volatile uint32_t *flag = tmem_slot + 1;    // epilogue broadcast: this block finishes the tile
-    volatile uint32_t *abort = tmem_slot + 2;   // set by the first wait that times out
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        griddep_launch_dependents();
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&full[s], 1 + kNumDeqWarps);
-            mbar_init(&empty[s], a.cluster ? 2 : 1);   // with a cluster: both blocks' MMAs
-        }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, kNumEpiWarps);
-        *abort = 0u;
-        mbar_fence_init();
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
-    }
-    if (warp == kWarpMma) {
-        __syncwarp();
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_addr((const void *)tmem_slot)),
-                     "r"(C::kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    // With a cluster, the peer's copies and commits reach this block's
-    // barriers: both blocks initialize theirs first.
-    if (a.cluster) cluster_sync();
-    const uint32_t crank = a.cluster ? cluster_rank() : 0u;
-
-    const long long P = gridDim.x, cta = blockIdx.x, U = a.U;
-    const long long ub = sk::range_begin(cta, U, P), ue = sk::range_begin(cta + 1, U, P);
-    const int Kt = a.Kt;
-    // A range that is exactly one whole tile: the dequantizing warps, idle
-    // after its last K step, help store it (5 warps per lane quarter).
-    const bool whole_only = ub % Kt == 0 && ue - ub == Kt;
-    constexpr int kEpiSlots = 1 + kNumDeqWarps / 4;
-
-    if (warp == kWarpTma) {
-        // X may be the previous kernel's output (programmatic dependent
-        // launch): wait for it.  The packed weights, which nothing on the
-        // stream writes while this library's kernels overlap, stream in
-        // meanwhile.
-        griddep_wait();
-        if (lane == 0) {
-            uint32_t it = 0;
-            for (long long u = ub; u < ue;) {
-                const Seg g = segment_at(u, ue, Kt);
-                int mb, nb;
-                tile_coords(g.t, a.MB, a.cluster, mb, nb);
-                const int m0 = mb * BT;
-                for (int k = g.ks; k < g.ke; ++k, ++it) {
-                    const uint32_t s = it % C::kStages, r = it / C::kStages;
-                    const bool half = a.tail_half && k == Kt - 1;
-                    if (r > 0 && !mbar_wait_or_abort(&empty[s], (r & 1) ^ 1, abort))
-                        raise_device_error(a.err, kErrTimeout);
-                    mbar_arrive_expect_tx(&full[s], half ? C::kBoxBytes : C::kXBytes);
-                    const uint32_t st = sbase + s * C::kXBytes;
-                    if (a.cluster) {
-                        // This block's half of the tokens, into both blocks.
-                        const uint32_t off = crank * (uint32_t)(BT / 2) * 128u;
-                        const int mr = m0 + (int)crank * (BT / 2);
-                        tma_load_2d_multicast(st + off, &tmX, k * kBK, mr, &full[s], 0x3);
-                        if (!half)
-                            tma_load_2d_multicast(st + C::kBoxBytes + off, &tmX, k * kBK + kBKBox, mr, &full[s], 0x3);
-                    } else {
-                        tma_load_2d(st, &tmX, k * kBK, m0, &full[s]);
-                        if (!half) tma_load_2d(st + C::kBoxBytes, &tmX, k * kBK + kBKBox, m0, &full[s]);
-                    }
-                }
-                u = g.t * Kt + g.ke;
-            }
-            // Every copy issued must have landed before the block exits, and
-            // with a cluster every commit of the peer's MMAs must have
-            // arrived here too.
-            for (uint32_t j = it > (uint32_t)C::kStages ? it - C::kStages : 0; j < it; ++j) {
-                if (!mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1)) raise_device_error(a.err, kErrTimeout);
-                if (a.cluster && !mbar_wait(&empty[j % C::kStages], (j / C::kStages) & 1))
-                    raise_device_error(a.err, kErrTimeout);
-            }
-        }
-    } else if (warp == kWarpMma) {
-        if (lane == 0) {
-            uint32_t it = 0, seg = 0;
-            for (long long u = ub; u < ue; ++seg) {
-                const Seg g = segment_at(u, ue, Kt);
-                if (seg > 0 && !mbar_wait_or_abort(acc_empty, (seg - 1) & 1, abort))
-                    raise_device_error(a.err, kErrTimeout);
-                tc_fence_after();
-                for (int k = g.ks; k < g.ke; ++k, ++it) {
-                    const uint32_t s = it % C::kStages, r = it / C::kStages;
-                    const int nk = (a.tail_half && k == Kt - 1) ? kBKBox / 16 : kBK / 16;
-                    if (!mbar_wait_or_abort(&full[s], r & 1, abort)) raise_device_error(a.err, kErrTimeout);
-                    tc_fence_after();
-                    const uint32_t xa = sbase + s * C::kXBytes;
-                    const uint32_t at = tmem + C::kACol0 + s * C::kACols;
+    // Weight n -> (n - 8) * scale: bias -(2^23 + 8*16^p) per position.
+    static __device__ __forceinline__ void dequant(const Fetch &f, uint32_t (&col)[16]) {
+        constexpr uint64_t kB01 = 0xCB000080CB000008ull, kB23 = 0xCB008000CB000800ull;
+        constexpr uint64_t kB42 = 0xCB000800CB080000ull, kB34 = 0xCB080000CB008000ull;
+        const NibPairs sp = nib_scale_pairs(f.s);
+        const uint32_t wv[4] = {f.q.x, f.q.y, f.q.z, f.q.w};
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        if (kk < nk)
-                            mma_bf16_ts(tmem, at + kk * 8, sw128_desc(xa + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32),
-                                        C::kIdesc, (k > g.ks || kk > 0) ? 1u : 0u);
-                    if (a.cluster)
-                        mma_commit_multicast(&empty[s], 0x3);   // frees the stage in both blocks
-                    else
-                        mma_commit(&empty[s]);
-                }
-                mma_commit(acc_full);
-                u = g.t * Kt + g.ke;
-            }
-        }
-    } else if (warp < kWarpEpi + kNumEpiWarps) {
-        // Epilogue of every segment of the range, in order (Y, the
-        // counters and the partial slots only after the previous kernel).
-        griddep_wait();
-        uint32_t seg = 0;
-        for (long long u = ub; u < ue; ++seg) {
-            const Seg g = segment_at(u, ue, Kt);
-            epilogue_segment<BT>(a, g, seg, tmem, warp & 3, lane, threadIdx.x - 32 * kWarpEpi, cta, U, P, Kt,
-                                 acc_full, acc_empty, flag, abort, whole_only ? kEpiSlots : 1);
-            u = g.t * Kt + g.ke;
-        }
-    } else {
-        // Dequantize.  Warp w may write tensor-memory lanes 32*(w % 4) ..
-        // +31 (weight rows of the tile); the four warps of a lane quarter
-        // split each K step into quarters kq = 0..3 of 32 weights (16 bytes),
-        // so every sub-partition holds four dequantizing warps.
-        const int q = warp & 3, kq = (warp - kWarpDeq) >> 2;
-        const int R = q * 32 + lane;
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + C::kACol0 + kq * (C::kACols / 4);
-        struct Fetch {
-            uint4 q;
-            float s;
-        };
-        // Fetch state: the next unit to load, this row's pointers, and the
-        // scale group of this thread's 32-weight quarter, advanced without
-        // divisions (one division per tile change).
-        long long pu = ub, pt = ub / Kt;
-        int pk = (int)(ub - pt * Kt);
-        const int gq = a.gs / 32;   // 32-weight quarters per scale group
-        const uint8_t *wrow = nullptr;
-        const float *srow = nullptr;
-        int gi = 0, gr = 0;
-        auto set_tile = [&]() {
-            int mb, nb;
-            tile_coords(pt, a.MB, a.cluster, mb, nb);
-            const int o = nb * kMmaM + R;
-            wrow = o < a.O ? a.w + (size_t)o * a.rowbytes + kq * 16 : nullptr;
-            srow = o < a.O ? a.scales + (size_t)o * a.ng : nullptr;
-            const int u0 = 4 * pk + kq;
-            gi = u0 / gq;
-            gr = u0 - gi * gq;
-        };
-        if (pu < ue) set_tile();
-        auto fetch = [&](Fetch &f) {
-            f.q = make_uint4(0u, 0u, 0u, 0u);
-            f.s = 0.f;
-            if (pu < ue) {
-                // The 64-wide last step of a row with I % 128 == 64 has no upper half.
-                if (wrow && !(kq >= 2 && a.tail_half && pk == Kt - 1)) {
-                    f.q = ldg_w16(wrow + pk * 64);
-                    f.s = __ldg(srow + gi);
-                }
-                ++pu;
-                if (++pk == Kt) {
-                    pk = 0;
-                    ++pt;
-                    if (pu < ue) set_tile();
-                } else {
-                    gr += 4;
-                    while (gr >= gq) {
-                        gr -= gq;
-                        ++gi;
-                    }
-                }
-            }
-        };
-        uint32_t it = 0;
-        auto step = [&](const Fetch &cur) {
-            const uint32_t s = it % C::kStages, r = it / C::kStages;
-            if (r > 0 && !mbar_wait_or_abort(&empty[s], (r & 1) ^ 1, abort)) raise_device_error(a.err, kErrTimeout);
-            tc_fence_after();
-            uint32_t col[16];
-            const ScalePairs sp = scale_pairs(cur.s);
-            const uint32_t wv[4] = {cur.q.x, cur.q.y, cur.q.z, cur.q.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t o4[4];
-                dequant_word(wv[j], sp, o4);
-#pragma unroll
-                for (int p = 0; p < 4; ++p) col[4 * j + p] = o4[p];
-            }
-            tmem_st16(ta + s * C::kACols, col);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[s]);
-            ++it;
-        };
-        // Three register buffers used in rotation with fixed names, so a
-        // buffer is read only when its loads were issued three K steps ago.
-        static_assert(kPrefetch == 3, "the loop below is unrolled for three buffers");
-        Fetch f0, f1, f2;
-        fetch(f0);
-        fetch(f1);
-        fetch(f2);
-        for (long long u = ub; u < ue;) {
-            step(f0);
-            fetch(f0);
-            if (++u >= ue) break;
-            step(f1);
-            fetch(f1);
-            if (++u >= ue) break;
-            step(f2);
-            fetch(f2);
-            ++u;
-        }
-        if (whole_only) {
-            griddep_wait();
-            store_tile_slice<BT>(a, segment_at(ub, ue, Kt), tmem, q, lane, 1 + kq, kEpiSlots, acc_full, abort);
+        for (int j = 0; j < 4; ++j) {
+            uint32_t lo[4], hi[4];
+            nib_positions(wv[j], lo, hi);
+            col[4 * j + 0] = nib_add_mul(lo[0], hi[0], kB01, sp.v[0]);
+            col[4 * j + 1] = nib_add_mul(lo[1], hi[1], kB23, sp.v[1]);
+            col[4 * j + 2] = nib_add_mul(lo[2], hi[2], kB42, sp.v[2]);
+            col[4 * j + 3] = nib_add_mul(lo[3], hi[3], kB34, sp.v[3]);
         }
     }
-
-    tc_fence_before();
-    __syncthreads();
-    if (a.cluster) cluster_sync();   // the peer no longer writes into this block
-    if (warp == kWarpMma) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols)
-                     : "memory");
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Host side
-// ---------------------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        cudaGetLastError();
-    });
-    return fn;
-}
-
-// The token widths compiled (MMA N).
-enum TileId { kT256 = 0, kT128, kT64, kNumTiles };
-constexpr int kTileBT[kNumTiles] = {256, 128, 64};
-
-struct Plan {
-    int tile, bt, MB, NB, Kt, P;
-    int cluster;          // whole tiles in pairs sharing X by multicast
-    long long T, U;
-    size_t counter_bytes, ws_bytes;
 };
 
-Plan make_plan(int tile, int M, int I, int O, int nsm) {
-    Plan p;
-    p.tile = tile;
-    p.bt = kTileBT[tile];
-    p.MB = (M + p.bt - 1) / p.bt;
-    p.NB = (O + kMmaM - 1) / kMmaM;
-    p.Kt = (I + kBK - 1) / kBK;
-    p.T = (long long)p.MB * p.NB;
-    p.U = p.T * p.Kt;
-    // One tile per block when the tiles fit in one wave; otherwise an even
-    // split of the units over all SMs.
-    p.P = (int)std::min<long long>(p.T <= nsm ? p.T : nsm, p.U);
-    // Pairs of whole tiles sharing X by multicast (cluster = 1) measured no
-    // faster on GB300: the bytes each SM receives per K step, not the copies
-    // it issues, bound the step, and multicast leaves those unchanged.  The
-    // planner does not pick it.
-    p.cluster = 0;
-    p.counter_bytes = ((size_t)p.T * sizeof(unsigned) + 255) & ~(size_t)255;
-    p.ws_bytes = p.counter_bytes + (size_t)2 * p.P * kMmaM * p.bt * sizeof(float);
-    return p;
-}
-
-// Estimated cycles of the busiest block, from measurements on GB300: a
-// 128-wide K step costs ~2300 cycles with 256 tokens per tile and ~2150 with
-// fewer (the dequantization of 128 x 128 weights bounds it), and a tile whose
-// K range is split over blocks costs ~14000 cycles per contributor for the
-// partial sums (written, then read back by the block that finishes it).
-double plan_cost(const Plan &p) {
-    const double step = (p.bt == 256 ? 2300.0 : 2150.0) * (p.cluster ? 0.75 : 1.0);
-    const double steps = (double)((p.U + p.P - 1) / p.P);
-    const bool split = (p.U / p.P) % p.Kt != 0 || p.U % p.P != 0;
-    const double contributors = (double)p.Kt / std::max(1.0, (double)(p.U / p.P)) + 1.0;
-    return steps * step + (split ? 14000.0 * contributors : 0.0);
-}
-
-// Both launch shapes for every token width: one whole tile per block when
-// the tiles fit in one wave, and the stream-K split over all SMs.
-Plan choose_plan(int M, int I, int O) {
-    const int nsm = num_sms();
-    Plan best = make_plan(0, M, I, O, nsm);
-    double best_cost = plan_cost(best);
-    for (int t = 0; t < kNumTiles; ++t) {
-        for (int mode = 0; mode < 2; ++mode) {
-            Plan p = make_plan(t, M, I, O, nsm);
-            if (mode == 1) {
-                if (p.T >= nsm) continue;   // already the split over all SMs
-                p.P = (int)std::min<long long>(nsm, p.U);
-                p.cluster = 0;
-                p.ws_bytes = p.counter_bytes + (size_t)2 * p.P * kMmaM * p.bt * sizeof(float);
-            }
-            const double c = plan_cost(p);
-            if (c < best_cost) {
-                best = p;
-                best_cost = c;
-            }
-        }
-    }
-    return best;
-}
-
-template <int BT>
-int launch_tile(const Plan &p, const CUtensorMap &tmX, const Args &args, cudaStream_t st) {
-    using C = Cfg<BT>;
-    static std::once_flag attr_once[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    std::call_once(attr_once[dev & 63], [] {
-        cudaFuncSetAttribute(gemm_i4g_tc_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::kSmemBytes);
-    });
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.P);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::kSmemBytes;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = p.cluster ? 2 : 1;
-    cudaLaunchKernelEx(&cfg, gemm_i4g_tc_kernel<BT>, tmX, args);
-    return check_launch("qgemm_i4g (tensor-core kernel)");
-}
-
-int launch_plan(const Plan &p, float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I,
-                int O, int gs, void *ws, cudaStream_t st) {
-    auto encode = encode_fn();
-    if (!encode) {
-        set_error_detail("qgemm_i4g: cuTensorMapEncodeTiled is not available from the driver");
-        return kECuda;
-    }
-    CUtensorMap tmX;
-    const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)M};
-    const cuuint64_t strides[1] = {(cuuint64_t)I * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBKBox, (cuuint32_t)(p.cluster ? p.bt / 2 : p.bt)};
-    const cuuint32_t es[2] = {1, 1};
-    CUresult r = encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(X), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-        set_error_detail("qgemm_i4g: tensor map of X refused (CUresult %d)", (int)r);
-        return kECuda;
-    }
-    Args args;
-    args.Y = Y;
-    args.w = w;
-    args.scales = scales;
-    args.counters = static_cast<unsigned *>(ws);
-    args.partials = reinterpret_cast<float *>(static_cast<unsigned char *>(ws) + p.counter_bytes);
-    args.M = M;
-    args.O = O;
-    args.gs = gs;
-    args.ng = (I + gs - 1) / gs;
-    args.MB = p.MB;
-    args.Kt = p.Kt;
-    args.tail_half = (I % kBK) != 0 ? 1 : 0;
-    args.cluster = p.cluster;
-    args.rowbytes = I / 2;
-    args.U = p.U;
-    args.err = device_error_word();
-    // Tile counters are only read when a tile's K range is split over blocks.
-    const bool split = !(p.U % p.P == 0 && (p.U / p.P) % p.Kt == 0);
-    if (split && cudaMemsetAsync(ws, 0, (size_t)p.T * sizeof(unsigned), st) != cudaSuccess)
-        return check_launch("qgemm_i4g (counter reset)");
-    switch (p.tile) {
-        case kT256: return launch_tile<256>(p, tmX, args, st);
-        case kT128: return launch_tile<128>(p, tmX, args, st);
-        default: return launch_tile<64>(p, tmX, args, st);
-    }
-}
-
+}  // namespace
 }  // namespace tc
 
-// Shapes the tensor-core kernel takes: K in whole 64-steps (a last step of 64), every 32-weight
-// half step inside one scale group, a 16-byte aligned w (its rows then start
-// on 16-byte boundaries too) and a TMA-aligned X.
-bool gemm_i4g_tc_ok(const uint16_t *X, const uint8_t *w, int I, int gs) {
+// Shapes the tensor-core kernel takes: K in whole 64-steps (a last step of 64),
+// every 32-weight quarter step inside one scale group, a 16-byte aligned w
+// (its rows then start on 16-byte boundaries too) and a TMA-aligned X.
+static bool gemm_i4g_tc_ok(const uint16_t *X, const uint8_t *w, int I, int gs) {
     return I % tc::kBKBox == 0 && gs % 32 == 0 && (uintptr_t)X % 16 == 0 && (uintptr_t)w % 16 == 0;
 }
 
 size_t ws_gemm_i4g(int M, int I, int O, int gs) {
     if (I % tc::kBKBox != 0 || gs % 32 != 0) return 0;
-    return tc::choose_plan(M, I, O).ws_bytes;
+    return tc::choose_plan(M, I, O, tc::PolicyI4G::sc_bytes(I, O, gs)).ws_bytes;
 }
 
 int run_gemm_i4g_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I, int O,
@@ -922,13 +104,19 @@ int run_gemm_i4g_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *
     *taken = false;
     if (!gemm_i4g_tc_ok(X, w, I, gs)) return kOk;
     *taken = true;
-    const tc::Plan p = tc::choose_plan(M, I, O);
+    const tc::Plan p = tc::choose_plan(M, I, O, tc::PolicyI4G::sc_bytes(I, O, gs));
     if (ws == nullptr || ws_bytes < p.ws_bytes) {
         set_error_detail("qgemm_i4g: this shape needs a workspace of %zu bytes (got %zu)", p.ws_bytes,
                          ws == nullptr ? (size_t)0 : ws_bytes);
         return kEWorkspace;
     }
-    return tc::launch_plan(p, Y, X, w, scales, M, I, O, gs, ws, st);
+    tc::Args args{};
+    args.w = w;
+    args.scales = scales;
+    args.gs = gs;
+    args.ng = (I + gs - 1) / gs;
+    args.rowbytes = I / 2;
+    return tc::launch_plan<tc::PolicyI4G>(p, Y, X, args, M, I, O, ws, st);
 }
 
 }  // namespace qg

@@ -1,0 +1,129 @@
+// gemm_mq4v2_tc.cu -- MQ4-V2 (hipfire qt=44) batched-prefill dequant-GEMM on
+// the tensor cores: the format policy of the kernel in gemm_tc.cuh.
+//
+// hipfire "MQ4 V2", sections 2 and 4: 136 bytes per 256 weights, a header
+// dword per 128-weight half (fp16 scale low, fp16 zero high) and 128 bytes
+// of nibbles; w_j = q_j * scale[h] + zero[h].  Here each weight is formed in
+// f32 with one rounding (a fused multiply-add of the exact q_j, scale and
+// zero), scaled by the row's power of two and rounded to fp16 for the MMA.
+// Row bound: |w| <= max_h (|zero_h| + 15 |scale_h|).
+//
+// A 128-wide K step is exactly one half of a block, so one dequantizing
+// thread takes one header dword and 16 payload bytes (32 weights) per step.
+// Blocks are 136 bytes, so payload addresses are only 8-byte aligned: two
+// 8-byte loads.
+#include "gemm_tc.cuh"
+
+namespace qg {
+namespace tc {
+namespace {
+
+__device__ __forceinline__ uint2 ldg_w8(const uint8_t *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L2::256B.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float f16_to_f32(uint32_t h) {
+    float f;
+    asm("{.reg .b16 t, u; mov.b32 {t, u}, %1; cvt.f32.f16 %0, t;}" : "=f"(f) : "r"(h));
+    return f;
+}
+
+struct PolicyMq4v2 {
+    static constexpr const char *kName = "qgemm_mq4v2 (tensor-core kernel)";
+    static constexpr int kBlockBytes = 136;
+    // Scaled headers: f32 pairs [O, I/128] (scale, zero) * 2^E[o], one per
+    // 128-weight half, i.e. per K step.
+    static size_t sc_bytes(int I, int O) { return (size_t)O * (I / 128) * sizeof(float2); }
+    static __device__ __forceinline__ void prep_row(const Args &a, int o, int lane) {
+        const uint8_t *row = a.w + (size_t)o * (size_t)a.rowbytes;
+        const int nb = (int)(a.rowbytes / kBlockBytes);
+        float b = 0.f;
+        for (int k = lane; k < nb; k += 32) {
+            const uint2 h = __ldg(reinterpret_cast<const uint2 *>(row + (size_t)k * kBlockBytes));
+            b = fmaxf(b, fabsf(f16_to_f32(h.x >> 16)) + 15.f * fabsf(f16_to_f32(h.x)));
+            b = fmaxf(b, fabsf(f16_to_f32(h.y >> 16)) + 15.f * fabsf(f16_to_f32(h.y)));
+        }
+        const int e = range_exponent(warp_max(b));
+        const float p2 = exp2_int(e);
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float2 *>(a.sc) + (size_t)o * 2 * nb);
+        for (int k = lane; k < nb; k += 32) {
+            const uint2 h = __ldg(reinterpret_cast<const uint2 *>(row + (size_t)k * kBlockBytes));
+            dst[k] = make_float4(f16_to_f32(h.x) * p2, f16_to_f32(h.x >> 16) * p2, f16_to_f32(h.y) * p2,
+                                 f16_to_f32(h.y >> 16) * p2);
+        }
+        if (lane == 0) a.wexp[o] = e;
+    }
+    struct Fetch {
+        uint4 q;
+        float2 sz;   // scaled (scale, zero) of the half
+    };
+    struct Row {
+        const uint8_t *b;     // this row's blocks; the payload quarter kq added
+        const float2 *sz;     // this row's scaled headers
+    };
+    static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int, Row &r) {
+        const bool in = o < a.O;
+        r.b = in ? a.w + (size_t)o * (size_t)a.rowbytes + 16 * kq : nullptr;
+        r.sz = in ? static_cast<const float2 *>(a.sc) + (size_t)o * a.Kt : nullptr;
+    }
+    static __device__ __forceinline__ void clear(Fetch &f) {
+        f.q = make_uint4(0u, 0u, 0u, 0u);
+        f.sz = make_float2(0.f, 0.f);
+    }
+    static __device__ __forceinline__ void fetch(const Args &, Row &r, int pk, int, bool, Fetch &f) {
+        if (r.b) {
+            // Payload of half pk & 1 of block pk >> 1, this thread's 16 bytes.
+            const uint8_t *pl = r.b + (size_t)(pk >> 1) * kBlockBytes + 8 + 64 * (pk & 1);
+            const uint2 lo = ldg_w8(pl);
+            const uint2 hi = ldg_w8(pl + 8);
+            f.q = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            f.sz = __ldg(r.sz + pk);
+        }
+    }
+    // q -> q * scale + zero: bias -2^23 at every position, then one fused
+    // multiply-add with (scale * 16^-p, zero).
+    static __device__ __forceinline__ void dequant(const Fetch &f, uint32_t (&col)[16]) {
+        constexpr uint64_t kBias = 0xCB000000CB000000ull;
+        const NibPairs sp = nib_scale_pairs(f.sz.x);
+        const uint64_t z2 = f32_pair(f.sz.y, f.sz.y);
+        const uint32_t wv[4] = {f.q.x, f.q.y, f.q.z, f.q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t lo[4], hi[4];
+            nib_positions(wv[j], lo, hi);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) col[4 * j + p] = nib_add_fma(lo[p], hi[p], kBias, sp.v[p], z2);
+        }
+    }
+};
+
+}  // namespace
+}  // namespace tc
+
+// The format fixes I % 256 == 0 and 8-byte aligned blocks (checked by the
+// entry point); the tensor-core kernel also wants a TMA-aligned X.
+size_t ws_gemm_mq4v2(int M, int I, int O) {
+    if (I % 256 != 0) return 0;
+    return tc::choose_plan(M, I, O, tc::PolicyMq4v2::sc_bytes(I, O)).ws_bytes;
+}
+
+int run_gemm_mq4v2_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
+                      size_t ws_bytes, cudaStream_t st, bool *taken) {
+    *taken = false;
+    if ((uintptr_t)X % 16 != 0 || I % 256 != 0) return kOk;
+    *taken = true;
+    const tc::Plan p = tc::choose_plan(M, I, O, tc::PolicyMq4v2::sc_bytes(I, O));
+    if (ws == nullptr || ws_bytes < p.ws_bytes) {
+        set_error_detail("qgemm_mq4v2: this shape needs a workspace of %zu bytes (got %zu)", p.ws_bytes,
+                         ws == nullptr ? (size_t)0 : ws_bytes);
+        return kEWorkspace;
+    }
+    tc::Args args{};
+    args.w = blocks;
+    args.rowbytes = (long long)(I / 256) * tc::PolicyMq4v2::kBlockBytes;
+    return tc::launch_plan<tc::PolicyMq4v2>(p, Y, X, args, M, I, O, ws, st);
+}
+
+}  // namespace qg
