@@ -7,8 +7,7 @@
 // Y[m, o] = sum_i X[m, i] * W[o, i].  Here each weight is formed in f32 (the
 // e4m3 value is exact in f16 and f32; one rounding of the product), scaled by
 // the row's power of two and rounded to fp16 for the MMA.  A NaN code stays
-// NaN and makes its output column NaN through the MMA.  Row bound:
-// |w| <= 448 max_k |scale_inv[o/128, k]|.
+// NaN and makes its output column NaN through the MMA.
 //
 // One dequantizing thread takes 32 codes of its row per K step (two 16-byte
 // loads).  A 128-row tile lies inside one block row of scale_inv and a K
@@ -39,20 +38,14 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint16_t two, uint64_t s
 
 struct PolicyFp8B128 {
     static constexpr const char *kName = "qgemm_fp8b128 (tensor-core kernel)";
-    // Scaled scales: f32 [ceil(O/128), nbi], scale_inv times 2^E of the block
-    // row (every row of a 128-row block shares the bound, hence E).
-    static size_t sc_bytes(int I, int O) { return (size_t)((O + 127) / 128) * ((I + 127) / 128) * sizeof(float); }
-    static __device__ __forceinline__ void prep_row(const Args &a, int o, int lane) {
+    // Bound on |w| over row o, |e4m3| <= 448: 448 max_k |scale_inv[o/128, k]|
+    // (the same for every row of a 128-row block).  Called by a whole warp.
+    static __device__ __forceinline__ float row_bound(const Args &a, int o, int lane) {
         const float *src = a.scales + (size_t)(o >> 7) * a.nbi;
         float b = 0.f;
+#pragma unroll 4
         for (int k = lane; k < a.nbi; k += 32) b = fmaxf(b, fabsf(__ldg(src + k)));
-        const int e = range_exponent(448.f * warp_max(b));   // |e4m3| <= 448
-        if ((o & 127) == 0) {
-            const float p2 = exp2_int(e);
-            float *dst = static_cast<float *>(a.sc) + (size_t)(o >> 7) * a.nbi;
-            for (int k = lane; k < a.nbi; k += 32) dst[k] = __ldg(src + k) * p2;
-        }
-        if (lane == 0) a.wexp[o] = e;
+        return 448.f * warp_max(b);
     }
     struct Fetch {
         uint4 q0, q1;
@@ -65,7 +58,7 @@ struct PolicyFp8B128 {
     static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int, Row &r) {
         const bool in = o < a.O;
         r.w = in ? a.w + (size_t)o * (size_t)a.rowbytes + kq * 32 : nullptr;
-        r.s = in ? static_cast<const float *>(a.sc) + (size_t)(o >> 7) * a.nbi : nullptr;
+        r.s = in ? a.scales + (size_t)(o >> 7) * a.nbi : nullptr;
     }
     static __device__ __forceinline__ void clear(Fetch &f) {
         f.q0 = make_uint4(0u, 0u, 0u, 0u);
@@ -80,8 +73,9 @@ struct PolicyFp8B128 {
             f.s = __ldg(r.s + pk);
         }
     }
-    static __device__ __forceinline__ void dequant(const Fetch &f, uint32_t (&col)[16]) {
-        const uint64_t s2 = f32_pair(f.s, f.s);
+    static __device__ __forceinline__ void dequant(const Fetch &f, float p2, uint32_t (&col)[16]) {
+        const float s = f.s * p2;
+        const uint64_t s2 = f32_pair(s, s);
         const uint32_t wv[8] = {f.q0.x, f.q0.y, f.q0.z, f.q0.w, f.q1.x, f.q1.y, f.q1.z, f.q1.w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -103,7 +97,7 @@ static bool gemm_fp8b128_tc_ok(const uint16_t *X, const uint8_t *w, int I) {
 
 size_t ws_gemm_fp8b128(int M, int I, int O) {
     if (I % tc::kBKBox != 0) return 0;
-    return tc::choose_plan(M, I, O, tc::PolicyFp8B128::sc_bytes(I, O)).ws_bytes;
+    return tc::choose_plan(M, I, O).ws_bytes;
 }
 
 int run_gemm_fp8b128_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv, int M, int I,
@@ -111,7 +105,7 @@ int run_gemm_fp8b128_tc(float *Y, const uint16_t *X, const uint8_t *w, const flo
     *taken = false;
     if (!gemm_fp8b128_tc_ok(X, w, I)) return kOk;
     *taken = true;
-    const tc::Plan p = tc::choose_plan(M, I, O, tc::PolicyFp8B128::sc_bytes(I, O));
+    const tc::Plan p = tc::choose_plan(M, I, O);
     if (ws == nullptr || ws_bytes < p.ws_bytes) {
         set_error_detail("qgemm_fp8b128: this shape needs a workspace of %zu bytes (got %zu)", p.ws_bytes,
                          ws == nullptr ? (size_t)0 : ws_bytes);

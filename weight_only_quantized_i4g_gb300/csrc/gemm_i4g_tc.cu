@@ -5,7 +5,7 @@
 // fmt=4 fixes", section 4: the large-batch path computes the same grouped
 // product as the GEMV, Y[m, o] = sum_i (n(o,i) - 8) * scale[o, i/gs] * X[m, i];
 // here each weight (n - 8) * scale is rounded once to f32 and, scaled by the
-// row's power of two, to fp16 for the MMA.  Row bound: |w| <= 8 max_g |scale_g|.
+// row's power of two, to fp16 for the MMA.
 //
 // Layout (section 11): row o holds (I+1)/2 bytes, weight i in byte i/2 (low
 // nibble for even i); scales f32 [O, ceil(I/gs)].  One dequantizing thread
@@ -19,17 +19,14 @@ namespace {
 
 struct PolicyI4G {
     static constexpr const char *kName = "qgemm_i4g (tensor-core kernel)";
-    // Scaled scales: f32 [O, ng], scale[o, g] * 2^E[o].
-    static size_t sc_bytes(int I, int O, int gs) { return (size_t)O * ((I + gs - 1) / gs) * sizeof(float); }
-    static __device__ __forceinline__ void prep_row(const Args &a, int o, int lane) {
+    // Bound on |w| over row o, |n - 8| <= 8: 8 max_g |scale[o, g]|.  Called by
+    // a whole warp; every lane gets the result.
+    static __device__ __forceinline__ float row_bound(const Args &a, int o, int lane) {
         const float *src = a.scales + (size_t)o * a.ng;
         float b = 0.f;
+#pragma unroll 4
         for (int g = lane; g < a.ng; g += 32) b = fmaxf(b, fabsf(__ldg(src + g)));
-        const int e = range_exponent(8.f * warp_max(b));   // |n - 8| <= 8
-        const float p2 = exp2_int(e);
-        float *dst = static_cast<float *>(a.sc) + (size_t)o * a.ng;
-        for (int g = lane; g < a.ng; g += 32) dst[g] = __ldg(src + g) * p2;
-        if (lane == 0) a.wexp[o] = e;
+        return 8.f * warp_max(b);
     }
     struct Fetch {
         uint4 q;
@@ -45,7 +42,7 @@ struct PolicyI4G {
     static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int pk, Row &r) {
         const bool in = o < a.O;
         r.w = in ? a.w + (size_t)o * (size_t)(a.rowbytes) + kq * 16 : nullptr;
-        r.s = in ? static_cast<const float *>(a.sc) + (size_t)o * a.ng : nullptr;
+        r.s = in ? a.scales + (size_t)o * a.ng : nullptr;
         const int gq = a.gs / 32, u0 = 4 * pk + kq;
         r.gi = u0 / gq;
         r.gr = u0 - r.gi * gq;
@@ -66,11 +63,11 @@ struct PolicyI4G {
             ++r.gi;
         }
     }
-    // Weight n -> (n - 8) * scale: bias -(2^23 + 8*16^p) per position.
-    static __device__ __forceinline__ void dequant(const Fetch &f, uint32_t (&col)[16]) {
+    // Weight n -> (n - 8) * scale * 2^E: bias -(2^23 + 8*16^p) per position.
+    static __device__ __forceinline__ void dequant(const Fetch &f, float p2, uint32_t (&col)[16]) {
         constexpr uint64_t kB01 = 0xCB000080CB000008ull, kB23 = 0xCB008000CB000800ull;
         constexpr uint64_t kB42 = 0xCB000800CB080000ull, kB34 = 0xCB080000CB008000ull;
-        const NibPairs sp = nib_scale_pairs(f.s);
+        const NibPairs sp = nib_scale_pairs(f.s * p2);
         const uint32_t wv[4] = {f.q.x, f.q.y, f.q.z, f.q.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -96,7 +93,7 @@ static bool gemm_i4g_tc_ok(const uint16_t *X, const uint8_t *w, int I, int gs) {
 
 size_t ws_gemm_i4g(int M, int I, int O, int gs) {
     if (I % tc::kBKBox != 0 || gs % 32 != 0) return 0;
-    return tc::choose_plan(M, I, O, tc::PolicyI4G::sc_bytes(I, O, gs)).ws_bytes;
+    return tc::choose_plan(M, I, O).ws_bytes;
 }
 
 int run_gemm_i4g_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I, int O,
@@ -104,7 +101,7 @@ int run_gemm_i4g_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *
     *taken = false;
     if (!gemm_i4g_tc_ok(X, w, I, gs)) return kOk;
     *taken = true;
-    const tc::Plan p = tc::choose_plan(M, I, O, tc::PolicyI4G::sc_bytes(I, O, gs));
+    const tc::Plan p = tc::choose_plan(M, I, O);
     if (ws == nullptr || ws_bytes < p.ws_bytes) {
         set_error_detail("qgemm_i4g: this shape needs a workspace of %zu bytes (got %zu)", p.ws_bytes,
                          ws == nullptr ? (size_t)0 : ws_bytes);

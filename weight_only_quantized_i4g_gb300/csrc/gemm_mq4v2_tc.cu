@@ -6,7 +6,6 @@
 // of nibbles; w_j = q_j * scale[h] + zero[h].  Here each weight is formed in
 // f32 with one rounding (a fused multiply-add of the exact q_j, scale and
 // zero), scaled by the row's power of two and rounded to fp16 for the MMA.
-// Row bound: |w| <= max_h (|zero_h| + 15 |scale_h|).
 //
 // A 128-wide K step is exactly one half of a block, so one dequantizing
 // thread takes one header dword and 16 payload bytes (32 weights) per step.
@@ -33,61 +32,51 @@ __device__ __forceinline__ float f16_to_f32(uint32_t h) {
 struct PolicyMq4v2 {
     static constexpr const char *kName = "qgemm_mq4v2 (tensor-core kernel)";
     static constexpr int kBlockBytes = 136;
-    // Scaled headers: f32 pairs [O, I/128] (scale, zero) * 2^E[o], one per
-    // 128-weight half, i.e. per K step.
-    static size_t sc_bytes(int I, int O) { return (size_t)O * (I / 128) * sizeof(float2); }
-    static __device__ __forceinline__ void prep_row(const Args &a, int o, int lane) {
+    // Bound on |w| over row o, q in 0..15: max over the halves of
+    // |zero| + 15 |scale|.  Called by a whole warp.
+    static __device__ __forceinline__ float row_bound(const Args &a, int o, int lane) {
         const uint8_t *row = a.w + (size_t)o * (size_t)a.rowbytes;
-        const int nb = (int)(a.rowbytes / kBlockBytes);
+        const int nb = a.Kt >> 1;
         float b = 0.f;
+#pragma unroll 4
         for (int k = lane; k < nb; k += 32) {
             const uint2 h = __ldg(reinterpret_cast<const uint2 *>(row + (size_t)k * kBlockBytes));
             b = fmaxf(b, fabsf(f16_to_f32(h.x >> 16)) + 15.f * fabsf(f16_to_f32(h.x)));
             b = fmaxf(b, fabsf(f16_to_f32(h.y >> 16)) + 15.f * fabsf(f16_to_f32(h.y)));
         }
-        const int e = range_exponent(warp_max(b));
-        const float p2 = exp2_int(e);
-        float4 *dst = reinterpret_cast<float4 *>(static_cast<float2 *>(a.sc) + (size_t)o * 2 * nb);
-        for (int k = lane; k < nb; k += 32) {
-            const uint2 h = __ldg(reinterpret_cast<const uint2 *>(row + (size_t)k * kBlockBytes));
-            dst[k] = make_float4(f16_to_f32(h.x) * p2, f16_to_f32(h.x >> 16) * p2, f16_to_f32(h.y) * p2,
-                                 f16_to_f32(h.y >> 16) * p2);
-        }
-        if (lane == 0) a.wexp[o] = e;
+        return warp_max(b);
     }
     struct Fetch {
         uint4 q;
-        float2 sz;   // scaled (scale, zero) of the half
+        uint32_t h;   // header of the half: fp16 scale (low), fp16 zero (high)
     };
     struct Row {
-        const uint8_t *b;     // this row's blocks; the payload quarter kq added
-        const float2 *sz;     // this row's scaled headers
+        const uint8_t *b;   // this row's blocks; the payload quarter kq added
     };
     static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int, Row &r) {
-        const bool in = o < a.O;
-        r.b = in ? a.w + (size_t)o * (size_t)a.rowbytes + 16 * kq : nullptr;
-        r.sz = in ? static_cast<const float2 *>(a.sc) + (size_t)o * a.Kt : nullptr;
+        r.b = o < a.O ? a.w + (size_t)o * (size_t)a.rowbytes + 16 * kq : nullptr;
     }
     static __device__ __forceinline__ void clear(Fetch &f) {
         f.q = make_uint4(0u, 0u, 0u, 0u);
-        f.sz = make_float2(0.f, 0.f);
+        f.h = 0u;   // scale 0, zero 0
     }
-    static __device__ __forceinline__ void fetch(const Args &, Row &r, int pk, int, bool, Fetch &f) {
+    static __device__ __forceinline__ void fetch(const Args &, Row &r, int pk, int kq, bool, Fetch &f) {
         if (r.b) {
-            // Payload of half pk & 1 of block pk >> 1, this thread's 16 bytes.
-            const uint8_t *pl = r.b + (size_t)(pk >> 1) * kBlockBytes + 8 + 64 * (pk & 1);
-            const uint2 lo = ldg_w8(pl);
-            const uint2 hi = ldg_w8(pl + 8);
+            const int h = pk & 1;
+            const uint8_t *blk = r.b + (size_t)(pk >> 1) * kBlockBytes;   // kq * 16 bytes past the block
+            const uint2 lo = ldg_w8(blk + 8 + 64 * h);
+            const uint2 hi = ldg_w8(blk + 16 + 64 * h);
             f.q = make_uint4(lo.x, lo.y, hi.x, hi.y);
-            f.sz = __ldg(r.sz + pk);
+            f.h = __ldg(reinterpret_cast<const unsigned *>(blk - 16 * kq + 4 * h));
         }
     }
-    // q -> q * scale + zero: bias -2^23 at every position, then one fused
-    // multiply-add with (scale * 16^-p, zero).
-    static __device__ __forceinline__ void dequant(const Fetch &f, uint32_t (&col)[16]) {
+    // q -> (q * scale + zero) * 2^E: bias -2^23 at every position, then one
+    // fused multiply-add with (scale * 2^E * 16^-p, zero * 2^E).
+    static __device__ __forceinline__ void dequant(const Fetch &f, float p2, uint32_t (&col)[16]) {
         constexpr uint64_t kBias = 0xCB000000CB000000ull;
-        const NibPairs sp = nib_scale_pairs(f.sz.x);
-        const uint64_t z2 = f32_pair(f.sz.y, f.sz.y);
+        const float z = f16_to_f32(f.h >> 16) * p2;
+        const NibPairs sp = nib_scale_pairs(f16_to_f32(f.h) * p2);
+        const uint64_t z2 = f32_pair(z, z);
         const uint32_t wv[4] = {f.q.x, f.q.y, f.q.z, f.q.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -106,7 +95,7 @@ struct PolicyMq4v2 {
 // entry point); the tensor-core kernel also wants a TMA-aligned X.
 size_t ws_gemm_mq4v2(int M, int I, int O) {
     if (I % 256 != 0) return 0;
-    return tc::choose_plan(M, I, O, tc::PolicyMq4v2::sc_bytes(I, O)).ws_bytes;
+    return tc::choose_plan(M, I, O).ws_bytes;
 }
 
 int run_gemm_mq4v2_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
@@ -114,7 +103,7 @@ int run_gemm_mq4v2_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M,
     *taken = false;
     if ((uintptr_t)X % 16 != 0 || I % 256 != 0) return kOk;
     *taken = true;
-    const tc::Plan p = tc::choose_plan(M, I, O, tc::PolicyMq4v2::sc_bytes(I, O));
+    const tc::Plan p = tc::choose_plan(M, I, O);
     if (ws == nullptr || ws_bytes < p.ws_bytes) {
         set_error_detail("qgemm_mq4v2: this shape needs a workspace of %zu bytes (got %zu)", p.ws_bytes,
                          ws == nullptr ? (size_t)0 : ws_bytes);

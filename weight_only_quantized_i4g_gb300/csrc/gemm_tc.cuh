@@ -5,9 +5,10 @@
 //   Y[m, o] = sum_i X[m, i] * w(o, i)       X bf16 [M, I], Y f32 [M, O]
 //
 // where w(o, i) is the format's dequantized weight.  A format supplies a
-// policy F (see gemm_i4g_tc.cu, gemm_fp8b128_tc.cu, gemm_mq4v2_tc.cu): how
-// one thread loads the bytes of 32 consecutive weights of one row for a
-// 128-wide K step, and how it turns them into 16 f16x2 words.
+// policy F (see gemm_i4g_tc.cu, gemm_fp8b128_tc.cu, gemm_mq4v2_tc.cu): a
+// bound on |w| over (part of) a row, how one thread loads the bytes of 32
+// consecutive weights of one row for a 128-wide K step, and how it turns
+// them into 16 f16x2 words.
 //
 // Operand precision.  Both MMA operands are fp16 (11 significant bits), so
 // every product carries a relative error of at most 2^-11 + 2^-24 < 1e-3 and
@@ -16,11 +17,11 @@
 // large terms dominate a sum).  fp16's range is kept by powers of two: a
 // preparation kernel converts each token row of X to fp16 as x * 2^-F[m],
 // with F[m] placing the row's largest finite |x| in [2^14, 2^15) (exact for
-// every element within 2^29 of that maximum), and gives each weight row a
-// scale 2^E[o] that places a bound on its |w| in [2^14, 2^15]; the weight is
-// formed in f32 (one rounding), scaled by 2^E[o] (exact) and rounded to
-// fp16.  The store multiplies the f32 accumulator by 2^(F[m] - E[o])
-// (exact).  The MMA runs at the same rate as with bf16.
+// every element within 2^29 of that maximum); each weight row gets a scale
+// 2^E[o] that places the format's bound on its |w| in [2^14, 2^15] (the
+// same kernel, one warp per row).  The weight is formed in f32 (one
+// rounding), scaled by 2^E[o] (exact) and rounded to fp16.  The store multiplies the f32 accumulator by
+// 2^(F[m] - E[o]) (exact).  The MMA runs at the same rate as with bf16.
 //
 // One persistent thread block per SM, warp-specialized.  Output tile: 128
 // outputs (the weight rows, MMA M) by BT tokens (MMA N), K in steps of 128.
@@ -320,12 +321,16 @@ struct Cfg {
     static constexpr uint32_t kACol0 = 256;                 // A ring after the accumulator
     static constexpr uint32_t kTmemCols = 512;
     static constexpr int kAStagesMax = (int)((kTmemCols - kACol0) / kACols);   // 4
-    static constexpr int kNumBarsFor(int st) { return 2 * st + 2; }
-    static constexpr uint32_t kFixed = 1024 + 16;           // alignment slack + tmem / flag words
-    static constexpr int kStagesFit = (int)((kSmemBudget - kFixed - 8 * kNumBarsFor(kAStagesMax)) / kXBytes);
+    static constexpr int kNumBarsFor(int st) { return 2 * st + 3; }
+    // After the X stages: the barriers, four words (tensor-memory address,
+    // flags), then, 16-byte aligned, the tile's 256 token scales.
+    static constexpr uint32_t kXsOffFor(int st) { return (8u * kNumBarsFor(st) + 16u + 15u) & ~15u; }
+    static constexpr uint32_t kTailFor(int st) { return kXsOffFor(st) + 256u * 4u; }
+    static constexpr int kStagesFit = (int)((kSmemBudget - 1024 - kTailFor(kAStagesMax)) / kXBytes);
     static constexpr int kStages = kStagesFit > kAStagesMax ? kAStagesMax : kStagesFit;
     static constexpr int kNumBars = kNumBarsFor(kStages);
-    static constexpr uint32_t kSmemBytes = kFixed + kStages * kXBytes + 8 * kNumBars;
+    static constexpr uint32_t kXsOff = kXsOffFor(kStages);
+    static constexpr uint32_t kSmemBytes = 1024 + kStages * kXBytes + kTailFor(kStages);   // + alignment slack
     static constexpr int kSlotFloats = kMmaM * BT;          // one partial slot
     static constexpr uint32_t kIdesc = idesc_f16(BT);
     static_assert(kStages >= 3, "at least three stages");
@@ -346,9 +351,8 @@ struct Args {
     long long U;          // (tile, K step) units
     // Written by the preparation kernel:
     uint16_t *xh;         // fp16 copy of X [M, I]: x * 2^-F[m]
-    float *xscale;        // 2^F[m] per token row
+    float *xscale;        // 2^F[m] per token row (padded to whole 256-token blocks)
     int *wexp;            // E[o] per weight row
-    void *sc;             // the format's scales times 2^E (layout per format)
     int *err;
 };
 
@@ -358,6 +362,23 @@ __device__ __forceinline__ float exp2_int(int k) { return __int_as_float((k + 12
 // The exponents F and E are clamped to [-kExpClamp, kExpClamp], so 2^(F-E)
 // is a normal f32 and the store's scaling is one exact product.
 constexpr int kExpClamp = 60;
+
+// Largest value over the warp (fmaxf ignores NaN).
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
+    return v;
+}
+
+// Exponent k with 2^k * v in [2^14, 2^15) for a finite v > 0, clamped;
+// 0 for v = 0 or a non-finite v.
+__device__ __forceinline__ int range_exponent(float v) {
+    if (!(v > 0.f && v <= 3.402823466e38f)) return 0;
+    int e;
+    frexpf(v, &e);   // v = f * 2^e, f in [0.5, 1)
+    return max(-kExpClamp, min(kExpClamp, 15 - e));
+}
+
 
 // Token block and output tile of tile index t.  Normally t = nb * MB + mb;
 // with clusters of two blocks the pair (2j, 2j+1) takes token block j % MB
@@ -387,12 +408,11 @@ __device__ __forceinline__ Seg segment_at(long long u, long long ue, int Kt) {
     return g;
 }
 
-// 16 token scales 2^F[m] from a 16-byte aligned address (the array is padded
-// to whole 256-token blocks).
+// 16 token scales 2^F[m] from shared memory (16-byte aligned).
 __device__ __forceinline__ void load_xscale16(const float *p, float (&xs)[16]) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(p) + j);
+        const float4 v = reinterpret_cast<const float4 *>(p)[j];
         xs[4 * j] = v.x;
         xs[4 * j + 1] = v.y;
         xs[4 * j + 2] = v.z;
@@ -410,13 +430,22 @@ __device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, con
                                               const int q, const int lane, const int et, const long long cta,
                                               const long long U, const long long P, const int Kt,
                                               uint64_t *acc_full, uint64_t *acc_empty, volatile uint32_t *flag,
-                                              volatile uint32_t *abort, const int nslots) {
+                                              volatile uint32_t *abort, const int nslots, float *sxs,
+                                              uint64_t *xs_ready) {
     using C = Cfg<BT>;
     const int row = q * 32 + lane;          // accumulator row = weight row within the tile
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
     int mb, nb;
     tile_coords(g.t, a.MB, a.cluster, mb, nb);
     const int m0 = mb * BT, o = nb * kMmaM + row;
+    const float pe = o < a.O ? exp2_int(-a.wexp[o]) : 0.f;   // 2^-E of this row
+    // The tile's token scales into shared memory, once every epilogue warp is
+    // done with the previous segment's.  With a whole tile (nslots > 1) the
+    // dequantizing warps read them too, after xs_ready.
+    named_sync(1, 32 * kNumEpiWarps);
+    for (int i = et; i < BT; i += 32 * kNumEpiWarps) sxs[i] = a.xscale[m0 + i];
+    named_sync(1, 32 * kNumEpiWarps);
+    if (nslots > 1 && lane == 0) mbar_arrive(xs_ready);
     {
         bool ok = true;
         if (lane == 0) ok = mbar_wait_backoff(acc_full, seg & 1, abort);
@@ -430,11 +459,10 @@ __device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, con
     };
     // Column j of the accumulator is token m0 + j; lanes hold 32
     // consecutive outputs, so each store of a warp is 128 bytes.
-    const float pe = o < a.O ? exp2_int(-a.wexp[o]) : 0.f;
     auto store_chunk = [&](int c, const float (&v)[16]) {
         if (o < a.O) {
             float xs[16];
-            load_xscale16(a.xscale + m0 + c * 16, xs);
+            load_xscale16(sxs + c * 16, xs);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int m = m0 + c * 16 + j;
@@ -533,15 +561,15 @@ __device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, con
 template <int BT>
 __device__ __forceinline__ void store_tile_slice(const Args &a, const Seg g, const uint32_t tmem, const int q,
                                                  const int lane, const int slot, const int nslots,
-                                                 uint64_t *acc_full, volatile uint32_t *abort) {
+                                                 uint64_t *acc_full, volatile uint32_t *abort, const float *sxs,
+                                                 uint64_t *xs_ready, const float pe) {
     bool ok = true;
-    if (lane == 0) ok = mbar_wait_backoff(acc_full, 0u, abort);
+    if (lane == 0) ok = mbar_wait_backoff(acc_full, 0u, abort) && mbar_wait_backoff(xs_ready, 0u, abort);
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) raise_device_error(a.err, kErrTimeout);
     tc_fence_after();
     int mb, nb;
     tile_coords(g.t, a.MB, a.cluster, mb, nb);
     const int o = nb * kMmaM + q * 32 + lane, m0 = mb * BT;
-    const float pe = o < a.O ? exp2_int(-a.wexp[o]) : 0.f;
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
     for (int c = slot; c < BT / 16; c += nslots) {
@@ -549,7 +577,7 @@ __device__ __forceinline__ void store_tile_slice(const Args &a, const Seg g, con
         tmem_ld16(tq + c * 16, r);
         if (o < a.O) {
             float xs[16];
-            load_xscale16(a.xscale + m0 + c * 16, xs);
+            load_xscale16(sxs + c * 16, xs);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int m = m0 + c * 16 + j;
@@ -570,10 +598,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
     const uint32_t sbase = smem_addr(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kXBytes);
     uint64_t *full = bars, *empty = bars + C::kStages;   // per stage: X bytes + dequantized A / MMA done
-    uint64_t *acc_full = empty + C::kStages, *acc_empty = acc_full + 1;
+    uint64_t *acc_full = empty + C::kStages, *acc_empty = acc_full + 1, *xs_ready = acc_full + 2;
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bars + C::kNumBars);
     volatile uint32_t *flag = tmem_slot + 1;    // epilogue broadcast: this block finishes the tile
     volatile uint32_t *abort = tmem_slot + 2;   // set by the first wait that times out
+    float *sxs = reinterpret_cast<float *>(smem + C::kStages * C::kXBytes + C::kXsOff);   // the tile's token scales
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -584,6 +613,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kNumEpiWarps);
+        mbar_init(xs_ready, kNumEpiWarps);
         *abort = 0u;
         mbar_fence_init();
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
@@ -691,7 +721,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         for (long long u = ub; u < ue; ++seg) {
             const Seg g = segment_at(u, ue, Kt);
             epilogue_segment<BT>(a, g, seg, tmem, warp & 3, lane, threadIdx.x - 32 * kWarpEpi, cta, U, P, Kt,
-                                 acc_full, acc_empty, flag, abort, whole_only ? kEpiSlots : 1);
+                                    acc_full, acc_empty, flag, abort, whole_only ? kEpiSlots : 1, sxs, xs_ready);
             u = g.t * Kt + g.ke;
         }
     } else {
@@ -703,8 +733,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         const int R = q * 32 + lane;
         const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + C::kACol0 + kq * (C::kACols / 4);
         using Fetch = typename F::Fetch;
-        // The row exponents come from the preparation kernel.
-        griddep_wait();
         // Fetch state: the next unit to load and the format's state of this
         // thread's row (set again when the tile changes).
         typename F::Row row;
@@ -729,18 +757,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
                 }
             }
         };
+        // Step state: the tile of the unit being dequantized and this row's
+        // 2^E there (E from the preparation kernel, read after its grid is
+        // done; once per tile).
+        long long st_t = ub / Kt;
+        int st_k = (int)(ub - st_t * Kt), e = 0;
+        float p2 = 0.f;
+        auto load_exp = [&]() {
+            int mb, nb;
+            tile_coords(st_t, a.MB, a.cluster, mb, nb);
+            const int o = nb * kMmaM + R;
+            e = o < a.O ? a.wexp[o] : 0;
+            p2 = exp2_int(e);
+        };
         uint32_t it = 0;
         auto step = [&](const Fetch &cur) {
             const uint32_t s = it % C::kStages, r = it / C::kStages;
             if (r > 0 && !mbar_wait_or_abort(&empty[s], (r & 1) ^ 1, abort)) raise_device_error(a.err, kErrTimeout);
             tc_fence_after();
             uint32_t col[16];
-            F::dequant(cur, col);
+            F::dequant(cur, p2, col);
             tmem_st16(ta + s * C::kACols, col);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[s]);
             ++it;
+            if (++st_k == Kt) {   // the next unit, if any, starts a tile
+                st_k = 0;
+                ++st_t;
+                if (ub + it < ue) load_exp();
+            }
         };
         // Three register buffers used in rotation with fixed names, so a
         // buffer is read only when its loads were issued three K steps ago.
@@ -749,6 +795,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         fetch(f0);
         fetch(f1);
         fetch(f2);
+        // The weights' loads are in flight; the row exponents come from the
+        // preparation kernel.
+        griddep_wait();
+        load_exp();
         for (long long u = ub; u < ue;) {
             step(f0);
             fetch(f0);
@@ -760,9 +810,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
             fetch(f2);
             ++u;
         }
-        if (whole_only) {
-            store_tile_slice<BT>(a, segment_at(ub, ue, Kt), tmem, q, lane, 1 + kq, kEpiSlots, acc_full, abort);
-        }
+        if (whole_only)
+            store_tile_slice<BT>(a, segment_at(ub, ue, Kt), tmem, q, lane, 1 + kq, kEpiSlots, acc_full, abort, sxs,
+                                 xs_ready, exp2_int(-e));
     }
 
     tc_fence_before();
@@ -775,30 +825,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
     }
 }
 
-// Largest value over the warp (fmaxf ignores NaN).
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, d));
-    return v;
-}
-
-// Exponent k with 2^k * v in [2^14, 2^15) for a finite v > 0, clamped;
-// 0 for v = 0 or a non-finite v.
-__device__ __forceinline__ int range_exponent(float v) {
-    if (!(v > 0.f && v <= 3.402823466e38f)) return 0;
-    int e;
-    frexpf(v, &e);   // v = f * 2^e, f in [0.5, 1)
-    return max(-kExpClamp, min(kExpClamp, 15 - e));
-}
-
 // Operand preparation.  Blocks 0 .. M-1 take one token row of X each: F[m]
-// from the row's largest finite |x|, then Xh = fp16(x * 2^-F[m]).  A row of
-// up to kPrepRegChunks * 2048 elements is held in registers (all its loads
-// in flight at once); a longer one is read twice (the second pass hits the
-// cache).  The remaining blocks take eight weight rows each, one warp per
-// row (F::prep_row): E[o] from the format's bound on |w(o, .)|, and the
-// row's scales times 2^E[o] into the workspace, so the main kernel's
-// dequantization needs no extra step.
+// from the row's largest finite |x|, then Xh = fp16(x * 2^-F[m]) and
+// xscale[m] = 2^F[m].  A row of up to kPrepRegChunks * 2048 elements is held
+// in registers (all its loads in flight at once); a longer one is read twice
+// (the second pass hits the cache).  The remaining blocks take eight weight
+// rows each, one warp per row: E[o] from the format's bound on |w(o, .)|.
 constexpr int kPrepThreads = 256;
 constexpr int kPrepRegChunks = 8;   // 16-byte chunks per thread kept in registers
 
@@ -822,58 +854,67 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v, float sc) {
 
 template <class F>
 __global__ void __launch_bounds__(kPrepThreads) gemm_tc_prep_kernel(Args a, const uint16_t *__restrict__ X, int I) {
+    // The main kernel may launch once every block of this one runs (its
+    // blocks take an SM as this kernel's leave it); it waits for this grid's
+    // completion before it reads what this one writes.
+    griddep_launch_dependents();
     // X may be the previous kernel's output, and that kernel may still read
     // this workspace.
     griddep_wait();
-    __shared__ float red[kPrepThreads / 32];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    if (blockIdx.x < (unsigned)a.M) {
-        const int m = blockIdx.x;
-        const uint4 *src = reinterpret_cast<const uint4 *>(X + (size_t)m * I);
-        uint4 *dst = reinterpret_cast<uint4 *>(a.xh + (size_t)m * I);
-        const int n8 = I / 8;
-        const bool in_regs = n8 <= kPrepRegChunks * kPrepThreads;
-        uint4 v[kPrepRegChunks];
-        float mx = 0.f;
-        if (in_regs) {
-#pragma unroll
-            for (int j = 0; j < kPrepRegChunks; ++j) {
-                const int c = threadIdx.x + j * kPrepThreads;
-                v[j] = c < n8 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int j = 0; j < kPrepRegChunks; ++j)
-                mx = bf16x2_absmax(v[j].w, bf16x2_absmax(v[j].z, bf16x2_absmax(v[j].y, bf16x2_absmax(v[j].x, mx))));
-        } else {
-#pragma unroll 4
-            for (int c = threadIdx.x; c < n8; c += kPrepThreads) {
-                const uint4 u = __ldg(src + c);
-                mx = bf16x2_absmax(u.w, bf16x2_absmax(u.z, bf16x2_absmax(u.y, bf16x2_absmax(u.x, mx))));
-            }
+    if (blockIdx.x >= (unsigned)a.M) {
+        const int o = (blockIdx.x - a.M) * (kPrepThreads / 32) + wid;
+        if (o < a.O) {
+            const int e = range_exponent(F::row_bound(a, o, lane));
+            if (lane == 0) a.wexp[o] = e;
         }
-        mx = warp_max(mx);
-        if (lane == 0) red[wid] = mx;
-        __syncthreads();
-        mx = red[0];
-#pragma unroll
-        for (int k = 1; k < kPrepThreads / 32; ++k) mx = fmaxf(mx, red[k]);
-        const int fm = -range_exponent(mx);
-        const float sc = exp2_int(-fm);
-        if (in_regs) {
-#pragma unroll
-            for (int j = 0; j < kPrepRegChunks; ++j) {
-                const int c = threadIdx.x + j * kPrepThreads;
-                if (c < n8) dst[c] = bf16x8_to_f16x8(v[j], sc);
-            }
-        } else {
-#pragma unroll 4
-            for (int c = threadIdx.x; c < n8; c += kPrepThreads) dst[c] = bf16x8_to_f16x8(__ldg(src + c), sc);
-        }
-        if (threadIdx.x == 0) a.xscale[m] = exp2_int(fm);
-    } else {
-        const long long o = (long long)(blockIdx.x - a.M) * (kPrepThreads / 32) + wid;
-        if (o < a.O) F::prep_row(a, (int)o, lane);
+        return;
     }
+    __shared__ float red[kPrepThreads / 32];
+    const int m = blockIdx.x;
+    uint16_t *xh = a.xh;
+    float *xscale = a.xscale;
+    const uint4 *src = reinterpret_cast<const uint4 *>(X + (size_t)m * I);
+    uint4 *dst = reinterpret_cast<uint4 *>(xh + (size_t)m * I);
+    const int n8 = I / 8;
+    const bool in_regs = n8 <= kPrepRegChunks * kPrepThreads;
+    uint4 v[kPrepRegChunks];
+    float mx = 0.f;
+    if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < kPrepRegChunks; ++j) {
+            const int c = threadIdx.x + j * kPrepThreads;
+            v[j] = c < n8 ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kPrepRegChunks; ++j)
+            mx = bf16x2_absmax(v[j].w, bf16x2_absmax(v[j].z, bf16x2_absmax(v[j].y, bf16x2_absmax(v[j].x, mx))));
+    } else {
+#pragma unroll 4
+        for (int c = threadIdx.x; c < n8; c += kPrepThreads) {
+            const uint4 u = __ldg(src + c);
+            mx = bf16x2_absmax(u.w, bf16x2_absmax(u.z, bf16x2_absmax(u.y, bf16x2_absmax(u.x, mx))));
+        }
+    }
+    mx = warp_max(mx);
+    if (lane == 0) red[wid] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int k = 1; k < kPrepThreads / 32; ++k) mx = fmaxf(mx, red[k]);
+    const int fm = -range_exponent(mx);
+    const float sc = exp2_int(-fm);
+    if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < kPrepRegChunks; ++j) {
+            const int c = threadIdx.x + j * kPrepThreads;
+            if (c < n8) dst[c] = bf16x8_to_f16x8(v[j], sc);
+        }
+    } else {
+#pragma unroll 4
+        for (int c = threadIdx.x; c < n8; c += kPrepThreads) dst[c] = bf16x8_to_f16x8(__ldg(src + c), sc);
+    }
+    if (threadIdx.x == 0) xscale[m] = exp2_int(fm);
 }
 
 // ---------------------------------------------------------------------------
@@ -904,26 +945,25 @@ struct Plan {
     int cluster;          // whole tiles in pairs sharing X by multicast
     long long T, U;
     // Workspace: tile counters, partial slots (split plans only), 2^F per
-    // token (padded to whole 256-token blocks), E per weight row, the
-    // scaled scales, the fp16 copy of X; every part 256-byte aligned.
-    size_t counter_bytes, xscale_off, wexp_off, sc_off, xh_off, ws_bytes;
+    // token (padded to whole 256-token blocks; the tail is never stored),
+    // E per weight row, the fp16 copy of X; every part 256-byte aligned.
+    size_t counter_bytes, xscale_off, wexp_off, xh_off, ws_bytes;
 };
 
 inline size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 inline bool plan_splits(const Plan &p) { return !(p.U % p.P == 0 && (p.U / p.P) % p.Kt == 0); }
 
-inline void plan_layout(Plan &p, int M, int I, int O, size_t sc_bytes) {
+inline void plan_layout(Plan &p, int M, int I, int O) {
     p.counter_bytes = align256((size_t)p.T * sizeof(unsigned));
     const size_t partial_bytes = plan_splits(p) ? (size_t)2 * p.P * kMmaM * p.bt * sizeof(float) : 0;
     p.xscale_off = p.counter_bytes + partial_bytes;
     p.wexp_off = p.xscale_off + align256((((size_t)M + 255) / 256) * 256 * sizeof(float));
-    p.sc_off = p.wexp_off + align256((size_t)O * sizeof(int));
-    p.xh_off = p.sc_off + align256(sc_bytes);
+    p.xh_off = p.wexp_off + align256((size_t)O * sizeof(int));
     p.ws_bytes = p.xh_off + align256((size_t)M * I * sizeof(uint16_t));
 }
 
-inline Plan make_plan(int tile, int M, int I, int O, int nsm, size_t sc_bytes) {
+inline Plan make_plan(int tile, int M, int I, int O, int nsm) {
     Plan p;
     p.tile = tile;
     p.bt = kTileBT[tile];
@@ -940,7 +980,7 @@ inline Plan make_plan(int tile, int M, int I, int O, int nsm, size_t sc_bytes) {
     // it issues, bound the step, and multicast leaves those unchanged.  The
     // planner does not pick it.
     p.cluster = 0;
-    plan_layout(p, M, I, O, sc_bytes);
+    plan_layout(p, M, I, O);
     return p;
 }
 
@@ -959,19 +999,18 @@ inline double plan_cost(const Plan &p) {
 
 // Both launch shapes for every token width: one whole tile per block when
 // the tiles fit in one wave, and the stream-K split over all SMs.
-// `sc_bytes`: the format's scaled-scale array.
-inline Plan choose_plan(int M, int I, int O, size_t sc_bytes) {
+inline Plan choose_plan(int M, int I, int O) {
     const int nsm = num_sms();
-    Plan best = make_plan(0, M, I, O, nsm, sc_bytes);
+    Plan best = make_plan(0, M, I, O, nsm);
     double best_cost = plan_cost(best);
     for (int t = 0; t < kNumTiles; ++t) {
         for (int mode = 0; mode < 2; ++mode) {
-            Plan p = make_plan(t, M, I, O, nsm, sc_bytes);
+            Plan p = make_plan(t, M, I, O, nsm);
             if (mode == 1) {
                 if (p.T >= nsm) continue;   // already the split over all SMs
                 p.P = (int)std::min<long long>(nsm, p.U);
                 p.cluster = 0;
-                plan_layout(p, M, I, O, sc_bytes);
+                plan_layout(p, M, I, O);
             }
             const double c = plan_cost(p);
             if (c < best_cost) {
@@ -1024,7 +1063,6 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, Args args, int M, in
     unsigned char *wsb = static_cast<unsigned char *>(ws);
     args.xscale = reinterpret_cast<float *>(wsb + p.xscale_off);
     args.wexp = reinterpret_cast<int *>(wsb + p.wexp_off);
-    args.sc = wsb + p.sc_off;
     args.xh = reinterpret_cast<uint16_t *>(wsb + p.xh_off);
     CUtensorMap tmX;
     const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)M};
