@@ -832,7 +832,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
 // (the second pass hits the cache).  The remaining blocks take eight weight
 // rows each, one warp per row: E[o] from the format's bound on |w(o, .)|.
 constexpr int kPrepThreads = 256;
-constexpr int kPrepRegChunks = 8;   // 16-byte chunks per thread kept in registers
+constexpr int kPrepRegChunks = 4;   // 16-byte chunks per thread kept in registers
 
 __device__ __forceinline__ float bf16x2_absmax(uint32_t w, float mx) {
     const float lo = fabsf(__uint_as_float(w << 16)), hi = fabsf(__uint_as_float(w & 0xFFFF0000u));
@@ -853,7 +853,7 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v, float sc) {
 }
 
 template <class F>
-__global__ void __launch_bounds__(kPrepThreads) gemm_tc_prep_kernel(Args a, const uint16_t *__restrict__ X, int I) {
+__global__ void __launch_bounds__(kPrepThreads, 8) gemm_tc_prep_kernel(Args a, const uint16_t *__restrict__ X, int I) {
     // The main kernel may launch once every block of this one runs (its
     // blocks take an SM as this kernel's leave it); it waits for this grid's
     // completion before it reads what this one writes.
