@@ -541,19 +541,22 @@ PREFILL_OTHER = (("fp8", 7168, 16384), ("fp8", 24576, 7168), ("mq4", 5120, 17408
 FMT_ID = {"i4g": 4, "fp8": 7, "mq4": 44}
 
 
-def prefill_measure(qg, torch, dev, stream, reps=20, other=True):
+def prefill_measure(qg, torch, dev, stream, reps=20, other=True, shapes=None):
     """The fmt=4 batched-prefill GEMM of the workload's prefill config:
     Y[512, O] = X[512, 7168] . W^T for O = 7168 and 2048, gs = 64, plus the
     fmt=7 and MQ4-V2 prefill GEMMs at M = 512 on their decode shapes
     ("other_formats").  Weights and activations from seeded generators on
     the device.  Each call is timed alone with CUDA events on its stream
     after a 256 MiB write that flushes L2; median of `reps`.  Returns TFLOP/s
-    (2*M*I*O per call) and the fraction of the measured dense bf16 peak."""
+    (2*M*I*O per call) and the fraction of the measured dense bf16 peak.
+    `shapes` (fmt, O, I) replaces all of them (profiling runs)."""
     peak, kind = load_tensor_peak()
     M, I = PREFILL_M, PREFILL_I
     out = {"workload": f"fmt4 int4-g64 prefill GEMM, M={M}, I={I}, O in {list(PREFILL_O)}, "
                        f"bf16 activations, f32 out",
-           "bound": "tensor", "peak": peak, "unit": "TFLOP/s", "peak_kind": kind, "calls": {}}
+           "bound": "tensor", "peak": peak, "unit": "TFLOP/s",
+           "peak_kind": f"{kind} bf16 x 1 (the contraction is fp16 x fp16 -> f32; fp16 and bf16 dense rates are "
+                        f"equal)", "calls": {}}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     launches = 0
 
@@ -575,6 +578,10 @@ def prefill_measure(qg, torch, dev, stream, reps=20, other=True):
         return {"us": round(t * 1e6, 2), "tflops": round(tf, 1), "frac": round(tf / peak, 4)}
 
     with torch.cuda.stream(stream):
+        if shapes is not None:
+            out["calls"] = {f"{fmt} {M}x{O}x{I2}": run_one(fmt, O, I2) for fmt, O, I2 in shapes}
+            out["launches_timed"] = launches
+            return out
         for O in PREFILL_O:
             out["calls"][f"{M}x{O}x{I}"] = run_one("i4g", O, I)
         if other:
@@ -715,13 +722,35 @@ def main():
     ap.add_argument("--no-prefill", dest="prefill", action="store_false",
                     help="skip the prefill GEMM measurement")
     ap.add_argument("--only", default="", help="comma-separated subset of the shapes (profiling runs)")
+    ap.add_argument("--prefill-only", default="",
+                    help="profiling runs: time only these prefill GEMMs (comma-separated fmt:O:I, fmt in "
+                         "i4g/fp8/mq4, M=512) and print their prefill object")
+    ap.add_argument("--prefill-reps", type=int, default=20)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.prefill_only:
+        prefill_only(args)
+    elif args.impl == "reference":
         reference_arm(args)
     else:
         ours_arm(args)
+
+
+def prefill_only(args):
+    import torch
+    import weight_only_quantized_i4g_gb300 as qg
+    shapes = []
+    for item in args.prefill_only.split(","):
+        fmt, O, I = item.split(":")
+        if fmt not in FMT_ID:
+            raise SystemExit(f"--prefill-only: unknown format {fmt!r}")
+        shapes.append((fmt, int(O), int(I)))
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream()
+    out = prefill_measure(qg, torch, dev, stream, reps=args.prefill_reps, shapes=shapes)
+    print(json.dumps({"prefill": out}), flush=True)
 
 
 if __name__ == "__main__":
