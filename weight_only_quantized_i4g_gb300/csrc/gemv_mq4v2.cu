@@ -15,6 +15,10 @@
 //
 // Paths: staged (gemv_tma.cuh) when the rows are a whole number of 16-byte
 // lines (I/256 even) and blocks and x are 16-byte aligned; direct otherwise.
+// The staged path at one token (FmtMq4v2H) multiplies in the mixed-precision
+// form fp16 x fp16 -> f32: one AND leaves two nibbles as fp16 subnormals
+// (exact), which halves the integer-pipe work per weight, the bottleneck of
+// the f32 pair form at batch 1; products stay exact and the accumulation f32.
 #include "gemv_cs.cuh"
 #include "gemv_tma.cuh"
 #include "launch.h"
@@ -195,6 +199,134 @@ struct FmtMq4v2 {
     }
 };
 
+// Batch-1 staged variant: fp16 activations, mixed-precision products.
+//
+// Per 32-bit word of nibbles n0..n7 (bits 4k), four ANDs leave f16x2 pairs
+//   (n0, n4) * 2^-24   (n1, n5) * 2^-20   (n2, n6) * 2^-24   (n3, n7) * 2^-20
+// (fp16 subnormals: the bit pattern n * 16^p with p <= 1 read as fp16 is
+// exactly n * 16^p * 2^-24); the second pair of each comes from the word
+// shifted down by 8.  Each multiplies, in fma.rn.f32.f16, the matching
+// activations held as fp16 pairs, pre-scaled by 2^(141 - F) for the 2^-24
+// positions and 2^(137 - F) for the 2^-20 ones, F being the exponent field
+// of the thread's largest finite |x|: the scaled activations stay below
+// 2^15, bf16 -> fp16 is exact for every x within 2^29 of that maximum (2^25
+// for the 2^-20 positions), and every product is n * x * 2^(117 - F)
+// exactly, accumulated in f32.
+struct FmtMq4v2H : FmtMq4v2 {
+    static constexpr int kPairsPerWord = 2;   // two 64-bit registers = four fp16 pairs per word
+
+    // Raw bf16 activations in slot order: word w of the unit holds slots
+    // (x[8w], x[8w+4]), (x[8w+1], x[8w+5]) in xp[2w] and (x[8w+2], x[8w+6]),
+    // (x[8w+3], x[8w+7]) in xp[2w+1]; prepare_x converts them to scaled fp16.
+    template <int XU, int NP>
+    __device__ static void load_x(const Params &p, int s, int u, uint64_t (&xp)[NP], float &xsum) {
+        static_assert(NP == XU / 4, "four activations per 64-bit register");
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < XU / 8; ++w) {
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (u >= 0) q = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)s * p.I + (size_t)u * XU) + w);
+            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) sum += __uint_as_float(wv[i] << 16) + __uint_as_float(wv[i] & 0xFFFF0000u);
+            uint32_t s0, s1, s2, s3;
+            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(s0) : "r"(q.x), "r"(q.z));
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(s1) : "r"(q.x), "r"(q.z));
+            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(s2) : "r"(q.y), "r"(q.w));
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(s3) : "r"(q.y), "r"(q.w));
+            xp[2 * w] = (uint64_t)s0 | ((uint64_t)s1 << 32);
+            xp[2 * w + 1] = (uint64_t)s2 | ((uint64_t)s3 << 32);
+        }
+        xsum = sum;
+    }
+
+    typedef Pow2Pair ThreadScale;   // 2^(F - 117) as two factors
+
+    // bf16 pair -> fp16 pair of x * k1 * k2 (both factors powers of two).
+    __device__ static uint32_t bf16x2_to_scaled_f16x2(uint32_t b, float k1, float k2) {
+        const float lo = __uint_as_float(b << 16) * k1 * k2, hi = __uint_as_float(b & 0xFFFF0000u) * k1 * k2;
+        uint32_t r;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+
+    template <int U, int S, int NP>
+    __device__ static ThreadScale prepare_x(uint64_t (&xp)[U][S][NP], float (&)[U][S]) {
+        // largest finite |x| as a bf16 magnitude pattern (patterns >= 0x7F80 are inf / NaN)
+        uint32_t m = 0;
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+#pragma unroll
+                for (int i = 0; i < NP; ++i)
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint32_t v = (uint32_t)(xp[j][s][i] >> (16 * h)) & 0x7FFFu;
+                        if (v < 0x7F80u && v > m) m = v;
+                    }
+        int F = (int)(m >> 7);                       // exponent field
+        if (F < 1) F = 1;
+        const int k24 = 141 - F, k20 = 137 - F;      // in [-117, 140]
+        const float a24 = pow2i(k24 >> 1), b24 = pow2i(k24 - (k24 >> 1));
+        const float a20 = pow2i(k20 >> 1), b20 = pow2i(k20 - (k20 >> 1));
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    // xp[2w] = slots (0, 1): 2^-24 then 2^-20 positions; xp[2w+1] likewise
+                    const uint32_t lo = (uint32_t)xp[j][s][i], hi = (uint32_t)(xp[j][s][i] >> 32);
+                    xp[j][s][i] = (uint64_t)bf16x2_to_scaled_f16x2(lo, a24, b24) |
+                                  ((uint64_t)bf16x2_to_scaled_f16x2(hi, a20, b20) << 32);
+                }
+        const int c = F - 117;                       // in [-116, 137]
+        return Pow2Pair{pow2i(c >> 1), pow2i(c - (c >> 1))};
+    }
+
+    // a0 += n(lo) * x(lo), a1 += n(hi) * x(hi), fp16 inputs, f32 result
+    __device__ static void fma_mixed2(float &a0, float &a1, uint32_t n2, uint32_t x2) {
+        asm("{.reg .f16 nl, nh, xl, xh;\n\t"
+            "mov.b32 {nl, nh}, %2;\n\t"
+            "mov.b32 {xl, xh}, %3;\n\t"
+            "fma.rn.f32.f16 %0, nl, xl, %0;\n\t"
+            "fma.rn.f32.f16 %1, nh, xh, %1;\n\t}"
+            : "+f"(a0), "+f"(a1)
+            : "r"(n2), "r"(x2));
+    }
+
+    // sum (q*scale + zero) * x = scale * 2^(F-117) * sum(q * x * 2^(117-F)) + zero * xsum
+    template <int S, int NW, int NP>
+    __device__ static void accumulate(const Words<NW> &wd, uint32_t hd, const uint64_t (&xp)[S][NP],
+                                      const float (&xsum)[S], ThreadScale ts, float *part) {
+        uint32_t n[NW][4];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const uint32_t v = wd.w[w] >> 8;
+            n[w][0] = wd.w[w] & 0x000F000Fu;
+            n[w][1] = wd.w[w] & 0x00F000F0u;
+            n[w][2] = v & 0x000F000Fu;
+            n[w][3] = v & 0x00F000F0u;
+        }
+        const float scale = f16_bits_to_f32((uint16_t)(hd & 0xFFFFu)) * ts.p1;
+        const float zero = f16_bits_to_f32((uint16_t)(hd >> 16));
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const uint64_t x01 = xp[s][2 * w], x23 = xp[s][2 * w + 1];
+                fma_mixed2(a0, a1, n[w][0], (uint32_t)x01);
+                fma_mixed2(a0, a1, n[w][1], (uint32_t)(x01 >> 32));
+                fma_mixed2(a0, a1, n[w][2], (uint32_t)x23);
+                fma_mixed2(a0, a1, n[w][3], (uint32_t)(x23 >> 32));
+            }
+            part[s] = fmaf(scale, (a0 + a1) * ts.p2, fmaf(zero, xsum[s], part[s]));
+        }
+    }
+};
+
 // ---------------------------------------------------------------------------
 // dispatch
 // ---------------------------------------------------------------------------
@@ -265,15 +397,17 @@ void launch_tma_mq4_u(const FmtMq4v2::Params &p, float *out, const TmaPlan &pl, 
     constexpr int NW = S <= 2 ? 4 : S <= 4 ? 2 : 1;
     if constexpr (S == 1) {
         if (pl.U == 2) {
-            launch_tma<FmtMq4v2, S, NW, 2, RB>(p, out, pl, st);
+            launch_tma<FmtMq4v2H, S, NW, 2, RB>(p, out, pl, st);
             return;
         }
         if (pl.U == 3) {
-            launch_tma<FmtMq4v2, S, NW, 3, RB>(p, out, pl, st);
+            launch_tma<FmtMq4v2H, S, NW, 3, RB>(p, out, pl, st);
             return;
         }
+        launch_tma<FmtMq4v2H, S, NW, 1, RB>(p, out, pl, st);
+    } else {
+        launch_tma<FmtMq4v2, S, NW, 1, RB>(p, out, pl, st);
     }
-    launch_tma<FmtMq4v2, S, NW, 1, RB>(p, out, pl, st);
 }
 
 template <int S>
