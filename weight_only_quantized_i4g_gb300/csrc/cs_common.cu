@@ -143,7 +143,7 @@ CsPlan cs_plan(int units, int O, int u, int rb, int regs_per_thread) {
 // ---------------------------------------------------------------------------
 // plan of the staged (TMA) kernel
 // ---------------------------------------------------------------------------
-bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl) {
+bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl, int max_per_sm) {
     int U = 1, splits = 1;
     int max_thr = tma_max_consumer_warps(S, 1) * 32;
     if (g.units > max_thr) {
@@ -173,7 +173,7 @@ bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan
     int nst = 0;
     int target = 16 / nc;
     if (target < 1) target = 1;
-    if (target > 8) target = 8;
+    if (target > max_per_sm) target = max_per_sm;
     for (; target >= 1; --target) {
         long budget = 233472L / target - 1024;
         if (budget > 232448) budget = 232448;
@@ -200,6 +200,18 @@ bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan
 }
 
 bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl) {
+    // A small matrix (a few MB) is over in a few microseconds, and every
+    // block loads the whole activation row: with several blocks per SM that
+    // load rivals the weights the SM streams (fmt=4 2048x7168 with f32 x:
+    // 28 KB of x per block against 54 KB of weights per SM).  One block per
+    // SM with 8-row batches measured 30% faster there (6.2 -> 4.3 us).
+    if (S <= 2 && (double)O * (g.rowbytes + g.arowbytes) < 32e6) {
+        TmaPlan t;
+        if (tma_plan(g, S, O, 8, next_pow2(8 * S), U_max, &t, 1) && (long)t.nrowb * t.splits >= num_sms()) {
+            *pl = t;
+            return true;
+        }
+    }
     const int cands[3] = {8, 4, 2};
     bool have = false, have_bal = false;
     TmaPlan last, bal;

@@ -436,10 +436,13 @@ struct TmaGeom {
     uint32_t arowbytes;       // staged side-data bytes per row
 };
 
-bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl);
+// Plan of RB-row batches; at most max_per_sm blocks per SM share its shared
+// memory (the ring is sized for that many).
+bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl, int max_per_sm = 8);
 
-// Plan with the largest batch (8, 4 or 2 rows; only 4 or 2 when S > 2, only 8
-// or 4 when a thread owns several units) that gives every resident block at
+// Plan for a matrix of a few MB at S <= 2: one block per SM, 8-row batches.
+// Otherwise the largest batch (8, 4 or 2 rows; only 4 or 2 when S > 2, only
+// 8 or 4 when a thread owns several units) that gives every resident block at
 // least three batches to overlap with an even last wave (mean batches per
 // block >= 92% of the maximum), else the most even of those; short matrices
 // get 2-row batches.
