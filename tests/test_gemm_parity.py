@@ -312,3 +312,63 @@ def test_gemm_mq4_repeatable(qg):
     Y1 = run_gemm_mq4(qg, X, blocks, M, I, O, ws)
     Y2 = run_gemm_mq4(qg, X, blocks, M, I, O, ws)
     assert np.array_equal(Y1, Y2)
+
+
+# ----------------------------------------------------------------------------
+# Range: the tensor-core path keeps fp16 operands in range with a power of
+# two per token row and per weight row; rows spanning many binades must
+# still meet the bound.
+# ----------------------------------------------------------------------------
+
+ROW_POW2 = np.array([-50, -33, -20, -1, 0, 7, 20, 33, 50], np.float64)
+
+
+def scaled_rows(X_bits, pows):
+    x = synth.bf16_to_f32(X_bits).astype(np.float64)
+    x *= np.exp2(pows[np.arange(x.shape[0]) % len(pows)])[:, None]
+    return synth.bf16_bits(x.astype(np.float32)).reshape(X_bits.shape)
+
+
+def test_gemm_i4g_rows_across_binades(qg):
+    M, I, O, gs = 18, 512, 260, 64
+    X, wq, sc = gemm_inputs(M, I, O, gs, 51)
+    X = scaled_rows(X, ROW_POW2)
+    sc = (sc.astype(np.float64) * np.exp2(ROW_POW2[np.arange(O) % len(ROW_POW2)])[:, None]).astype(np.float32)
+    Y = run_gemm(qg, X, wq, sc, M, I, O, gs)
+    ref, mag = par_rows(orc().qgemm_i4g, O, X, wq, sc, M, I, O, gs)
+    compare(Y, ref, mag, what="fmt4 gemm rows across binades")
+
+
+def test_gemm_fp8_rows_across_binades(qg):
+    M, I, O = 18, 512, 384
+    codes, scales, X = fp8_inputs(O, I, M, tag=52)
+    X = scaled_rows(X, ROW_POW2)
+    scales = (scales.astype(np.float64) * np.exp2(np.array([-40.0, 0.0, 40.0]))[:, None]).astype(np.float32)
+    Y = run_gemm_fp8(qg, X, codes, scales, M, I, O)
+    ref, mag = par_rows(orc().qgemv_fp8b128, O, X, codes, scales, M, I, O, step=128)
+    compare(Y, ref, mag, what="fp8 gemm rows across binades")
+
+
+def test_gemm_mq4_rows_across_binades(qg):
+    M, I, O = 18, 512, 200
+    X, blocks = mq4_inputs(O, I, M, tag=53)
+    X = scaled_rows(X, ROW_POW2)
+    Y = run_gemm_mq4(qg, X, blocks, M, I, O)
+    ref, mag = par_rows(orc().qgemv_mq4v2, O, X, blocks, M, I, O)
+    compare(Y, ref, mag, what="mq4 gemm rows across binades")
+
+
+def test_gemm_nonfinite_x_propagates(qg):
+    """An inf or NaN activation makes its token row's outputs non-finite,
+    as in the oracle (the row's power of two comes from its finite values)."""
+    M, I, O, gs = 6, 256, 130, 64
+    X, wq, sc = gemm_inputs(M, I, O, gs, 54)
+    X = X.copy()
+    X[1, 17] = 0x7FC0          # NaN
+    X[4, 200] = 0x7F80         # +inf
+    Y = run_gemm(qg, X, wq, sc, M, I, O, gs)
+    ref, mag = par_rows(orc().qgemm_i4g, O, X, wq, sc, M, I, O, gs)
+    assert np.array_equal(np.isnan(Y), np.isnan(ref))
+    assert np.array_equal(np.isinf(Y), np.isinf(ref))
+    fin = np.isfinite(ref)
+    compare(Y[fin], ref[fin], mag[fin], what="gemm finite rows")
