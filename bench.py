@@ -365,9 +365,16 @@ def ours_arm(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # W warm-up steps, then more until at least half a second of GPU work has
+    # run: the SM clock of an idle GPU takes a while to reach its maximum.
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
+        t_warm = time.time()
+        while time.time() - t_warm < 0.5:
+            for _ in range(50):
+                step()
+            torch.cuda.synchronize()
     barrier()
 
     # The dominant call is bracketed by CUDA events on every DOM_EVERY-th

@@ -143,7 +143,8 @@ CsPlan cs_plan(int units, int O, int u, int rb, int regs_per_thread) {
 // ---------------------------------------------------------------------------
 // plan of the staged (TMA) kernel
 // ---------------------------------------------------------------------------
-bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl, int max_per_sm) {
+bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl, int max_per_sm,
+              int one_block_slots) {
     int U = 1, splits = 1;
     int max_thr = tma_max_consumer_warps(S, 1) * 32;
     if (g.units > max_thr) {
@@ -179,6 +180,7 @@ bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan
         if (budget > 232448) budget = 232448;
         nst = (int)(budget / per_slot);
         if (nst > 6) nst = 6;
+        if (target == 1 && nst > one_block_slots) nst = one_block_slots;
         if (nst >= 2) break;
     }
     if (nst < 2) return false;
@@ -207,7 +209,7 @@ bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl) {
     // SM with 8-row batches measured 30% faster there (6.2 -> 4.3 us).
     if (S <= 2 && (double)O * (g.rowbytes + g.arowbytes) < 32e6) {
         TmaPlan t;
-        if (tma_plan(g, S, O, 8, next_pow2(8 * S), U_max, &t, 1) && (long)t.nrowb * t.splits >= num_sms()) {
+        if (tma_plan(g, S, O, 8, next_pow2(8 * S), U_max, &t, 1, 6) && (long)t.nrowb * t.splits >= num_sms()) {
             *pl = t;
             return true;
         }
