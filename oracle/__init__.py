@@ -56,6 +56,14 @@ def _declare(lib):
     lib.oracle_mq4v2_weight.restype = ctypes.c_double
     lib.oracle_qgemv_mq4v2.argtypes = [P, P, P, P, i, i, i]
     lib.oracle_encode_mq4v2.argtypes = [P, P, i, i]
+    lib.oracle_mq4v1_weight.argtypes = [P, i]
+    lib.oracle_mq4v1_weight.restype = ctypes.c_double
+    lib.oracle_mq4c_weight.argtypes = [P, i]
+    lib.oracle_mq4c_weight.restype = ctypes.c_double
+    lib.oracle_qgemv_mq4v1.argtypes = [P, P, P, P, i, i, i]
+    lib.oracle_qgemv_mq4c.argtypes = [P, P, P, P, i, i, i]
+    lib.oracle_encode_mq4v1.argtypes = [P, P, i, i]
+    lib.oracle_encode_mq4c.argtypes = [P, P, i, i]
     lib.oracle_fwht256.argtypes = [P, P, P, z]
     lib.oracle_ifwht256.argtypes = [P, P, P, z]
     return lib
@@ -184,6 +192,45 @@ class Oracle:
         w = np.ascontiguousarray(w, np.float32)
         blocks = np.empty((O, (I // 256) * 136), np.uint8)
         self.lib.oracle_encode_mq4v2(_p(blocks), _p(w), O, I)
+        return blocks
+
+    # MQ4 v1 (qt=13) and MQ4C pad (qt=45) ------------------------------------
+    def mq4v1_weight(self, block: np.ndarray, j: int) -> float:
+        block = np.ascontiguousarray(block, np.uint8)
+        return self.lib.oracle_mq4v1_weight(_p(block), j)
+
+    def mq4c_weight(self, block: np.ndarray, j: int) -> float:
+        block = np.ascontiguousarray(block, np.uint8)
+        return self.lib.oracle_mq4c_weight(_p(block), j)
+
+    def _qgemv_one_header(self, fn, x_bf16, blocks, S, I, O, rows=None):
+        x = np.ascontiguousarray(x_bf16, np.uint16)
+        blocks = np.ascontiguousarray(blocks, np.uint8)
+        o0, o1 = rows if rows is not None else (0, O)
+        rowbytes = (I // 256) * 136
+        bs = np.ascontiguousarray(blocks.reshape(O, rowbytes)[o0:o1])
+        n = o1 - o0
+        y = np.empty((S, n), np.float64)
+        mag = np.empty((S, n), np.float64)
+        fn(_p(y), _p(mag), _p(x), _p(bs), S, I, n)
+        return y, mag
+
+    def qgemv_mq4v1(self, x_bf16, blocks, S, I, O, rows=None):
+        return self._qgemv_one_header(self.lib.oracle_qgemv_mq4v1, x_bf16, blocks, S, I, O, rows)
+
+    def qgemv_mq4c(self, x_bf16, blocks, S, I, O, rows=None):
+        return self._qgemv_one_header(self.lib.oracle_qgemv_mq4c, x_bf16, blocks, S, I, O, rows)
+
+    def encode_mq4v1(self, w, O, I):
+        w = np.ascontiguousarray(w, np.float32)
+        blocks = np.empty((O, (I // 256) * 136), np.uint8)
+        self.lib.oracle_encode_mq4v1(_p(blocks), _p(w), O, I)
+        return blocks
+
+    def encode_mq4c(self, w, O, I):
+        w = np.ascontiguousarray(w, np.float32)
+        blocks = np.empty((O, (I // 256) * 136), np.uint8)
+        self.lib.oracle_encode_mq4c(_p(blocks), _p(w), O, I)
         return blocks
 
     # FWHT -------------------------------------------------------------------

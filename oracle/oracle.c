@@ -15,7 +15,7 @@
  *
  *   [colibri #457]  "metal: grouped-int4 (fmt=4) GEMV support", sections 3-5, 11
  *   [colibri #528]  "fmt=7: fp8-e4m3-b128 passthrough weight format", Design
- *   [hipfire MQ4V2] "MQ4 V2" docs, sections 1e, 2, 3, 4
+ *   [hipfire MQ4V2] "MQ4 V2" docs, sections 1b, 1c, 1e, 2, 3, 4
  *
  * No function here blocks, fuses or reorders beyond what its definition
  * states; loops run in the order the definition reads.
@@ -358,6 +358,149 @@ void oracle_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I)
             }
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* MQ4 v1 (qt=13) and MQ4C pad (qt=45) ([hipfire MQ4V2] sections 1b, 1e)     */
+/*   The same 136-byte block per 256 weights and the same nibble payload at  */
+/*   [8,136) as MQ4-V2, with one header for all 256 weights of the block:    */
+/*     v1:   [0,4) f32 scale, [4,8) f32 zero                                 */
+/*     pad:  [0,2) fp16 scale, [2,4) fp16 zero, [4,8) zero bytes             */
+/*   w_j = q_j * scale + zero.                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Nibble of weight j of a 136-byte block: payload byte j/2 after the 8
+ * header bytes, the low nibble for even j. */
+static int mq4_payload_nibble(const uint8_t *block, int j)
+{
+    const uint8_t *payload = block + 8;
+    uint8_t b = payload[j >> 1];
+    return (j & 1) ? (b >> 4) : (b & 0xF);
+}
+
+static double f32_at(const uint8_t *p)
+{
+    uint32_t u = le32(p);
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double oracle_mq4v1_weight(const uint8_t *block, int j)
+{
+    double scale = f32_at(block);
+    double zero = f32_at(block + 4);
+    return (double)mq4_payload_nibble(block, j) * scale + zero;
+}
+
+double oracle_mq4c_weight(const uint8_t *block, int j)
+{
+    uint32_t pair = le32(block);
+    double scale = oracle_f16_value((uint16_t)(pair & 0xFFFFu));
+    double zero = oracle_f16_value((uint16_t)(pair >> 16));
+    return (double)mq4_payload_nibble(block, j) * scale + zero;
+}
+
+/* y[s,o] = sum_j w(o, j) x[s, j] over the row's I/256 blocks, one block
+ * after another; mag the same sum of |terms|. */
+static void mq4_one_header_gemv(double (*weight)(const uint8_t *, int), double *y, double *mag,
+                                const uint16_t *x, const uint8_t *blocks, int S, int I, int O)
+{
+    const size_t row_blocks = (size_t)I / 256;
+    for (int s = 0; s < S; ++s)
+        for (int o = 0; o < O; ++o) {
+            double sum = 0.0, sum_abs = 0.0;
+            const uint8_t *row = blocks + (size_t)o * row_blocks * 136;
+            for (int i = 0; i < I; ++i) {
+                double t = weight(row + (size_t)(i / 256) * 136, i % 256) *
+                           oracle_bf16_value(x[(size_t)s * I + (size_t)i]);
+                sum += t;
+                sum_abs += fabs(t);
+            }
+            y[(size_t)s * O + o] = sum;
+            mag[(size_t)s * O + o] = sum_abs;
+        }
+}
+
+void oracle_qgemv_mq4v1(double *y, double *mag, const uint16_t *x, const uint8_t *blocks, int S, int I,
+                        int O)
+{
+    mq4_one_header_gemv(oracle_mq4v1_weight, y, mag, x, blocks, S, I, O);
+}
+
+void oracle_qgemv_mq4c(double *y, double *mag, const uint16_t *x, const uint8_t *blocks, int S, int I,
+                       int O)
+{
+    mq4_one_header_gemv(oracle_mq4c_weight, y, mag, x, blocks, S, I, O);
+}
+
+/* Encoders: the MQ4 rule ("level placement uniform over [min, max]",
+ * [hipfire MQ4V2] section 1c) over the whole 256-weight block.
+ *   lo = min, hi = max, step = (hi - lo) / 15         (binary32)
+ *   v1:  scale = step, zero = lo stored as f32; q against them
+ *   pad: scale = f16(step), zero = f16(lo) stored; q against the
+ *        round-tripped values; bytes [4,8) zero
+ *   q = clamp(rint((w - zero) / scale), 0, 15)        (binary32)
+ * A constant block (hi == lo), or one whose stored step is 0, stores
+ * scale 0 and q = 0 (the MQ4-V2 encoder's reading).                       */
+static void mq4_encode_one_header(uint8_t *blocks, const float *w, int O, int I, int fp16_header)
+{
+    const size_t row_blocks = (size_t)I / 256;
+    for (int o = 0; o < O; ++o)
+        for (size_t b = 0; b < row_blocks; ++b) {
+            uint8_t *out = blocks + ((size_t)o * row_blocks + b) * 136;
+            const float *v = w + (size_t)o * I + b * 256;
+            float lo = v[0], hi = v[0];
+            for (int j = 1; j < 256; ++j) {
+                lo = v[j] < lo ? v[j] : lo;
+                hi = v[j] > hi ? v[j] : hi;
+            }
+            volatile float span = hi - lo;
+            volatile float step = span / 15.0f;
+            float scale, zero;
+            uint32_t word0, word1;
+            if (fp16_header) {
+                uint16_t s16 = (hi == lo) ? (uint16_t)0 : oracle_f16_from_f32(step);
+                uint16_t z16 = oracle_f16_from_f32(lo);
+                scale = (float)oracle_f16_value(s16);
+                zero = (float)oracle_f16_value(z16);
+                word0 = (uint32_t)s16 | ((uint32_t)z16 << 16);
+                word1 = 0u;
+            } else {
+                scale = (hi == lo) ? 0.0f : step;
+                zero = lo;
+                memcpy(&word0, &scale, 4);
+                memcpy(&word1, &zero, 4);
+            }
+            for (int k = 0; k < 4; ++k) {
+                out[k] = (uint8_t)(word0 >> (8 * k));
+                out[4 + k] = (uint8_t)(word1 >> (8 * k));
+            }
+            for (int j = 0; j < 256; j += 2) {
+                int q2[2];
+                for (int e = 0; e < 2; ++e) {
+                    int q = 0;
+                    if (scale != 0.0f) {
+                        volatile float d = v[j + e] - zero;
+                        volatile float r = d / scale;
+                        float qf = rintf(r);
+                        q = qf < 0.0f ? 0 : qf > 15.0f ? 15 : (int)qf;
+                    }
+                    q2[e] = q;
+                }
+                out[8 + j / 2] = (uint8_t)(q2[0] | (q2[1] << 4));
+            }
+        }
+}
+
+void oracle_encode_mq4v1(uint8_t *blocks, const float *w, int O, int I)
+{
+    mq4_encode_one_header(blocks, w, O, I, 0);
+}
+
+void oracle_encode_mq4c(uint8_t *blocks, const float *w, int O, int I)
+{
+    mq4_encode_one_header(blocks, w, O, I, 1);
 }
 
 /* ------------------------------------------------------------------------ */

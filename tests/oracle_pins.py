@@ -472,6 +472,134 @@ def pin_mq4v2_extremes(orc):
 
 
 # ---------------------------------------------------------------------------
+# MQ4 v1 (qt=13) and MQ4C pad (qt=45): one header per 256-weight block
+# ---------------------------------------------------------------------------
+
+def _dequant_mq4c_numpy(blocks, O, I):
+    """The pad reading: fp16 scale at +0, fp16 zero at +2, for all 256."""
+    nb = I // 256
+    b = np.asarray(blocks, np.uint8).reshape(O, nb, 136)
+    hdr = np.ascontiguousarray(b[:, :, 0:4]).view("<u2").view(np.float16).reshape(O, nb, 2)
+    hdr = hdr.astype(np.float64)
+    pay = b[:, :, 8:136]
+    q = np.stack([pay & 0xF, pay >> 4], -1).reshape(O, nb, 256).astype(np.float64)
+    return (q * hdr[:, :, 0:1] + hdr[:, :, 1:2]).reshape(O, I)
+
+
+def _golden_one_header(orc, name, weight_fn, gemv_fn):
+    g = _golden(name)
+    blk = np.array(g["header"] + [g["payload_byte"]] * 128, np.uint8)
+    assert blk.size == 136
+    for j, v in g["weights"].items():
+        assert weight_fn(blk, int(j)) == v, (name, j, weight_fn(blk, int(j)), v)
+    x = synth.bf16_bits(np.ones(256, np.float32))
+    y, mag = gemv_fn(x, blk, 1, 256, 1)
+    assert y[0, 0] == g["y_ones"] and mag[0, 0] == g["mag_ones"], (name, y, mag)
+
+
+def pin_mq4v1_golden(orc):
+    _golden_one_header(orc, "mq4v1_hand.json", orc.mq4v1_weight, orc.qgemv_mq4v1)
+
+
+def pin_mq4c_golden(orc):
+    _golden_one_header(orc, "mq4c_hand.json", orc.mq4c_weight, orc.qgemv_mq4c)
+
+
+def pin_mq4_one_header_bruteforce(orc):
+    """Oracle GEMVs == numpy dequantize + matmul, with a distinct random header
+    per block over several blocks and rows (discriminates stride, header
+    position and field order) and a payload whose first bytes differ from the
+    pad (a decoder reading the payload at +4 picks up the zero pad)."""
+    rng = np.random.default_rng(41)
+    for (O, I, S) in [(1, 256, 1), (3, 512, 2), (4, 1280, 3)]:
+        nb = I // 256
+        pay = rng.integers(0, 256, (O, nb, 128), dtype=np.uint8)
+        pay[:, :, 0:4] = 0xFF
+        s = rng.uniform(1e-3, 1e-2, (O, nb))
+        z = rng.uniform(-0.1, 0.1, (O, nb))
+        v1 = np.zeros((O, nb, 136), np.uint8)
+        v1[:, :, 0:8] = np.stack([s, z], -1).astype("<f4").view(np.uint8).reshape(O, nb, 8)
+        v1[:, :, 8:] = pay
+        c = np.zeros((O, nb, 136), np.uint8)
+        c[:, :, 0:4] = np.stack([s, z], -1).astype(np.float16).view(np.uint8).reshape(O, nb, 4)
+        c[:, :, 8:] = pay
+        xb = synth.bf16_bits(rng.standard_normal(S * I).astype(np.float32))
+        X = synth.bf16_to_f32(xb).reshape(S, I).astype(np.float64)
+        for blocks, fn, ref in ((v1, orc.qgemv_mq4v1, _dequant_mq4v1_numpy),
+                                (c, orc.qgemv_mq4c, _dequant_mq4c_numpy)):
+            y, mag = fn(xb, blocks, S, I, O)
+            W = ref(blocks, O, I)
+            _close(y, X @ W.T, np.abs(X) @ np.abs(W).T, what=f"one-header O={O} I={I}")
+
+
+def pin_mq4_three_layouts_agree(orc):
+    """The same fp16-representable scale and zero in each layout (v2 with
+    equal half headers, v1 as f32, pad as fp16) decode the same nibbles to
+    identical weights (hipfire MQ4 V2 section 1e)."""
+    rng = np.random.default_rng(42)
+    O, I = 2, 512
+    nb = I // 256
+    pay = rng.integers(0, 256, (O, nb, 128), dtype=np.uint8)
+    s16 = rng.uniform(1e-3, 1e-2, (O, nb)).astype(np.float16)
+    z16 = rng.uniform(-0.1, 0.1, (O, nb)).astype(np.float16)
+    pair = np.stack([s16, z16], -1).view(np.uint8).reshape(O, nb, 4)
+    v2 = np.zeros((O, nb, 136), np.uint8)
+    v2[:, :, 0:4] = pair
+    v2[:, :, 4:8] = pair
+    v2[:, :, 8:] = pay
+    c = np.zeros((O, nb, 136), np.uint8)
+    c[:, :, 0:4] = pair
+    c[:, :, 8:] = pay
+    v1 = np.zeros((O, nb, 136), np.uint8)
+    v1[:, :, 0:8] = np.stack([s16.astype(np.float32), z16.astype(np.float32)], -1).view(np.uint8).reshape(O, nb, 8)
+    v1[:, :, 8:] = pay
+    for o in range(O):
+        for b in range(nb):
+            for j in range(256):
+                a = orc.mq4v2_weight(v2[o, b], j)
+                assert orc.mq4v1_weight(v1[o, b], j) == a and orc.mq4c_weight(c[o, b], j) == a
+
+
+def _one_header_encoder_checks(orc, encode, decode_np, fp16):
+    O, I = 8, 1024
+    w = synth.normal(43, O * I, 0.02).reshape(O, I)
+    blocks = encode(w, O, I)
+    assert blocks.size == 136 * O * I // 256
+    b = blocks.reshape(O, I // 256, 136)
+    if fp16:
+        assert not b[:, :, 4:8].any(), "pad bytes must be zero"
+    W = decode_np(blocks, O, I)
+    for o in range(O):
+        for k in range(I // 256):
+            src = w[o, 256 * k:256 * k + 256].astype(np.float64)
+            pay = b[o, k, 8:]
+            q = np.stack([pay & 0xF, pay >> 4], -1).reshape(256)
+            assert q[np.argmin(src)] == 0 and q[np.argmax(src)] == 15
+            lo, hi = src.min(), src.max()
+            step = (hi - lo) / 15
+            hb = (2.0 ** -11 if fp16 else 2.0 ** -23) * (abs(lo) + 15 * step) + 2.0 ** -24
+            rec = W[o, 256 * k:256 * k + 256]
+            assert abs(rec[np.argmin(src)] - lo) <= hb and abs(rec[np.argmax(src)] - hi) <= hb
+            # every weight within half a step (plus header rounding) of its code
+            assert np.all(np.abs(rec - src) <= 0.5 * step * (1 + 2.0 ** -9) + hb)
+    # a constant block stores scale 0 and decodes to its value (rounded to the header type)
+    wc = np.full((1, 256), 0.0123, np.float32)
+    bc = encode(wc, 1, 256)[0]
+    want = float(np.float16(np.float32(0.0123))) if fp16 else float(np.float32(0.0123))
+    assert not bc[8:].any()
+    for j in (0, 1, 255):
+        assert (orc.mq4c_weight if fp16 else orc.mq4v1_weight)(bc, j) == want
+
+
+def pin_mq4v1_encoder(orc):
+    _one_header_encoder_checks(orc, orc.encode_mq4v1, _dequant_mq4v1_numpy, fp16=False)
+
+
+def pin_mq4c_encoder(orc):
+    _one_header_encoder_checks(orc, orc.encode_mq4c, _dequant_mq4c_numpy, fp16=True)
+
+
+# ---------------------------------------------------------------------------
 # FWHT rotation
 # ---------------------------------------------------------------------------
 

@@ -62,6 +62,19 @@ MUTATIONS = [
     ("mq4_enc_step_16", "volatile float step = diff / 15.0f;", "volatile float step = diff / 16.0f;"),
     ("mq4_enc_truncate", "float qr = rintf(r);\n                        if (qr < 0.0f)",
      "float qr = truncf(r);\n                        if (qr < 0.0f)"),
+    # MQ4 v1 / MQ4C pad
+    ("mq4v1_fields_swapped", "double scale = f32_at(block);\n    double zero = f32_at(block + 4);",
+     "double scale = f32_at(block + 4);\n    double zero = f32_at(block);"),
+    ("mq4c_reads_pad_as_zero", "double zero = oracle_f16_value((uint16_t)(pair >> 16));",
+     "double zero = oracle_f16_value((uint16_t)(le32(block + 4) & 0xFFFFu));"),
+    ("mq4_one_header_payload_plus4", "const uint8_t *payload = block + 8;", "const uint8_t *payload = block + 4;"),
+    ("mq4_one_header_stride_132", "double t = weight(row + (size_t)(i / 256) * 136, i % 256) *",
+     "double t = weight(row + (size_t)(i / 256) * 132, i % 256) *"),
+    ("mq4_one_header_nibble_order", "return (j & 1) ? (b >> 4) : (b & 0xF);", "return (j & 1) ? (b & 0xF) : (b >> 4);"),
+    ("mq4v1_enc_fp16_roundtrip", "scale = (hi == lo) ? 0.0f : step;\n                zero = lo;",
+     "scale = (hi == lo) ? 0.0f : (float)oracle_f16_value(oracle_f16_from_f32(step));\n                zero = lo;"),
+    ("mq4c_enc_no_pad_zero", "word1 = 0u;", "word1 = word0;"),
+    ("mq4_one_header_enc_step_16", "volatile float step = span / 15.0f;", "volatile float step = span / 16.0f;"),
     # FWHT
     ("fwht_norm_8", "out[b * 256 + (size_t)j] = (float)(v[j] / 16.0);",
      "out[b * 256 + (size_t)j] = (float)(v[j] / 8.0);"),
