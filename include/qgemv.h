@@ -9,6 +9,8 @@
  *   fmt=7  FP8-e4m3 b128    colibri PR #528 "fmt=7: fp8-e4m3-b128 passthrough
  *                           weight format", section "Design"
  *   MQ4-V2 (qt=44)          hipfire docs "MQ4 V2", sections 2, 3, 4
+ *   MQ4 v1 (qt=13),         hipfire docs "MQ4 V2", sections 1b, 1c, 1e
+ *   MQ4C pad (qt=45)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -78,7 +80,7 @@ const char *qg_last_error(void);
 int qg_device_status(int *status);
 
 /* Format ids for qg_workspace_bytes. */
-enum { QG_FMT_I4G = 4, QG_FMT_FP8B128 = 7, QG_FMT_MQ4V2 = 44 };
+enum { QG_FMT_I4G = 4, QG_FMT_FP8B128 = 7, QG_FMT_MQ4V1 = 13, QG_FMT_MQ4V2 = 44, QG_FMT_MQ4C = 45 };
 
 /* Bytes of workspace that the GEMV entry point of format `fmt` needs for
  * this shape on the current device (0 when the call does not split the
@@ -171,6 +173,22 @@ int qgemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks,
                 int S, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* MQ4 v1 (hipfire qt=13) and MQ4C pad (hipfire qt=45), decode GEMV        */
+/* hipfire "MQ4 V2", sections 1b and 1e: the MQ4-V2 block geometry (136 B  */
+/* per 256 weights, nibbles at [8,136), weight j in payload byte j/2, low   */
+/* nibble for even j) with ONE header for all 256 weights of the block:     */
+/*   qgemv_mq4v1: [0,4) f32 scale, [4,8) f32 zero                           */
+/*   qgemv_mq4c:  [0,2) fp16 scale, [2,4) fp16 zero, [4,8) zero bytes       */
+/*   w_j = q_j * scale + zero.  Arguments, alignment, workspace            */
+/*   (qg_workspace_bytes with QG_FMT_MQ4V1 / QG_FMT_MQ4C), errors and      */
+/*   precision exactly as qgemv_mq4v2.                                      */
+/* ------------------------------------------------------------------------ */
+int qgemv_mq4v1(float *y, const uint16_t *x, const uint8_t *blocks,
+                int S, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+int qgemv_mq4c(float *y, const uint16_t *x, const uint8_t *blocks,
+               int S, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* fmt=4 batched prefill dequant-GEMM on the tensor cores                   */
 /* colibri PR #457, section 4 (the large-batch GEMM path takes the same     */
 /* grouped layout as the GEMV).                                             */
@@ -235,6 +253,18 @@ int qgemm_mq4v2(float *Y, const uint16_t *X, const uint8_t *blocks,
                 int M, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* MQ4 v1 and MQ4C pad batched prefill dequant-GEMM on the tensor cores     */
+/* The same contract as qgemm_mq4v2 (fp16 operands with powers of two, the */
+/* row bound max over the row's blocks of |zero| + 15 |scale|), with the     */
+/* formats of qgemv_mq4v1 / qgemv_mq4c; workspace from                      */
+/* qg_gemm_workspace_bytes with QG_FMT_MQ4V1 / QG_FMT_MQ4C.                 */
+/* ------------------------------------------------------------------------ */
+int qgemm_mq4v1(float *Y, const uint16_t *X, const uint8_t *blocks,
+                int M, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+int qgemm_mq4c(float *Y, const uint16_t *X, const uint8_t *blocks,
+               int M, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Weight preparation on the device (not on the decode path)                */
 /* ------------------------------------------------------------------------ */
 
@@ -254,6 +284,16 @@ int qg_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, in
  *   w f32 [O, I] (device, 4-byte aligned), I % 256 == 0;
  *   blocks uint8 [O, I/256, 136] (device, 8-byte aligned) */
 int qg_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, qg_stream_t stream);
+
+/* MQ4 v1 and MQ4C pad encoders: the MQ4 rule (levels uniform over the
+ * block's [min, max], hipfire "MQ4 V2" section 1c) over each 256-weight
+ * block: step = (max - min) / 15 in binary32; v1 stores scale = step and
+ * zero = min as f32; pad stores fp16(step), fp16(min) and four zero bytes and
+ * quantizes against the round-tripped values; q = clamp(rint((w - zero) /
+ * scale), 0, 15); a constant block (or a zero stored step) stores scale 0
+ * and q = 0.  Same arguments and errors as qg_encode_mq4v2. */
+int qg_encode_mq4v1(uint8_t *blocks, const float *w, int O, int I, qg_stream_t stream);
+int qg_encode_mq4c(uint8_t *blocks, const float *w, int O, int I, qg_stream_t stream);
 
 /* Signed Walsh-Hadamard rotation of 256-element blocks (hipfire "MQ4 V2"
  * sections 1 and 3: the MQ line rotates weights and activations with the

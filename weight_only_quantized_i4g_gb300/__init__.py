@@ -25,7 +25,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 QG_OK, QG_EINVAL, QG_EGS, QG_ESHAPE, QG_EALIGN, QG_EWORKSPACE, QG_ECUDA, QG_ETIMEOUT = (
     0, -1, -2, -3, -4, -5, -6, -7)
-QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_MQ4V2 = 4, 7, 44
+QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_MQ4V1, QG_FMT_MQ4V2, QG_FMT_MQ4C = 4, 7, 13, 44, 45
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -44,6 +44,12 @@ _SIGNATURES = {
     "qgemm_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_fp8b128": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_mq4v2": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemv_mq4v1": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemv_mq4c": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemm_mq4v1": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemm_mq4c": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qg_encode_mq4v1": ([_P, _P, _I, _I, _P], _I),
+    "qg_encode_mq4c": ([_P, _P, _I, _I, _P], _I),
     "qg_quantize_i4g": ([_P, _P, _P, _I, _I, _I, _P], _I),
     "qg_encode_mq4v2": ([_P, _P, _I, _I, _P], _I),
     "qg_fwht256": ([_P, _P, _P, _Z, _P], _I),
@@ -142,6 +148,30 @@ def qgemm_fp8b128(Y, X, w, scale_inv, M, I, O, ws=None, ws_bytes=0, stream=None)
 
 def qgemm_mq4v2(Y, X, blocks, M, I, O, ws=None, ws_bytes=0, stream=None) -> int:
     return _lib.qgemm_mq4v2(_ptr(Y), _ptr(X), _ptr(blocks), M, I, O, _ptr(ws), ws_bytes, _stream(stream))
+
+
+def qgemv_mq4v1(y, x, blocks, S, I, O, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemv_mq4v1(_ptr(y), _ptr(x), _ptr(blocks), S, I, O, _ptr(ws), ws_bytes, _stream(stream))
+
+
+def qgemv_mq4c(y, x, blocks, S, I, O, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemv_mq4c(_ptr(y), _ptr(x), _ptr(blocks), S, I, O, _ptr(ws), ws_bytes, _stream(stream))
+
+
+def qgemm_mq4v1(Y, X, blocks, M, I, O, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemm_mq4v1(_ptr(Y), _ptr(X), _ptr(blocks), M, I, O, _ptr(ws), ws_bytes, _stream(stream))
+
+
+def qgemm_mq4c(Y, X, blocks, M, I, O, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemm_mq4c(_ptr(Y), _ptr(X), _ptr(blocks), M, I, O, _ptr(ws), ws_bytes, _stream(stream))
+
+
+def qg_encode_mq4v1(blocks, w, O, I, stream=None) -> int:
+    return _lib.qg_encode_mq4v1(_ptr(blocks), _ptr(w), O, I, _stream(stream))
+
+
+def qg_encode_mq4c(blocks, w, O, I, stream=None) -> int:
+    return _lib.qg_encode_mq4c(_ptr(blocks), _ptr(w), O, I, _stream(stream))
 
 
 def qg_quantize_i4g(wq, scales, w, O, I, gs, stream=None) -> int:

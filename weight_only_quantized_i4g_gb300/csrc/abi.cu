@@ -25,6 +25,16 @@ int run_gemm_mq4v2_general(float *Y, const uint16_t *X, const uint8_t *blocks, i
 int run_gemm_mq4v2_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
                       size_t ws_bytes, cudaStream_t st, bool *taken);
 size_t ws_gemm_mq4v2(int M, int I, int O);
+int run_gemm_mq4v1_general(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O,
+                           cudaStream_t st);
+int run_gemm_mq4v1_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
+                      size_t ws_bytes, cudaStream_t st, bool *taken);
+size_t ws_gemm_mq4v1(int M, int I, int O);
+int run_gemm_mq4c_general(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O,
+                          cudaStream_t st);
+int run_gemm_mq4c_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
+                     size_t ws_bytes, cudaStream_t st, bool *taken);
+size_t ws_gemm_mq4c(int M, int I, int O);
 }  // namespace qg
 
 using namespace qg;
@@ -90,6 +100,8 @@ size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs) {
         case QG_FMT_I4G: return (gs >= 2 && !(gs & 1)) ? ws_i4g(S, I, O, gs) : 0;
         case QG_FMT_FP8B128: return ws_fp8b128(S, I, O);
         case QG_FMT_MQ4V2: return (I % 256 == 0) ? ws_mq4v2(S, I, O) : 0;
+        case QG_FMT_MQ4V1: return (I % 256 == 0) ? ws_mq4v1(S, I, O) : 0;
+        case QG_FMT_MQ4C: return (I % 256 == 0) ? ws_mq4c(S, I, O) : 0;
         default: return 0;
     }
 }
@@ -100,6 +112,8 @@ size_t qg_gemm_workspace_bytes(int fmt, int M, int I, int O, int gs) {
         case QG_FMT_I4G: return (gs >= 2 && !(gs & 1)) ? ws_gemm_i4g(M, I, O, gs) : 0;
         case QG_FMT_FP8B128: return ws_gemm_fp8b128(M, I, O);
         case QG_FMT_MQ4V2: return ws_gemm_mq4v2(M, I, O);
+        case QG_FMT_MQ4V1: return ws_gemm_mq4v1(M, I, O);
+        case QG_FMT_MQ4C: return ws_gemm_mq4c(M, I, O);
         default: return 0;
     }
 }
@@ -131,18 +145,64 @@ int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *sc
     return run_gemv_fp8b128(y, x, w, scale_inv, S, I, O, ws, ws_bytes, as_stream(stream));
 }
 
-int qgemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
-                size_t ws_bytes, qg_stream_t stream) {
-    const char *fn = "qgemv_mq4v2";
-    int rc = check_dims(fn, "S", S, I, O);
+}  // extern "C"
+
+namespace {
+
+typedef int (*Mq4GemvFn)(float *, const uint16_t *, const uint8_t *, int, int, int, void *, size_t, cudaStream_t);
+typedef int (*Mq4GemmTcFn)(float *, const uint16_t *, const uint8_t *, int, int, int, void *, size_t,
+                           cudaStream_t, bool *);
+typedef int (*Mq4GemmGenFn)(float *, const uint16_t *, const uint8_t *, int, int, int, cudaStream_t);
+
+// Checks shared by the three 136-byte MQ4 formats (the same block geometry).
+int check_mq4(const char *fn, const char *sname, int S, int I, int O, const void *y, const void *x,
+              const void *blocks, const void *ws) {
+    int rc = check_dims(fn, sname, S, I, O);
     if (rc) return rc;
     if (I % 256) QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 256", fn, I);
-    if (!y || !x || !blocks) QG_REFUSE(kEInval, "%s: y, x and blocks must be non-NULL", fn);
+    if (!y || !x || !blocks) QG_REFUSE(kEInval, "%s: output, activations and blocks must be non-NULL", fn);
     if (!aligned(y, 4) || !aligned(x, 2) || !aligned(blocks, 8))
-        QG_REFUSE(kEAlign, "%s: y must be 4-byte, x 2-byte and blocks 8-byte aligned", fn);
+        QG_REFUSE(kEAlign, "%s: the output must be 4-byte, the activations 2-byte and blocks 8-byte aligned", fn);
     if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    return kOk;
+}
+
+int mq4_gemv(const char *fn, Mq4GemvFn run, float *y, const uint16_t *x, const uint8_t *blocks, int S, int I,
+             int O, void *ws, size_t ws_bytes, qg_stream_t stream) {
+    const int rc = check_mq4(fn, "S", S, I, O, y, x, blocks, ws);
+    if (rc) return rc;
     cudaGetLastError();
-    return run_gemv_mq4v2(y, x, blocks, S, I, O, ws, ws_bytes, as_stream(stream));
+    return run(y, x, blocks, S, I, O, ws, ws_bytes, as_stream(stream));
+}
+
+int mq4_gemm(const char *fn, Mq4GemmTcFn tc, Mq4GemmGenFn gen, float *Y, const uint16_t *X,
+             const uint8_t *blocks, int M, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream) {
+    int rc = check_mq4(fn, "M", M, I, O, Y, X, blocks, ws);
+    if (rc) return rc;
+    cudaGetLastError();
+    bool taken = false;
+    rc = tc(Y, X, blocks, M, I, O, ws, ws_bytes, as_stream(stream), &taken);
+    if (taken) return rc;
+    return gen(Y, X, blocks, M, I, O, as_stream(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int qgemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+                size_t ws_bytes, qg_stream_t stream) {
+    return mq4_gemv("qgemv_mq4v2", run_gemv_mq4v2, y, x, blocks, S, I, O, ws, ws_bytes, stream);
+}
+
+int qgemv_mq4v1(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+                size_t ws_bytes, qg_stream_t stream) {
+    return mq4_gemv("qgemv_mq4v1", run_gemv_mq4v1, y, x, blocks, S, I, O, ws, ws_bytes, stream);
+}
+
+int qgemv_mq4c(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+               size_t ws_bytes, qg_stream_t stream) {
+    return mq4_gemv("qgemv_mq4c", run_gemv_mq4c, y, x, blocks, S, I, O, ws, ws_bytes, stream);
 }
 
 int qgemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales, int M, int I, int O, int gs,
@@ -180,19 +240,20 @@ int qgemm_fp8b128(float *Y, const uint16_t *X, const uint8_t *w, const float *sc
 
 int qgemm_mq4v2(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
                 size_t ws_bytes, qg_stream_t stream) {
-    const char *fn = "qgemm_mq4v2";
-    int rc = check_dims(fn, "M", M, I, O);
-    if (rc) return rc;
-    if (I % 256) QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 256", fn, I);
-    if (!Y || !X || !blocks) QG_REFUSE(kEInval, "%s: Y, X and blocks must be non-NULL", fn);
-    if (!aligned(Y, 4) || !aligned(X, 2) || !aligned(blocks, 8))
-        QG_REFUSE(kEAlign, "%s: Y must be 4-byte, X 2-byte and blocks 8-byte aligned", fn);
-    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
-    cudaGetLastError();
-    bool taken = false;
-    rc = run_gemm_mq4v2_tc(Y, X, blocks, M, I, O, ws, ws_bytes, as_stream(stream), &taken);
-    if (taken) return rc;
-    return run_gemm_mq4v2_general(Y, X, blocks, M, I, O, as_stream(stream));
+    return mq4_gemm("qgemm_mq4v2", run_gemm_mq4v2_tc, run_gemm_mq4v2_general, Y, X, blocks, M, I, O, ws,
+                    ws_bytes, stream);
+}
+
+int qgemm_mq4v1(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
+                size_t ws_bytes, qg_stream_t stream) {
+    return mq4_gemm("qgemm_mq4v1", run_gemm_mq4v1_tc, run_gemm_mq4v1_general, Y, X, blocks, M, I, O, ws,
+                    ws_bytes, stream);
+}
+
+int qgemm_mq4c(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
+               size_t ws_bytes, qg_stream_t stream) {
+    return mq4_gemm("qgemm_mq4c", run_gemm_mq4c_tc, run_gemm_mq4c_general, Y, X, blocks, M, I, O, ws,
+                    ws_bytes, stream);
 }
 
 int qg_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs, qg_stream_t stream) {
@@ -216,6 +277,26 @@ int qg_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, qg_stream_t s
         QG_REFUSE(kEAlign, "%s: w must be 4-byte and blocks 8-byte aligned", fn);
     cudaGetLastError();
     return run_encode_mq4v2(blocks, w, O, I, as_stream(stream));
+}
+
+static int encode_mq4_one_header(const char *fn, uint8_t *blocks, const float *w, int O, int I, bool fp16,
+                                 qg_stream_t stream) {
+    int rc = check_dims(fn, "O", 1, I, O);
+    if (rc) return rc;
+    if (I % 256) QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 256", fn, I);
+    if (!blocks || !w) QG_REFUSE(kEInval, "%s: blocks and w must be non-NULL", fn);
+    if (!aligned(w, 4) || !aligned(blocks, 8))
+        QG_REFUSE(kEAlign, "%s: w must be 4-byte and blocks 8-byte aligned", fn);
+    cudaGetLastError();
+    return run_encode_mq4_one_header(blocks, w, O, I, fp16, as_stream(stream));
+}
+
+int qg_encode_mq4v1(uint8_t *blocks, const float *w, int O, int I, qg_stream_t stream) {
+    return encode_mq4_one_header("qg_encode_mq4v1", blocks, w, O, I, false, stream);
+}
+
+int qg_encode_mq4c(uint8_t *blocks, const float *w, int O, int I, qg_stream_t stream) {
+    return encode_mq4_one_header("qg_encode_mq4c", blocks, w, O, I, true, stream);
 }
 
 int qg_fwht256(float *out, const float *in, const int8_t *signs, size_t n_blocks, qg_stream_t stream) {

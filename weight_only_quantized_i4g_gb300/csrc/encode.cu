@@ -114,6 +114,69 @@ int run_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, cudaStream_t
 }
 
 // ---------------------------------------------------------------------------
+// MQ4 v1 (f32 header) and MQ4C pad (fp16 header, four zero bytes) encoders:
+// one thread per 256-weight block, the MQ4 rule over the whole block
+// (hipfire "MQ4 V2", sections 1b and 1c).
+// ---------------------------------------------------------------------------
+template <bool kFp16>
+__global__ void encode_mq4_one_header_kernel(uint8_t *__restrict__ blocks, const float *__restrict__ w, int O,
+                                             int I) {
+    const size_t nb = (size_t)I / 256;
+    const size_t total = (size_t)O * nb;
+    for (size_t t = blockIdx.x * (size_t)blockDim.x + threadIdx.x; t < total; t += (size_t)gridDim.x * blockDim.x) {
+        const size_t o = t / nb, b = t - o * nb;
+        const float *v = w + o * (size_t)I + b * 256;
+        uint32_t *blk = reinterpret_cast<uint32_t *>(blocks + t * 136);
+        float lo = v[0], hi = v[0];
+        for (int j = 1; j < 256; ++j) {
+            const float x = v[j];
+            if (x < lo) lo = x;
+            if (x > hi) hi = x;
+        }
+        const float step = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+        float scale, zero;
+        if (kFp16) {
+            const __half s16 = hi == lo ? __ushort_as_half((unsigned short)0) : __float2half_rn(step);
+            const __half z16 = __float2half_rn(lo);
+            scale = __half2float(s16);
+            zero = __half2float(z16);
+            blk[0] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+            blk[1] = 0u;
+        } else {
+            scale = hi == lo ? 0.f : step;
+            zero = lo;
+            blk[0] = __float_as_uint(scale);
+            blk[1] = __float_as_uint(zero);
+        }
+        for (int k = 0; k < 32; ++k) {               // word k holds weights 8k..8k+7
+            uint32_t word = 0u;
+            for (int m = 0; m < 8; ++m) {
+                int q = 0;
+                if (scale != 0.f) {
+                    float r = rintf(__fdiv_rn(__fsub_rn(v[8 * k + m], zero), scale));
+                    r = r < 0.f ? 0.f : (r > 15.f ? 15.f : r);
+                    q = (int)r;
+                }
+                word |= (uint32_t)q << (4 * m);
+            }
+            blk[2 + k] = word;
+        }
+    }
+}
+
+int run_encode_mq4_one_header(uint8_t *blocks, const float *w, int O, int I, bool fp16_header, cudaStream_t st) {
+    const size_t total = (size_t)O * (I / 256);
+    size_t nblk = (total + 127) / 128;
+    if (nblk > 65535) nblk = 65535;
+    if (fp16_header) {
+        encode_mq4_one_header_kernel<true><<<(unsigned)nblk, 128, 0, st>>>(blocks, w, O, I);
+        return check_launch("qg_encode_mq4c");
+    }
+    encode_mq4_one_header_kernel<false><<<(unsigned)nblk, 128, 0, st>>>(blocks, w, O, I);
+    return check_launch("qg_encode_mq4v1");
+}
+
+// ---------------------------------------------------------------------------
 // signed FWHT-256: one warp per block; lane l holds elements 8l..8l+7.
 // Butterfly distances 1, 2, 4 inside a lane, 8..128 across lanes (xor 1..16).
 // ---------------------------------------------------------------------------

@@ -6,6 +6,7 @@
 //   fmt=4   w = (n(o,i) - 8) * scale[o, i/gs]      colibri PR #457, sections 3, 4
 //   fmt=7   w = e4m3(code) * scale_inv[o/128, i/128]  colibri PR #528, "Design"
 //   MQ4-V2  w = q * scale[h] + zero[h]              hipfire "MQ4 V2", sections 2, 4
+//   MQ4 v1, MQ4C pad: one header per 256 weights    hipfire "MQ4 V2", sections 1b, 1e
 //
 // This kernel covers every shape and alignment with CUDA cores: a 64x64
 // output tile per block, K in steps of 32; the weight tile is dequantized to
@@ -44,16 +45,23 @@ struct WeightFp8B128 {
     }
 };
 
-struct WeightMq4v2 {
+// HK = 44: MQ4-V2 (fp16 pair per half), 45: MQ4C pad (one fp16 pair), 13:
+// MQ4 v1 (f32 scale and zero).
+template <int HK>
+struct WeightMq4 {
     const uint8_t *blocks;
     int nb;   // blocks per row, I / 256
     __device__ float operator()(int o, int i) const {
         const uint8_t *b = blocks + ((size_t)o * nb + (i >> 8)) * 136;
         const int j = i & 255;
-        const uint8_t *h = b + 4 * (j >> 7);
-        const uint16_t sc = (uint16_t)(h[0] | (h[1] << 8)), ze = (uint16_t)(h[2] | (h[3] << 8));
         const uint8_t p = b[8 + (j >> 1)];
         const float q = (float)((j & 1) ? (p >> 4) : (p & 0xF));
+        if (HK == 13) {
+            const float *h = reinterpret_cast<const float *>(b);   // blocks are 8-byte aligned
+            return fmaf(q, h[0], h[1]);
+        }
+        const uint8_t *h = b + (HK == 44 ? 4 * (j >> 7) : 0);
+        const uint16_t sc = (uint16_t)(h[0] | (h[1] << 8)), ze = (uint16_t)(h[2] | (h[3] << 8));
         return fmaf(q, f16_bits_to_f32(sc), f16_bits_to_f32(ze));
     }
 };
@@ -126,8 +134,20 @@ int run_gemm_fp8b128_general(float *Y, const uint16_t *X, const uint8_t *w, cons
 
 int run_gemm_mq4v2_general(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O,
                            cudaStream_t st) {
-    const WeightMq4v2 wat{blocks, I / 256};
+    const WeightMq4<44> wat{blocks, I / 256};
     return launch_general(Y, X, wat, M, I, O, st, "qgemm_mq4v2 (general kernel)");
+}
+
+int run_gemm_mq4v1_general(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O,
+                           cudaStream_t st) {
+    const WeightMq4<13> wat{blocks, I / 256};
+    return launch_general(Y, X, wat, M, I, O, st, "qgemm_mq4v1 (general kernel)");
+}
+
+int run_gemm_mq4c_general(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O,
+                          cudaStream_t st) {
+    const WeightMq4<45> wat{blocks, I / 256};
+    return launch_general(Y, X, wat, M, I, O, st, "qgemm_mq4c (general kernel)");
 }
 
 }  // namespace qg

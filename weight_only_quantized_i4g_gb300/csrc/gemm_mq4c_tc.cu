@@ -1,0 +1,14 @@
+// gemm_mq4c_tc.cu -- MQ4C pad (hipfire qt=45) batched-prefill dequant-GEMM on the tensor cores
+// (the format policy is in gemm_mq4_tc.cuh, the kernel in gemm_tc.cuh).
+#include "gemm_mq4_tc.cuh"
+
+namespace qg {
+
+size_t ws_gemm_mq4c(int M, int I, int O) { return ws_gemm_mq4(M, I, O); }
+
+int run_gemm_mq4c_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
+                      size_t ws_bytes, cudaStream_t st, bool *taken) {
+    return run_gemm_mq4_tc<45>(Y, X, blocks, M, I, O, ws, ws_bytes, st, taken, "qgemm_mq4c");
+}
+
+}  // namespace qg

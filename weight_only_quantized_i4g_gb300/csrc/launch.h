@@ -23,6 +23,8 @@ int read_device_error(int *status);
 size_t ws_i4g(int S, int I, int O, int gs);
 size_t ws_fp8b128(int S, int I, int O);
 size_t ws_mq4v2(int S, int I, int O);
+size_t ws_mq4v1(int S, int I, int O);
+size_t ws_mq4c(int S, int I, int O);
 
 int run_gemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,
                  int gs, void *ws, size_t ws_bytes, cudaStream_t st);
@@ -30,10 +32,15 @@ int run_gemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float 
                      int I, int O, void *ws, size_t ws_bytes, cudaStream_t st);
 int run_gemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
                    size_t ws_bytes, cudaStream_t st);
+int run_gemv_mq4v1(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+                   size_t ws_bytes, cudaStream_t st);
+int run_gemv_mq4c(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+                  size_t ws_bytes, cudaStream_t st);
 
 
 int run_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs, cudaStream_t st);
 int run_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, cudaStream_t st);
+int run_encode_mq4_one_header(uint8_t *blocks, const float *w, int O, int I, bool fp16_header, cudaStream_t st);
 int run_fwht256(float *out, const float *in, const int8_t *signs, size_t nblocks, cudaStream_t st);
 
 }  // namespace qg
