@@ -441,6 +441,8 @@ def ours_arm(args):
     per_format = per_format_breakdown(qg, torch, calls, stream, hbm_peak) if args.breakdown else None
     if per_format is not None:
         per_format.update(batched_breakdown(qg, torch, calls, stream, hbm_peak, dev))
+        if len(shapes) == len(SHAPES):
+            per_format.update(one_header_breakdown(qg, torch, stream, hbm_peak, dev))
     prefill = prefill_measure(qg, torch, dev, stream) if args.prefill else None
 
     cpu = None
@@ -509,9 +511,10 @@ def _time_alone(fn, flush, stream, reps, torch):
 def _prefill_inputs(qg, torch, dev, stream, fmt, O, I, M):
     """Seeded device inputs of one prefill GEMM shape: the decode workloads'
     weight recipes (fmt=4 quantized N(0, 0.02); fmt=7 uniform e4m3 codes
-    without the NaN codes and log-uniform [1e-4, 1e-2] block scales; MQ4-V2
-    N(0, 0.02) rotated by the seeded sign-FWHT and encoded) and bf16 N(0, 1)
-    activations (rotated for MQ4-V2).  Returns the launch closure's args."""
+    without the NaN codes and log-uniform [1e-4, 1e-2] block scales; the MQ4
+    formats (V2, v1, pad) N(0, 0.02) rotated by the seeded sign-FWHT and
+    encoded) and bf16 N(0, 1) activations (rotated for MQ4).  Returns the
+    weights and X."""
     g = torch.Generator(device=dev)
     g.manual_seed(4000 + O + 7 * I)
     if fmt == "i4g":
@@ -533,26 +536,33 @@ def _prefill_inputs(qg, torch, dev, stream, fmt, O, I, M):
         w = torch.randn(O, I, generator=g, device=dev) * 0.02
         qg.check(qg.qg_fwht256(w, w, signs, O * I // 256, stream=stream))
         blocks = torch.empty(O * (I // 256) * 136, dtype=torch.uint8, device=dev)
-        qg.check(qg.qg_encode_mq4v2(blocks, w, O, I, stream=stream))
+        qg.check(MQ4_ENCODE[fmt](qg)(blocks, w, O, I, stream=stream))
         del w
         weights = (blocks, signs)
     g.manual_seed(5000 + O + 7 * I)
     x = torch.randn(M, I, generator=g, device=dev)
-    if fmt == "mq4":
+    if fmt in MQ4_ENCODE:
         qg.check(qg.qg_fwht256(x, x, weights[1], M * I // 256, stream=stream))
     X = x.to(torch.bfloat16).view(torch.int16)
     return weights, X
 
 
-PREFILL_OTHER = (("fp8", 7168, 16384), ("fp8", 24576, 7168), ("mq4", 5120, 17408), ("mq4", 17408, 5120))
-FMT_ID = {"i4g": 4, "fp8": 7, "mq4": 44}
+PREFILL_OTHER = (("fp8", 7168, 16384), ("fp8", 24576, 7168), ("mq4", 5120, 17408), ("mq4", 17408, 5120),
+                 ("mq4v1", 5120, 17408), ("mq4v1", 17408, 5120), ("mq4c", 5120, 17408), ("mq4c", 17408, 5120))
+FMT_ID = {"i4g": 4, "fp8": 7, "mq4": 44, "mq4v1": 13, "mq4c": 45}
+# MQ4 block formats: V2 (a header per 128-weight half), v1 (one f32 header),
+# pad (one fp16 header and four zero bytes); 136 bytes per 256 weights each
+MQ4_ENCODE = {"mq4": lambda qg: qg.qg_encode_mq4v2, "mq4v1": lambda qg: qg.qg_encode_mq4v1,
+              "mq4c": lambda qg: qg.qg_encode_mq4c}
+MQ4_GEMV = {"mq4": "qgemv_mq4v2", "mq4v1": "qgemv_mq4v1", "mq4c": "qgemv_mq4c"}
+MQ4_GEMM = {"mq4": "qgemm_mq4v2", "mq4v1": "qgemm_mq4v1", "mq4c": "qgemm_mq4c"}
 
 
 def prefill_measure(qg, torch, dev, stream, reps=20, other=True, shapes=None):
     """The fmt=4 batched-prefill GEMM of the workload's prefill config:
     Y[512, O] = X[512, 7168] . W^T for O = 7168 and 2048, gs = 64, plus the
-    fmt=7 and MQ4-V2 prefill GEMMs at M = 512 on their decode shapes
-    ("other_formats").  Weights and activations from seeded generators on
+    fmt=7 and MQ4 (V2, v1, pad) prefill GEMMs at M = 512 on their decode
+    shapes ("other_formats").  Weights and activations from seeded generators on
     the device.  Each call is timed alone with CUDA events on its stream
     after a 256 MiB write that flushes L2; median of `reps`.  Returns TFLOP/s
     (2*M*I*O per call) and the fraction of the measured dense bf16 peak.
@@ -578,7 +588,8 @@ def prefill_measure(qg, torch, dev, stream, reps=20, other=True, shapes=None):
         elif fmt == "fp8":
             fn = lambda: qg.check(qg.qgemm_fp8b128(Y, X, weights[0], weights[1], M, I, O, ws, n, stream=stream))
         else:
-            fn = lambda: qg.check(qg.qgemm_mq4v2(Y, X, weights[0], M, I, O, ws, n, stream=stream))
+            gemm = getattr(qg, MQ4_GEMM[fmt])
+            fn = lambda: qg.check(gemm(Y, X, weights[0], M, I, O, ws, n, stream=stream))
         t = _time_alone(fn, flush, stream, reps, torch)
         launches += reps
         tf = 2.0 * M * I * O / t / 1e12
@@ -646,6 +657,63 @@ def per_format_breakdown(qg, torch, calls, stream, hbm_peak):
         gbs = c["bytes"] / (best * 1e-3) / 1e9
         out[c["name"]] = {"us_per_call": round(best * 1e3, 3), "weight_gbs": round(gbs, 1),
                           "pct_hbm_peak": round(100 * gbs / hbm_peak, 1), "weight_copies": copies}
+    return out
+
+
+def _graph_per_call(torch, stream, reps, issue):
+    """Capture `reps` back-to-back calls (issue(r) launches call r) in a CUDA
+    graph on `stream`; returns the mean ms per call, best of 4 replays."""
+    gr = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(gr, stream=stream):
+        for r in range(reps):
+            issue(r)
+    best = None
+    for _ in range(4):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            gr.replay()
+            b.record(stream)
+        b.synchronize()
+        t = a.elapsed_time(b) / reps
+        best = t if best is None else min(best, t)
+    del gr
+    return best
+
+
+ONE_HEADER = (("mq4v1", 5120, 17408), ("mq4v1", 17408, 5120), ("mq4c", 5120, 17408), ("mq4c", 17408, 5120))
+
+
+def one_header_breakdown(qg, torch, stream, hbm_peak, dev):
+    """Kernel-only batch-1 GEMV time of the one-header MQ4 block formats (v1:
+    f32 scale and zero per 256 weights; pad: fp16 pair and four zero bytes)
+    on the MQ4-V2 decode shapes, same weight recipe and timing scheme as
+    per_format_breakdown (graph of calls over >= 3x L2 of weight copies)."""
+    out = {}
+    l2 = 129 * 2 ** 20
+    lib = qg._lib
+    st = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for fmt, O, I in ONE_HEADER:
+            weights, X = _prefill_inputs(qg, torch, dev, stream, fmt, O, I, 1)
+            y = torch.empty(O, dtype=torch.float32, device=dev)
+            assert qg.qg_workspace_bytes(FMT_ID[fmt], 1, I, O, 0) == 0
+            nbytes = weight_bytes("mq4", O, I)
+            copies = min(64, max(1, -(-3 * l2 // nbytes)))
+            wcopies = [weights[0]] + [weights[0].clone() for _ in range(copies - 1)]
+            gemv = getattr(lib, MQ4_GEMV[fmt])
+
+            def issue(r):
+                rc = gemv(y.data_ptr(), X.data_ptr(), wcopies[r % copies].data_ptr(), 1, I, O, None, 0, st)
+                if rc:
+                    raise qg.QGError(rc)
+            best = _graph_per_call(torch, stream, max(copies, 60), issue)
+            del wcopies
+            gbs = nbytes / (best * 1e-3) / 1e9
+            out[f"{fmt}_{O}x{I}"] = {"us_per_call": round(best * 1e3, 3), "weight_gbs": round(gbs, 1),
+                                     "pct_hbm_peak": round(100 * gbs / hbm_peak, 1), "weight_copies": copies}
     return out
 
 
@@ -731,7 +799,7 @@ def main():
     ap.add_argument("--only", default="", help="comma-separated subset of the shapes (profiling runs)")
     ap.add_argument("--prefill-only", default="",
                     help="profiling runs: time only these prefill GEMMs (comma-separated fmt:O:I, fmt in "
-                         "i4g/fp8/mq4, M=512) and print their prefill object")
+                         "i4g/fp8/mq4/mq4v1/mq4c, M=512) and print their prefill object")
     ap.add_argument("--prefill-reps", type=int, default=20)
     args = ap.parse_args()
     if args.warmup < 3:
