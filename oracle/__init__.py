@@ -64,6 +64,7 @@ def _declare(lib):
     lib.oracle_qgemv_mq4c.argtypes = [P, P, P, P, i, i, i]
     lib.oracle_encode_mq4v1.argtypes = [P, P, i, i]
     lib.oracle_encode_mq4c.argtypes = [P, P, i, i]
+    lib.oracle_qgemv_moe.argtypes = [i, P, P, P, z, P, P, i, P, i, i, i, i, i]
     lib.oracle_fwht256.argtypes = [P, P, P, z]
     lib.oracle_ifwht256.argtypes = [P, P, P, z]
     return lib
@@ -232,6 +233,24 @@ class Oracle:
         blocks = np.empty((O, (I // 256) * 136), np.uint8)
         self.lib.oracle_encode_mq4c(_p(blocks), _p(w), O, I)
         return blocks
+
+    # routed experts -----------------------------------------------------------
+    def qgemv_moe(self, fmt, x, x_slot_stride, weights, scales, ids, S, I, O, gs=0):
+        """y, mag (float64 [n_slots, S, O]).  ``weights`` / ``scales`` are
+        per-expert numpy arrays (scales None for the MQ4 formats); ``x`` is f32
+        for fmt=4 and bf16 bits otherwise."""
+        x = np.ascontiguousarray(x, np.float32 if fmt == 4 else np.uint16)
+        ws = [np.ascontiguousarray(w, np.uint8) for w in weights]
+        ss = [None if sc is None else np.ascontiguousarray(sc, np.float32) for sc in scales]
+        ids = np.ascontiguousarray(ids, np.int32)
+        n = len(ids)
+        wp = (ctypes.c_void_p * len(ws))(*[w.ctypes.data for w in ws])
+        sp = (ctypes.c_void_p * len(ss))(*[0 if sc is None else sc.ctypes.data for sc in ss])
+        y = np.empty((n, S, O), np.float64)
+        mag = np.empty((n, S, O), np.float64)
+        self.lib.oracle_qgemv_moe(fmt, _p(y), _p(mag), _p(x), x_slot_stride, ctypes.cast(wp, ctypes.c_void_p),
+                                  ctypes.cast(sp, ctypes.c_void_p), len(ws), _p(ids), n, S, I, O, gs)
+        return y, mag
 
     # FWHT -------------------------------------------------------------------
     def fwht256(self, v, signs):

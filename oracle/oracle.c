@@ -13,9 +13,9 @@
  * only rounding is the order of summation.  Each function cites the passage
  * of the page it follows:
  *
- *   [colibri #457]  "metal: grouped-int4 (fmt=4) GEMV support", sections 3-5, 11
+ *   [colibri #457]  "metal: grouped-int4 (fmt=4) GEMV support", sections 3-5, 7, 11
  *   [colibri #528]  "fmt=7: fp8-e4m3-b128 passthrough weight format", Design
- *   [hipfire MQ4V2] "MQ4 V2" docs, sections 1b, 1c, 1e, 2, 3, 4
+ *   [hipfire MQ4V2] "MQ4 V2" docs, sections 1b, 1c, 1e, 2, 3, 4, 9
  *
  * No function here blocks, fuses or reorders beyond what its definition
  * states; loops run in the order the definition reads.
@@ -501,6 +501,55 @@ void oracle_encode_mq4v1(uint8_t *blocks, const float *w, int O, int I)
 void oracle_encode_mq4c(uint8_t *blocks, const float *w, int O, int I)
 {
     mq4_encode_one_header(blocks, w, O, I, 1);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Routed experts ([colibri #457] section 7: the batched routed-expert path  */
+/* walks a per-expert pointer array with one format and group size per       */
+/* tensor; [hipfire MQ4V2] section 9: MoE decode on MQ4-V2).                 */
+/*   Slot r multiplies the expert ids[r] of the table with its own           */
+/*   activations x_r = x + r * x_slot_stride (elements; 0: every slot reads  */
+/*   the same x) into y_r = y + r * S * O:  y_r = W_{ids[r]} x_r, the         */
+/*   single-matrix definition of `fmt` applied slot by slot.  A slot whose   */
+/*   id names no expert of the table has no value: NaN.                      */
+/* ------------------------------------------------------------------------ */
+void oracle_qgemv_moe(int fmt, double *y, double *mag, const void *x, size_t x_slot_stride,
+                      const void *const *w, const float *const *scales, int n_experts,
+                      const int *ids, int n_slots, int S, int I, int O, int gs)
+{
+    const size_t out_n = (size_t)S * O;
+    for (int r = 0; r < n_slots; ++r) {
+        double *yr = y + (size_t)r * out_n;
+        double *mr = mag + (size_t)r * out_n;
+        const int id = ids[r];
+        const size_t xo = (size_t)r * x_slot_stride;
+        const uint8_t *we = (id >= 0 && id < n_experts) ? (const uint8_t *)w[id] : NULL;
+        if (we == NULL) {
+            for (size_t k = 0; k < out_n; ++k)
+                yr[k] = mr[k] = NAN;
+            continue;
+        }
+        switch (fmt) {
+        case 4:
+            oracle_qgemv_i4g(yr, mr, (const float *)x + xo, we, scales[id], S, I, O, gs);
+            break;
+        case 7:
+            oracle_qgemv_fp8b128(yr, mr, (const uint16_t *)x + xo, we, scales[id], S, I, O);
+            break;
+        case 13:
+            oracle_qgemv_mq4v1(yr, mr, (const uint16_t *)x + xo, we, S, I, O);
+            break;
+        case 44:
+            oracle_qgemv_mq4v2(yr, mr, (const uint16_t *)x + xo, we, S, I, O);
+            break;
+        case 45:
+            oracle_qgemv_mq4c(yr, mr, (const uint16_t *)x + xo, we, S, I, O);
+            break;
+        default:
+            for (size_t k = 0; k < out_n; ++k)
+                yr[k] = mr[k] = NAN;
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------ */

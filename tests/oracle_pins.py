@@ -603,6 +603,83 @@ def pin_mq4c_encoder(orc):
 # FWHT rotation
 # ---------------------------------------------------------------------------
 
+def _moe_experts(rng, fmt, n_experts, O, I, gs):
+    """Random experts of one format: (weights, scales, numpy dequantizer)."""
+    ws, ss, deq = [], [], []
+    for _ in range(n_experts):
+        if fmt == 4:
+            rb, ng = (I + 1) // 2, (I + gs - 1) // gs
+            w = rng.integers(0, 256, O * rb, dtype=np.uint8)
+            sc = rng.uniform(-2, 2, O * ng).astype(np.float32)
+            deq.append(_dequant_i4g_numpy(w, sc, O, I, gs))
+        elif fmt == 7:
+            w = synth.bytes_excluding(int(rng.integers(1 << 30)), O * I)
+            nbo, nbi = (O + 127) // 128, (I + 127) // 128
+            sc = synth.log_uniform(int(rng.integers(1 << 30)), nbo * nbi, 1e-4, 1e-2)
+            deq.append(_dequant_fp8_numpy(w, sc, O, I))
+        else:
+            nb = I // 256
+            w = rng.integers(0, 256, (O, nb, 136), dtype=np.uint8)
+            hs = rng.uniform(1e-3, 1e-2, (O, nb, 2))
+            hz = rng.uniform(-0.1, 0.1, (O, nb, 2))
+            if fmt == 44:
+                w[:, :, 0:8] = np.stack([hs[..., 0], hz[..., 0], hs[..., 1], hz[..., 1]], -1).astype(
+                    np.float16).view(np.uint8).reshape(O, nb, 8)
+                deq.append(_dequant_mq4v2_numpy(w, O, I))
+            elif fmt == 13:
+                w[:, :, 0:8] = np.stack([hs[..., 0], hz[..., 0]], -1).astype("<f4").view(np.uint8).reshape(O, nb, 8)
+                deq.append(_dequant_mq4v1_numpy(w, O, I))
+            else:
+                w[:, :, 0:4] = np.stack([hs[..., 0], hz[..., 0]], -1).astype(np.float16).view(np.uint8).reshape(
+                    O, nb, 4)
+                w[:, :, 4:8] = 0
+                deq.append(_dequant_mq4c_numpy(w, O, I))
+            sc = None
+        ws.append(w)
+        ss.append(sc)
+    return ws, ss, deq
+
+
+def pin_moe_bruteforce(orc):
+    """Routed experts == numpy dequantize + matmul slot by slot, every format,
+    with repeated ids, ids out of order, a shared x and one x per slot; a slot
+    whose id names no expert is NaN."""
+    rng = np.random.default_rng(51)
+    for fmt, (O, I, gs) in ((4, (3, 200, 64)), (7, (130, 260, 0)), (44, (3, 512, 0)), (13, (2, 768, 0)),
+                            (45, (2, 512, 0))):
+        E = 4
+        ws, ss, deq = _moe_experts(rng, fmt, E, O, I, gs)
+        ids = np.array([2, 0, 2, 3, 1], np.int32)
+        S = 2
+        for shared in (True, False):
+            n_x = 1 if shared else len(ids)
+            xf = rng.standard_normal(n_x * S * I).astype(np.float32)
+            xin = xf if fmt == 4 else synth.bf16_bits(xf)
+            X = (xf if fmt == 4 else synth.bf16_to_f32(xin)).reshape(n_x, S, I).astype(np.float64)
+            y, mag = orc.qgemv_moe(fmt, xin, 0 if shared else S * I, ws, ss, ids, S, I, O, gs)
+            assert y.shape == (len(ids), S, O)
+            for r, e in enumerate(ids):
+                Xr = X[0 if shared else r]
+                _close(y[r], Xr @ deq[e].T, np.abs(Xr) @ np.abs(deq[e]).T, what=f"moe fmt={fmt} slot {r}")
+                _close(mag[r], np.abs(Xr) @ np.abs(deq[e]).T, np.abs(Xr) @ np.abs(deq[e]).T, what="moe mag")
+        bad = np.array([1, -1, E], np.int32)
+        y, mag = orc.qgemv_moe(fmt, xin, 0, ws, ss, bad, S, I, O, gs)
+        assert not np.isnan(y[0]).any() and np.isnan(y[1]).all() and np.isnan(y[2]).all()
+
+
+def pin_moe_permutation(orc):
+    """Permuting the slots (ids with their x rows) permutes the outputs."""
+    rng = np.random.default_rng(52)
+    O, I, gs, S = 4, 128, 32, 1
+    ws, ss, _ = _moe_experts(rng, 4, 5, O, I, gs)
+    ids = np.array([4, 1, 0, 3], np.int32)
+    x = rng.standard_normal((4, S, I)).astype(np.float32)
+    y, _ = orc.qgemv_moe(4, x, S * I, ws, ss, ids, S, I, O, gs)
+    perm = np.array([2, 0, 3, 1])
+    yp, _ = orc.qgemv_moe(4, x[perm], S * I, ws, ss, ids[perm], S, I, O, gs)
+    assert np.array_equal(yp, y[perm])
+
+
 def pin_fwht_vs_scipy(orc):
     from scipy.linalg import hadamard
     H = hadamard(256).astype(np.float64)

@@ -14,6 +14,12 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 # (name, original text, replacement).  Each original must occur exactly once.
 MUTATIONS = [
+    # routed experts
+    ("moe_first_expert_only", "const uint8_t *we = (id >= 0 && id < n_experts) ? (const uint8_t *)w[id] : NULL;",
+     "const uint8_t *we = (id >= 0 && id < n_experts) ? (const uint8_t *)w[0] : NULL;"),
+    ("moe_shared_x_always", "const size_t xo = (size_t)r * x_slot_stride;", "const size_t xo = 0 * x_slot_stride;"),
+    ("moe_bad_id_zero", "if (we == NULL) {\n            for (size_t k = 0; k < out_n; ++k)\n                yr[k] = mr[k] = NAN;",
+     "if (we == NULL) {\n            for (size_t k = 0; k < out_n; ++k)\n                yr[k] = mr[k] = 0.0;"),
     # fmt=4
     ("i4g_swapped_nibbles", "(i % 2 == 0) ? (byte & 0xF) : (byte >> 4);\n    return nib - 8;",
      "(i % 2 == 0) ? (byte >> 4) : (byte & 0xF);\n    return nib - 8;"),
