@@ -59,7 +59,9 @@ typedef enum {
     QG_EALIGN = -4,      /* pointer misaligned for its element type          */
     QG_EWORKSPACE = -5,  /* workspace NULL or smaller than required          */
     QG_ECUDA = -6,       /* CUDA runtime error (no device, launch failure)   */
-    QG_ETIMEOUT = -7     /* a kernel gave up waiting (see qg_device_status)  */
+    QG_ETIMEOUT = -7,    /* a kernel gave up waiting (see qg_device_status)  */
+    QG_EEXPERT = -8      /* qgemv_moe: a slot's expert id was out of range   */
+                         /* or its weights misaligned (qg_device_status)     */
 } qg_status;
 
 /* Static name of a status code ("QG_EGS: ..."). Never NULL. */
@@ -74,7 +76,8 @@ const char *qg_last_error(void);
  * through shared memory wait on hardware barriers; every such wait is bounded
  * and, if it ever gives up (which no valid call does), the kernel stops early
  * and records QG_ETIMEOUT in a per-device error word instead of hanging the
- * GPU.  This call synchronizes the device, stores that word (QG_OK when
+ * GPU.  qgemv_moe records QG_EEXPERT there for a slot whose expert it cannot
+ * read (its arguments live in device memory, out of the host's reach).  This call synchronizes the device, stores that word (QG_OK when
  * clean) in *status and clears it.  Returns QG_OK, QG_EINVAL for a NULL
  * status, or QG_ECUDA. */
 int qg_device_status(int *status);
@@ -152,6 +155,50 @@ int qgemv_i4g_noalloc(float *y, const float *x, const uint8_t *w, const float *s
 /* ------------------------------------------------------------------------ */
 int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv,
                   int S, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Routed experts: many decode GEMVs of one format and shape in one launch  */
+/* colibri PR #457, section 7 (fmt=4 is mostly an expert format; the        */
+/* batched routed-expert path takes a per-expert pointer array and one      */
+/* format and group size per tensor) and hipfire docs "MQ4 V2", section 9   */
+/* (MoE decode on MQ4-V2).                                                  */
+/*                                                                          */
+/*   experts  DEVICE array [n_experts] of qg_expert: each expert's packed   */
+/*            weights `w` and, for fmt=4 and fmt=7, its `scales` (NULL for  */
+/*            the MQ4 formats), laid out exactly as the single-matrix entry */
+/*            point of `fmt` takes them, all experts with the same O x I    */
+/*            (and gs for fmt=4)                                            */
+/*   ids      DEVICE int32 [n_slots]: slot r uses expert ids[r]; the same   */
+/*            expert may appear in several slots                            */
+/*   x        DEVICE [n_slots or 1][S, I] activations, f32 for fmt=4 and    */
+/*            bf16 otherwise: slot r reads x + r * x_slot_stride (elements; */
+/*            0 = every slot reads the same x, e.g. gate and up projections */
+/*            of one token)                                                 */
+/*   y        DEVICE f32 [n_slots][S, O]: y[r][s][o] = sum_i                */
+/*            W_{ids[r]}[o, i] * x_r[s, i] with the format's dequantization */
+/*   fmt      QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_MQ4V2, QG_FMT_MQ4V1 or     */
+/*            QG_FMT_MQ4C;  gs is read for fmt=4 only                       */
+/*   S        tokens per slot, 1..8 (decode)                                */
+/* experts and ids may be written by earlier kernels on `stream` (a        */
+/* router): the kernel reads them after those kernels finish.  n_slots = 0 */
+/* returns QG_OK and launches nothing.  Needs x 16-byte aligned (and        */
+/* x_slot_stride a whole number of 16-byte lines), each expert's w 16-byte */
+/* aligned (fmt=4 scales too; fmt=7 scales 4-byte), and rows short enough   */
+/* for one thread block (fmt=4: I % 32 == 0, gs % 32 == 0, ceil(I/gs) % 4  */
+/* == 0; fmt=7: I % 16 == 0; MQ4: I/256 even), else QG_ESHAPE / QG_EALIGN. */
+/* A slot whose id is outside [0, n_experts) or whose expert pointers are  */
+/* NULL or misaligned is not computed: its outputs are set to NaN and the   */
+/* device error word records QG_EEXPERT (see qg_device_status).  No        */
+/* workspace.                                                               */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    const void *w;
+    const float *scales;
+} qg_expert;
+
+int qgemv_moe(int fmt, float *y, const void *x, size_t x_slot_stride,
+              const qg_expert *experts, int n_experts, const int *ids, int n_slots,
+              int S, int I, int O, int gs, qg_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* MQ4-V2 (hipfire qt=44), decode GEMV                                      */

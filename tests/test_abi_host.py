@@ -33,7 +33,8 @@ def test_header_lists_the_entry_points():
     names = declared_functions()
     for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qgemm_fp8b128", "qgemm_mq4v2",
                  "qg_workspace_bytes", "qg_gemm_workspace_bytes", "qg_device_status",
-                 "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256"]:
+                 "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256",
+                 "qgemv_moe"]:
         assert must in names, names
 
 
@@ -45,7 +46,7 @@ def test_library_exports_every_declared_symbol(qg):
 
 
 def test_strerror(qg):
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         assert qg.strerror(code).startswith("QG_")
     assert "unknown" in qg.strerror(-99)
 
@@ -91,6 +92,25 @@ def test_mq4_refusals(qg):
     assert "300" in qg.last_error()
     assert qg.qgemv_mq4v2(P, P, P + 4, 1, 256, 4, stream=0) == qg.QG_EALIGN
     assert qg.qgemv_mq4v2(P, P, P, 1, 256, 0, stream=0) == qg.QG_EINVAL
+
+
+def test_moe_refusals(qg):
+    P = POISON
+    moe = qg.qgemv_moe
+    assert moe(4, P, P, 0, P, 4, P, 2, 9, 256, 64, 64, stream=0) == qg.QG_EINVAL      # S > 8
+    assert "S = 9" in qg.last_error()
+    assert moe(5, P, P, 0, P, 4, P, 2, 1, 256, 64, 64, stream=0) == qg.QG_EINVAL      # no such format
+    assert moe(4, P, P, 0, P, 4, P, 2, 1, 256, 64, 7, stream=0) == qg.QG_EGS
+    assert moe(44, P, P, 0, P, 4, P, 2, 1, 300, 64, 0, stream=0) == qg.QG_ESHAPE
+    assert moe(4, P, P, 0, P, 0, P, 2, 1, 256, 64, 64, stream=0) == qg.QG_EINVAL      # empty table
+    assert moe(4, P, P, 0, P, 4, P, -1, 1, 256, 64, 64, stream=0) == qg.QG_EINVAL     # negative slots
+    assert moe(4, P, P, 0, P, 4, P, 70000, 1, 256, 64, 64, stream=0) == qg.QG_EINVAL  # grid.z limit
+    assert moe(4, P, None, 0, P, 4, P, 2, 1, 256, 64, 64, stream=0) == qg.QG_EINVAL
+    assert moe(4, P, P + 8, 0, P, 4, P, 2, 1, 256, 64, 64, stream=0) == qg.QG_EALIGN  # x not 16-byte aligned
+    assert moe(4, P, P, 258, P, 4, P, 2, 1, 256, 64, 64, stream=0) == qg.QG_EALIGN    # 1032-byte slot stride
+    assert moe(4, P, P, 100, P, 4, P, 2, 1, 256, 64, 64, stream=0) == qg.QG_EINVAL    # slots overlap
+    assert moe(4, P, P, 0, P + 4, 4, P, 2, 1, 256, 64, 64, stream=0) == qg.QG_EALIGN  # table alignment
+    assert moe(4, P, P, 0, P, 4, P, 0, 1, 256, 64, 64, stream=0) == qg.QG_OK          # nothing to do
 
 
 def test_gemm_and_prep_refusals(qg):

@@ -23,8 +23,8 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-QG_OK, QG_EINVAL, QG_EGS, QG_ESHAPE, QG_EALIGN, QG_EWORKSPACE, QG_ECUDA, QG_ETIMEOUT = (
-    0, -1, -2, -3, -4, -5, -6, -7)
+QG_OK, QG_EINVAL, QG_EGS, QG_ESHAPE, QG_EALIGN, QG_EWORKSPACE, QG_ECUDA, QG_ETIMEOUT, QG_EEXPERT = (
+    0, -1, -2, -3, -4, -5, -6, -7, -8)
 QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_MQ4V1, QG_FMT_MQ4V2, QG_FMT_MQ4C = 4, 7, 13, 44, 45
 
 _P = ctypes.c_void_p
@@ -48,6 +48,7 @@ _SIGNATURES = {
     "qgemv_mq4c": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_mq4v1": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_mq4c": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemv_moe": ([_I, _P, _P, _Z, _P, _I, _P, _I, _I, _I, _I, _I, _P], _I),
     "qg_encode_mq4v1": ([_P, _P, _I, _I, _P], _I),
     "qg_encode_mq4c": ([_P, _P, _I, _I, _P], _I),
     "qg_quantize_i4g": ([_P, _P, _P, _I, _I, _I, _P], _I),
@@ -125,6 +126,21 @@ def qgemv_i4g(y, x, w, scales, S, I, O, gs, ws=None, ws_bytes=0, stream=None) ->
 
 def qgemv_i4g_noalloc(y, x, w, scales, S, I, O, gs, stream=None) -> int:
     return _lib.qgemv_i4g_noalloc(_ptr(y), _ptr(x), _ptr(w), _ptr(scales), S, I, O, gs, _stream(stream))
+
+
+def qgemv_moe(fmt, y, x, x_slot_stride, experts, n_experts, ids, n_slots, S, I, O, gs=0, stream=None) -> int:
+    """Routed-expert GEMV; `experts` is a device array of qg_expert {w, scales}
+    pointer pairs (see ``expert_table``), `ids` a device int32 array."""
+    return _lib.qgemv_moe(fmt, _ptr(y), _ptr(x), x_slot_stride, _ptr(experts), n_experts, _ptr(ids), n_slots,
+                          S, I, O, gs, _stream(stream))
+
+
+def expert_table(pairs):
+    """Host bytes of a qg_expert array: one (weights, scales) pair of device
+    pointers (tensors, ints or None) per expert, two little-endian uint64
+    each.  Upload them to device memory to pass to qgemv_moe."""
+    import struct
+    return b"".join(struct.pack("<QQ", _ptr(w) or 0, _ptr(sc) or 0) for w, sc in pairs)
 
 
 def qgemv_fp8b128(y, x, w, scale_inv, S, I, O, ws=None, ws_bytes=0, stream=None) -> int:

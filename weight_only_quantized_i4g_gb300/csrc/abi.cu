@@ -78,6 +78,7 @@ const char *qg_strerror(int status) {
         case QG_EWORKSPACE: return "QG_EWORKSPACE: workspace missing or smaller than qg_workspace_bytes()";
         case QG_ECUDA: return "QG_ECUDA: CUDA runtime error";
         case QG_ETIMEOUT: return "QG_ETIMEOUT: a kernel gave up waiting on a barrier";
+        case QG_EEXPERT: return "QG_EEXPERT: a routed slot named a missing expert or one with misaligned weights";
         default: return "unknown qg_status";
     }
 }
@@ -143,6 +144,53 @@ int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *sc
     if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
     cudaGetLastError();
     return run_gemv_fp8b128(y, x, w, scale_inv, S, I, O, ws, ws_bytes, as_stream(stream));
+}
+
+int qgemv_moe(int fmt, float *y, const void *x, size_t x_slot_stride, const qg_expert *experts, int n_experts,
+              const int *ids, int n_slots, int S, int I, int O, int gs, qg_stream_t stream) {
+    const char *fn = "qgemv_moe";
+    int rc = check_dims(fn, "S", S, I, O);
+    if (rc) return rc;
+    if (fmt != QG_FMT_I4G && fmt != QG_FMT_FP8B128 && fmt != QG_FMT_MQ4V2 && fmt != QG_FMT_MQ4V1 &&
+        fmt != QG_FMT_MQ4C)
+        QG_REFUSE(kEInval, "%s: unknown format id %d", fn, fmt);
+    if (fmt == QG_FMT_I4G && (rc = check_gs(fn, gs))) return rc;
+    if ((fmt == QG_FMT_MQ4V2 || fmt == QG_FMT_MQ4V1 || fmt == QG_FMT_MQ4C) && I % 256)
+        QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 256", fn, I);
+    if (S > 8) QG_REFUSE(kEInval, "%s: S = %d tokens per slot, must be <= 8", fn, S);
+    if (n_slots < 0 || n_slots > 65535) QG_REFUSE(kEInval, "%s: n_slots = %d, must be in [0, 65535]", fn, n_slots);
+    if (n_experts < 1) QG_REFUSE(kEInval, "%s: n_experts = %d, must be >= 1", fn, n_experts);
+    if (n_slots == 0) return kOk;
+    if (!y || !x || !experts || !ids) QG_REFUSE(kEInval, "%s: y, x, experts and ids must be non-NULL", fn);
+    const size_t esz = fmt == QG_FMT_I4G ? 4 : 2;
+    if (x_slot_stride != 0 && x_slot_stride < (size_t)S * I)
+        QG_REFUSE(kEInval, "%s: x_slot_stride = %zu is below S * I = %zu (slots would overlap)", fn, x_slot_stride,
+                  (size_t)S * I);
+    if ((size_t)n_slots * S * O > (size_t)INT_MAX * 64 || x_slot_stride > (size_t)INT_MAX * 64)
+        QG_REFUSE(kEInval, "%s: sizes overflow", fn);
+    if (!aligned(y, 4) || !aligned(ids, 4) || !aligned(experts, 8))
+        QG_REFUSE(kEAlign, "%s: y and ids must be 4-byte and experts 8-byte aligned", fn);
+    if (!aligned(x, 16) || (x_slot_stride * esz) % 16)
+        QG_REFUSE(kEAlign, "%s: x and every slot's x (x_slot_stride * %zu bytes) must be 16-byte aligned", fn, esz);
+    cudaGetLastError();
+    const cudaStream_t st = as_stream(stream);
+    switch (fmt) {
+        case QG_FMT_I4G:
+            return run_gemv_moe_i4g(y, static_cast<const float *>(x), x_slot_stride, experts, n_experts, ids,
+                                    n_slots, S, I, O, gs, st);
+        case QG_FMT_FP8B128:
+            return run_gemv_moe_fp8b128(y, static_cast<const uint16_t *>(x), x_slot_stride, experts, n_experts,
+                                        ids, n_slots, S, I, O, st);
+        case QG_FMT_MQ4V2:
+            return run_gemv_moe_mq4v2(y, static_cast<const uint16_t *>(x), x_slot_stride, experts, n_experts,
+                                      ids, n_slots, S, I, O, st);
+        case QG_FMT_MQ4V1:
+            return run_gemv_moe_mq4v1(y, static_cast<const uint16_t *>(x), x_slot_stride, experts, n_experts,
+                                      ids, n_slots, S, I, O, st);
+        default:
+            return run_gemv_moe_mq4c(y, static_cast<const uint16_t *>(x), x_slot_stride, experts, n_experts,
+                                     ids, n_slots, S, I, O, st);
+    }
 }
 
 }  // extern "C"

@@ -82,6 +82,17 @@ struct FmtFp8B128 {
     // ---- staged (TMA) kernel -------------------------------------------------
     struct TConst { uint32_t uoff; int ib; };   // unit byte offset, 128-column block
     struct StageConst { float sc; };            // the batch's block scale for that column block
+    // routed experts: 16-byte aligned codes for the staged copies; the block
+    // scales are read as f32 from global memory
+    __device__ static bool expert_ok(const Params &, const void *w, const float *scales) {
+        return w != nullptr && scales != nullptr && ((uintptr_t)w % 16 == 0) && ((uintptr_t)scales % 4 == 0);
+    }
+    __device__ static Params with_expert(Params p, const void *w, const float *scales, size_t x_off) {
+        p.w = static_cast<const uint8_t *>(w);
+        p.scale_inv = scales;
+        p.x += x_off;
+        return p;
+    }
 
     __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.I; }
     __device__ static uint32_t aux_row_bytes(const Params &) { return 0u; }
@@ -240,34 +251,36 @@ void launch_cs_fp8_s(const FmtFp8B128::Params &p, float *out, const CsPlan &pl, 
 }
 
 template <int S, int RB>
-void launch_tma_fp8_u(const FmtFp8B128::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+void launch_tma_fp8_u(const FmtFp8B128::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
+                      const MoeLaunch *moe = nullptr) {
     constexpr int NW = S <= 4 ? 4 : 2;
     if constexpr (S == 1) {
         if (pl.U == 2) {
-            launch_tma<FmtFp8B128, S, NW, 2, RB>(p, out, pl, st);
+            launch_tma<FmtFp8B128, S, NW, 2, RB>(p, out, pl, st, moe);
             return;
         }
         if (pl.U == 3) {
-            launch_tma<FmtFp8B128, S, NW, 3, RB>(p, out, pl, st);
+            launch_tma<FmtFp8B128, S, NW, 3, RB>(p, out, pl, st, moe);
             return;
         }
     }
-    launch_tma<FmtFp8B128, S, NW, 1, RB>(p, out, pl, st);
+    launch_tma<FmtFp8B128, S, NW, 1, RB>(p, out, pl, st, moe);
 }
 
 template <int S>
-void launch_tma_fp8_s(const FmtFp8B128::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+void launch_tma_fp8_s(const FmtFp8B128::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
+                      const MoeLaunch *moe = nullptr) {
     if constexpr (S <= 2) {
         if (pl.rb == 8) {
-            launch_tma_fp8_u<S, 8>(p, out, pl, st);
+            launch_tma_fp8_u<S, 8>(p, out, pl, st, moe);
             return;
         }
     }
     if (pl.rb == 2) {
-        launch_tma<FmtFp8B128, S, (S <= 4 ? 4 : 2), 1, 2>(p, out, pl, st);
+        launch_tma<FmtFp8B128, S, (S <= 4 ? 4 : 2), 1, 2>(p, out, pl, st, moe);
         return;
     }
-    launch_tma_fp8_u<S, 4>(p, out, pl, st);
+    launch_tma_fp8_u<S, 4>(p, out, pl, st, moe);
 }
 
 int gemv_fp8_chunk(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S, int I,
@@ -346,6 +359,28 @@ int run_gemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float 
         if (rc != kOk) return rc;
     }
     return kOk;
+}
+
+
+// Routed experts (fmt=7): every slot on the staged kernel, one launch.
+int run_gemv_moe_fp8b128(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
+                         const int *ids, int n_slots, int S, int I, int O, cudaStream_t st) {
+    const uint8_t *probe = reinterpret_cast<const uint8_t *>(uintptr_t(256));   // stands for any 16-byte aligned expert
+    TmaPlan tp;
+    if (!fp8_tma_ok(x, probe, I, S) || !fp8_tma_plan(S, I, O, &tp) || tp.splits != 1) {
+        set_error_detail("qgemv_moe: fmt=7 routed experts need I %% 16 == 0, a 16-byte aligned x and rows "
+                         "short enough for one block (I = %d)", I);
+        return kEShape;
+    }
+    FmtFp8B128::Params p;
+    p.x = x; p.w = nullptr; p.scale_inv = nullptr; p.I = I; p.O = O; p.nbi = (I + 127) / 128;
+    const MoeLaunch m{MoeSlots{static_cast<const ExpertW *>(table), ids, n_experts, x_stride}, n_slots};
+    switch (S) {
+#define QG_CASE(SS) case SS: launch_tma_fp8_s<SS>(p, y, tp, st, &m); break;
+        QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+    }
+    return check_launch("qgemv_moe");
 }
 
 }  // namespace qg

@@ -103,6 +103,16 @@ struct FmtI4G {
     // ---- staged (TMA) kernel -------------------------------------------------
     struct TConst { uint32_t uoff; uint32_t goff; };   // unit byte offset, scale byte offset
     struct StageConst {};
+    // routed experts: the staged copies want both arrays 16-byte aligned
+    __device__ static bool expert_ok(const Params &, const void *w, const float *scales) {
+        return w != nullptr && scales != nullptr && ((uintptr_t)w % 16 == 0) && ((uintptr_t)scales % 16 == 0);
+    }
+    __device__ static Params with_expert(Params p, const void *w, const float *scales, size_t x_off) {
+        p.w = static_cast<const uint8_t *>(w);
+        p.scales = scales;
+        p.x += x_off;
+        return p;
+    }
 
     __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.rb; }
     __device__ static uint32_t aux_row_bytes(const Params &p) { return (uint32_t)p.ng * 4u; }
@@ -289,30 +299,32 @@ void launch_cs_i4g_s(const FmtI4G::Params &p, float *out, const CsPlan &pl, int 
 }
 
 template <int S, int RB>
-void launch_tma_i4g_u(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+void launch_tma_i4g_u(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
+                      const MoeLaunch *moe = nullptr) {
     constexpr int NW = S <= 2 ? 4 : S <= 4 ? 2 : 1;
     if constexpr (S == 1) {
         if (pl.U == 2) {
-            launch_tma<FmtI4G, S, NW, 2, RB>(p, out, pl, st);
+            launch_tma<FmtI4G, S, NW, 2, RB>(p, out, pl, st, moe);
             return;
         }
     }
-    launch_tma<FmtI4G, S, NW, 1, RB>(p, out, pl, st);
+    launch_tma<FmtI4G, S, NW, 1, RB>(p, out, pl, st, moe);
 }
 
 template <int S>
-void launch_tma_i4g_s(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+void launch_tma_i4g_s(const FmtI4G::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
+                      const MoeLaunch *moe = nullptr) {
     if constexpr (S <= 2) {
         if (pl.rb == 8) {
-            launch_tma_i4g_u<S, 8>(p, out, pl, st);
+            launch_tma_i4g_u<S, 8>(p, out, pl, st, moe);
             return;
         }
     }
     if (pl.rb == 2) {
-        launch_tma<FmtI4G, S, (S <= 2 ? 4 : S <= 4 ? 2 : 1), 1, 2>(p, out, pl, st);
+        launch_tma<FmtI4G, S, (S <= 2 ? 4 : S <= 4 ? 2 : 1), 1, 2>(p, out, pl, st, moe);
         return;
     }
-    launch_tma_i4g_u<S, 4>(p, out, pl, st);
+    launch_tma_i4g_u<S, 4>(p, out, pl, st, moe);
 }
 
 int gemv_i4g_chunk(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,
@@ -393,6 +405,30 @@ int run_gemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales
         if (rc != kOk) return rc;
     }
     return kOk;
+}
+
+
+// Routed experts (fmt=4): every slot on the staged kernel, one launch.
+int run_gemv_moe_i4g(float *y, const float *x, size_t x_stride, const void *table, int n_experts,
+                     const int *ids, int n_slots, int S, int I, int O, int gs, cudaStream_t st) {
+    const uint8_t *probe = reinterpret_cast<const uint8_t *>(uintptr_t(256));   // stands for any 16-byte aligned expert
+    TmaPlan tp;
+    if (!i4g_tma_ok(x, probe, reinterpret_cast<const float *>(probe), I, gs, S) ||
+        !i4g_tma_plan(S, I, O, gs, &tp) || tp.splits != 1) {
+        set_error_detail("qgemv_moe: fmt=4 routed experts need I %% 32 == 0, gs %% 32 == 0, ceil(I/gs) %% 4 == 0, "
+                         "a 16-byte aligned x and rows short enough for one block (I = %d, gs = %d)", I, gs);
+        return kEShape;
+    }
+    FmtI4G::Params p;
+    p.x = x; p.w = nullptr; p.scales = nullptr; p.I = I; p.O = O; p.gs = gs;
+    p.ng = (I + gs - 1) / gs; p.rb = ((size_t)I + 1) / 2;
+    const MoeLaunch m{MoeSlots{static_cast<const ExpertW *>(table), ids, n_experts, x_stride}, n_slots};
+    switch (S) {
+#define QG_CASE(SS) case SS: launch_tma_i4g_s<SS>(p, y, tp, st, &m); break;
+        QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+    }
+    return check_launch("qgemv_moe");
 }
 
 }  // namespace qg

@@ -154,6 +154,15 @@ struct FmtMq4 {
     // ---- staged (TMA) kernel -------------------------------------------------
     struct TConst { uint32_t uoff; uint32_t hoff; };   // unit and header byte offsets in the segment
     struct StageConst {};
+    // routed experts: 16-byte aligned blocks for the staged copies (no side array)
+    __device__ static bool expert_ok(const Params &, const void *w, const float *) {
+        return w != nullptr && ((uintptr_t)w % 16 == 0);
+    }
+    __device__ static Params with_expert(Params p, const void *w, const float *, size_t x_off) {
+        p.blocks = static_cast<const uint8_t *>(w);
+        p.x += x_off;
+        return p;
+    }
 
     __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.rowbytes; }
     __device__ static uint32_t aux_row_bytes(const Params &) { return 0u; }
@@ -447,36 +456,38 @@ void launch_cs_mq4_s(const Mq4Params &p, float *out, const CsPlan &pl, int units
 }
 
 template <int HK, int S, int RB>
-void launch_tma_mq4_u(const Mq4Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+void launch_tma_mq4_u(const Mq4Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
+                      const MoeLaunch *moe = nullptr) {
     constexpr int NW = S <= 2 ? 4 : S <= 4 ? 2 : 1;
     if constexpr (S == 1) {
         if (pl.U == 2) {
-            launch_tma<FmtMq4H<HK>, S, NW, 2, RB>(p, out, pl, st);
+            launch_tma<FmtMq4H<HK>, S, NW, 2, RB>(p, out, pl, st, moe);
             return;
         }
         if (pl.U == 3) {
-            launch_tma<FmtMq4H<HK>, S, NW, 3, RB>(p, out, pl, st);
+            launch_tma<FmtMq4H<HK>, S, NW, 3, RB>(p, out, pl, st, moe);
             return;
         }
-        launch_tma<FmtMq4H<HK>, S, NW, 1, RB>(p, out, pl, st);
+        launch_tma<FmtMq4H<HK>, S, NW, 1, RB>(p, out, pl, st, moe);
     } else {
-        launch_tma<FmtMq4<HK>, S, NW, 1, RB>(p, out, pl, st);
+        launch_tma<FmtMq4<HK>, S, NW, 1, RB>(p, out, pl, st, moe);
     }
 }
 
 template <int HK, int S>
-void launch_tma_mq4_s(const Mq4Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+void launch_tma_mq4_s(const Mq4Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
+                      const MoeLaunch *moe = nullptr) {
     if constexpr (S <= 2) {
         if (pl.rb == 8) {
-            launch_tma_mq4_u<HK, S, 8>(p, out, pl, st);
+            launch_tma_mq4_u<HK, S, 8>(p, out, pl, st, moe);
             return;
         }
     }
     if (pl.rb == 2) {
-        launch_tma<FmtMq4<HK>, S, (S <= 2 ? 4 : S <= 4 ? 2 : 1), 1, 2>(p, out, pl, st);
+        launch_tma<FmtMq4<HK>, S, (S <= 2 ? 4 : S <= 4 ? 2 : 1), 1, 2>(p, out, pl, st, moe);
         return;
     }
-    launch_tma_mq4_u<HK, S, 4>(p, out, pl, st);
+    launch_tma_mq4_u<HK, S, 4>(p, out, pl, st, moe);
 }
 
 template <int HK>
@@ -550,6 +561,29 @@ int run_gemv_mq4(float *y, const uint16_t *x, const uint8_t *blocks, int S, int 
         if (rc != kOk) return rc;
     }
     return kOk;
+}
+
+
+// Routed experts (the MQ4 formats): every slot on the staged kernel, one launch.
+template <int HK>
+int run_gemv_moe_mq4(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
+                     const int *ids, int n_slots, int S, int I, int O, cudaStream_t st) {
+    const uint8_t *probe = reinterpret_cast<const uint8_t *>(uintptr_t(256));   // stands for any 16-byte aligned expert
+    TmaPlan tp;
+    if (!mq4::mq4_tma_ok(x, probe, I) || !mq4::mq4_tma_plan(S, I, O, &tp) || tp.splits != 1) {
+        set_error_detail("qgemv_moe: MQ4 routed experts need an even number of 256-weight blocks per row, a "
+                         "16-byte aligned x and rows short enough for one block (I = %d)", I);
+        return kEShape;
+    }
+    Mq4Params p;
+    p.x = x; p.blocks = nullptr; p.I = I; p.O = O; p.rowbytes = (size_t)(I / 256) * 136;
+    const MoeLaunch m{MoeSlots{static_cast<const ExpertW *>(table), ids, n_experts, x_stride}, n_slots};
+    switch (S) {
+#define QG_CASE(SS) case SS: mq4::launch_tma_mq4_s<HK, SS>(p, y, tp, st, &m); break;
+        QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
+#undef QG_CASE
+    }
+    return check_launch("qgemv_moe");
 }
 
 }  // namespace qg

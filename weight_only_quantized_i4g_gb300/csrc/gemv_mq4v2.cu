@@ -11,4 +11,10 @@ int run_gemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, in
     return run_gemv_mq4<44>(y, x, blocks, S, I, O, ws, ws_bytes, st, "qgemv_mq4v2");
 }
 
+
+int run_gemv_moe_mq4v2(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
+                        const int *ids, int n_slots, int S, int I, int O, cudaStream_t st) {
+    return run_gemv_moe_mq4<44>(y, x, x_stride, table, n_experts, ids, n_slots, S, I, O, st);
+}
+
 }  // namespace qg

@@ -251,9 +251,9 @@ struct TmaLayout {
 };
 
 template <class F, int S, int NW, int U, int RB>
-__global__ void __launch_bounds__(32 * (tma_max_consumer_warps(S, U) + 1), 1)
-gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, int units_per_split,
-                int nrowb, int nst, TmaLayout L, int *err)
+__device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float *__restrict__ out, int units,
+                                              int units_per_split, int nrowb, int nst, const TmaLayout &L,
+                                              int *err)
 {
     constexpr int XU = NW * F::kElemsPerWord;
     constexpr int NP = NW * F::kPairsPerWord;
@@ -411,6 +411,57 @@ gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, 
     }
 }
 
+template <class F, int S, int NW, int U, int RB>
+__global__ void __launch_bounds__(32 * (tma_max_consumer_warps(S, U) + 1), 1)
+gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, int units_per_split,
+                int nrowb, int nst, TmaLayout L, int *err)
+{
+    gemv_tma_body<F, S, NW, U, RB>(p, out, units, units_per_split, nrowb, nst, L, err);
+}
+
+// ---------------------------------------------------------------------------
+// Routed experts: one launch for n_slots GEMVs of one format and shape.
+// Slot r (blockIdx.z) multiplies the expert table[ids[r]] (device arrays,
+// possibly written by the previous kernel on the stream, hence the wait
+// before they are read) with x + r * x_stride into out + r * S * O.  An
+// expert id outside [0, n_experts) or an expert whose pointers the staged
+// copies cannot take (F::expert_ok) raises kErrExpert; that slot's outputs
+// are then written as NaN.
+// ---------------------------------------------------------------------------
+struct ExpertW {            // same layout as qg_expert in qgemv.h
+    const void *w;
+    const float *scales;
+};
+struct MoeSlots {
+    const ExpertW *table;
+    const int *ids;
+    int n_experts;
+    size_t x_stride;         // activation elements between consecutive slots (0: shared x)
+};
+constexpr int kErrExpert = -8;
+
+template <class F, int S, int NW, int U, int RB>
+__global__ void __launch_bounds__(32 * (tma_max_consumer_warps(S, U) + 1), 1)
+gemv_tma_moe_kernel(const typename F::Params p0, float *__restrict__ out0, MoeSlots m, int units,
+                    int units_per_split, int nrowb, int nst, TmaLayout L, int *err)
+{
+    griddep_wait();          // the routing (ids) may be the previous kernel's output
+    const int r = blockIdx.z;
+    float *out = out0 + (size_t)r * S * p0.O;
+    const int id = m.ids[r];
+    ExpertW e = {nullptr, nullptr};
+    if (id >= 0 && id < m.n_experts) e = m.table[id];
+    if (!F::expert_ok(p0, e.w, e.scales)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_device_error(err, kErrExpert);
+        if (blockIdx.y == 0)
+            for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < S * p0.O; i += gridDim.x * blockDim.x)
+                out[i] = __int_as_float(0x7FC00000);
+        return;
+    }
+    const typename F::Params p = F::with_expert(p0, e.w, e.scales, (size_t)r * m.x_stride);
+    gemv_tma_body<F, S, NW, U, RB>(p, out, units, units_per_split, nrowb, nst, L, err);
+}
+
 // ---------------------------------------------------------------------------
 // Host side: plan and launch
 // ---------------------------------------------------------------------------
@@ -457,30 +508,43 @@ bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl);
 int *device_error_word();
 
 // Launch gemv_tma_kernel<F, S, NW, U, RB> with plan `pl`.
+// With `moe`, the routed-expert kernel over moe->n_slots slots (grid.z; the
+// plan must not split the reduction); each slot gets an equal share of the
+// resident blocks (at least one).
+struct MoeLaunch {
+    MoeSlots slots;
+    int n_slots;
+};
+
 template <class F, int S, int NW, int U, int RB>
-void launch_tma(const typename F::Params &p, float *out, const TmaPlan &pl, cudaStream_t st) {
+void launch_tma(const typename F::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
+                const MoeLaunch *moe = nullptr) {
     auto kern = gemv_tma_kernel<F, S, NW, U, RB>;
-    static int attr_set_mask = 0;   // one bit per device ordinal (< 31)
+    auto kern_moe = gemv_tma_moe_kernel<F, S, NW, U, RB>;
+    const void *kfn = moe ? reinterpret_cast<const void *>(kern_moe) : reinterpret_cast<const void *>(kern);
+    static int attr_set_mask[2] = {0, 0};   // one bit per device ordinal (< 31), per kernel
+    int &mask = attr_set_mask[moe ? 1 : 0];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 31 && !(__atomic_load_n(&attr_set_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-        __atomic_fetch_or(&attr_set_mask, 1 << dev, __ATOMIC_ACQ_REL);
+    if (dev < 31 && !(__atomic_load_n(&mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+        cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+        __atomic_fetch_or(&mask, 1 << dev, __ATOMIC_ACQ_REL);
     }
     const int threads = 32 * (pl.nc + 1);
     int per_sm = 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, pl.L.total) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, threads, pl.L.total) != cudaSuccess ||
         per_sm < 1) {
         cudaGetLastError();
         per_sm = 1;
     }
     long resident = (long)num_sms() * per_sm / pl.splits;
+    if (moe) resident /= moe->n_slots;
     if (resident < 1) resident = 1;
     const int grid_x = pl.nrowb < resident ? pl.nrowb : (int)resident;
     // Programmatic dependent launch: the kernel may start while the previous
     // kernel on the stream finishes (see griddep_wait).
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid_x, pl.splits);
+    cfg.gridDim = dim3(grid_x, pl.splits, moe ? moe->n_slots : 1);
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = pl.L.total;
     cfg.stream = st;
@@ -489,8 +553,12 @@ void launch_tma(const typename F::Params &p, float *out, const TmaPlan &pl, cuda
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, kern, p, out, pl.units, pl.units_per_split, pl.nrowb, pl.nst, pl.L,
-                       device_error_word());
+    if (moe)
+        cudaLaunchKernelEx(&cfg, kern_moe, p, out, moe->slots, pl.units, pl.units_per_split, pl.nrowb, pl.nst,
+                           pl.L, device_error_word());
+    else
+        cudaLaunchKernelEx(&cfg, kern, p, out, pl.units, pl.units_per_split, pl.nrowb, pl.nst, pl.L,
+                           device_error_word());
 }
 
 }  // namespace qg

@@ -38,6 +38,20 @@ int run_gemv_mq4c(float *y, const uint16_t *x, const uint8_t *blocks, int S, int
                   size_t ws_bytes, cudaStream_t st);
 
 
+// Routed experts: n_slots GEMVs of one shape in one launch; `table` is a
+// device array of {weights, scales} pointer pairs (qg_expert), `ids` a device
+// array of n_slots expert ids, slot r reads x + r * x_stride (elements).
+int run_gemv_moe_i4g(float *y, const float *x, size_t x_stride, const void *table, int n_experts,
+                     const int *ids, int n_slots, int S, int I, int O, int gs, cudaStream_t st);
+int run_gemv_moe_fp8b128(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
+                         const int *ids, int n_slots, int S, int I, int O, cudaStream_t st);
+int run_gemv_moe_mq4v2(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
+                       const int *ids, int n_slots, int S, int I, int O, cudaStream_t st);
+int run_gemv_moe_mq4v1(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
+                       const int *ids, int n_slots, int S, int I, int O, cudaStream_t st);
+int run_gemv_moe_mq4c(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
+                      const int *ids, int n_slots, int S, int I, int O, cudaStream_t st);
+
 int run_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs, cudaStream_t st);
 int run_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, cudaStream_t st);
 int run_encode_mq4_one_header(uint8_t *blocks, const float *w, int O, int I, bool fp16_header, cudaStream_t st);
