@@ -443,6 +443,7 @@ def ours_arm(args):
         per_format.update(batched_breakdown(qg, torch, calls, stream, hbm_peak, dev))
         if len(shapes) == len(SHAPES):
             per_format.update(one_header_breakdown(qg, torch, stream, hbm_peak, dev))
+            per_format.update(moe_breakdown(qg, torch, stream, hbm_peak, dev))
     prefill = prefill_measure(qg, torch, dev, stream) if args.prefill else None
 
     cpu = None
@@ -717,6 +718,91 @@ def one_header_breakdown(qg, torch, stream, hbm_peak, dev):
     return out
 
 
+MOE_E, MOE_K = 32, 8     # experts in the table, routed experts per token
+
+
+def moe_breakdown(qg, torch, stream, hbm_peak, dev):
+    """Routed-expert decode at batch 1 on the routed-expert shapes: the gate and
+    up projections of K = 8 routed experts (16 slots of 2048x7168 reading the
+    token's x) and their down projections (8 slots of 7168x2048, one x each),
+    fmt=4 g64 and MQ4-V2, one qgemv_moe launch each.  A table of 32 experts
+    (>= 3x L2 of weights); every call routes to a different seeded set of 8,
+    so the weights come from HBM.  Kernel-only time per call from a CUDA graph
+    of back-to-back calls (best of 4 replays), against the same work as one
+    single-matrix launch per slot."""
+    out = {}
+    lib = qg._lib
+    st = stream.cuda_stream
+    g = torch.Generator(device=dev)
+    sets = 12
+    for fmt_name, fmt in (("fmt4", 4), ("mq4v2", 44)):
+        for proj, O, I, shared in (("gate_up", 2048, 7168, True), ("down", 7168, 2048, False)):
+            per = 2 if proj == "gate_up" else 1            # matrices per expert
+            n_tab = MOE_E * per
+            g.manual_seed(7000 + O + fmt)
+            mats, scs = [], []
+            with torch.cuda.stream(stream):
+                for _ in range(n_tab):
+                    w = torch.randn(O, I, generator=g, device=dev) * 0.02
+                    if fmt == 4:
+                        wq = torch.empty(O * I // 2, dtype=torch.uint8, device=dev)
+                        sc = torch.empty(O * (I // GS), dtype=torch.float32, device=dev)
+                        qg.check(qg.qg_quantize_i4g(wq, sc, w, O, I, GS, stream=st))
+                        mats.append(wq); scs.append(sc)
+                    else:
+                        blocks = torch.empty(O * (I // 256) * 136, dtype=torch.uint8, device=dev)
+                        qg.check(qg.qg_encode_mq4v2(blocks, w, O, I, stream=st))
+                        mats.append(blocks); scs.append(None)
+                    del w
+            stream.synchronize()
+            table = torch.frombuffer(bytearray(qg.expert_table(list(zip(mats, scs)))), dtype=torch.uint8).to(dev)
+            n_slots = MOE_K * per
+            id_sets = []
+            for k in range(sets):
+                experts = torch.randperm(MOE_E, generator=torch.Generator().manual_seed(100 * k + O))[:MOE_K]
+                ids = torch.stack([experts * per + j for j in range(per)], 1).reshape(-1)
+                id_sets.append(ids.to(torch.int32).to(dev))
+            n_x = 1 if shared else n_slots
+            xs = torch.randn(n_x, I, generator=g, device=dev)
+            x = xs if fmt == 4 else xs.to(torch.bfloat16).view(torch.int16)
+            y = torch.empty(n_slots * O, dtype=torch.float32, device=dev)
+            stride = 0 if shared else I
+            nbytes = n_slots * weight_bytes("i4g" if fmt == 4 else "mq4", O, I)
+
+            def issue_moe(r):
+                rc = lib.qgemv_moe(fmt, y.data_ptr(), x.data_ptr(), stride, table.data_ptr(), n_tab,
+                                   id_sets[r % sets].data_ptr(), n_slots, 1, I, O, GS if fmt == 4 else 0, st)
+                if rc:
+                    raise qg.QGError(rc)
+            host_ids = [s.cpu().tolist() for s in id_sets]
+
+            def issue_single(r):
+                for j, e in enumerate(host_ids[r % sets]):
+                    xp = x.data_ptr() + (0 if shared else j * I * x.element_size())
+                    yp = y.data_ptr() + j * O * 4
+                    if fmt == 4:
+                        rc = lib.qgemv_i4g(yp, xp, mats[e].data_ptr(), scs[e].data_ptr(), 1, I, O, GS, None, 0, st)
+                    else:
+                        rc = lib.qgemv_mq4v2(yp, xp, mats[e].data_ptr(), 1, I, O, None, 0, st)
+                    if rc:
+                        raise qg.QGError(rc)
+            with torch.cuda.stream(stream):             # first launches set kernel attributes, outside capture
+                issue_moe(0)
+                issue_single(0)
+            stream.synchronize()
+            reps = 48
+            t_moe = _graph_per_call(torch, stream, reps, issue_moe)
+            t_one = _graph_per_call(torch, stream, reps, issue_single)
+            gbs = nbytes / (t_moe * 1e-3) / 1e9
+            out[f"moe_{fmt_name}_{proj}_{n_slots}x{O}x{I}"] = {
+                "us_per_call": round(t_moe * 1e3, 3), "weight_gbs": round(gbs, 1),
+                "pct_hbm_peak": round(100 * gbs / hbm_peak, 1),
+                "single_matrix_launches_us": round(t_one * 1e3, 3), "slots": n_slots,
+                "x": "shared" if shared else "per slot"}
+            del mats, scs, table
+    return out
+
+
 BATCHED = {"i4g": 4, "mq4": 8}     # the configs' batched decode cases: fmt4 at batch 4, MQ4-V2 at 8
 
 
@@ -801,15 +887,28 @@ def main():
                     help="profiling runs: time only these prefill GEMMs (comma-separated fmt:O:I, fmt in "
                          "i4g/fp8/mq4/mq4v1/mq4c, M=512) and print their prefill object")
     ap.add_argument("--prefill-reps", type=int, default=20)
+    ap.add_argument("--moe-only", action="store_true", help="profiling runs: print only the routed-expert lines")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.prefill_only:
         prefill_only(args)
+    elif args.moe_only:
+        moe_only(args)
     elif args.impl == "reference":
         reference_arm(args)
     else:
         ours_arm(args)
+
+
+def moe_only(args):
+    import torch
+    import weight_only_quantized_i4g_gb300 as qg
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream()
+    hbm_peak, _ = load_peaks()
+    print(json.dumps({"moe": moe_breakdown(qg, torch, stream, hbm_peak, dev)}), flush=True)
 
 
 def prefill_only(args):

@@ -367,13 +367,14 @@ int run_gemv_moe_fp8b128(float *y, const uint16_t *x, size_t x_stride, const voi
                          const int *ids, int n_slots, int S, int I, int O, cudaStream_t st) {
     const uint8_t *probe = reinterpret_cast<const uint8_t *>(uintptr_t(256));   // stands for any 16-byte aligned expert
     TmaPlan tp;
-    if (!fp8_tma_ok(x, probe, I, S) || !fp8_tma_plan(S, I, O, &tp) || tp.splits != 1) {
+    if (!fp8_tma_ok(x, probe, I, S) || !fp8_tma_plan(S, I, moe_plan_rows(O, n_slots), &tp) || tp.splits != 1) {
         set_error_detail("qgemv_moe: fmt=7 routed experts need I %% 16 == 0, a 16-byte aligned x and rows "
                          "short enough for one block (I = %d)", I);
         return kEShape;
     }
     FmtFp8B128::Params p;
     p.x = x; p.w = nullptr; p.scale_inv = nullptr; p.I = I; p.O = O; p.nbi = (I + 127) / 128;
+    tp.nrowb = (O + tp.rb - 1) / tp.rb;            // the plan sized the launch for all slots' rows
     const MoeLaunch m{MoeSlots{static_cast<const ExpertW *>(table), ids, n_experts, x_stride}, n_slots};
     switch (S) {
 #define QG_CASE(SS) case SS: launch_tma_fp8_s<SS>(p, y, tp, st, &m); break;

@@ -414,7 +414,7 @@ int run_gemv_moe_i4g(float *y, const float *x, size_t x_stride, const void *tabl
     const uint8_t *probe = reinterpret_cast<const uint8_t *>(uintptr_t(256));   // stands for any 16-byte aligned expert
     TmaPlan tp;
     if (!i4g_tma_ok(x, probe, reinterpret_cast<const float *>(probe), I, gs, S) ||
-        !i4g_tma_plan(S, I, O, gs, &tp) || tp.splits != 1) {
+        !i4g_tma_plan(S, I, moe_plan_rows(O, n_slots), gs, &tp) || tp.splits != 1) {
         set_error_detail("qgemv_moe: fmt=4 routed experts need I %% 32 == 0, gs %% 32 == 0, ceil(I/gs) %% 4 == 0, "
                          "a 16-byte aligned x and rows short enough for one block (I = %d, gs = %d)", I, gs);
         return kEShape;
@@ -422,6 +422,7 @@ int run_gemv_moe_i4g(float *y, const float *x, size_t x_stride, const void *tabl
     FmtI4G::Params p;
     p.x = x; p.w = nullptr; p.scales = nullptr; p.I = I; p.O = O; p.gs = gs;
     p.ng = (I + gs - 1) / gs; p.rb = ((size_t)I + 1) / 2;
+    tp.nrowb = (O + tp.rb - 1) / tp.rb;            // the plan sized the launch for all slots' rows
     const MoeLaunch m{MoeSlots{static_cast<const ExpertW *>(table), ids, n_experts, x_stride}, n_slots};
     switch (S) {
 #define QG_CASE(SS) case SS: launch_tma_i4g_s<SS>(p, y, tp, st, &m); break;

@@ -570,13 +570,15 @@ int run_gemv_moe_mq4(float *y, const uint16_t *x, size_t x_stride, const void *t
                      const int *ids, int n_slots, int S, int I, int O, cudaStream_t st) {
     const uint8_t *probe = reinterpret_cast<const uint8_t *>(uintptr_t(256));   // stands for any 16-byte aligned expert
     TmaPlan tp;
-    if (!mq4::mq4_tma_ok(x, probe, I) || !mq4::mq4_tma_plan(S, I, O, &tp) || tp.splits != 1) {
+    if (!mq4::mq4_tma_ok(x, probe, I) || !mq4::mq4_tma_plan(S, I, moe_plan_rows(O, n_slots), &tp) ||
+        tp.splits != 1) {
         set_error_detail("qgemv_moe: MQ4 routed experts need an even number of 256-weight blocks per row, a "
                          "16-byte aligned x and rows short enough for one block (I = %d)", I);
         return kEShape;
     }
     Mq4Params p;
     p.x = x; p.blocks = nullptr; p.I = I; p.O = O; p.rowbytes = (size_t)(I / 256) * 136;
+    tp.nrowb = (O + tp.rb - 1) / tp.rb;            // the plan sized the launch for all slots' rows
     const MoeLaunch m{MoeSlots{static_cast<const ExpertW *>(table), ids, n_experts, x_stride}, n_slots};
     switch (S) {
 #define QG_CASE(SS) case SS: mq4::launch_tma_mq4_s<HK, SS>(p, y, tp, st, &m); break;

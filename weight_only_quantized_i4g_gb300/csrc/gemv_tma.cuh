@@ -511,6 +511,13 @@ int *device_error_word();
 // With `moe`, the routed-expert kernel over moe->n_slots slots (grid.z; the
 // plan must not split the reduction); each slot gets an equal share of the
 // resident blocks (at least one).
+// Rows a routed-expert launch is planned for: all slots' rows together (one
+// launch streams them all), capped to an int.
+inline int moe_plan_rows(int O, int n_slots) {
+    const long long r = (long long)O * n_slots;
+    return r > 0x7FFFFFFF ? 0x7FFFFFFF : (int)r;
+}
+
 struct MoeLaunch {
     MoeSlots slots;
     int n_slots;
