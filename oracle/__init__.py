@@ -52,6 +52,9 @@ def _declare(lib):
     lib.oracle_qgemm_i4g.argtypes = [P, P, P, P, P, i, i, i, i]
     lib.oracle_quantize_i4g.argtypes = [P, P, P, i, i, i]
     lib.oracle_qgemv_fp8b128.argtypes = [P, P, P, P, P, i, i, i]
+    lib.oracle_e8m0_value.argtypes = [ctypes.c_uint8]
+    lib.oracle_e8m0_value.restype = ctypes.c_double
+    lib.oracle_qgemv_fp8ue8m0.argtypes = [P, P, P, P, P, i, i, i]
     lib.oracle_mq4v2_weight.argtypes = [P, i]
     lib.oracle_mq4v2_weight.restype = ctypes.c_double
     lib.oracle_qgemv_mq4v2.argtypes = [P, P, P, P, i, i, i]
@@ -172,6 +175,27 @@ class Oracle:
         self.lib.oracle_qgemv_fp8b128(_p(y), _p(mag), _p(x), _p(ws), _p(ss), S, I, n)
         return y, mag
 
+    # fmt=7 with UE8M0 scales ---------------------------------------------------
+    def e8m0_value(self, code: int) -> float:
+        return self.lib.oracle_e8m0_value(code)
+
+    def qgemv_fp8ue8m0(self, x_bf16, w, scale_e8m0, S, I, O, rows=None):
+        """``rows`` = (o0, o1) with o0 a multiple of 128 restricts to a row slice."""
+        x = np.ascontiguousarray(x_bf16, np.uint16)
+        w = np.ascontiguousarray(w, np.uint8)
+        sc = np.ascontiguousarray(scale_e8m0, np.uint8)
+        o0, o1 = rows if rows is not None else (0, O)
+        assert o0 % 128 == 0
+        nbi = (I + 127) // 128
+        nbo = (O + 127) // 128
+        ws = np.ascontiguousarray(w.reshape(O, I)[o0:o1])
+        ss = np.ascontiguousarray(sc.reshape(nbo, nbi)[o0 // 128:])
+        n = o1 - o0
+        y = np.empty((S, n), np.float64)
+        mag = np.empty((S, n), np.float64)
+        self.lib.oracle_qgemv_fp8ue8m0(_p(y), _p(mag), _p(x), _p(ws), _p(ss), S, I, n)
+        return y, mag
+
     # MQ4-V2 -----------------------------------------------------------------
     def mq4v2_weight(self, block: np.ndarray, j: int) -> float:
         block = np.ascontiguousarray(block, np.uint8)
@@ -241,7 +265,8 @@ class Oracle:
         for fmt=4 and bf16 bits otherwise."""
         x = np.ascontiguousarray(x, np.float32 if fmt == 4 else np.uint16)
         ws = [np.ascontiguousarray(w, np.uint8) for w in weights]
-        ss = [None if sc is None else np.ascontiguousarray(sc, np.float32) for sc in scales]
+        sdt = np.uint8 if fmt == 71 else np.float32       # UE8M0 scales are bytes
+        ss = [None if sc is None else np.ascontiguousarray(sc, sdt) for sc in scales]
         ids = np.ascontiguousarray(ids, np.int32)
         n = len(ids)
         wp = (ctypes.c_void_p * len(ws))(*[w.ctypes.data for w in ws])

@@ -15,6 +15,7 @@
  *
  *   [colibri #457]  "metal: grouped-int4 (fmt=4) GEMV support", sections 3-5, 7, 11
  *   [colibri #528]  "fmt=7: fp8-e4m3-b128 passthrough weight format", Design
+ *                   (f32 block scales, and the UE8M0 scale encoding it names)
  *   [hipfire MQ4V2] "MQ4 V2" docs, sections 1b, 1c, 1e, 2, 3, 4, 9
  *
  * No function here blocks, fuses or reorders beyond what its definition
@@ -240,6 +241,41 @@ void oracle_qgemv_fp8b128(double *y, double *mag, const uint16_t *x, const uint8
             for (int i = 0; i < I; ++i) {
                 double wv = oracle_e4m3_value(w[(size_t)o * I + i]);
                 double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];
+                double t = wv * sc * oracle_bf16_value(x[(size_t)s * I + i]);
+                acc += t;
+                m += fabs(t);
+            }
+            y[(size_t)s * O + o] = acc;
+            mag[(size_t)s * O + o] = m;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* fmt=7 with UE8M0 block scales ([colibri #528] Design: the scale encoding  */
+/* is a declared property of the format; DeepSeek-V4 ships the same e4m3     */
+/* geometry with one byte per 128x128 block holding a power-of-two exponent, */
+/* dtype F8_E8M0).  The page gives no bias; the reading taken is the OCP MX  */
+/* E8M0 type that name denotes: byte e means 2^(e - 127), e = 255 is NaN.    */
+/*   W[o,i] = e4m3(w[o*I+i]) * 2^(scale_e8m0[(o/128)*ceil(I/128) + i/128] - 127) */
+/* ------------------------------------------------------------------------ */
+double oracle_e8m0_value(uint8_t e)
+{
+    if (e == 255)
+        return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+void oracle_qgemv_fp8ue8m0(double *y, double *mag, const uint16_t *x, const uint8_t *w,
+                           const uint8_t *scale_e8m0, int S, int I, int O)
+{
+    size_t nbi = ((size_t)I + 127) / 128;
+    for (int s = 0; s < S; ++s) {
+        for (int o = 0; o < O; ++o) {
+            double acc = 0.0, m = 0.0;
+            for (int i = 0; i < I; ++i) {
+                double wv = oracle_e4m3_value(w[(size_t)o * I + i]);
+                double sc = oracle_e8m0_value(scale_e8m0[(size_t)(o / 128) * nbi + (size_t)(i / 128)]);
                 double t = wv * sc * oracle_bf16_value(x[(size_t)s * I + i]);
                 acc += t;
                 m += fabs(t);
@@ -535,6 +571,9 @@ void oracle_qgemv_moe(int fmt, double *y, double *mag, const void *x, size_t x_s
             break;
         case 7:
             oracle_qgemv_fp8b128(yr, mr, (const uint16_t *)x + xo, we, scales[id], S, I, O);
+            break;
+        case 71: /* fmt=7 with UE8M0 scales: the table's scale pointer holds the bytes */
+            oracle_qgemv_fp8ue8m0(yr, mr, (const uint16_t *)x + xo, we, (const uint8_t *)scales[id], S, I, O);
             break;
         case 13:
             oracle_qgemv_mq4v1(yr, mr, (const uint16_t *)x + xo, we, S, I, O);

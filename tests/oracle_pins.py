@@ -284,6 +284,56 @@ def pin_fp8_bruteforce(orc):
         _close(y, X @ W.T, np.abs(X) @ np.abs(W).T, what=f"fp8 O={O} I={I}")
 
 
+def pin_e8m0_vs_torch(orc):
+    """All 256 UE8M0 bytes against torch.float8_e8m0fnu (an independent
+    implementation of the OCP E8M0 type): 2^(e-127), 255 is NaN."""
+    import torch
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e8m0fnu).double().numpy()
+    got = np.array([orc.e8m0_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref)) and np.isnan(got[255]) and np.isnan(got).sum() == 1
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert got[127] == 1.0 and got[0] == 2.0 ** -127 and got[254] == 2.0 ** 127
+
+
+def pin_fp8ue8m0_golden(orc):
+    g = _golden("fp8ue8m0_hand.json")
+    for c in g["cases"]:
+        O, I = c["O"], c["I"]
+        codes = np.full(O * I, c["fill"], np.uint8) if c["codes"] is None else np.array(c["codes"], np.uint8)
+        x = np.ones(I, np.float32) if c["x"] == "ones" else np.array(c["x"], np.float32)
+        xb = synth.bf16_bits(x)
+        if "scale_cases" in c:
+            for byte, want in c["scale_cases"]:
+                y, _ = orc.qgemv_fp8ue8m0(xb, codes, np.array([byte], np.uint8), 1, I, O)
+                assert (np.isnan(y[0, 0]) if want == "nan" else y[0, 0] == want), (byte, y)
+            continue
+        y, mag = orc.qgemv_fp8ue8m0(xb, codes, np.array(c["scales"], np.uint8), 1, I, O)
+        if "y" in c:
+            assert np.array_equal(y[0], c["y"]) and np.array_equal(mag[0], c["mag"]), (y, mag)
+        for row, want in c.get("y_rows", {}).items():
+            assert y[0, int(row)] == want, (row, y[0, int(row)], want)
+
+
+def pin_fp8ue8m0_bruteforce(orc):
+    """Edge shapes and every exponent byte but NaN: oracle == numpy dequantize
+    (e4m3 via torch, 2.0 ** (e - 127)) + matmul; and the same codes with the
+    equivalent f32 scales give the fmt=7 f32 result exactly."""
+    rng = np.random.default_rng(23)
+    for (O, I, S) in [(1, 1, 1), (130, 200, 2), (129, 128, 1), (384, 6144, 3), (5, 300, 4)]:
+        codes = synth.bytes_excluding(int(rng.integers(1 << 30)), O * I)
+        nbo, nbi = (O + 127) // 128, (I + 127) // 128
+        eb = rng.integers(100, 150, nbo * nbi).astype(np.uint8)
+        xb = synth.bf16_bits(rng.standard_normal(S * I).astype(np.float32))
+        y, mag = orc.qgemv_fp8ue8m0(xb, codes, eb, S, I, O)
+        f32 = (2.0 ** (eb.astype(np.float64) - 127)).astype(np.float32)
+        W = _dequant_fp8_numpy(codes, f32, O, I)
+        X = synth.bf16_to_f32(xb).reshape(S, I).astype(np.float64)
+        _close(y, X @ W.T, np.abs(X) @ np.abs(W).T, what=f"fp8ue8m0 O={O} I={I}")
+        y2, _ = orc.qgemv_fp8b128(xb, codes, f32, S, I, O)
+        assert np.array_equal(y, y2)
+
+
 def pin_fp8_nan_rows(orc):
     """A NaN code poisons exactly its own output row."""
     O, I = 130, 130
@@ -612,11 +662,15 @@ def _moe_experts(rng, fmt, n_experts, O, I, gs):
             w = rng.integers(0, 256, O * rb, dtype=np.uint8)
             sc = rng.uniform(-2, 2, O * ng).astype(np.float32)
             deq.append(_dequant_i4g_numpy(w, sc, O, I, gs))
-        elif fmt == 7:
+        elif fmt in (7, 71):
             w = synth.bytes_excluding(int(rng.integers(1 << 30)), O * I)
             nbo, nbi = (O + 127) // 128, (I + 127) // 128
-            sc = synth.log_uniform(int(rng.integers(1 << 30)), nbo * nbi, 1e-4, 1e-2)
-            deq.append(_dequant_fp8_numpy(w, sc, O, I))
+            if fmt == 7:
+                sc = synth.log_uniform(int(rng.integers(1 << 30)), nbo * nbi, 1e-4, 1e-2)
+                deq.append(_dequant_fp8_numpy(w, sc, O, I))
+            else:
+                sc = rng.integers(110, 125, nbo * nbi).astype(np.uint8)
+                deq.append(_dequant_fp8_numpy(w, (2.0 ** (sc.astype(np.float64) - 127)).astype(np.float32), O, I))
         else:
             nb = I // 256
             w = rng.integers(0, 256, (O, nb, 136), dtype=np.uint8)
@@ -645,8 +699,8 @@ def pin_moe_bruteforce(orc):
     with repeated ids, ids out of order, a shared x and one x per slot; a slot
     whose id names no expert is NaN."""
     rng = np.random.default_rng(51)
-    for fmt, (O, I, gs) in ((4, (3, 200, 64)), (7, (130, 260, 0)), (44, (3, 512, 0)), (13, (2, 768, 0)),
-                            (45, (2, 512, 0))):
+    for fmt, (O, I, gs) in ((4, (3, 200, 64)), (7, (130, 260, 0)), (71, (130, 260, 0)), (44, (3, 512, 0)),
+                            (13, (2, 768, 0)), (45, (2, 512, 0))):
         E = 4
         ws, ss, deq = _moe_experts(rng, fmt, E, O, I, gs)
         ids = np.array([2, 0, 2, 3, 1], np.int32)

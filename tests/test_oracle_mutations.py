@@ -45,9 +45,17 @@ MUTATIONS = [
     ("fp8_block_transposed",
      "double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];",
      "double sc = (double)scale_inv[((size_t)(i / 128) * nbi + (size_t)(o / 128)) % (nbi * (((size_t)O + 127) / 128))];"),
-    ("fp8_divide_scale", "double t = wv * sc * oracle_bf16_value", "double t = wv / sc * oracle_bf16_value"),
+    ("fp8_divide_scale",
+     "double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];\n                double t = wv * sc",
+     "double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];\n                double t = wv / sc"),
     ("fp8_block_64", "double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];",
      "double sc = (double)scale_inv[((size_t)(o / 128) * nbi + (size_t)(i / 64)) % (nbi * (((size_t)O + 127) / 128))];"),
+    # UE8M0 scales
+    ("e8m0_bias_126", "return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 126);"),
+    ("e8m0_no_nan", "    if (e == 255)\n        return NAN;\n    return ldexp", "    if (e == 256)\n        return NAN;\n    return ldexp"),
+    ("fp8ue8m0_block_transposed",
+     "double sc = oracle_e8m0_value(scale_e8m0[(size_t)(o / 128) * nbi + (size_t)(i / 128)]);",
+     "double sc = oracle_e8m0_value(scale_e8m0[((size_t)(i / 128) * nbi + (size_t)(o / 128)) % (nbi * (((size_t)O + 127) / 128))]);"),
     # f16 / bf16
     ("f16_truncate", "double frac = rint((a / ldexp(1.0, e) - 1.0) * 1024.0);",
      "double frac = floor((a / ldexp(1.0, e) - 1.0) * 1024.0);"),
