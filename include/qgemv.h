@@ -83,7 +83,15 @@ const char *qg_last_error(void);
 int qg_device_status(int *status);
 
 /* Format ids for qg_workspace_bytes. */
-enum { QG_FMT_I4G = 4, QG_FMT_FP8B128 = 7, QG_FMT_MQ4V1 = 13, QG_FMT_MQ4V2 = 44, QG_FMT_MQ4C = 45 };
+enum {
+    QG_FMT_I4G = 4,         /* grouped int4 (fmt=4)                            */
+    QG_FMT_FP8B128 = 7,     /* FP8-e4m3, 128x128 f32 block scales (fmt=7)      */
+    QG_FMT_FP8UE8M0 = 71,   /* FP8-e4m3, 128x128 UE8M0 block scales (fmt=7 with */
+                            /* the page's second scale encoding; a library id) */
+    QG_FMT_MQ4V1 = 13,      /* MQ4 v1 (qt=13)                                  */
+    QG_FMT_MQ4V2 = 44,      /* MQ4-V2 (qt=44)                                  */
+    QG_FMT_MQ4C = 45        /* MQ4C pad (qt=45)                                */
+};
 
 /* Bytes of workspace that the GEMV entry point of format `fmt` needs for
  * this shape on the current device (0 when the call does not split the
@@ -157,6 +165,22 @@ int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *sc
                   int S, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* fmt=7 with UE8M0 block scales, decode GEMV                               */
+/* colibri PR #528, section "Design": the scale encoding is a property of   */
+/* the format; DeepSeek-V4 ships the same e4m3 weight geometry with UE8M0   */
+/* scales, one byte per 128x128 block holding a power-of-two exponent.      */
+/*                                                                          */
+/*   w           e4m3 [O, I] as for qgemv_fp8b128                           */
+/*   scale_e8m0  uint8 [ceil(O/128), ceil(I/128)]: byte e means 2^(e - 127) */
+/*               (OCP MX E8M0; e = 255 is NaN and poisons its block)        */
+/*   y[s,o] = sum_i e4m3(w[o,i]) * 2^(scale_e8m0[o/128, i/128] - 127) * x[s,i] */
+/* Everything else (x, y, workspace, alignment, paths) as qgemv_fp8b128,    */
+/* except that scale_e8m0 needs no alignment.                               */
+/* ------------------------------------------------------------------------ */
+int qgemv_fp8ue8m0(float *y, const uint16_t *x, const uint8_t *w, const uint8_t *scale_e8m0,
+                   int S, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Routed experts: many decode GEMVs of one format and shape in one launch  */
 /* colibri PR #457, section 7 (fmt=4 is mostly an expert format; the        */
 /* batched routed-expert path takes a per-expert pointer array and one      */
@@ -176,14 +200,15 @@ int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *sc
 /*            of one token)                                                 */
 /*   y        DEVICE f32 [n_slots][S, O]: y[r][s][o] = sum_i                */
 /*            W_{ids[r]}[o, i] * x_r[s, i] with the format's dequantization */
-/*   fmt      QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_MQ4V2, QG_FMT_MQ4V1 or     */
-/*            QG_FMT_MQ4C;  gs is read for fmt=4 only                       */
+/*   fmt      QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_FP8UE8M0 (scales are then  */
+/*            the UE8M0 bytes), QG_FMT_MQ4V2, QG_FMT_MQ4V1 or QG_FMT_MQ4C;  */
+/*            gs is read for fmt=4 only                                     */
 /*   S        tokens per slot, 1..8 (decode)                                */
 /* experts and ids may be written by earlier kernels on `stream` (a        */
 /* router): the kernel reads them after those kernels finish.  n_slots = 0 */
 /* returns QG_OK and launches nothing.  Needs x 16-byte aligned (and        */
 /* x_slot_stride a whole number of 16-byte lines), each expert's w 16-byte */
-/* aligned (fmt=4 scales too; fmt=7 scales 4-byte), and rows short enough   */
+/* aligned (fmt=4 scales too; fmt=7 f32 scales 4-byte), and rows short enough */
 /* for one thread block (fmt=4: I % 32 == 0, gs % 32 == 0, ceil(I/gs) % 4  */
 /* == 0; fmt=7: I % 16 == 0; MQ4: I/256 even), else QG_ESHAPE / QG_EALIGN. */
 /* A slot whose id is outside [0, n_experts) or whose expert pointers are  */
@@ -279,6 +304,12 @@ int qgemm_i4g(float *Y, const uint16_t *X, const uint8_t *w, const float *scales
 /* ------------------------------------------------------------------------ */
 int qgemm_fp8b128(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv,
                   int M, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* qgemm_fp8b128 with UE8M0 block scales (the byte e means 2^(e - 127), see  */
+/* qgemv_fp8ue8m0): same X, Y, workspace (qg_gemm_workspace_bytes with      */
+/* QG_FMT_FP8UE8M0), paths, precision and errors as qgemm_fp8b128.          */
+int qgemm_fp8ue8m0(float *Y, const uint16_t *X, const uint8_t *w, const uint8_t *scale_e8m0,
+                   int M, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* MQ4-V2 batched prefill dequant-GEMM on the tensor cores                  */

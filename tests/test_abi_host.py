@@ -94,6 +94,15 @@ def test_mq4_refusals(qg):
     assert qg.qgemv_mq4v2(P, P, P, 1, 256, 0, stream=0) == qg.QG_EINVAL
 
 
+def test_fp8ue8m0_refusals(qg):
+    P = POISON
+    assert qg.qgemv_fp8ue8m0(P, P, P, None, 1, 256, 4, stream=0) == qg.QG_EINVAL
+    assert qg.qgemv_fp8ue8m0(P, P + 1, P, P + 1, 1, 256, 4, stream=0) == qg.QG_EALIGN   # x odd; scales any
+    assert qg.qgemv_fp8ue8m0(P, P, P, P, 1, 256, 0, stream=0) == qg.QG_EINVAL
+    assert qg.qgemm_fp8ue8m0(P, P, P, P, 0, 256, 4, stream=0) == qg.QG_EINVAL
+    assert qg.qgemm_fp8ue8m0(P + 2, P, P, P, 4, 256, 4, stream=0) == qg.QG_EALIGN
+
+
 def test_moe_refusals(qg):
     P = POISON
     moe = qg.qgemv_moe

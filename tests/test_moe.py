@@ -14,7 +14,7 @@ from gpu_util import TOL, compare, dev, orc, torch
 
 pytestmark = pytest.mark.gpu
 
-FMTS = (4, 7, 44, 13, 45)
+FMTS = (4, 7, 71, 44, 13, 45)
 
 
 @pytest.fixture(scope="module")
@@ -34,6 +34,10 @@ def experts(fmt, E, O, I, gs, tag):
         elif fmt == 7:
             codes, sc, _ = synth.fmt7_raw(O, I, 1, tag + e)
             ws.append(codes.reshape(-1)); ss.append(sc.reshape(-1))
+        elif fmt == 71:
+            codes, _, _ = synth.fmt7_raw(O, I, 1, tag + e)
+            nb = ((O + 127) // 128) * ((I + 127) // 128)
+            ws.append(codes.reshape(-1)); ss.append((113 + synth.uint64(tag + e, nb) % 8).astype(np.uint8))
         else:
             w, _, d = synth.mq4_raw(O, I, 1, tag + e)
             wr = orc().fwht256(w, d)
@@ -73,7 +77,7 @@ def run(qg, fmt, ws, ss, ids, x, x_stride, S, I, O, gs, keep=None):
 @pytest.mark.parametrize("S", [1, 2, 5, 8])
 @pytest.mark.parametrize("shared", [True, False])
 def test_moe_small(qg, fmt, S, shared):
-    O, I, gs = (300, 1024, 64) if fmt != 7 else (300, 1040, 0)
+    O, I, gs = (300, 1024, 64) if fmt not in (7, 71) else (300, 1040, 0)
     ws, ss = experts(fmt, 6, O, I, gs, tag=100 * fmt + S)
     ids = [3, 0, 3, 5, 1]
     n_x = 1 if shared else len(ids)

@@ -20,6 +20,11 @@ int run_gemm_fp8b128_general(float *Y, const uint16_t *X, const uint8_t *w, cons
 int run_gemm_fp8b128_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv, int M, int I,
                         int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken);
 size_t ws_gemm_fp8b128(int M, int I, int O);
+int run_gemm_fp8ue8m0_general(float *Y, const uint16_t *X, const uint8_t *w, const uint8_t *scale_e8m0, int M,
+                              int I, int O, cudaStream_t st);
+int run_gemm_fp8ue8m0_tc(float *Y, const uint16_t *X, const uint8_t *w, const uint8_t *scale_e8m0, int M, int I,
+                         int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken);
+size_t ws_gemm_fp8ue8m0(int M, int I, int O);
 int run_gemm_mq4v2_general(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O,
                            cudaStream_t st);
 int run_gemm_mq4v2_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,
@@ -100,6 +105,7 @@ size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs) {
     switch (fmt) {
         case QG_FMT_I4G: return (gs >= 2 && !(gs & 1)) ? ws_i4g(S, I, O, gs) : 0;
         case QG_FMT_FP8B128: return ws_fp8b128(S, I, O);
+        case QG_FMT_FP8UE8M0: return ws_fp8ue8m0(S, I, O);
         case QG_FMT_MQ4V2: return (I % 256 == 0) ? ws_mq4v2(S, I, O) : 0;
         case QG_FMT_MQ4V1: return (I % 256 == 0) ? ws_mq4v1(S, I, O) : 0;
         case QG_FMT_MQ4C: return (I % 256 == 0) ? ws_mq4c(S, I, O) : 0;
@@ -112,6 +118,7 @@ size_t qg_gemm_workspace_bytes(int fmt, int M, int I, int O, int gs) {
     switch (fmt) {
         case QG_FMT_I4G: return (gs >= 2 && !(gs & 1)) ? ws_gemm_i4g(M, I, O, gs) : 0;
         case QG_FMT_FP8B128: return ws_gemm_fp8b128(M, I, O);
+        case QG_FMT_FP8UE8M0: return ws_gemm_fp8ue8m0(M, I, O);
         case QG_FMT_MQ4V2: return ws_gemm_mq4v2(M, I, O);
         case QG_FMT_MQ4V1: return ws_gemm_mq4v1(M, I, O);
         case QG_FMT_MQ4C: return ws_gemm_mq4c(M, I, O);
@@ -146,13 +153,25 @@ int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *sc
     return run_gemv_fp8b128(y, x, w, scale_inv, S, I, O, ws, ws_bytes, as_stream(stream));
 }
 
+int qgemv_fp8ue8m0(float *y, const uint16_t *x, const uint8_t *w, const uint8_t *scale_e8m0, int S, int I, int O,
+                   void *ws, size_t ws_bytes, qg_stream_t stream) {
+    const char *fn = "qgemv_fp8ue8m0";
+    int rc = check_dims(fn, "S", S, I, O);
+    if (rc) return rc;
+    if (!y || !x || !w || !scale_e8m0) QG_REFUSE(kEInval, "%s: y, x, w and scale_e8m0 must be non-NULL", fn);
+    if (!aligned(y, 4) || !aligned(x, 2)) QG_REFUSE(kEAlign, "%s: y must be 4-byte and x 2-byte aligned", fn);
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    cudaGetLastError();
+    return run_gemv_fp8ue8m0(y, x, w, scale_e8m0, S, I, O, ws, ws_bytes, as_stream(stream));
+}
+
 int qgemv_moe(int fmt, float *y, const void *x, size_t x_slot_stride, const qg_expert *experts, int n_experts,
               const int *ids, int n_slots, int S, int I, int O, int gs, qg_stream_t stream) {
     const char *fn = "qgemv_moe";
     int rc = check_dims(fn, "S", S, I, O);
     if (rc) return rc;
-    if (fmt != QG_FMT_I4G && fmt != QG_FMT_FP8B128 && fmt != QG_FMT_MQ4V2 && fmt != QG_FMT_MQ4V1 &&
-        fmt != QG_FMT_MQ4C)
+    if (fmt != QG_FMT_I4G && fmt != QG_FMT_FP8B128 && fmt != QG_FMT_FP8UE8M0 && fmt != QG_FMT_MQ4V2 &&
+        fmt != QG_FMT_MQ4V1 && fmt != QG_FMT_MQ4C)
         QG_REFUSE(kEInval, "%s: unknown format id %d", fn, fmt);
     if (fmt == QG_FMT_I4G && (rc = check_gs(fn, gs))) return rc;
     if ((fmt == QG_FMT_MQ4V2 || fmt == QG_FMT_MQ4V1 || fmt == QG_FMT_MQ4C) && I % 256)
@@ -178,6 +197,9 @@ int qgemv_moe(int fmt, float *y, const void *x, size_t x_slot_stride, const qg_e
         case QG_FMT_I4G:
             return run_gemv_moe_i4g(y, static_cast<const float *>(x), x_slot_stride, experts, n_experts, ids,
                                     n_slots, S, I, O, gs, st);
+        case QG_FMT_FP8UE8M0:
+            return run_gemv_moe_fp8ue8m0(y, static_cast<const uint16_t *>(x), x_slot_stride, experts, n_experts,
+                                         ids, n_slots, S, I, O, st);
         case QG_FMT_FP8B128:
             return run_gemv_moe_fp8b128(y, static_cast<const uint16_t *>(x), x_slot_stride, experts, n_experts,
                                         ids, n_slots, S, I, O, st);
@@ -284,6 +306,21 @@ int qgemm_fp8b128(float *Y, const uint16_t *X, const uint8_t *w, const float *sc
     rc = run_gemm_fp8b128_tc(Y, X, w, scale_inv, M, I, O, ws, ws_bytes, as_stream(stream), &taken);
     if (taken) return rc;
     return run_gemm_fp8b128_general(Y, X, w, scale_inv, M, I, O, as_stream(stream));
+}
+
+int qgemm_fp8ue8m0(float *Y, const uint16_t *X, const uint8_t *w, const uint8_t *scale_e8m0, int M, int I, int O,
+                   void *ws, size_t ws_bytes, qg_stream_t stream) {
+    const char *fn = "qgemm_fp8ue8m0";
+    int rc = check_dims(fn, "M", M, I, O);
+    if (rc) return rc;
+    if (!Y || !X || !w || !scale_e8m0) QG_REFUSE(kEInval, "%s: Y, X, w and scale_e8m0 must be non-NULL", fn);
+    if (!aligned(Y, 4) || !aligned(X, 2)) QG_REFUSE(kEAlign, "%s: Y must be 4-byte and X 2-byte aligned", fn);
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    cudaGetLastError();
+    bool taken = false;
+    rc = run_gemm_fp8ue8m0_tc(Y, X, w, scale_e8m0, M, I, O, ws, ws_bytes, as_stream(stream), &taken);
+    if (taken) return rc;
+    return run_gemm_fp8ue8m0_general(Y, X, w, scale_e8m0, M, I, O, as_stream(stream));
 }
 
 int qgemm_mq4v2(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O, void *ws,

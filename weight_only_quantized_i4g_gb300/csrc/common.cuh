@@ -43,6 +43,34 @@ __device__ __forceinline__ float ld_nc_f32(const float *p) {
     asm("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
     return v;
 }
+
+// UE8M0 (OCP MX E8M0): the byte e means 2^(e - 127), e = 0xFF is NaN.  Every
+// value is an f32 value: e in 1..254 is the normal 2^(e-127) (the bits e << 23),
+// e = 0 the subnormal 2^-127 (mantissa bit 22).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
+    return __uint_as_float(e == 0u ? 0x00400000u : e == 255u ? 0x7FC00000u : e << 23);
+}
+
+// fmt=7 block-scale encodings: the stored type, its value and the entry
+// points' names.  f32 is the encoding colibri PR #528 implements; UE8M0 (one
+// byte per block, a power-of-two exponent) the DeepSeek-V4 encoding the same
+// page names as the follow-up.
+struct ScaleF32 {
+    typedef float T;
+    static constexpr const char *kGemv = "qgemv_fp8b128";
+    static constexpr const char *kGemm = "qgemm_fp8b128";
+    static constexpr const char *kGemmTc = "qgemm_fp8b128 (tensor-core kernel)";
+    static constexpr const char *kGemmGeneral = "qgemm_fp8b128 (general kernel)";
+    __device__ static float get(const float *p, size_t i) { return ld_nc_f32(p + i); }
+};
+struct ScaleE8M0 {
+    typedef uint8_t T;
+    static constexpr const char *kGemv = "qgemv_fp8ue8m0";
+    static constexpr const char *kGemm = "qgemm_fp8ue8m0";
+    static constexpr const char *kGemmTc = "qgemm_fp8ue8m0 (tensor-core kernel)";
+    static constexpr const char *kGemmGeneral = "qgemm_fp8ue8m0 (general kernel)";
+    __device__ static float get(const uint8_t *p, size_t i) { return e8m0_to_f32(__ldg(p + i)); }
+};
 __device__ __forceinline__ uint32_t ld_nc_u32(const void *p) {
     uint32_t v;
     asm("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));

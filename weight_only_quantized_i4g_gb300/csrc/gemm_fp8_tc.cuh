@@ -1,6 +1,7 @@
-// gemm_fp8b128_tc.cu -- fmt=7 (FP8-e4m3, 128x128 block scales) batched-prefill
+// gemm_fp8_tc.cuh -- fmt=7 (FP8-e4m3, 128x128 block scales) batched-prefill
 // dequant-GEMM on the tensor cores: the format policy of the kernel in
-// gemm_tc.cuh.
+// gemm_tc.cuh, templated on the block-scale encoding SC (f32 or UE8M0;
+// instantiated by gemm_fp8b128_tc.cu and gemm_fp8ue8m0_tc.cu).
 //
 // colibri PR #528 "fmt=7: fp8-e4m3-b128 passthrough weight format", section
 // "Design": W[o, i] = e4m3(code) * scale_inv[o/128, i/128] (a multiply), and
@@ -12,11 +13,11 @@
 // One dequantizing thread takes 32 codes of its row per K step (two 16-byte
 // loads).  A 128-row tile lies inside one block row of scale_inv and a K
 // step inside one block column, so the thread needs one scale per step.
+#pragma once
 #include "gemm_tc.cuh"
 
 namespace qg {
 namespace tc {
-namespace {
 
 // Two e4m3 codes (the low and high byte of `two`) -> f16x2 of code * s,
 // low byte in the low half.
@@ -36,15 +37,20 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint16_t two, uint64_t s
     return r;
 }
 
-struct PolicyFp8B128 {
-    static constexpr const char *kName = "qgemm_fp8b128 (tensor-core kernel)";
+// Args::scales carries the block scales as SC::T (bytes for UE8M0).
+template <class SC>
+struct PolicyFp8 {
+    static constexpr const char *kName = SC::kGemmTc;
+    static __device__ __forceinline__ const typename SC::T *scales_of(const Args &a) {
+        return reinterpret_cast<const typename SC::T *>(a.scales);
+    }
     // Bound on |w| over row o, |e4m3| <= 448: 448 max_k |scale_inv[o/128, k]|
     // (the same for every row of a 128-row block).  Called by a whole warp.
     static __device__ __forceinline__ float row_bound(const Args &a, int o, int lane) {
-        const float *src = a.scales + (size_t)(o >> 7) * a.nbi;
+        const typename SC::T *src = scales_of(a) + (size_t)(o >> 7) * a.nbi;
         float b = 0.f;
 #pragma unroll 4
-        for (int k = lane; k < a.nbi; k += 32) b = fmaxf(b, fabsf(__ldg(src + k)));
+        for (int k = lane; k < a.nbi; k += 32) b = fmaxf(b, fabsf(SC::get(src, k)));
         return 448.f * warp_max(b);
     }
     struct Fetch {
@@ -53,12 +59,12 @@ struct PolicyFp8B128 {
     };
     struct Row {
         const uint8_t *w;
-        const float *s;
+        const typename SC::T *s;
     };
     static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int, Row &r) {
         const bool in = o < a.O;
         r.w = in ? a.w + (size_t)o * (size_t)a.rowbytes + kq * 32 : nullptr;
-        r.s = in ? a.scales + (size_t)(o >> 7) * a.nbi : nullptr;
+        r.s = in ? scales_of(a) + (size_t)(o >> 7) * a.nbi : nullptr;
     }
     static __device__ __forceinline__ void clear(Fetch &f) {
         f.q0 = make_uint4(0u, 0u, 0u, 0u);
@@ -70,7 +76,7 @@ struct PolicyFp8B128 {
             const uint8_t *p = r.w + (size_t)pk * kBK;
             f.q0 = ldg_w16(p);
             f.q1 = ldg_w16(p + 16);
-            f.s = __ldg(r.s + pk);
+            f.s = SC::get(r.s, pk);
         }
     }
     static __device__ __forceinline__ void dequant(const Fetch &f, float p2, uint32_t (&col)[16]) {
@@ -85,38 +91,38 @@ struct PolicyFp8B128 {
     }
 };
 
-}  // namespace
 }  // namespace tc
 
 // Shapes the tensor-core kernel takes: K in whole 64-steps (a last step of
 // 64), 16-byte aligned w (rows of I bytes then start on 16-byte boundaries)
 // and a TMA-aligned X.
-static bool gemm_fp8b128_tc_ok(const uint16_t *X, const uint8_t *w, int I) {
+inline bool gemm_fp8_tc_ok(const uint16_t *X, const uint8_t *w, int I) {
     return I % tc::kBKBox == 0 && (uintptr_t)X % 16 == 0 && (uintptr_t)w % 16 == 0;
 }
 
-size_t ws_gemm_fp8b128(int M, int I, int O) {
+inline size_t ws_gemm_fp8(int M, int I, int O) {
     if (I % tc::kBKBox != 0) return 0;
     return tc::choose_plan(M, I, O).ws_bytes;
 }
 
-int run_gemm_fp8b128_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv, int M, int I,
-                        int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken) {
+template <class SC>
+int run_gemm_fp8_tc(float *Y, const uint16_t *X, const uint8_t *w, const typename SC::T *scale_inv, int M, int I,
+                    int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken) {
     *taken = false;
-    if (!gemm_fp8b128_tc_ok(X, w, I)) return kOk;
+    if (!gemm_fp8_tc_ok(X, w, I)) return kOk;
     *taken = true;
     const tc::Plan p = tc::choose_plan(M, I, O);
     if (ws == nullptr || ws_bytes < p.ws_bytes) {
-        set_error_detail("qgemm_fp8b128: this shape needs a workspace of %zu bytes (got %zu)", p.ws_bytes,
+        set_error_detail("%s: this shape needs a workspace of %zu bytes (got %zu)", SC::kGemm, p.ws_bytes,
                          ws == nullptr ? (size_t)0 : ws_bytes);
         return kEWorkspace;
     }
     tc::Args args{};
     args.w = w;
-    args.scales = scale_inv;
+    args.scales = reinterpret_cast<const float *>(scale_inv);   // read back as SC::T by the policy
     args.nbi = (I + tc::kBK - 1) / tc::kBK;
     args.rowbytes = I;
-    return tc::launch_plan<tc::PolicyFp8B128>(p, Y, X, args, M, I, O, ws, st);
+    return tc::launch_plan<tc::PolicyFp8<SC>>(p, Y, X, args, M, I, O, ws, st);
 }
 
 }  // namespace qg

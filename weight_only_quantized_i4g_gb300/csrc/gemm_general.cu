@@ -34,14 +34,15 @@ struct WeightI4G {
     }
 };
 
-struct WeightFp8B128 {
+template <class SC>
+struct WeightFp8 {
     const uint8_t *w;
-    const float *scale_inv;
+    const typename SC::T *scale_inv;
     int I, nbi;
     __device__ float operator()(int o, int i) const {
         uint32_t h2;
         asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)w[(size_t)o * I + i]));
-        return f16_bits_to_f32((uint16_t)h2) * scale_inv[(size_t)(o >> 7) * nbi + (i >> 7)];
+        return f16_bits_to_f32((uint16_t)h2) * SC::get(scale_inv, (size_t)(o >> 7) * nbi + (i >> 7));
     }
 };
 
@@ -128,8 +129,14 @@ int run_gemm_i4g_general(float *Y, const uint16_t *X, const uint8_t *w, const fl
 
 int run_gemm_fp8b128_general(float *Y, const uint16_t *X, const uint8_t *w, const float *scale_inv, int M,
                              int I, int O, cudaStream_t st) {
-    const WeightFp8B128 wat{w, scale_inv, I, (I + 127) / 128};
-    return launch_general(Y, X, wat, M, I, O, st, "qgemm_fp8b128 (general kernel)");
+    const WeightFp8<ScaleF32> wat{w, scale_inv, I, (I + 127) / 128};
+    return launch_general(Y, X, wat, M, I, O, st, ScaleF32::kGemmGeneral);
+}
+
+int run_gemm_fp8ue8m0_general(float *Y, const uint16_t *X, const uint8_t *w, const uint8_t *scale_e8m0, int M,
+                              int I, int O, cudaStream_t st) {
+    const WeightFp8<ScaleE8M0> wat{w, scale_e8m0, I, (I + 127) / 128};
+    return launch_general(Y, X, wat, M, I, O, st, ScaleE8M0::kGemmGeneral);
 }
 
 int run_gemm_mq4v2_general(float *Y, const uint16_t *X, const uint8_t *blocks, int M, int I, int O,

@@ -1,8 +1,12 @@
-// gemv_fp8b128.cu -- fmt=7 FP8-e4m3 decode GEMV with 128x128 f32 block scales.
+// gemv_fp8.cuh -- fmt=7 FP8-e4m3 decode GEMV with 128x128 block scales,
+// templated on the scale encoding SC (instantiated by gemv_fp8b128.cu for f32
+// scales and gemv_fp8ue8m0.cu for UE8M0 scales).
 //
 // Format (colibri PR #528, "Design"): O*I raw OCP E4M3-FN codes, row-major;
-// scale_inv f32 [ceil(O/128), ceil(I/128)] in row-major block order;
-//     W[o,i] = e4m3(code) * scale_inv[o/128, i/128]   (multiply, not divide)
+// one scale per 128x128 block, [ceil(O/128), ceil(I/128)] in row-major block
+// order, either f32 (the encoding the page implements) or UE8M0 (the page's
+// DeepSeek-V4 encoding: one byte per block, a power-of-two exponent):
+//     W[o,i] = e4m3(code) * scale[o/128, i/128]   (multiply, not divide)
 // The only NaN codes are 0x7F and 0xFF; a NaN weight propagates to its row.
 //
 // Decode: the hardware e4m3x2 -> f16x2 conversion (exact for every code:
@@ -13,11 +17,13 @@
 //
 // Paths, fastest first: staged (gemv_tma.cuh; 16-byte aligned w and x,
 // I % 16 == 0), direct (gemv_cs.cuh; 16- or 8-byte global loads), general.
+#pragma once
 #include "gemv_cs.cuh"
 #include "gemv_tma.cuh"
 #include "launch.h"
 
 namespace qg {
+
 
 __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
     uint32_t h2;
@@ -28,13 +34,14 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two_codes) {
     return make_float2(a, b);
 }
 
-struct FmtFp8B128 {
+template <class SC>
+struct FmtFp8 {
     static constexpr int kElemsPerWord = 4;
     static constexpr int kPairsPerWord = 2;
     struct Params {
         const uint16_t *x;
         const uint8_t *w;
-        const float *scale_inv;
+        const typename SC::T *scale_inv;
         int I, O, nbi;
     };
     struct ThreadConst { int ib; };  // 128-column block of the thread's unit
@@ -47,7 +54,7 @@ struct FmtFp8B128 {
         return p.w + (size_t)o * p.I + (size_t)u * XU;
     }
     __device__ static Aux unit_aux(const Params &p, int o, int, ThreadConst tc) {
-        return ld_nc_f32(p.scale_inv + (size_t)(o >> 7) * p.nbi + tc.ib);
+        return SC::get(p.scale_inv, (size_t)(o >> 7) * p.nbi + tc.ib);
     }
     __device__ static Aux zero_aux() { return 0.f; }
 
@@ -83,13 +90,14 @@ struct FmtFp8B128 {
     struct TConst { uint32_t uoff; int ib; };   // unit byte offset, 128-column block
     struct StageConst { float sc; };            // the batch's block scale for that column block
     // routed experts: 16-byte aligned codes for the staged copies; the block
-    // scales are read as f32 from global memory
+    // scales are read one at a time from global memory
     __device__ static bool expert_ok(const Params &, const void *w, const float *scales) {
-        return w != nullptr && scales != nullptr && ((uintptr_t)w % 16 == 0) && ((uintptr_t)scales % 4 == 0);
+        return w != nullptr && scales != nullptr && ((uintptr_t)w % 16 == 0) &&
+               ((uintptr_t)scales % alignof(typename SC::T) == 0);
     }
     __device__ static Params with_expert(Params p, const void *w, const float *scales, size_t x_off) {
         p.w = static_cast<const uint8_t *>(w);
-        p.scale_inv = scales;
+        p.scale_inv = reinterpret_cast<const typename SC::T *>(scales);
         p.x += x_off;
         return p;
     }
@@ -106,7 +114,7 @@ struct FmtFp8B128 {
     }
     // rows of a batch share one 128-row block (the batch size divides 128)
     __device__ static StageConst stage_const(const Params &p, int o0, TConst tc) {
-        return StageConst{o0 < p.O ? ld_nc_f32(p.scale_inv + (size_t)(o0 >> 7) * p.nbi + tc.ib) : 0.f};
+        return StageConst{o0 < p.O ? SC::get(p.scale_inv, (size_t)(o0 >> 7) * p.nbi + tc.ib) : 0.f};
     }
     template <int NW>
     __device__ static Words<NW> lds_unit(uint32_t a) { return lds_at<NW, true>(a); }
@@ -158,10 +166,10 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
     return e4m3x2_to_f32x2((uint32_t)c).x;
 }
 
-template <int S>
+template <class SC, int S>
 __global__ void __launch_bounds__(256)
 gemv_fp8_general_kernel(float *__restrict__ y, const uint16_t *__restrict__ x, const uint8_t *__restrict__ w,
-                        const float *__restrict__ scale_inv, int I, int O) {
+                        const typename SC::T *__restrict__ scale_inv, int I, int O) {
     const int lane = threadIdx.x & 31;
     const int nbi = (I + 127) / 128;
     for (int o = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); o < O;
@@ -170,9 +178,9 @@ gemv_fp8_general_kernel(float *__restrict__ y, const uint16_t *__restrict__ x, c
 #pragma unroll
         for (int s = 0; s < S; ++s) acc[s] = 0.f;
         const uint8_t *wr = w + (size_t)o * I;
-        const float *sr = scale_inv + (size_t)(o >> 7) * nbi;
+        const size_t sb = (size_t)(o >> 7) * nbi;
         for (int i = lane; i < I; i += 32) {
-            const float wv = e4m3_to_f32(wr[i]) * sr[i >> 7];
+            const float wv = e4m3_to_f32(wr[i]) * SC::get(scale_inv, sb + (i >> 7));
 #pragma unroll
             for (int s = 0; s < S; ++s) acc[s] = fmaf(wv, bf16_bits_to_f32(x[(size_t)s * I + i]), acc[s]);
         }
@@ -187,22 +195,22 @@ gemv_fp8_general_kernel(float *__restrict__ y, const uint16_t *__restrict__ x, c
 // ---------------------------------------------------------------------------
 // dispatch
 // ---------------------------------------------------------------------------
-namespace {
+namespace fp8 {
 
-int fp8_nw(int S) { return S <= 4 ? 4 : 2; }       // activation registers 4*NW*S <= 64
-int fp8_rb(int S, int U) { return S <= 2 ? (U == 1 ? 8 : 4) : 4; }
+inline int fp8_nw(int S) { return S <= 4 ? 4 : 2; }       // activation registers 4*NW*S <= 64
+inline int fp8_rb(int S, int U) { return S <= 2 ? (U == 1 ? 8 : 4) : 4; }
 
-bool fp8_fast_ok(const uint16_t *x, const uint8_t *w, int I, int S) {
+inline bool fp8_fast_ok(const uint16_t *x, const uint8_t *w, int I, int S) {
     const int nw = fp8_nw(S);
     return (I % (4 * nw) == 0) && ((uintptr_t)w % (4 * nw) == 0) && ((uintptr_t)x % 2 == 0);
 }
 
 
-bool fp8_tma_ok(const uint16_t *x, const uint8_t *w, int I, int S) {
+inline bool fp8_tma_ok(const uint16_t *x, const uint8_t *w, int I, int S) {
     return fp8_fast_ok(x, w, I, S) && (I % 16 == 0) && ((uintptr_t)w % 16 == 0) && ((uintptr_t)x % 16 == 0);
 }
 
-bool fp8_tma_plan(int S, int I, int O, TmaPlan *pl) {
+inline bool fp8_tma_plan(int S, int I, int O, TmaPlan *pl) {
     const int nw = fp8_nw(S);
     TmaGeom g;
     g.units = I / (4 * nw);
@@ -213,7 +221,7 @@ bool fp8_tma_plan(int S, int I, int O, TmaPlan *pl) {
     return tma_plan_rows(g, S, O, S == 1 ? 3 : 1, pl);
 }
 
-CsPlan fp8_plan(int S, int I, int O, int *U_out) {
+inline CsPlan fp8_plan(int S, int I, int O, int *U_out) {
     const int nw = fp8_nw(S);
     const int units = I / (4 * nw);
     // up to three units per thread at S = 1 (at S > 1 more than one spills
@@ -224,86 +232,87 @@ CsPlan fp8_plan(int S, int I, int O, int *U_out) {
     return cs_plan(units, O, U, fp8_rb(S, U), regs);
 }
 
-template <int S, int NW, int U>
-void launch_cs_fp8(const FmtFp8B128::Params &p, float *out, const CsPlan &pl, int units, cudaStream_t st) {
+template <class SC, int S, int NW, int U>
+void launch_cs_fp8(const typename FmtFp8<SC>::Params &p, float *out, const CsPlan &pl, int units, cudaStream_t st) {
     constexpr int RB = S <= 2 ? (U == 1 ? 8 : 4) : 4;
     dim3 grid(pl.grid_x, pl.splits);
-    gemv_cs_kernel<FmtFp8B128, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
+    gemv_cs_kernel<FmtFp8<SC>, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
                                                                          pl.nrowb);
 }
 
-template <int S>
-void launch_cs_fp8_s(const FmtFp8B128::Params &p, float *out, const CsPlan &pl, int units, int U,
+template <class SC, int S>
+void launch_cs_fp8_s(const typename FmtFp8<SC>::Params &p, float *out, const CsPlan &pl, int units, int U,
                      cudaStream_t st) {
     constexpr int NW = S <= 4 ? 4 : 2;
     if constexpr (S == 1) {
         if (U == 2) {
-            launch_cs_fp8<S, NW, 2>(p, out, pl, units, st);
+            launch_cs_fp8<SC, S, NW, 2>(p, out, pl, units, st);
             return;
         }
         if (U == 3) {
-            launch_cs_fp8<S, NW, 3>(p, out, pl, units, st);
+            launch_cs_fp8<SC, S, NW, 3>(p, out, pl, units, st);
             return;
         }
     }
     (void)U;
-    launch_cs_fp8<S, NW, 1>(p, out, pl, units, st);
+    launch_cs_fp8<SC, S, NW, 1>(p, out, pl, units, st);
 }
 
-template <int S, int RB>
-void launch_tma_fp8_u(const FmtFp8B128::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
+template <class SC, int S, int RB>
+void launch_tma_fp8_u(const typename FmtFp8<SC>::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
                       const MoeLaunch *moe = nullptr) {
     constexpr int NW = S <= 4 ? 4 : 2;
     if constexpr (S == 1) {
         if (pl.U == 2) {
-            launch_tma<FmtFp8B128, S, NW, 2, RB>(p, out, pl, st, moe);
+            launch_tma<FmtFp8<SC>, S, NW, 2, RB>(p, out, pl, st, moe);
             return;
         }
         if (pl.U == 3) {
-            launch_tma<FmtFp8B128, S, NW, 3, RB>(p, out, pl, st, moe);
+            launch_tma<FmtFp8<SC>, S, NW, 3, RB>(p, out, pl, st, moe);
             return;
         }
     }
-    launch_tma<FmtFp8B128, S, NW, 1, RB>(p, out, pl, st, moe);
+    launch_tma<FmtFp8<SC>, S, NW, 1, RB>(p, out, pl, st, moe);
 }
 
-template <int S>
-void launch_tma_fp8_s(const FmtFp8B128::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
+template <class SC, int S>
+void launch_tma_fp8_s(const typename FmtFp8<SC>::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
                       const MoeLaunch *moe = nullptr) {
     if constexpr (S <= 2) {
         if (pl.rb == 8) {
-            launch_tma_fp8_u<S, 8>(p, out, pl, st, moe);
+            launch_tma_fp8_u<SC, S, 8>(p, out, pl, st, moe);
             return;
         }
     }
     if (pl.rb == 2) {
-        launch_tma<FmtFp8B128, S, (S <= 4 ? 4 : 2), 1, 2>(p, out, pl, st, moe);
+        launch_tma<FmtFp8<SC>, S, (S <= 4 ? 4 : 2), 1, 2>(p, out, pl, st, moe);
         return;
     }
-    launch_tma_fp8_u<S, 4>(p, out, pl, st, moe);
+    launch_tma_fp8_u<SC, S, 4>(p, out, pl, st, moe);
 }
 
-int gemv_fp8_chunk(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S, int I,
-                   int O, void *ws, size_t ws_bytes, cudaStream_t st) {
-    FmtFp8B128::Params p;
+template <class SC>
+int gemv_fp8_chunk(float *y, const uint16_t *x, const uint8_t *w, const typename SC::T *scale_inv, int S, int I,
+                   int O, void *ws, size_t ws_bytes, cudaStream_t st, const char *name) {
+    typename FmtFp8<SC>::Params p;
     p.x = x; p.w = w; p.scale_inv = scale_inv; p.I = I; p.O = O; p.nbi = (I + 127) / 128;
 
     TmaPlan tp;
     if (fp8_tma_ok(x, w, I, S) && fp8_tma_plan(S, I, O, &tp)) {
         const size_t need = tp.splits > 1 ? (size_t)tp.splits * S * O * sizeof(float) : 0;
         if (need > 0 && (ws == nullptr || ws_bytes < need)) {
-            set_error_detail("qgemv_fp8b128: this shape splits the reduction and needs %zu bytes of "
-                             "workspace (got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
+            set_error_detail("%s: this shape splits the reduction and needs %zu bytes of "
+                             "workspace (got %zu)", name, need, ws == nullptr ? (size_t)0 : ws_bytes);
             return kEWorkspace;
         }
         float *out = tp.splits > 1 ? static_cast<float *>(ws) : y;
         switch (S) {
-#define QG_CASE(SS) case SS: launch_tma_fp8_s<SS>(p, out, tp, st); break;
+#define QG_CASE(SS) case SS: launch_tma_fp8_s<SC, SS>(p, out, tp, st); break;
             QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
 #undef QG_CASE
         }
         if (tp.splits > 1) launch_splitk_reduce(y, static_cast<float *>(ws), tp.splits, S, O, st);
-        return check_launch("qgemv_fp8b128");
+        return check_launch(name);
     }
 
     if (!fp8_fast_ok(x, w, I, S)) {
@@ -311,34 +320,35 @@ int gemv_fp8_chunk(float *y, const uint16_t *x, const uint8_t *w, const float *s
         const int cap = num_sms() * 16;
         const int grid = blocks_needed < cap ? blocks_needed : cap;
         switch (S) {
-#define QG_CASE(SS) case SS: gemv_fp8_general_kernel<SS><<<grid, 256, 0, st>>>(y, x, w, scale_inv, I, O); break;
+#define QG_CASE(SS) case SS: gemv_fp8_general_kernel<SC, SS><<<grid, 256, 0, st>>>(y, x, w, scale_inv, I, O); break;
             QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
 #undef QG_CASE
         }
-        return check_launch("qgemv_fp8b128 (general kernel)");
+        return check_launch(name);
     }
     int U = 1;
     const CsPlan pl = fp8_plan(S, I, O, &U);
     const int units = I / (4 * fp8_nw(S));
     const size_t need = cs_ws_bytes(pl, S, O);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) {
-        set_error_detail("qgemv_fp8b128: this shape splits the reduction and needs %zu bytes of "
-                         "workspace (got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
+        set_error_detail("%s: this shape splits the reduction and needs %zu bytes of "
+                         "workspace (got %zu)", name, need, ws == nullptr ? (size_t)0 : ws_bytes);
         return kEWorkspace;
     }
     float *out = pl.splits > 1 ? static_cast<float *>(ws) : y;
     switch (S) {
-#define QG_CASE(SS) case SS: launch_cs_fp8_s<SS>(p, out, pl, units, U, st); break;
+#define QG_CASE(SS) case SS: launch_cs_fp8_s<SC, SS>(p, out, pl, units, U, st); break;
         QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
 #undef QG_CASE
     }
     if (pl.splits > 1) launch_splitk_reduce(y, static_cast<float *>(ws), pl.splits, S, O, st);
-    return check_launch("qgemv_fp8b128");
+    return check_launch(name);
 }
 
-}  // namespace
+}  // namespace fp8
+using namespace fp8;
 
-size_t ws_fp8b128(int S, int I, int O) {
+inline size_t ws_fp8(int S, int I, int O) {
     const int s = S < 8 ? S : 8;
     if (I % (4 * fp8_nw(s)) != 0) return 0;
     // the larger of the staged and the direct plan (the pointers decide the path)
@@ -350,12 +360,13 @@ size_t ws_fp8b128(int S, int I, int O) {
     return need > cs ? need : cs;
 }
 
-int run_gemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S, int I,
-                     int O, void *ws, size_t ws_bytes, cudaStream_t st) {
+template <class SC>
+int run_gemv_fp8(float *y, const uint16_t *x, const uint8_t *w, const typename SC::T *scale_inv, int S, int I,
+                 int O, void *ws, size_t ws_bytes, cudaStream_t st, const char *name) {
     for (int s0 = 0; s0 < S; s0 += 8) {
         const int sc = S - s0 < 8 ? S - s0 : 8;
-        const int rc = gemv_fp8_chunk(y + (size_t)s0 * O, x + (size_t)s0 * I, w, scale_inv, sc, I, O, ws,
-                                      ws_bytes, st);
+        const int rc = gemv_fp8_chunk<SC>(y + (size_t)s0 * O, x + (size_t)s0 * I, w, scale_inv, sc, I, O, ws,
+                                          ws_bytes, st, name);
         if (rc != kOk) return rc;
     }
     return kOk;
@@ -363,7 +374,8 @@ int run_gemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float 
 
 
 // Routed experts (fmt=7): every slot on the staged kernel, one launch.
-int run_gemv_moe_fp8b128(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
+template <class SC>
+int run_gemv_moe_fp8(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
                          const int *ids, int n_slots, int S, int I, int O, cudaStream_t st) {
     const uint8_t *probe = reinterpret_cast<const uint8_t *>(uintptr_t(256));   // stands for any 16-byte aligned expert
     TmaPlan tp;
@@ -372,12 +384,12 @@ int run_gemv_moe_fp8b128(float *y, const uint16_t *x, size_t x_stride, const voi
                          "short enough for one block (I = %d)", I);
         return kEShape;
     }
-    FmtFp8B128::Params p;
+    typename FmtFp8<SC>::Params p;
     p.x = x; p.w = nullptr; p.scale_inv = nullptr; p.I = I; p.O = O; p.nbi = (I + 127) / 128;
     tp.nrowb = (O + tp.rb - 1) / tp.rb;            // the plan sized the launch for all slots' rows
     const MoeLaunch m{MoeSlots{static_cast<const ExpertW *>(table), ids, n_experts, x_stride}, n_slots};
     switch (S) {
-#define QG_CASE(SS) case SS: launch_tma_fp8_s<SS>(p, y, tp, st, &m); break;
+#define QG_CASE(SS) case SS: launch_tma_fp8_s<SC, SS>(p, y, tp, st, &m); break;
         QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
 #undef QG_CASE
     }

@@ -22,6 +22,7 @@ int read_device_error(int *status);
 
 size_t ws_i4g(int S, int I, int O, int gs);
 size_t ws_fp8b128(int S, int I, int O);
+size_t ws_fp8ue8m0(int S, int I, int O);
 size_t ws_mq4v2(int S, int I, int O);
 size_t ws_mq4v1(int S, int I, int O);
 size_t ws_mq4c(int S, int I, int O);
@@ -30,6 +31,8 @@ int run_gemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales
                  int gs, void *ws, size_t ws_bytes, cudaStream_t st);
 int run_gemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *scale_inv, int S,
                      int I, int O, void *ws, size_t ws_bytes, cudaStream_t st);
+int run_gemv_fp8ue8m0(float *y, const uint16_t *x, const uint8_t *w, const uint8_t *scale_e8m0, int S,
+                      int I, int O, void *ws, size_t ws_bytes, cudaStream_t st);
 int run_gemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
                    size_t ws_bytes, cudaStream_t st);
 int run_gemv_mq4v1(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
@@ -45,6 +48,8 @@ int run_gemv_moe_i4g(float *y, const float *x, size_t x_stride, const void *tabl
                      const int *ids, int n_slots, int S, int I, int O, int gs, cudaStream_t st);
 int run_gemv_moe_fp8b128(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
                          const int *ids, int n_slots, int S, int I, int O, cudaStream_t st);
+int run_gemv_moe_fp8ue8m0(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
+                          const int *ids, int n_slots, int S, int I, int O, cudaStream_t st);
 int run_gemv_moe_mq4v2(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
                        const int *ids, int n_slots, int S, int I, int O, cudaStream_t st);
 int run_gemv_moe_mq4v1(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
