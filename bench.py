@@ -65,6 +65,8 @@ def weight_bytes(fmt, O, I):
         return O * ((I + 1) // 2) + O * ((I + GS - 1) // GS) * 4
     if fmt == "fp8":
         return O * I + ((O + 127) // 128) * ((I + 127) // 128) * 4
+    if fmt == "fp8ue8m0":
+        return O * I + ((O + 127) // 128) * ((I + 127) // 128)
     return O * (I // 256) * 136
 
 
@@ -89,7 +91,7 @@ def load_tensor_peak():
 
 # Sources of the dominant kernel (the staged fmt=7 GEMV); the committed DRAM
 # traffic figure is valid only for the build these hash to.
-DOMINANT_SOURCES = ("gemv_tma.cuh", "gemv_fp8b128.cu", "common.cuh", "pipeline.cuh")
+DOMINANT_SOURCES = ("gemv_tma.cuh", "gemv_fp8.cuh", "gemv_fp8b128.cu", "common.cuh", "pipeline.cuh")
 
 
 def source_hash():
@@ -467,9 +469,10 @@ def ours_arm(args):
                        "l2": "inputs larger than L2: 404 MB of weights per step (L2 129 MB), "
                              "every call streams from HBM",
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": DOMINANT, "achieved": round(achieved, 2),
+            "roofline": {"bound": "hbm", "kernel": calls[dom]["name"], "achieved": round(achieved, 2),
                          "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-                         "traffic": load_traffic(), "algorithmic_bytes": dom_bytes,
+                         "traffic": load_traffic() if calls[dom]["name"] == DOMINANT else None,
+                         "algorithmic_bytes": dom_bytes,
                          "avg_launch_us": round(dom_ms * 1e3, 3),
                          "launches_sampled": len(dom_events),
                          "peak_kind": f"{peak_kind} (copy bandwidth)"},
@@ -512,7 +515,8 @@ def _time_alone(fn, flush, stream, reps, torch):
 def _prefill_inputs(qg, torch, dev, stream, fmt, O, I, M):
     """Seeded device inputs of one prefill GEMM shape: the decode workloads'
     weight recipes (fmt=4 quantized N(0, 0.02); fmt=7 uniform e4m3 codes
-    without the NaN codes and log-uniform [1e-4, 1e-2] block scales; the MQ4
+    without the NaN codes and log-uniform [1e-4, 1e-2] block scales (UE8M0:
+    exponent bytes uniform in 113..120, the same range in powers of two); the MQ4
     formats (V2, v1, pad) N(0, 0.02) rotated by the seeded sign-FWHT and
     encoded) and bf16 N(0, 1) activations (rotated for MQ4).  Returns the
     weights and X."""
@@ -525,12 +529,15 @@ def _prefill_inputs(qg, torch, dev, stream, fmt, O, I, M):
         qg.check(qg.qg_quantize_i4g(wq, sc, w, O, I, GS, stream=stream))
         del w
         weights = (wq, sc)
-    elif fmt == "fp8":
+    elif fmt in ("fp8", "fp8ue8m0"):
         codes = torch.randint(0, 254, (O * I,), generator=g, device=dev, dtype=torch.int32)
         codes = (codes + (codes >= 0x7F).to(torch.int32)).to(torch.uint8)   # skip 0x7F; 0xFF unreachable
         nbo, nbi = -(-O // 128), -(-I // 128)
-        u = torch.rand(nbo * nbi, generator=g, device=dev, dtype=torch.float64)
-        sc = torch.exp(math.log(1e-4) + u * (math.log(1e-2) - math.log(1e-4))).to(torch.float32)
+        if fmt == "fp8":
+            u = torch.rand(nbo * nbi, generator=g, device=dev, dtype=torch.float64)
+            sc = torch.exp(math.log(1e-4) + u * (math.log(1e-2) - math.log(1e-4))).to(torch.float32)
+        else:                                   # UE8M0 bytes 113..120: 2^-14..2^-7
+            sc = torch.randint(113, 121, (nbo * nbi,), generator=g, device=dev, dtype=torch.int32).to(torch.uint8)
         weights = (codes, sc)
     else:
         signs = (torch.randint(0, 2, (256,), generator=g, device=dev, dtype=torch.int32) * 2 - 1).to(torch.int8)
@@ -548,9 +555,10 @@ def _prefill_inputs(qg, torch, dev, stream, fmt, O, I, M):
     return weights, X
 
 
-PREFILL_OTHER = (("fp8", 7168, 16384), ("fp8", 24576, 7168), ("mq4", 5120, 17408), ("mq4", 17408, 5120),
-                 ("mq4v1", 5120, 17408), ("mq4v1", 17408, 5120), ("mq4c", 5120, 17408), ("mq4c", 17408, 5120))
-FMT_ID = {"i4g": 4, "fp8": 7, "mq4": 44, "mq4v1": 13, "mq4c": 45}
+PREFILL_OTHER = (("fp8", 7168, 16384), ("fp8", 24576, 7168), ("fp8ue8m0", 7168, 16384), ("fp8ue8m0", 24576, 7168),
+                 ("mq4", 5120, 17408), ("mq4", 17408, 5120), ("mq4v1", 5120, 17408), ("mq4v1", 17408, 5120),
+                 ("mq4c", 5120, 17408), ("mq4c", 17408, 5120))
+FMT_ID = {"i4g": 4, "fp8": 7, "fp8ue8m0": 71, "mq4": 44, "mq4v1": 13, "mq4c": 45}
 # MQ4 block formats: V2 (a header per 128-weight half), v1 (one f32 header),
 # pad (one fp16 header and four zero bytes); 136 bytes per 256 weights each
 MQ4_ENCODE = {"mq4": lambda qg: qg.qg_encode_mq4v2, "mq4v1": lambda qg: qg.qg_encode_mq4v1,
@@ -588,6 +596,8 @@ def prefill_measure(qg, torch, dev, stream, reps=20, other=True, shapes=None):
             fn = lambda: qg.check(qg.qgemm_i4g(Y, X, weights[0], weights[1], M, I, O, GS, ws, n, stream=stream))
         elif fmt == "fp8":
             fn = lambda: qg.check(qg.qgemm_fp8b128(Y, X, weights[0], weights[1], M, I, O, ws, n, stream=stream))
+        elif fmt == "fp8ue8m0":
+            fn = lambda: qg.check(qg.qgemm_fp8ue8m0(Y, X, weights[0], weights[1], M, I, O, ws, n, stream=stream))
         else:
             gemm = getattr(qg, MQ4_GEMM[fmt])
             fn = lambda: qg.check(gemm(Y, X, weights[0], M, I, O, ws, n, stream=stream))
@@ -684,14 +694,17 @@ def _graph_per_call(torch, stream, reps, issue):
     return best
 
 
-ONE_HEADER = (("mq4v1", 5120, 17408), ("mq4v1", 17408, 5120), ("mq4c", 5120, 17408), ("mq4c", 17408, 5120))
+ONE_HEADER = (("mq4v1", 5120, 17408), ("mq4v1", 17408, 5120), ("mq4c", 5120, 17408), ("mq4c", 17408, 5120),
+              ("fp8ue8m0", 7168, 16384), ("fp8ue8m0", 24576, 7168))
 
 
 def one_header_breakdown(qg, torch, stream, hbm_peak, dev):
-    """Kernel-only batch-1 GEMV time of the one-header MQ4 block formats (v1:
-    f32 scale and zero per 256 weights; pad: fp16 pair and four zero bytes)
-    on the MQ4-V2 decode shapes, same weight recipe and timing scheme as
-    per_format_breakdown (graph of calls over >= 3x L2 of weight copies)."""
+    """Kernel-only batch-1 GEMV time of the format variants: the one-header
+    MQ4 block formats (v1: f32 scale and zero per 256 weights; pad: fp16 pair
+    and four zero bytes) on the MQ4-V2 decode shapes and fmt=7 with UE8M0
+    block scales on the fmt=7 decode shapes; same weight recipes and timing
+    scheme as per_format_breakdown (graph of calls over >= 3x L2 of weight
+    copies)."""
     out = {}
     l2 = 129 * 2 ** 20
     lib = qg._lib
@@ -701,13 +714,16 @@ def one_header_breakdown(qg, torch, stream, hbm_peak, dev):
             weights, X = _prefill_inputs(qg, torch, dev, stream, fmt, O, I, 1)
             y = torch.empty(O, dtype=torch.float32, device=dev)
             assert qg.qg_workspace_bytes(FMT_ID[fmt], 1, I, O, 0) == 0
-            nbytes = weight_bytes("mq4", O, I)
+            nbytes = weight_bytes(fmt if fmt == "fp8ue8m0" else "mq4", O, I)
             copies = min(64, max(1, -(-3 * l2 // nbytes)))
             wcopies = [weights[0]] + [weights[0].clone() for _ in range(copies - 1)]
-            gemv = getattr(lib, MQ4_GEMV[fmt])
 
             def issue(r):
-                rc = gemv(y.data_ptr(), X.data_ptr(), wcopies[r % copies].data_ptr(), 1, I, O, None, 0, st)
+                wp = wcopies[r % copies].data_ptr()
+                if fmt == "fp8ue8m0":
+                    rc = lib.qgemv_fp8ue8m0(y.data_ptr(), X.data_ptr(), wp, weights[1].data_ptr(), 1, I, O, None, 0, st)
+                else:
+                    rc = getattr(lib, MQ4_GEMV[fmt])(y.data_ptr(), X.data_ptr(), wp, 1, I, O, None, 0, st)
                 if rc:
                     raise qg.QGError(rc)
             best = _graph_per_call(torch, stream, max(copies, 60), issue)
@@ -885,7 +901,7 @@ def main():
     ap.add_argument("--only", default="", help="comma-separated subset of the shapes (profiling runs)")
     ap.add_argument("--prefill-only", default="",
                     help="profiling runs: time only these prefill GEMMs (comma-separated fmt:O:I, fmt in "
-                         "i4g/fp8/mq4/mq4v1/mq4c, M=512) and print their prefill object")
+                         "i4g/fp8/fp8ue8m0/mq4/mq4v1/mq4c, M=512) and print their prefill object")
     ap.add_argument("--prefill-reps", type=int, default=20)
     ap.add_argument("--moe-only", action="store_true", help="profiling runs: print only the routed-expert lines")
     args = ap.parse_args()
