@@ -146,9 +146,10 @@ CsPlan cs_plan(int units, int O, int u, int rb, int regs_per_thread) {
 bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan *pl, int max_per_sm,
               int one_block_slots) {
     int U = 1, splits = 1;
-    int max_thr = tma_max_consumer_warps(S, 1) * 32;
+    // unit slots per block: consumer threads / token groups
+    int max_thr = tma_max_consumer_warps(S, 1) * 32 / g.tg;
     if (g.units > max_thr) {
-        max_thr = tma_max_consumer_warps(S, 2) * 32;
+        max_thr = tma_max_consumer_warps(S, 2) * 32 / g.tg;
         if (g.units <= max_thr * U_max) {
             U = cdiv(g.units, max_thr);
         } else {
@@ -164,7 +165,7 @@ bool tma_plan(const TmaGeom &g, int S, int O, int RB, int NV, int U_max, TmaPlan
     if (cdiv(ups, U) > max_thr) return false;
     const uint32_t seg = splits == 1 ? g.rowbytes : (uint32_t)(ups / g.granule) * g.granule_bytes;
     if (seg % 16 != 0 || g.rowbytes % 16 != 0 || g.arowbytes % 4 != 0) return false;
-    const int nc = cdiv(cdiv(ups, U), 32);
+    const int nc = cdiv(cdiv(ups, U) * g.tg, 32);
     const uint32_t stage_w = (uint32_t)round_up((int)(RB * seg), 128);
     const uint32_t stage_a = (uint32_t)round_up((int)(RB * g.arowbytes), 128);
     const uint32_t red_stage = (uint32_t)(nc * NV * 4);

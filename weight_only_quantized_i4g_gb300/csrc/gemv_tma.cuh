@@ -250,7 +250,12 @@ struct TmaLayout {
     uint32_t total;      // dynamic shared memory bytes
 };
 
-template <class F, int S, int NW, int U, int RB>
+// TG > 1 (token split): the consumer threads of a unit form TG groups (lanes
+// with equal lane % TG), each holding the activations of ST = ceil(S / TG)
+// tokens only; the groups' partial sums are reduced across the lanes of the
+// same group.  Used where S tokens of activations per thread would not fit
+// in registers.
+template <class F, int S, int NW, int U, int RB, int TG = 1>
 __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float *__restrict__ out, int units,
                                               int units_per_split, int nrowb, int nst, const TmaLayout &L,
                                               int *err)
@@ -258,7 +263,10 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
     constexpr int XU = NW * F::kElemsPerWord;
     constexpr int NP = NW * F::kPairsPerWord;
     constexpr int NV = NextPow2<RB * S>::value;
+    constexpr int ST = (S + TG - 1) / TG;             // tokens per consumer thread
+    constexpr int NT = TG == 1 ? NV : RB * ST;        // partial sums per consumer thread
     static_assert(RB * S <= 32, "RB * S must be <= 32");
+    static_assert(TG == 1 || TG == 2 || TG == 4, "token groups must divide a warp evenly");
 
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -341,21 +349,26 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
     griddep_wait();   // x may be the previous kernel's output
     const int cw = warp - 1;
     const int ct = tid - 32;
-    const int ncth = nc * 32;
+    const int tg = TG == 1 ? 0 : ct % TG;             // token group (lane % TG)
+    const int nuth = nc * 32 / TG;                    // unit slots per block
     int uidx[U];
     bool uok[U];
     typename F::TConst tc[U];   // a thread past the last unit takes unit ubeg (zero activations)
-    uint64_t xp[U][S][NP];
-    float xsum[U][S];
+    uint64_t xp[U][ST][NP];
+    float xsum[U][ST];
 #pragma unroll
     for (int j = 0; j < U; ++j) {
-        uidx[j] = ubeg + ct + j * ncth;
+        uidx[j] = ubeg + (TG == 1 ? ct : ct / TG) + j * nuth;
         uok[j] = uidx[j] < uend;
         tc[j] = F::tconst(p, uok[j] ? uidx[j] : ubeg, XU, seg_col);
 #pragma unroll
-        for (int s = 0; s < S; ++s) F::template load_x<XU, NP>(p, s, uok[j] ? uidx[j] : -1, xp[j][s], xsum[j][s]);
+        for (int s = 0; s < ST; ++s) {
+            const int tok = tg * ST + s;              // a padding token (tok >= S) reads zeros
+            F::template load_x<XU, NP>(p, tok < S ? tok : 0, (uok[j] && tok < S) ? uidx[j] : -1, xp[j][s],
+                                       xsum[j][s]);
+        }
     }
-    const typename F::ThreadScale ts = F::template prepare_x<U, S, NP>(xp, xsum);
+    const typename F::ThreadScale ts = F::template prepare_x<U, ST, NP>(xp, xsum);
     typename F::StageConst scur[U], snext[U];
 #pragma unroll
     for (int j = 0; j < U; ++j) scur[j] = F::stage_const(p, b * RB, tc[j]);
@@ -371,9 +384,9 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
         }
         const uint32_t swb = sw0 + (uint32_t)slot * L.stage_w;
         const uint32_t sab = sa0 + (uint32_t)slot * L.stage_a;
-        float part[NV];
+        float part[NT];
 #pragma unroll
-        for (int v = 0; v < NV; ++v) part[v] = 0.f;
+        for (int v = 0; v < NT; ++v) part[v] = 0.f;
         // Rows in sub-batches of RS: the sub-batch's shared-memory reads first,
         // then its arithmetic.  No predicates: a thread without a unit of its
         // own reads unit ubeg of the same row with zero activations (adds 0),
@@ -398,12 +411,29 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
             for (int rr = 0; rr < RS; ++rr)
 #pragma unroll
                 for (int j = 0; j < U; ++j)
-                    F::template accumulate<S, NW, NP>(wd[rr][j], ax[rr][j], xp[j], xsum[j], ts,
-                                                      &part[(r0 + rr) * S]);
+                    F::template accumulate<ST, NW, NP>(wd[rr][j], ax[rr][j], xp[j], xsum[j], ts,
+                                                       &part[(r0 + rr) * ST]);
         }
-        const float tot = warp_reduce_scatter<NV>(part, lane);
-        if ((lane & ((32 / NV) - 1)) == 0)
-            red[((size_t)slot * nc + cw) * NV + reduce_scatter_index<NV>(lane)] = tot;
+        if constexpr (TG == 1) {
+            const float tot = warp_reduce_scatter<NV>(part, lane);
+            if ((lane & ((32 / NV) - 1)) == 0)
+                red[((size_t)slot * nc + cw) * NV + reduce_scatter_index<NV>(lane)] = tot;
+        } else {
+            // sum over the lanes of this token group; lanes 0 .. TG-1 write
+            // (row r, token) at r * S + token, the layout the producer reads
+#pragma unroll
+            for (int off = TG; off < 32; off <<= 1)
+#pragma unroll
+                for (int v = 0; v < NT; ++v) part[v] += __shfl_xor_sync(0xFFFFFFFFu, part[v], off);
+            if (lane < TG) {
+#pragma unroll
+                for (int r = 0; r < RB; ++r)
+#pragma unroll
+                    for (int t = 0; t < ST; ++t)
+                        if (lane * ST + t < S)
+                            red[((size_t)slot * nc + cw) * NV + r * S + lane * ST + t] = part[r * ST + t];
+            }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
 #pragma unroll
@@ -411,12 +441,14 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
     }
 }
 
-template <class F, int S, int NW, int U, int RB>
-__global__ void __launch_bounds__(32 * (tma_max_consumer_warps(S, U) + 1), 1)
+// A token-split kernel is capped for two blocks per SM (64 registers): the
+// occupancy is worth more than the few spilled bytes (measured at S = 8).
+template <class F, int S, int NW, int U, int RB, int TG = 1>
+__global__ void __launch_bounds__(32 * (tma_max_consumer_warps(S, U) + 1), TG > 1 ? 2 : 1)
 gemv_tma_kernel(const typename F::Params p, float *__restrict__ out, int units, int units_per_split,
                 int nrowb, int nst, TmaLayout L, int *err)
 {
-    gemv_tma_body<F, S, NW, U, RB>(p, out, units, units_per_split, nrowb, nst, L, err);
+    gemv_tma_body<F, S, NW, U, RB, TG>(p, out, units, units_per_split, nrowb, nst, L, err);
 }
 
 // ---------------------------------------------------------------------------
@@ -440,8 +472,8 @@ struct MoeSlots {
 };
 constexpr int kErrExpert = -8;
 
-template <class F, int S, int NW, int U, int RB>
-__global__ void __launch_bounds__(32 * (tma_max_consumer_warps(S, U) + 1), 1)
+template <class F, int S, int NW, int U, int RB, int TG = 1>
+__global__ void __launch_bounds__(32 * (tma_max_consumer_warps(S, U) + 1), TG > 1 ? 2 : 1)
 gemv_tma_moe_kernel(const typename F::Params p0, float *__restrict__ out0, MoeSlots m, int units,
                     int units_per_split, int nrowb, int nst, TmaLayout L, int *err)
 {
@@ -459,7 +491,7 @@ gemv_tma_moe_kernel(const typename F::Params p0, float *__restrict__ out0, MoeSl
         return;
     }
     const typename F::Params p = F::with_expert(p0, e.w, e.scales, (size_t)r * m.x_stride);
-    gemv_tma_body<F, S, NW, U, RB>(p, out, units, units_per_split, nrowb, nst, L, err);
+    gemv_tma_body<F, S, NW, U, RB, TG>(p, out, units, units_per_split, nrowb, nst, L, err);
 }
 
 // ---------------------------------------------------------------------------
@@ -485,6 +517,7 @@ struct TmaGeom {
     uint32_t rowbytes;        // staged bytes of a whole row
     uint32_t granule_bytes;   // staged bytes of one granule
     uint32_t arowbytes;       // staged side-data bytes per row
+    int tg = 1;               // token groups (consumer threads per unit)
 };
 
 // Plan of RB-row batches; at most max_per_sm blocks per SM share its shared
@@ -523,11 +556,11 @@ struct MoeLaunch {
     int n_slots;
 };
 
-template <class F, int S, int NW, int U, int RB>
+template <class F, int S, int NW, int U, int RB, int TG = 1>
 void launch_tma(const typename F::Params &p, float *out, const TmaPlan &pl, cudaStream_t st,
                 const MoeLaunch *moe = nullptr) {
-    auto kern = gemv_tma_kernel<F, S, NW, U, RB>;
-    auto kern_moe = gemv_tma_moe_kernel<F, S, NW, U, RB>;
+    auto kern = gemv_tma_kernel<F, S, NW, U, RB, TG>;
+    auto kern_moe = gemv_tma_moe_kernel<F, S, NW, U, RB, TG>;
     const void *kfn = moe ? reinterpret_cast<const void *>(kern_moe) : reinterpret_cast<const void *>(kern);
     static int attr_set_mask[2] = {0, 0};   // one bit per device ordinal (< 31), per kernel
     int &mask = attr_set_mask[moe ? 1 : 0];
