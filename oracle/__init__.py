@@ -68,6 +68,7 @@ def _declare(lib):
     lib.oracle_encode_mq4v1.argtypes = [P, P, i, i]
     lib.oracle_encode_mq4c.argtypes = [P, P, i, i]
     lib.oracle_qgemv_moe.argtypes = [i, P, P, P, z, P, P, i, P, i, i, i, i, i]
+    lib.oracle_qgemm_moe.argtypes = [i, P, P, P, P, P, i, P, P, i, i, i, i]
     lib.oracle_fwht256.argtypes = [P, P, P, z]
     lib.oracle_ifwht256.argtypes = [P, P, P, z]
     return lib
@@ -276,6 +277,23 @@ class Oracle:
         self.lib.oracle_qgemv_moe(fmt, _p(y), _p(mag), _p(x), x_slot_stride, ctypes.cast(wp, ctypes.c_void_p),
                                   ctypes.cast(sp, ctypes.c_void_p), len(ws), _p(ids), n, S, I, O, gs)
         return y, mag
+
+    def qgemm_moe(self, fmt, X_bf16, weights, scales, group_expert, offsets, I, O, gs=0):
+        """Y, mag (float64 [M, O], M = offsets[-1]; rows no group covers are NaN)."""
+        X = np.ascontiguousarray(X_bf16, np.uint16)
+        ws = [np.ascontiguousarray(w, np.uint8) for w in weights]
+        sdt = np.uint8 if fmt == 71 else np.float32
+        ss = [None if sc is None else np.ascontiguousarray(sc, sdt) for sc in scales]
+        ge = np.ascontiguousarray(group_expert, np.int32)
+        off = np.ascontiguousarray(offsets, np.int32)
+        M = int(off[-1])
+        wp = (ctypes.c_void_p * len(ws))(*[w.ctypes.data for w in ws])
+        sp = (ctypes.c_void_p * len(ss))(*[0 if sc is None else sc.ctypes.data for sc in ss])
+        Y = np.full((M, O), np.nan)
+        mag = np.full((M, O), np.nan)
+        self.lib.oracle_qgemm_moe(fmt, _p(Y), _p(mag), _p(X), ctypes.cast(wp, ctypes.c_void_p),
+                                  ctypes.cast(sp, ctypes.c_void_p), len(ws), _p(ge), _p(off), len(ge), I, O, gs)
+        return Y, mag
 
     # FWHT -------------------------------------------------------------------
     def fwht256(self, v, signs):

@@ -591,6 +591,49 @@ void oracle_qgemv_moe(int fmt, double *y, double *mag, const void *x, size_t x_s
     }
 }
 
+/* Routed-expert prefill: tokens sorted by expert; group g multiplies the rows
+ * [off[g], off[g+1]) of X (bf16 [M, I]) by the expert group_expert[g] into the
+ * same rows of Y, with the single-matrix prefill definition of `fmt` (the
+ * fmt=4 GEMM; the GEMV definitions of the other formats with S = the group's
+ * rows).  Rows that no group covers are left untouched.                     */
+void oracle_qgemm_moe(int fmt, double *Y, double *mag, const uint16_t *X, const void *const *w,
+                      const float *const *scales, int n_experts, const int *group_expert,
+                      const int *off, int n_groups, int I, int O, int gs)
+{
+    for (int g = 0; g < n_groups; ++g) {
+        const int e = group_expert[g];
+        const int m = off[g + 1] - off[g];
+        if (m <= 0 || e < 0 || e >= n_experts)
+            continue;
+        double *yg = Y + (size_t)off[g] * O;
+        double *mg = mag + (size_t)off[g] * O;
+        const uint16_t *xg = X + (size_t)off[g] * I;
+        const uint8_t *we = (const uint8_t *)w[e];
+        switch (fmt) {
+        case 4:
+            oracle_qgemm_i4g(yg, mg, xg, we, scales[e], m, I, O, gs);
+            break;
+        case 7:
+            oracle_qgemv_fp8b128(yg, mg, xg, we, scales[e], m, I, O);
+            break;
+        case 71:
+            oracle_qgemv_fp8ue8m0(yg, mg, xg, we, (const uint8_t *)scales[e], m, I, O);
+            break;
+        case 13:
+            oracle_qgemv_mq4v1(yg, mg, xg, we, m, I, O);
+            break;
+        case 44:
+            oracle_qgemv_mq4v2(yg, mg, xg, we, m, I, O);
+            break;
+        case 45:
+            oracle_qgemv_mq4c(yg, mg, xg, we, m, I, O);
+            break;
+        default:
+            break;
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Seeded sign-FWHT over 256-element blocks ([hipfire MQ4V2] sections 1, 1d, */
 /* 3: the MQ line rotates every 256-block with a signed Walsh-Hadamard       */

@@ -734,6 +734,27 @@ def pin_moe_permutation(orc):
     assert np.array_equal(yp, y[perm])
 
 
+def pin_moe_gemm_bruteforce(orc):
+    """Routed-expert prefill == numpy dequantize + matmul group by group, every
+    format, with an empty group, a repeated expert and groups out of expert
+    order; rows of the token-sorted X map to the same rows of Y."""
+    rng = np.random.default_rng(53)
+    for fmt, (O, I, gs) in ((4, (3, 200, 64)), (7, (130, 260, 0)), (71, (130, 260, 0)), (44, (3, 512, 0)),
+                            (13, (2, 768, 0)), (45, (2, 512, 0))):
+        ws, ss, deq = _moe_experts(rng, fmt, 4, O, I, gs)
+        ge = np.array([2, 0, 3, 2], np.int32)
+        off = np.array([0, 3, 3, 8, 9], np.int32)          # group 1 is empty
+        M = int(off[-1])
+        xf = rng.standard_normal(M * I).astype(np.float32)
+        xb = synth.bf16_bits(xf)
+        X = synth.bf16_to_f32(xb).reshape(M, I).astype(np.float64)
+        Y, mag = orc.qgemm_moe(fmt, xb, ws, ss, ge, off, I, O, gs)
+        for g, e in enumerate(ge):
+            r = slice(off[g], off[g + 1])
+            _close(Y[r], X[r] @ deq[e].T, np.abs(X[r]) @ np.abs(deq[e]).T, what=f"moe gemm fmt={fmt} group {g}")
+        assert not np.isnan(Y).any()
+
+
 def pin_fwht_vs_scipy(orc):
     from scipy.linalg import hadamard
     H = hadamard(256).astype(np.float64)

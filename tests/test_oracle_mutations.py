@@ -50,6 +50,8 @@ MUTATIONS = [
      "double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];\n                double t = wv / sc"),
     ("fp8_block_64", "double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];",
      "double sc = (double)scale_inv[((size_t)(o / 128) * nbi + (size_t)(i / 64)) % (nbi * (((size_t)O + 127) / 128))];"),
+    ("moe_gemm_rows_from_zero", "const uint16_t *xg = X + (size_t)off[g] * I;", "const uint16_t *xg = X;"),
+    ("moe_gemm_expert_of_slot", "const int e = group_expert[g];", "const int e = group_expert[0];"),
     # UE8M0 scales
     ("e8m0_bias_126", "return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 126);"),
     ("e8m0_no_nan", "    if (e == 255)\n        return NAN;\n    return ldexp", "    if (e == 256)\n        return NAN;\n    return ldexp"),
