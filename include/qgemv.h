@@ -225,6 +225,28 @@ int qgemv_moe(int fmt, float *y, const void *x, size_t x_slot_stride,
               const qg_expert *experts, int n_experts, const int *ids, int n_slots,
               int S, int I, int O, int gs, qg_stream_t stream);
 
+/* Routed experts, batched prefill: the tokens of a prompt sorted by routed
+ * expert (colibri PR #457, section 7; hipfire docs "MQ4 V2", section 9: the
+ * grouped MoE prefill).  Group g multiplies rows [group_offsets[g],
+ * group_offsets[g+1]) of X by expert experts[group_expert[g]] into the same
+ * rows of Y, each group as one call of the format's prefill GEMM (qgemm_i4g,
+ * qgemm_fp8b128, qgemm_fp8ue8m0, qgemm_mq4v2, qgemm_mq4v1, qgemm_mq4c; same
+ * layouts, precision and paths), one after another on `stream`.
+ *   experts        HOST array [n_experts] of qg_expert (device pointers)
+ *   group_expert   HOST int32 [n_groups], each in [0, n_experts)
+ *   group_offsets  HOST int32 [n_groups + 1], non-decreasing, >= 0 (a group
+ *                  may be empty; rows outside every group are not written)
+ *   X, Y           DEVICE bf16 [M, I] and f32 [M, O], M >= group_offsets[n_groups]
+ *   ws             shared by the groups: at least the largest of
+ *                  qg_gemm_workspace_bytes(fmt, rows of g, I, O, gs)
+ * The group sizes decide the launches, so they are host data here (a
+ * router's counts are read back once per prompt).  Errors: QG_EINVAL for a
+ * bad format, group table or size; QG_EWORKSPACE; otherwise the first
+ * failing group's status from its GEMM (qg_last_error names it). */
+int qgemm_moe(int fmt, float *Y, const uint16_t *X, const qg_expert *experts, int n_experts,
+              const int *group_expert, const int *group_offsets, int n_groups,
+              int I, int O, int gs, void *ws, size_t ws_bytes, qg_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* MQ4-V2 (hipfire qt=44), decode GEMV                                      */
 /* hipfire "MQ4 V2", section 2 (layout) and section 4 (decoder).            */

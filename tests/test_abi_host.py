@@ -34,7 +34,7 @@ def test_header_lists_the_entry_points():
     for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qgemm_fp8b128", "qgemm_mq4v2",
                  "qg_workspace_bytes", "qg_gemm_workspace_bytes", "qg_device_status",
                  "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256",
-                 "qgemv_moe"]:
+                 "qgemv_moe", "qgemm_moe"]:
         assert must in names, names
 
 
@@ -120,6 +120,22 @@ def test_moe_refusals(qg):
     assert moe(4, P, P, 100, P, 4, P, 2, 1, 256, 64, 64, stream=0) == qg.QG_EINVAL    # slots overlap
     assert moe(4, P, P, 0, P + 4, 4, P, 2, 1, 256, 64, 64, stream=0) == qg.QG_EALIGN  # table alignment
     assert moe(4, P, P, 0, P, 4, P, 0, 1, 256, 64, 64, stream=0) == qg.QG_OK          # nothing to do
+
+
+def test_moe_gemm_refusals(qg):
+    P = POISON
+    tab = qg.expert_table([(P, P), (P, P)])
+    mm = qg.qgemm_moe
+    assert mm(5, P, P, tab, 2, [0], [0, 4], 1, 256, 64, 64, stream=0) == qg.QG_EINVAL      # no such format
+    assert mm(4, P, P, tab, 2, [2], [0, 4], 1, 256, 64, 64, stream=0) == qg.QG_EINVAL      # expert 2 of 2
+    assert "expert 2" in qg.last_error()
+    assert mm(4, P, P, tab, 2, [0, 1], [0, 4, 3], 2, 256, 64, 64, stream=0) == qg.QG_EINVAL  # offsets decrease
+    assert mm(4, P, P, tab, 2, [0], [-1, 4], 1, 256, 64, 64, stream=0) == qg.QG_EINVAL     # negative offset
+    assert mm(4, P, P, tab, 0, [0], [0, 4], 1, 256, 64, 64, stream=0) == qg.QG_EINVAL      # empty table
+    assert mm(4, P, P, tab, 2, [0], [0, 4], -1, 256, 64, 64, stream=0) == qg.QG_EINVAL     # negative groups
+    assert mm(4, None, P, tab, 2, [0], [0, 4], 1, 256, 64, 64, stream=0) == qg.QG_EINVAL
+    assert mm(4, P, P, tab, 2, [0, 1], [3, 3, 3], 2, 256, 64, 64, stream=0) == qg.QG_OK      # only empty groups
+    assert mm(4, P, P, tab, 2, [], [0], 0, 256, 64, 64, stream=0) == qg.QG_OK
 
 
 def test_gemm_and_prep_refusals(qg):

@@ -164,3 +164,53 @@ def test_moe_no_slots(qg):
     y = t.full((8,), 7.0, device="cuda:0")
     assert qg.qgemv_moe(4, y, y, 0, y, 1, y, 0, 1, 64, 4, 64) == qg.QG_OK
     assert (y.cpu() == 7.0).all()
+
+
+# ----------------------------------------------------------------------------
+# routed-expert prefill GEMM (qgemm_moe)
+# ----------------------------------------------------------------------------
+
+GEMM_FMTS = (4, 7, 71, 44, 13, 45)
+
+
+@pytest.mark.parametrize("fmt", GEMM_FMTS)
+def test_moe_gemm_groups(qg, fmt):
+    """Five groups of 0, 1, 70, 130 and 257 token rows (tensor-core tiles of
+    several sizes and a ragged tail), experts repeated and out of order; the
+    rows before the first group are left alone."""
+    t = torch()
+    O, I, gs = (256, 1024, 64) if fmt not in (7, 71) else (260, 1024, 0)
+    ws, ss = experts(fmt, 4, O, I, gs, tag=900 + fmt)
+    ge = [2, 0, 3, 0, 1]
+    off = [5, 5, 6, 76, 206, 463]
+    M = off[-1]
+    x = synth.normal(950 + fmt, M * I).astype(np.float32)
+    xb = synth.bf16_bits(x).reshape(M, I)
+    ws_d = [dev(w) for w in ws]
+    ss_d = [None if s is None else dev(s) for s in ss]
+    table = qg.expert_table(list(zip(ws_d, ss_d)))
+    n = max(qg.qg_gemm_workspace_bytes(fmt, m, I, O, gs) for m in (1, 70, 130, 257))
+    buf = t.empty(max(n, 1), dtype=t.uint8, device="cuda:0")
+    Y = t.full((M * O,), float("nan"), dtype=t.float32, device="cuda:0")
+    qg.check(qg.qgemm_moe(fmt, Y, dev(xb), table, 4, ge, off, len(ge), I, O, gs, buf, n))
+    Yh = Y.cpu().numpy().astype(np.float64).reshape(M, O)
+    assert np.isnan(Yh[:5]).all()
+    ref, mag = orc().qgemm_moe(fmt, xb, ws, ss, ge, off, I, O, gs)
+    compare(Yh[5:], ref[5:], mag[5:], what=f"moe gemm fmt={fmt}")
+
+
+def test_moe_gemm_general_kernel_rows(qg):
+    """I not a multiple of 64: every group takes the general kernel."""
+    t = torch()
+    fmt, O, I, gs = 4, 96, 200, 40
+    ws, ss = experts(fmt, 3, O, I, gs, tag=990)
+    ge, off = [1, 2, 1], [0, 9, 10, 40]
+    M = off[-1]
+    xb = synth.bf16_bits(synth.normal(991, M * I).astype(np.float32)).reshape(M, I)
+    ws_d = [dev(w) for w in ws]                   # kept alive until the call has run
+    ss_d = [dev(s) for s in ss]
+    table = qg.expert_table(list(zip(ws_d, ss_d)))
+    Y = t.full((M * O,), float("nan"), dtype=t.float32, device="cuda:0")
+    qg.check(qg.qgemm_moe(fmt, Y, dev(xb), table, 3, ge, off, len(ge), I, O, gs))
+    ref, mag = orc().qgemm_moe(fmt, xb, ws, ss, ge, off, I, O, gs)
+    compare(Y.cpu().numpy().astype(np.float64).reshape(M, O), ref, mag, what="moe gemm general")

@@ -51,6 +51,7 @@ _SIGNATURES = {
     "qgemv_fp8ue8m0": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_fp8ue8m0": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_moe": ([_I, _P, _P, _Z, _P, _I, _P, _I, _I, _I, _I, _I, _P], _I),
+    "qgemm_moe": ([_I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
     "qg_encode_mq4v1": ([_P, _P, _I, _I, _P], _I),
     "qg_encode_mq4c": ([_P, _P, _I, _I, _P], _I),
     "qg_quantize_i4g": ([_P, _P, _P, _I, _I, _I, _P], _I),
@@ -145,6 +146,19 @@ def qgemv_moe(fmt, y, x, x_slot_stride, experts, n_experts, ids, n_slots, S, I, 
     pointer pairs (see ``expert_table``), `ids` a device int32 array."""
     return _lib.qgemv_moe(fmt, _ptr(y), _ptr(x), x_slot_stride, _ptr(experts), n_experts, _ptr(ids), n_slots,
                           S, I, O, gs, _stream(stream))
+
+
+def qgemm_moe(fmt, Y, X, experts, n_experts, group_expert, group_offsets, n_groups, I, O, gs=0, ws=None,
+              ws_bytes=0, stream=None) -> int:
+    """Routed-expert prefill GEMM.  ``experts`` (bytes from ``expert_table``),
+    ``group_expert`` and ``group_offsets`` (int sequences) are host data."""
+    import array
+    ge = array.array("i", [int(v) for v in group_expert])
+    off = array.array("i", [int(v) for v in group_offsets])
+    ex = ctypes.create_string_buffer(bytes(experts), len(experts)) if experts is not None else None
+    return _lib.qgemm_moe(fmt, _ptr(Y), _ptr(X), ctypes.addressof(ex) if ex is not None else None, n_experts,
+                          ge.buffer_info()[0] if len(ge) else None, off.buffer_info()[0] if len(off) else None,
+                          n_groups, I, O, gs, _ptr(ws), ws_bytes, _stream(stream))
 
 
 def expert_table(pairs):

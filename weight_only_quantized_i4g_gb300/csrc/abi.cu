@@ -165,6 +165,65 @@ int qgemv_fp8ue8m0(float *y, const uint16_t *x, const uint8_t *w, const uint8_t 
     return run_gemv_fp8ue8m0(y, x, w, scale_e8m0, S, I, O, ws, ws_bytes, as_stream(stream));
 }
 
+int qgemm_moe(int fmt, float *Y, const uint16_t *X, const qg_expert *experts, int n_experts,
+              const int *group_expert, const int *group_offsets, int n_groups, int I, int O, int gs, void *ws,
+              size_t ws_bytes, qg_stream_t stream) {
+    const char *fn = "qgemm_moe";
+    if (fmt != QG_FMT_I4G && fmt != QG_FMT_FP8B128 && fmt != QG_FMT_FP8UE8M0 && fmt != QG_FMT_MQ4V2 &&
+        fmt != QG_FMT_MQ4V1 && fmt != QG_FMT_MQ4C)
+        QG_REFUSE(kEInval, "%s: unknown format id %d", fn, fmt);
+    if (n_groups < 0) QG_REFUSE(kEInval, "%s: n_groups = %d, must be >= 0", fn, n_groups);
+    if (n_groups == 0) return kOk;
+    if (!experts || !group_expert || !group_offsets)
+        QG_REFUSE(kEInval, "%s: experts, group_expert and group_offsets must be non-NULL", fn);
+    if (n_experts < 1) QG_REFUSE(kEInval, "%s: n_experts = %d, must be >= 1", fn, n_experts);
+    if (I < 1 || O < 1) QG_REFUSE(kEInval, "%s: I = %d and O = %d must be >= 1", fn, I, O);
+    if (group_offsets[0] < 0) QG_REFUSE(kEInval, "%s: group_offsets[0] = %d is negative", fn, group_offsets[0]);
+    int m_max = 0;
+    for (int g = 0; g < n_groups; ++g) {
+        const int m = group_offsets[g + 1] - group_offsets[g];
+        if (m < 0) QG_REFUSE(kEInval, "%s: group_offsets decrease at group %d", fn, g);
+        if (group_expert[g] < 0 || group_expert[g] >= n_experts)
+            QG_REFUSE(kEInval, "%s: group %d names expert %d of %d", fn, g, group_expert[g], n_experts);
+        if (m > m_max) m_max = m;
+    }
+    if (m_max == 0) return kOk;
+    if (!Y || !X) QG_REFUSE(kEInval, "%s: Y and X must be non-NULL", fn);
+    // the groups run one after another on `stream` and share the workspace
+    size_t need = 0;
+    for (int g = 0; g < n_groups; ++g) {
+        const int m = group_offsets[g + 1] - group_offsets[g];
+        if (m == 0) continue;
+        const size_t n = qg_gemm_workspace_bytes(fmt, m, I, O, gs);
+        if (n > need) need = n;
+    }
+    if (need > 0 && (ws == nullptr || ws_bytes < need))
+        QG_REFUSE(kEWorkspace, "%s: the largest group needs a workspace of %zu bytes (got %zu)", fn, need,
+                  ws == nullptr ? (size_t)0 : ws_bytes);
+    for (int g = 0; g < n_groups; ++g) {
+        const int m = group_offsets[g + 1] - group_offsets[g];
+        if (m == 0) continue;
+        const qg_expert e = experts[group_expert[g]];
+        float *Yg = Y + (size_t)group_offsets[g] * O;
+        const uint16_t *Xg = X + (size_t)group_offsets[g] * I;
+        const uint8_t *w = static_cast<const uint8_t *>(e.w);
+        int rc;
+        switch (fmt) {
+            case QG_FMT_I4G: rc = qgemm_i4g(Yg, Xg, w, e.scales, m, I, O, gs, ws, ws_bytes, stream); break;
+            case QG_FMT_FP8B128: rc = qgemm_fp8b128(Yg, Xg, w, e.scales, m, I, O, ws, ws_bytes, stream); break;
+            case QG_FMT_FP8UE8M0:
+                rc = qgemm_fp8ue8m0(Yg, Xg, w, reinterpret_cast<const uint8_t *>(e.scales), m, I, O, ws, ws_bytes,
+                                    stream);
+                break;
+            case QG_FMT_MQ4V2: rc = qgemm_mq4v2(Yg, Xg, w, m, I, O, ws, ws_bytes, stream); break;
+            case QG_FMT_MQ4V1: rc = qgemm_mq4v1(Yg, Xg, w, m, I, O, ws, ws_bytes, stream); break;
+            default: rc = qgemm_mq4c(Yg, Xg, w, m, I, O, ws, ws_bytes, stream); break;
+        }
+        if (rc != kOk) return rc;   // qg_last_error names the group's failed condition
+    }
+    return kOk;
+}
+
 int qgemv_moe(int fmt, float *y, const void *x, size_t x_slot_stride, const qg_expert *experts, int n_experts,
               const int *ids, int n_slots, int S, int I, int O, int gs, qg_stream_t stream) {
     const char *fn = "qgemv_moe";
