@@ -447,6 +447,8 @@ def ours_arm(args):
             per_format.update(one_header_breakdown(qg, torch, stream, hbm_peak, dev))
             per_format.update(moe_breakdown(qg, torch, stream, hbm_peak, dev))
     prefill = prefill_measure(qg, torch, dev, stream) if args.prefill else None
+    if prefill is not None and len(shapes) == len(SHAPES):
+        prefill["routed_experts"] = moe_prefill_measure(qg, torch, stream, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -819,6 +821,60 @@ def moe_breakdown(qg, torch, stream, hbm_peak, dev):
     return out
 
 
+def moe_prefill_measure(qg, torch, stream, dev, reps=10):
+    """Routed-expert prefill: 512 tokens, each routed to 8 of 32 experts
+    (seeded), sorted by expert into 4096 rows; the gate projection 2048x7168
+    of every expert as one qgemm_moe call (one tensor-core launch over every
+    group's tiles).  Timed alone after a 256 MiB write that flushes L2,
+    median of `reps`; TFLOP/s over the routed rows (2 * 4096 * 7168 * 2048)."""
+    peak, kind = load_tensor_peak()
+    out = {"workload": "512 tokens x top-8 of 32 experts, gate projection 2048x7168 per expert, bf16 X, f32 Y",
+           "peak": peak, "unit": "TFLOP/s", "calls": {}}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    T, K, E, O, I = 512, 8, 32, 2048, 7168
+    gen = torch.Generator().manual_seed(77)
+    routes = torch.stack([torch.randperm(E, generator=gen)[:K] for _ in range(T)])     # [T, K]
+    counts = torch.bincount(routes.reshape(-1), minlength=E).tolist()
+    offsets = [0]
+    for c in counts:
+        offsets.append(offsets[-1] + c)
+    M = offsets[-1]
+    g = torch.Generator(device=dev)
+    for name, fmt in (("fmt4", 4), ("mq4v2", 44)):
+        g.manual_seed(8100 + fmt)
+        mats, scs = [], []
+        with torch.cuda.stream(stream):
+            for _ in range(E):
+                w = torch.randn(O, I, generator=g, device=dev) * 0.02
+                if fmt == 4:
+                    wq = torch.empty(O * I // 2, dtype=torch.uint8, device=dev)
+                    sc = torch.empty(O * (I // GS), dtype=torch.float32, device=dev)
+                    qg.check(qg.qg_quantize_i4g(wq, sc, w, O, I, GS, stream=stream))
+                    mats.append(wq); scs.append(sc)
+                else:
+                    blocks = torch.empty(O * (I // 256) * 136, dtype=torch.uint8, device=dev)
+                    qg.check(qg.qg_encode_mq4v2(blocks, w, O, I, stream=stream))
+                    mats.append(blocks); scs.append(None)
+                del w
+            X = torch.randn(M, I, generator=g, device=dev).to(torch.bfloat16).view(torch.int16)
+            Y = torch.empty(M * O, dtype=torch.float32, device=dev)
+        stream.synchronize()
+        table = qg.expert_table(list(zip(mats, scs)))
+        gs = GS if fmt == 4 else 0
+        n = qg.qg_moe_gemm_workspace_bytes(fmt, offsets, E, I, O, gs)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        fn = lambda: qg.check(qg.qgemm_moe(fmt, Y, X, table, E, list(range(E)), offsets, E, I, O, gs, ws, n,
+                                           stream=stream))
+        with torch.cuda.stream(stream):
+            t = _time_alone(fn, flush, stream, reps, torch)
+        tf = 2.0 * M * I * O / t / 1e12
+        out["calls"][f"{name} {M} rows"] = {"us": round(t * 1e6, 1), "tflops": round(tf, 1),
+                                            "frac": round(tf / peak, 4), "groups": sum(1 for c in counts if c),
+                                            "rows_per_group": [min(counts), max(counts)]}
+        del mats, scs
+    return out
+
+
 BATCHED = {"i4g": 4, "mq4": 8}     # the configs' batched decode cases: fmt4 at batch 4, MQ4-V2 at 8
 
 
@@ -924,7 +980,8 @@ def moe_only(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream()
     hbm_peak, _ = load_peaks()
-    print(json.dumps({"moe": moe_breakdown(qg, torch, stream, hbm_peak, dev)}), flush=True)
+    print(json.dumps({"moe": moe_breakdown(qg, torch, stream, hbm_peak, dev),
+                      "moe_prefill": moe_prefill_measure(qg, torch, stream, dev)}), flush=True)
 
 
 def prefill_only(args):

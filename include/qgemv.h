@@ -237,12 +237,21 @@ int qgemv_moe(int fmt, float *y, const void *x, size_t x_slot_stride,
  *   group_offsets  HOST int32 [n_groups + 1], non-decreasing, >= 0 (a group
  *                  may be empty; rows outside every group are not written)
  *   X, Y           DEVICE bf16 [M, I] and f32 [M, O], M >= group_offsets[n_groups]
- *   ws             shared by the groups: at least the largest of
- *                  qg_gemm_workspace_bytes(fmt, rows of g, I, O, gs)
- * The group sizes decide the launches, so they are host data here (a
- * router's counts are read back once per prompt).  Errors: QG_EINVAL for a
- * bad format, group table or size; QG_EWORKSPACE; otherwise the first
- * failing group's status from its GEMM (qg_last_error names it). */
+ *   ws             qg_moe_gemm_workspace_bytes(fmt, group_offsets, n_groups,
+ *                  I, O, gs) bytes, 256-byte aligned
+ * Up to 64 non-empty groups run as ONE tensor-core launch (every group's
+ * token blocks times the output tiles form one range of tiles, each tile
+ * dequantizing its group's weights); a chunk whose shapes or pointers the
+ * tensor-core kernel cannot take runs group by group through the format's
+ * GEMM entry point instead.  The group sizes decide the launches, so they
+ * are host data here (a router's counts are read back once per prompt).
+ * Errors: QG_EINVAL for a bad format, group table or size; QG_EGS /
+ * QG_ESHAPE as the format's GEMM; QG_EWORKSPACE; otherwise the first failing
+ * group's status from its GEMM (qg_last_error names it). */
+/* Workspace of qgemm_moe for these groups (host group_offsets [n_groups+1]);
+ * 0 for invalid arguments. */
+size_t qg_moe_gemm_workspace_bytes(int fmt, const int *group_offsets, int n_groups, int I, int O, int gs);
+
 int qgemm_moe(int fmt, float *Y, const uint16_t *X, const qg_expert *experts, int n_experts,
               const int *group_expert, const int *group_offsets, int n_groups,
               int I, int O, int gs, void *ws, size_t ws_bytes, qg_stream_t stream);

@@ -189,7 +189,7 @@ def test_moe_gemm_groups(qg, fmt):
     ws_d = [dev(w) for w in ws]
     ss_d = [None if s is None else dev(s) for s in ss]
     table = qg.expert_table(list(zip(ws_d, ss_d)))
-    n = max(qg.qg_gemm_workspace_bytes(fmt, m, I, O, gs) for m in (1, 70, 130, 257))
+    n = qg.qg_moe_gemm_workspace_bytes(fmt, off, len(ge), I, O, gs)
     buf = t.empty(max(n, 1), dtype=t.uint8, device="cuda:0")
     Y = t.full((M * O,), float("nan"), dtype=t.float32, device="cuda:0")
     qg.check(qg.qgemm_moe(fmt, Y, dev(xb), table, 4, ge, off, len(ge), I, O, gs, buf, n))
@@ -211,6 +211,59 @@ def test_moe_gemm_general_kernel_rows(qg):
     ss_d = [dev(s) for s in ss]
     table = qg.expert_table(list(zip(ws_d, ss_d)))
     Y = t.full((M * O,), float("nan"), dtype=t.float32, device="cuda:0")
+    assert qg.qg_moe_gemm_workspace_bytes(fmt, off, len(ge), I, O, gs) == 0
     qg.check(qg.qgemm_moe(fmt, Y, dev(xb), table, 3, ge, off, len(ge), I, O, gs))
     ref, mag = orc().qgemm_moe(fmt, xb, ws, ss, ge, off, I, O, gs)
     compare(Y.cpu().numpy().astype(np.float64).reshape(M, O), ref, mag, what="moe gemm general")
+
+
+def run_moe_gemm(qg, fmt, ws, ss, ge, off, I, O, gs, xb, keep_w=None):
+    t = torch()
+    M = off[-1]
+    ws_d = keep_w if keep_w is not None else [dev(w) for w in ws]
+    ss_d = [None if s is None else dev(s) for s in ss]
+    table = qg.expert_table(list(zip(ws_d, ss_d)))
+    n = qg.qg_moe_gemm_workspace_bytes(fmt, off, len(ge), I, O, gs)
+    buf = t.empty(max(n, 1), dtype=t.uint8, device="cuda:0")
+    Y = t.full((M * O,), float("nan"), dtype=t.float32, device="cuda:0")
+    qg.check(qg.qgemm_moe(fmt, Y, dev(xb), table, len(ws), ge, off, len(ge), I, O, gs, buf, n))
+    return Y.cpu().numpy().astype(np.float64).reshape(M, O)
+
+
+@pytest.mark.parametrize("fmt", [4, 44])
+def test_moe_gemm_many_groups(qg, fmt):
+    """70 non-empty groups (two grouped launches: 64 + 6) of 1..40 rows, four
+    empty groups in between."""
+    O, I, gs = 256, 512, 64
+    ws, ss = experts(fmt, 8, O, I, gs, tag=1200 + fmt)
+    sizes = [int(v) for v in (1 + synth.uint64(1300 + fmt, 74) % 40)]
+    for g in (5, 30, 31, 60):
+        sizes[g] = 0
+    off = [0]
+    for c in sizes:
+        off.append(off[-1] + c)
+    ge = [int(v) for v in synth.uint64(1400 + fmt, 74) % 8]
+    M = off[-1]
+    xb = synth.bf16_bits(synth.normal(1500 + fmt, M * I).astype(np.float32)).reshape(M, I)
+    Y = run_moe_gemm(qg, fmt, ws, ss, ge, off, I, O, gs, xb)
+    ref, mag = orc().qgemm_moe(fmt, xb, ws, ss, ge, off, I, O, gs)
+    compare(Y, ref, mag, what=f"moe gemm 74 groups fmt={fmt}")
+
+
+def test_moe_gemm_misaligned_expert_falls_back(qg):
+    """An expert's weights 8 bytes off a 16-byte line: that chunk runs group by
+    group (the fmt=7 tensor-core kernel needs 16-byte aligned codes; the
+    general kernel takes it), still exact."""
+    t = torch()
+    fmt, O, I, gs = 7, 130, 512, 0
+    ws, ss = experts(fmt, 2, O, I, gs, tag=1600)
+    w0 = dev(ws[0])
+    padded = t.zeros(ws[1].size + 16, dtype=t.uint8, device="cuda:0")
+    padded[8:8 + ws[1].size].copy_(dev(ws[1]))
+    ge, off = [0, 1, 0], [0, 70, 140, 150]
+    M = off[-1]
+    xb = synth.bf16_bits(synth.normal(1601, M * I).astype(np.float32)).reshape(M, I)
+    Y = run_moe_gemm(qg, fmt, ws, ss, ge, off, I, O, gs, xb, keep_w=[w0, padded.data_ptr() + 8])
+    ref, mag = orc().qgemm_moe(fmt, xb, ws, ss, ge, off, I, O, gs)
+    compare(Y, ref, mag, what="moe gemm fallback")
+    del padded

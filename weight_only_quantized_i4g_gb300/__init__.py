@@ -52,6 +52,7 @@ _SIGNATURES = {
     "qgemm_fp8ue8m0": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_moe": ([_I, _P, _P, _Z, _P, _I, _P, _I, _I, _I, _I, _I, _P], _I),
     "qgemm_moe": ([_I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
+    "qg_moe_gemm_workspace_bytes": ([_I, _P, _I, _I, _I, _I], _Z),
     "qg_encode_mq4v1": ([_P, _P, _I, _I, _P], _I),
     "qg_encode_mq4c": ([_P, _P, _I, _I, _P], _I),
     "qg_quantize_i4g": ([_P, _P, _P, _I, _I, _I, _P], _I),
@@ -159,6 +160,12 @@ def qgemm_moe(fmt, Y, X, experts, n_experts, group_expert, group_offsets, n_grou
     return _lib.qgemm_moe(fmt, _ptr(Y), _ptr(X), ctypes.addressof(ex) if ex is not None else None, n_experts,
                           ge.buffer_info()[0] if len(ge) else None, off.buffer_info()[0] if len(off) else None,
                           n_groups, I, O, gs, _ptr(ws), ws_bytes, _stream(stream))
+
+
+def qg_moe_gemm_workspace_bytes(fmt, group_offsets, n_groups, I, O, gs=0) -> int:
+    import array
+    off = array.array("i", [int(v) for v in group_offsets])
+    return _lib.qg_moe_gemm_workspace_bytes(fmt, off.buffer_info()[0] if len(off) else None, n_groups, I, O, gs)
 
 
 def expert_table(pairs):

@@ -69,6 +69,73 @@ int check_gs(const char *fn, int gs) {
 
 cudaStream_t as_stream(qg_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// One grouped tensor-core launch for the non-empty groups g0 .. g1 (at most
+// kMoeGroupsPerLaunch), rows [lo, hi) of X and Y; *taken false when the
+// shapes or pointers do not suit it.
+int moe_gemm_chunk_tc(int fmt, float *Y, const uint16_t *X, const qg_expert *experts, const int *ge,
+                             const int *off, const int *idx, int n, int I, int O, int gs, void *ws, size_t ws_bytes,
+                             cudaStream_t st, bool *taken) {
+    int row0[kMoeGroupsPerLaunch], rows[kMoeGroupsPerLaunch];
+    const uint8_t *w[kMoeGroupsPerLaunch];
+    const float *sc[kMoeGroupsPerLaunch];
+    const int lo = off[idx[0]], hi = off[idx[n - 1] + 1];
+    for (int i = 0; i < n; ++i) {
+        const int g = idx[i];
+        row0[i] = off[g] - lo;
+        rows[i] = off[g + 1] - off[g];
+        w[i] = static_cast<const uint8_t *>(experts[ge[g]].w);
+        sc[i] = experts[ge[g]].scales;
+    }
+    float *Yc = Y + (size_t)lo * O;
+    const uint16_t *Xc = X + (size_t)lo * I;
+    const int M = hi - lo;
+    switch (fmt) {
+        case QG_FMT_I4G:
+            return run_gemm_moe_i4g_tc(Yc, Xc, row0, rows, w, sc, n, M, I, O, gs, ws, ws_bytes, st, taken);
+        case QG_FMT_FP8B128:
+            return run_gemm_moe_fp8b128_tc(Yc, Xc, row0, rows, w, sc, n, M, I, O, ws, ws_bytes, st, taken);
+        case QG_FMT_FP8UE8M0:
+            return run_gemm_moe_fp8ue8m0_tc(Yc, Xc, row0, rows, w, sc, n, M, I, O, ws, ws_bytes, st, taken);
+        case QG_FMT_MQ4V2: return run_gemm_moe_mq4v2_tc(Yc, Xc, row0, rows, w, n, M, I, O, ws, ws_bytes, st, taken);
+        case QG_FMT_MQ4V1: return run_gemm_moe_mq4v1_tc(Yc, Xc, row0, rows, w, n, M, I, O, ws, ws_bytes, st, taken);
+        default: return run_gemm_moe_mq4c_tc(Yc, Xc, row0, rows, w, n, M, I, O, ws, ws_bytes, st, taken);
+    }
+}
+
+size_t moe_chunk_ws(int fmt, const int *off, const int *idx, int n, int I, int O, int gs) {
+    int rows[kMoeGroupsPerLaunch];
+    for (int i = 0; i < n; ++i) rows[i] = off[idx[i] + 1] - off[idx[i]];
+    const int M = off[idx[n - 1] + 1] - off[idx[0]];
+    switch (fmt) {
+        case QG_FMT_I4G: return ws_gemm_moe_i4g(rows, n, M, I, O, gs);
+        case QG_FMT_FP8B128:
+        case QG_FMT_FP8UE8M0: return ws_gemm_moe_fp8(rows, n, M, I, O);
+        default: return ws_gemm_moe_mq4(rows, n, M, I, O);
+    }
+}
+
+bool moe_fmt_ok(int fmt) {
+    return fmt == QG_FMT_I4G || fmt == QG_FMT_FP8B128 || fmt == QG_FMT_FP8UE8M0 || fmt == QG_FMT_MQ4V2 ||
+           fmt == QG_FMT_MQ4V1 || fmt == QG_FMT_MQ4C;
+}
+
+// Calls fn(idx, n) for the non-empty groups in chunks of at most
+// kMoeGroupsPerLaunch; stops at the first non-zero return.
+template <class Fn>
+int for_each_moe_chunk(const int *off, int n_groups, Fn fn) {
+    int idx[kMoeGroupsPerLaunch], n = 0;
+    for (int g = 0; g < n_groups; ++g) {
+        if (off[g + 1] == off[g]) continue;
+        idx[n++] = g;
+        if (n == kMoeGroupsPerLaunch) {
+            const int rc = fn(idx, n);
+            if (rc) return rc;
+            n = 0;
+        }
+    }
+    return n ? fn(idx, n) : 0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -165,19 +232,39 @@ int qgemv_fp8ue8m0(float *y, const uint16_t *x, const uint8_t *w, const uint8_t 
     return run_gemv_fp8ue8m0(y, x, w, scale_e8m0, S, I, O, ws, ws_bytes, as_stream(stream));
 }
 
+size_t qg_moe_gemm_workspace_bytes(int fmt, const int *group_offsets, int n_groups, int I, int O, int gs) {
+    if (!moe_fmt_ok(fmt) || n_groups < 1 || !group_offsets || I < 1 || O < 1) return 0;
+    if (fmt == QG_FMT_I4G && (gs < 2 || (gs & 1))) return 0;
+    for (int g = 0; g < n_groups; ++g)
+        if (group_offsets[g] < 0 || group_offsets[g + 1] < group_offsets[g]) return 0;
+    size_t need = 0;
+    // the grouped launches, and the group-by-group calls taken when pointers do not suit them
+    for_each_moe_chunk(group_offsets, n_groups, [&](const int *idx, int n) {
+        const size_t c = moe_chunk_ws(fmt, group_offsets, idx, n, I, O, gs);
+        if (c > need) need = c;
+        for (int i = 0; i < n; ++i) {
+            const size_t s1 = qg_gemm_workspace_bytes(fmt, group_offsets[idx[i] + 1] - group_offsets[idx[i]], I, O, gs);
+            if (s1 > need) need = s1;
+        }
+        return 0;
+    });
+    return need;
+}
+
 int qgemm_moe(int fmt, float *Y, const uint16_t *X, const qg_expert *experts, int n_experts,
               const int *group_expert, const int *group_offsets, int n_groups, int I, int O, int gs, void *ws,
               size_t ws_bytes, qg_stream_t stream) {
     const char *fn = "qgemm_moe";
-    if (fmt != QG_FMT_I4G && fmt != QG_FMT_FP8B128 && fmt != QG_FMT_FP8UE8M0 && fmt != QG_FMT_MQ4V2 &&
-        fmt != QG_FMT_MQ4V1 && fmt != QG_FMT_MQ4C)
-        QG_REFUSE(kEInval, "%s: unknown format id %d", fn, fmt);
+    if (!moe_fmt_ok(fmt)) QG_REFUSE(kEInval, "%s: unknown format id %d", fn, fmt);
     if (n_groups < 0) QG_REFUSE(kEInval, "%s: n_groups = %d, must be >= 0", fn, n_groups);
     if (n_groups == 0) return kOk;
     if (!experts || !group_expert || !group_offsets)
         QG_REFUSE(kEInval, "%s: experts, group_expert and group_offsets must be non-NULL", fn);
     if (n_experts < 1) QG_REFUSE(kEInval, "%s: n_experts = %d, must be >= 1", fn, n_experts);
     if (I < 1 || O < 1) QG_REFUSE(kEInval, "%s: I = %d and O = %d must be >= 1", fn, I, O);
+    if (fmt == QG_FMT_I4G && check_gs(fn, gs)) return kEGs;
+    if ((fmt == QG_FMT_MQ4V2 || fmt == QG_FMT_MQ4V1 || fmt == QG_FMT_MQ4C) && I % 256)
+        QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 256", fn, I);
     if (group_offsets[0] < 0) QG_REFUSE(kEInval, "%s: group_offsets[0] = %d is negative", fn, group_offsets[0]);
     int m_max = 0;
     for (int g = 0; g < n_groups; ++g) {
@@ -189,39 +276,42 @@ int qgemm_moe(int fmt, float *Y, const uint16_t *X, const qg_expert *experts, in
     }
     if (m_max == 0) return kOk;
     if (!Y || !X) QG_REFUSE(kEInval, "%s: Y and X must be non-NULL", fn);
-    // the groups run one after another on `stream` and share the workspace
-    size_t need = 0;
-    for (int g = 0; g < n_groups; ++g) {
-        const int m = group_offsets[g + 1] - group_offsets[g];
-        if (m == 0) continue;
-        const size_t n = qg_gemm_workspace_bytes(fmt, m, I, O, gs);
-        if (n > need) need = n;
-    }
+    const size_t need = qg_moe_gemm_workspace_bytes(fmt, group_offsets, n_groups, I, O, gs);
     if (need > 0 && (ws == nullptr || ws_bytes < need))
-        QG_REFUSE(kEWorkspace, "%s: the largest group needs a workspace of %zu bytes (got %zu)", fn, need,
+        QG_REFUSE(kEWorkspace, "%s: needs a workspace of %zu bytes (qg_moe_gemm_workspace_bytes; got %zu)", fn, need,
                   ws == nullptr ? (size_t)0 : ws_bytes);
-    for (int g = 0; g < n_groups; ++g) {
-        const int m = group_offsets[g + 1] - group_offsets[g];
-        if (m == 0) continue;
-        const qg_expert e = experts[group_expert[g]];
-        float *Yg = Y + (size_t)group_offsets[g] * O;
-        const uint16_t *Xg = X + (size_t)group_offsets[g] * I;
-        const uint8_t *w = static_cast<const uint8_t *>(e.w);
-        int rc;
-        switch (fmt) {
-            case QG_FMT_I4G: rc = qgemm_i4g(Yg, Xg, w, e.scales, m, I, O, gs, ws, ws_bytes, stream); break;
-            case QG_FMT_FP8B128: rc = qgemm_fp8b128(Yg, Xg, w, e.scales, m, I, O, ws, ws_bytes, stream); break;
-            case QG_FMT_FP8UE8M0:
-                rc = qgemm_fp8ue8m0(Yg, Xg, w, reinterpret_cast<const uint8_t *>(e.scales), m, I, O, ws, ws_bytes,
-                                    stream);
-                break;
-            case QG_FMT_MQ4V2: rc = qgemm_mq4v2(Yg, Xg, w, m, I, O, ws, ws_bytes, stream); break;
-            case QG_FMT_MQ4V1: rc = qgemm_mq4v1(Yg, Xg, w, m, I, O, ws, ws_bytes, stream); break;
-            default: rc = qgemm_mq4c(Yg, Xg, w, m, I, O, ws, ws_bytes, stream); break;
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    cudaGetLastError();
+    const cudaStream_t st = as_stream(stream);
+    // up to kMoeGroupsPerLaunch groups per tensor-core launch; group by group
+    // through the format's GEMM entry point when the chunk does not suit it
+    return for_each_moe_chunk(group_offsets, n_groups, [&](const int *idx, int n) {
+        bool taken = false;
+        int rc = moe_gemm_chunk_tc(fmt, Y, X, experts, group_expert, group_offsets, idx, n, I, O, gs, ws, ws_bytes,
+                                   st, &taken);
+        if (taken) return rc == kOk ? check_launch(fn) : rc;
+        for (int i = 0; i < n; ++i) {
+            const int g = idx[i];
+            const int m = group_offsets[g + 1] - group_offsets[g];
+            const qg_expert e = experts[group_expert[g]];
+            float *Yg = Y + (size_t)group_offsets[g] * O;
+            const uint16_t *Xg = X + (size_t)group_offsets[g] * I;
+            const uint8_t *w = static_cast<const uint8_t *>(e.w);
+            switch (fmt) {
+                case QG_FMT_I4G: rc = qgemm_i4g(Yg, Xg, w, e.scales, m, I, O, gs, ws, ws_bytes, stream); break;
+                case QG_FMT_FP8B128: rc = qgemm_fp8b128(Yg, Xg, w, e.scales, m, I, O, ws, ws_bytes, stream); break;
+                case QG_FMT_FP8UE8M0:
+                    rc = qgemm_fp8ue8m0(Yg, Xg, w, reinterpret_cast<const uint8_t *>(e.scales), m, I, O, ws, ws_bytes,
+                                        stream);
+                    break;
+                case QG_FMT_MQ4V2: rc = qgemm_mq4v2(Yg, Xg, w, m, I, O, ws, ws_bytes, stream); break;
+                case QG_FMT_MQ4V1: rc = qgemm_mq4v1(Yg, Xg, w, m, I, O, ws, ws_bytes, stream); break;
+                default: rc = qgemm_mq4c(Yg, Xg, w, m, I, O, ws, ws_bytes, stream); break;
+            }
+            if (rc != kOk) return rc;   // qg_last_error names the group's failed condition
         }
-        if (rc != kOk) return rc;   // qg_last_error names the group's failed condition
-    }
-    return kOk;
+        return (int)kOk;
+    });
 }
 
 int qgemv_moe(int fmt, float *y, const void *x, size_t x_slot_stride, const qg_expert *experts, int n_experts,

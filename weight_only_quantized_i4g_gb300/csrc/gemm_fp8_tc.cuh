@@ -41,13 +41,14 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint16_t two, uint64_t s
 template <class SC>
 struct PolicyFp8 {
     static constexpr const char *kName = SC::kGemmTc;
-    static __device__ __forceinline__ const typename SC::T *scales_of(const Args &a) {
-        return reinterpret_cast<const typename SC::T *>(a.scales);
+    static __device__ __forceinline__ const typename SC::T *scales_of(const float *scales) {
+        return reinterpret_cast<const typename SC::T *>(scales);
     }
     // Bound on |w| over row o, |e4m3| <= 448: 448 max_k |scale_inv[o/128, k]|
     // (the same for every row of a 128-row block).  Called by a whole warp.
-    static __device__ __forceinline__ float row_bound(const Args &a, int o, int lane) {
-        const typename SC::T *src = scales_of(a) + (size_t)(o >> 7) * a.nbi;
+    static __device__ __forceinline__ float row_bound(const Args &a, const uint8_t *, const float *scales, int o,
+                                                      int lane) {
+        const typename SC::T *src = scales_of(scales) + (size_t)(o >> 7) * a.nbi;
         float b = 0.f;
 #pragma unroll 4
         for (int k = lane; k < a.nbi; k += 32) b = fmaxf(b, fabsf(SC::get(src, k)));
@@ -61,10 +62,11 @@ struct PolicyFp8 {
         const uint8_t *w;
         const typename SC::T *s;
     };
-    static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int, Row &r) {
+    static __device__ __forceinline__ void row_begin(const Args &a, const uint8_t *w, const float *scales, int o,
+                                                     int kq, int, Row &r) {
         const bool in = o < a.O;
-        r.w = in ? a.w + (size_t)o * (size_t)a.rowbytes + kq * 32 : nullptr;
-        r.s = in ? scales_of(a) + (size_t)(o >> 7) * a.nbi : nullptr;
+        r.w = in ? w + (size_t)o * (size_t)a.rowbytes + kq * 32 : nullptr;
+        r.s = in ? scales_of(scales) + (size_t)(o >> 7) * a.nbi : nullptr;
     }
     static __device__ __forceinline__ void clear(Fetch &f) {
         f.q0 = make_uint4(0u, 0u, 0u, 0u);
@@ -123,6 +125,20 @@ int run_gemm_fp8_tc(float *Y, const uint16_t *X, const uint8_t *w, const typenam
     args.nbi = (I + tc::kBK - 1) / tc::kBK;
     args.rowbytes = I;
     return tc::launch_plan<tc::PolicyFp8<SC>>(p, Y, X, args, M, I, O, ws, st);
+}
+
+template <class SC>
+int run_gemm_moe_fp8_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                        const float *const *scales, int n, int M, int I, int O, void *ws, size_t ws_bytes,
+                        cudaStream_t st, bool *taken) {
+    *taken = false;
+    for (int g = 0; g < n; ++g)
+        if (!gemm_fp8_tc_ok(X, w[g], I)) return kOk;
+    *taken = true;
+    tc::Args args{};
+    args.nbi = (I + tc::kBK - 1) / tc::kBK;
+    args.rowbytes = I;
+    return tc::launch_grouped<tc::PolicyFp8<SC>>(Y, X, args, row0, rows, w, scales, n, M, I, O, ws, ws_bytes, st);
 }
 
 }  // namespace qg

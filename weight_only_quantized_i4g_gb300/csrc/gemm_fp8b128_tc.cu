@@ -11,4 +11,15 @@ int run_gemm_fp8b128_tc(float *Y, const uint16_t *X, const uint8_t *w, const flo
     return run_gemm_fp8_tc<ScaleF32>(Y, X, w, scale_inv, M, I, O, ws, ws_bytes, st, taken);
 }
 
+size_t ws_gemm_moe_fp8(const int *rows, int n, int M, int I, int O) {
+    if (I % tc::kBKBox != 0) return 0;
+    return tc::group_plan(rows, n, M, I, O).ws_bytes;
+}
+
+int run_gemm_moe_fp8b128_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                            const float *const *scales, int n, int M, int I, int O, void *ws, size_t ws_bytes,
+                            cudaStream_t st, bool *taken) {
+    return run_gemm_moe_fp8_tc<ScaleF32>(Y, X, row0, rows, w, scales, n, M, I, O, ws, ws_bytes, st, taken);
+}
+
 }  // namespace qg

@@ -21,8 +21,9 @@ struct PolicyI4G {
     static constexpr const char *kName = "qgemm_i4g (tensor-core kernel)";
     // Bound on |w| over row o, |n - 8| <= 8: 8 max_g |scale[o, g]|.  Called by
     // a whole warp; every lane gets the result.
-    static __device__ __forceinline__ float row_bound(const Args &a, int o, int lane) {
-        const float *src = a.scales + (size_t)o * a.ng;
+    static __device__ __forceinline__ float row_bound(const Args &a, const uint8_t *, const float *scales, int o,
+                                                      int lane) {
+        const float *src = scales + (size_t)o * a.ng;
         float b = 0.f;
 #pragma unroll 4
         for (int g = lane; g < a.ng; g += 32) b = fmaxf(b, fabsf(__ldg(src + g)));
@@ -39,10 +40,11 @@ struct PolicyI4G {
         const float *s;
         int gi, gr;
     };
-    static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int pk, Row &r) {
+    static __device__ __forceinline__ void row_begin(const Args &a, const uint8_t *w, const float *scales, int o,
+                                                     int kq, int pk, Row &r) {
         const bool in = o < a.O;
-        r.w = in ? a.w + (size_t)o * (size_t)(a.rowbytes) + kq * 16 : nullptr;
-        r.s = in ? a.scales + (size_t)o * a.ng : nullptr;
+        r.w = in ? w + (size_t)o * (size_t)(a.rowbytes) + kq * 16 : nullptr;
+        r.s = in ? scales + (size_t)o * a.ng : nullptr;
         const int gq = a.gs / 32, u0 = 4 * pk + kq;
         r.gi = u0 / gq;
         r.gr = u0 - r.gi * gq;
@@ -114,6 +116,25 @@ int run_gemm_i4g_tc(float *Y, const uint16_t *X, const uint8_t *w, const float *
     args.ng = (I + gs - 1) / gs;
     args.rowbytes = I / 2;
     return tc::launch_plan<tc::PolicyI4G>(p, Y, X, args, M, I, O, ws, st);
+}
+
+size_t ws_gemm_moe_i4g(const int *rows, int n, int M, int I, int O, int gs) {
+    if (I % tc::kBKBox != 0 || gs % 32 != 0) return 0;
+    return tc::group_plan(rows, n, M, I, O).ws_bytes;
+}
+
+int run_gemm_moe_i4g_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                        const float *const *scales, int n, int M, int I, int O, int gs, void *ws, size_t ws_bytes,
+                        cudaStream_t st, bool *taken) {
+    *taken = false;
+    for (int g = 0; g < n; ++g)
+        if (!gemm_i4g_tc_ok(X, w[g], I, gs)) return kOk;
+    *taken = true;
+    tc::Args args{};
+    args.gs = gs;
+    args.ng = (I + gs - 1) / gs;
+    args.rowbytes = I / 2;
+    return tc::launch_grouped<tc::PolicyI4G>(Y, X, args, row0, rows, w, scales, n, M, I, O, ws, ws_bytes, st);
 }
 
 }  // namespace qg

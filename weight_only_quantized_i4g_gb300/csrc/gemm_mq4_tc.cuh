@@ -82,8 +82,9 @@ struct PolicyMq4 {
     static constexpr int kBlockBytes = 136;
     // Bound on |w| over row o, q in 0..15: max over the row's headers of
     // |zero| + 15 |scale|.  Called by a whole warp.
-    static __device__ __forceinline__ float row_bound(const Args &a, int o, int lane) {
-        const uint8_t *row = a.w + (size_t)o * (size_t)a.rowbytes;
+    static __device__ __forceinline__ float row_bound(const Args &a, const uint8_t *w, const float *, int o,
+                                                      int lane) {
+        const uint8_t *row = w + (size_t)o * (size_t)a.rowbytes;
         const int nb = a.Kt >> 1;
         float b = 0.f;
 #pragma unroll 4
@@ -98,8 +99,9 @@ struct PolicyMq4 {
     struct Row {
         const uint8_t *b;   // this row's blocks; the payload quarter kq added
     };
-    static __device__ __forceinline__ void row_begin(const Args &a, int o, int kq, int, Row &r) {
-        r.b = o < a.O ? a.w + (size_t)o * (size_t)a.rowbytes + 16 * kq : nullptr;
+    static __device__ __forceinline__ void row_begin(const Args &a, const uint8_t *w, const float *, int o, int kq,
+                                                     int, Row &r) {
+        r.b = o < a.O ? w + (size_t)o * (size_t)a.rowbytes + 16 * kq : nullptr;
     }
     static __device__ __forceinline__ void clear(Fetch &f) {
         f.q = make_uint4(0u, 0u, 0u, 0u);
@@ -158,6 +160,25 @@ int run_gemm_mq4_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M, i
     args.w = blocks;
     args.rowbytes = (long long)(I / 256) * tc::PolicyMq4<HK>::kBlockBytes;
     return tc::launch_plan<tc::PolicyMq4<HK>>(p, Y, X, args, M, I, O, ws, st);
+}
+
+inline size_t ws_gemm_moe_mq4_impl(const int *rows, int n, int M, int I, int O) {
+    if (I % 256 != 0) return 0;
+    return tc::group_plan(rows, n, M, I, O).ws_bytes;
+}
+
+template <int HK>
+int run_gemm_moe_mq4_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                        int n, int M, int I, int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken) {
+    *taken = false;
+    if ((uintptr_t)X % 16 != 0 || I % 256 != 0) return kOk;
+    for (int g = 0; g < n; ++g)
+        if ((uintptr_t)w[g] % 8 != 0) return kOk;
+    *taken = true;
+    const float *none[tc::kMaxGroups] = {};
+    tc::Args args{};
+    args.rowbytes = (long long)(I / 256) * tc::PolicyMq4<HK>::kBlockBytes;
+    return tc::launch_grouped<tc::PolicyMq4<HK>>(Y, X, args, row0, rows, w, none, n, M, I, O, ws, ws_bytes, st);
 }
 
 }  // namespace qg

@@ -11,4 +11,9 @@ int run_gemm_mq4v1_tc(float *Y, const uint16_t *X, const uint8_t *blocks, int M,
     return run_gemm_mq4_tc<13>(Y, X, blocks, M, I, O, ws, ws_bytes, st, taken, "qgemm_mq4v1");
 }
 
+int run_gemm_moe_mq4v1_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                          int n, int M, int I, int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken) {
+    return run_gemm_moe_mq4_tc<13>(Y, X, row0, rows, w, n, M, I, O, ws, ws_bytes, st, taken);
+}
+
 }  // namespace qg

@@ -338,6 +338,22 @@ struct Cfg {
     static_assert(kACol0 >= (uint32_t)BT && kACol0 + kStages * kACols <= kTmemCols, "tensor memory map");
 };
 
+// Routed experts in one launch: group g multiplies token rows [row0[g],
+// row0[g] + rows[g]) of X (tokens sorted by expert) by its own weights and
+// owns tiles [tile0[g], tile0[g+1]) (ceil(rows[g] / BT) token blocks times
+// the output tiles, token block fastest); its row exponents are
+// wexp[g * O + o].  n = 0: one matrix (Args::w, Args::scales, rows [0, M)).
+constexpr int kMaxGroups = 64;
+static_assert(kMaxGroups == kMoeGroupsPerLaunch, "one group table per launch");
+struct Groups {
+    int n;
+    int tile0[kMaxGroups + 1];
+    int row0[kMaxGroups];
+    int rows[kMaxGroups];
+    const uint8_t *w[kMaxGroups];
+    const float *scales[kMaxGroups];
+};
+
 struct Args {
     float *Y;
     const uint8_t *w;     // packed weights (format-specific layout)
@@ -352,8 +368,9 @@ struct Args {
     // Written by the preparation kernel:
     uint16_t *xh;         // fp16 copy of X [M, I]: x * 2^-F[m]
     float *xscale;        // 2^F[m] per token row (padded to whole 256-token blocks)
-    int *wexp;            // E[o] per weight row
+    int *wexp;            // E[o] per weight row (per group and row when grouped)
     int *err;
+    Groups grp;
 };
 
 // 2^k as an f32, |k| <= 126.
@@ -393,6 +410,38 @@ __device__ __forceinline__ void tile_coords(long long t, int MB, int cluster, in
         mb = (int)(t % MB);
         nb = (int)(t / MB);
     }
+}
+
+// Where tile t sits: its first token row m0, the end of its token rows (the
+// matrix's, or its group's), its output tile nb and its group g.
+struct TileLoc {
+    int m0, mend, nb, g;
+};
+template <int BT>
+__device__ __forceinline__ TileLoc tile_loc(const Args &a, long long t) {
+    TileLoc L;
+    if (a.grp.n == 0) {
+        int mb, nb;
+        tile_coords(t, a.MB, a.cluster, mb, nb);
+        L.m0 = mb * BT;
+        L.mend = a.M;
+        L.nb = nb;
+        L.g = 0;
+        return L;
+    }
+    int g = 0;
+    while (g + 1 < a.grp.n && t >= a.grp.tile0[g + 1]) ++g;   // groups hold at least one tile
+    const int local = (int)(t - a.grp.tile0[g]);
+    const int mbg = (a.grp.rows[g] + BT - 1) / BT;
+    L.m0 = a.grp.row0[g] + (local % mbg) * BT;
+    L.mend = a.grp.row0[g] + a.grp.rows[g];
+    L.nb = local / mbg;
+    L.g = g;
+    return L;
+}
+__device__ __forceinline__ const uint8_t *group_w(const Args &a, int g) { return a.grp.n ? a.grp.w[g] : a.w; }
+__device__ __forceinline__ const float *group_scales(const Args &a, int g) {
+    return a.grp.n ? a.grp.scales[g] : a.scales;
 }
 
 // Segment of a block's range that starts at unit u: tile t, K steps [ks, ke).
@@ -435,10 +484,9 @@ __device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, con
     using C = Cfg<BT>;
     const int row = q * 32 + lane;          // accumulator row = weight row within the tile
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-    int mb, nb;
-    tile_coords(g.t, a.MB, a.cluster, mb, nb);
-    const int m0 = mb * BT, o = nb * kMmaM + row;
-    const float pe = o < a.O ? exp2_int(-a.wexp[o]) : 0.f;   // 2^-E of this row
+    const TileLoc L = tile_loc<BT>(a, g.t);
+    const int m0 = L.m0, o = L.nb * kMmaM + row;
+    const float pe = o < a.O ? exp2_int(-a.wexp[(size_t)L.g * a.O + o]) : 0.f;   // 2^-E of this row
     // The tile's token scales into shared memory, once every epilogue warp is
     // done with the previous segment's.  With a whole tile (nslots > 1) the
     // dequantizing warps read them too, after xs_ready.
@@ -466,7 +514,7 @@ __device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, con
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int m = m0 + c * 16 + j;
-                if (m < a.M) a.Y[(size_t)m * a.O + o] = v[j] * (xs[j] * pe);
+                if (m < L.mend) a.Y[(size_t)m * a.O + o] = v[j] * (xs[j] * pe);
             }
         }
     };
@@ -567,9 +615,8 @@ __device__ __forceinline__ void store_tile_slice(const Args &a, const Seg g, con
     if (lane == 0) ok = mbar_wait_backoff(acc_full, 0u, abort) && mbar_wait_backoff(xs_ready, 0u, abort);
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) raise_device_error(a.err, kErrTimeout);
     tc_fence_after();
-    int mb, nb;
-    tile_coords(g.t, a.MB, a.cluster, mb, nb);
-    const int o = nb * kMmaM + q * 32 + lane, m0 = mb * BT;
+    const TileLoc L = tile_loc<BT>(a, g.t);
+    const int o = L.nb * kMmaM + q * 32 + lane, m0 = L.m0;
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
     for (int c = slot; c < BT / 16; c += nslots) {
@@ -581,7 +628,7 @@ __device__ __forceinline__ void store_tile_slice(const Args &a, const Seg g, con
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int m = m0 + c * 16 + j;
-                if (m < a.M) a.Y[(size_t)m * a.O + o] = __uint_as_float(r[j]) * (xs[j] * pe);
+                if (m < L.mend) a.Y[(size_t)m * a.O + o] = __uint_as_float(r[j]) * (xs[j] * pe);
             }
         }
     }
@@ -651,9 +698,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
             uint32_t it = 0;
             for (long long u = ub; u < ue;) {
                 const Seg g = segment_at(u, ue, Kt);
-                int mb, nb;
-                tile_coords(g.t, a.MB, a.cluster, mb, nb);
-                const int m0 = mb * BT;
+                const int m0 = tile_loc<BT>(a, g.t).m0;
                 for (int k = g.ks; k < g.ke; ++k, ++it) {
                     const uint32_t s = it % C::kStages, r = it / C::kStages;
                     const bool half = a.tail_half && k == Kt - 1;
@@ -739,9 +784,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         long long pu = ub, pt = ub / Kt;
         int pk = (int)(ub - pt * Kt);
         auto set_tile = [&]() {
-            int mb, nb;
-            tile_coords(pt, a.MB, a.cluster, mb, nb);
-            F::row_begin(a, nb * kMmaM + R, kq, pk, row);
+            const TileLoc L = tile_loc<BT>(a, pt);
+            F::row_begin(a, group_w(a, L.g), group_scales(a, L.g), L.nb * kMmaM + R, kq, pk, row);
         };
         if (pu < ue) set_tile();
         auto fetch = [&](Fetch &f) {
@@ -764,10 +808,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         int st_k = (int)(ub - st_t * Kt), e = 0;
         float p2 = 0.f;
         auto load_exp = [&]() {
-            int mb, nb;
-            tile_coords(st_t, a.MB, a.cluster, mb, nb);
-            const int o = nb * kMmaM + R;
-            e = o < a.O ? a.wexp[o] : 0;
+            const TileLoc L = tile_loc<BT>(a, st_t);
+            const int o = L.nb * kMmaM + R;
+            e = o < a.O ? a.wexp[(size_t)L.g * a.O + o] : 0;
             p2 = exp2_int(e);
         };
         uint32_t it = 0;
@@ -863,10 +906,12 @@ __global__ void __launch_bounds__(kPrepThreads, 8) gemm_tc_prep_kernel(Args a, c
     griddep_wait();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     if (blockIdx.x >= (unsigned)a.M) {
-        const int o = (blockIdx.x - a.M) * (kPrepThreads / 32) + wid;
-        if (o < a.O) {
-            const int e = range_exponent(F::row_bound(a, o, lane));
-            if (lane == 0) a.wexp[o] = e;
+        // weight row o of group g (one group when the call is not grouped)
+        const int go = (blockIdx.x - a.M) * (kPrepThreads / 32) + wid;
+        const int g = go / a.O, o = go - g * a.O;
+        if (g < (a.grp.n ? a.grp.n : 1)) {
+            const int e = range_exponent(F::row_bound(a, group_w(a, g), group_scales(a, g), o, lane));
+            if (lane == 0) a.wexp[go] = e;
         }
         return;
     }
@@ -954,12 +999,14 @@ inline size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 inline bool plan_splits(const Plan &p) { return !(p.U % p.P == 0 && (p.U / p.P) % p.Kt == 0); }
 
-inline void plan_layout(Plan &p, int M, int I, int O) {
+// `groups` > 0: a grouped call (one E per group and weight row; a group's last
+// token block may start anywhere, so 2^F is padded by one more block).
+inline void plan_layout(Plan &p, int M, int I, int O, int groups = 0) {
     p.counter_bytes = align256((size_t)p.T * sizeof(unsigned));
     const size_t partial_bytes = plan_splits(p) ? (size_t)2 * p.P * kMmaM * p.bt * sizeof(float) : 0;
     p.xscale_off = p.counter_bytes + partial_bytes;
-    p.wexp_off = p.xscale_off + align256((((size_t)M + 255) / 256) * 256 * sizeof(float));
-    p.xh_off = p.wexp_off + align256((size_t)O * sizeof(int));
+    p.wexp_off = p.xscale_off + align256((((size_t)M + 255) / 256 + (groups ? 1 : 0)) * 256 * sizeof(float));
+    p.xh_off = p.wexp_off + align256((size_t)(groups ? groups : 1) * O * sizeof(int));
     p.ws_bytes = p.xh_off + align256((size_t)M * I * sizeof(uint16_t));
 }
 
@@ -1092,7 +1139,8 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, Args args, int M, in
         return check_launch(F::kName);
     {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(M + (O + kPrepThreads / 32 - 1) / (kPrepThreads / 32)));
+        const long long wrows = (long long)(args.grp.n ? args.grp.n : 1) * O;
+        cfg.gridDim = dim3((unsigned)(M + (wrows + kPrepThreads / 32 - 1) / (kPrepThreads / 32)));
         cfg.blockDim = dim3(kPrepThreads);
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -1109,6 +1157,68 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, Args args, int M, in
         case kT128: return launch_tile<F, 128>(p, tmX, args, st);
         default: return launch_tile<F, 64>(p, tmX, args, st);
     }
+}
+
+// Plan of a grouped call: n groups of rows[g] > 0 token rows, M rows in all.
+// Every token block of a group dequantizes the group's whole weight tile, so
+// the tile width minimises the token blocks times the cost of a K step
+// (plan_cost's per-step figures); the tiles of all groups are one range,
+// whole tiles per block when they fit in one wave, else split evenly over
+// the SMs (stream-K).
+inline Plan group_plan(const int *rows, int n, int M, int I, int O) {
+    const int nsm = num_sms();
+    int best_tile = kT256;
+    double best = 0.0;
+    for (int t = 0; t < kNumTiles; ++t) {
+        const int bt = kTileBT[t];
+        long long blocks = 0;
+        for (int g = 0; g < n; ++g) blocks += (rows[g] + bt - 1) / bt;
+        const double c = (double)blocks * (bt == 256 ? 2300.0 : 2150.0);
+        if (t == 0 || c < best) {
+            best = c;
+            best_tile = t;
+        }
+    }
+    Plan p;
+    p.tile = best_tile;
+    p.bt = kTileBT[p.tile];
+    p.NB = (O + kMmaM - 1) / kMmaM;
+    p.Kt = (I + kBK - 1) / kBK;
+    p.MB = 0;
+    p.T = 0;
+    for (int g = 0; g < n; ++g) p.T += (long long)((rows[g] + p.bt - 1) / p.bt) * p.NB;
+    p.U = p.T * p.Kt;
+    p.P = (int)std::min<long long>(p.T <= nsm ? p.T : nsm, p.U);
+    p.cluster = 0;
+    plan_layout(p, M, I, O, n);
+    return p;
+}
+
+// A grouped call on the tensor cores: `args` carries the format's fields
+// except the weights; group g is rows [row0[g], row0[g] + rows[g]) of X and
+// Y with weights w[g] / scales[g] (rows[g] > 0, n <= kMaxGroups).
+template <class F>
+int launch_grouped(float *Y, const uint16_t *X, Args args, const int *row0, const int *rows,
+                   const uint8_t *const *w, const float *const *scales, int n, int M, int I, int O, void *ws,
+                   size_t ws_bytes, cudaStream_t st) {
+    const Plan p = group_plan(rows, n, M, I, O);
+    if (ws == nullptr || ws_bytes < p.ws_bytes) {
+        set_error_detail("%s: this grouped call needs a workspace of %zu bytes (got %zu)", F::kName, p.ws_bytes,
+                         ws == nullptr ? (size_t)0 : ws_bytes);
+        return kEWorkspace;
+    }
+    args.grp.n = n;
+    int t = 0;
+    for (int g = 0; g < n; ++g) {
+        args.grp.tile0[g] = t;
+        args.grp.row0[g] = row0[g];
+        args.grp.rows[g] = rows[g];
+        args.grp.w[g] = w[g];
+        args.grp.scales[g] = scales[g];
+        t += ((rows[g] + p.bt - 1) / p.bt) * p.NB;
+    }
+    args.grp.tile0[n] = t;
+    return launch_plan<F>(p, Y, X, args, M, I, O, ws, st);
 }
 
 }  // namespace tc

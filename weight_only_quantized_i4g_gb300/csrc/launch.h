@@ -57,6 +57,30 @@ int run_gemv_moe_mq4v1(float *y, const uint16_t *x, size_t x_stride, const void 
 int run_gemv_moe_mq4c(float *y, const uint16_t *x, size_t x_stride, const void *table, int n_experts,
                       const int *ids, int n_slots, int S, int I, int O, cudaStream_t st);
 
+// Routed-expert prefill on the tensor cores: up to kMoeGroupsPerLaunch groups
+// of token-sorted rows in one launch (row0[g], rows[g] > 0 relative to X and
+// Y; w[g], scales[g] the group's weights).  *taken is false when the shapes
+// or pointers do not suit the tensor-core kernel (nothing is launched).
+constexpr int kMoeGroupsPerLaunch = 64;
+size_t ws_gemm_moe_i4g(const int *rows, int n, int M, int I, int O, int gs);
+size_t ws_gemm_moe_fp8(const int *rows, int n, int M, int I, int O);
+size_t ws_gemm_moe_mq4(const int *rows, int n, int M, int I, int O);
+int run_gemm_moe_i4g_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                        const float *const *scales, int n, int M, int I, int O, int gs, void *ws, size_t ws_bytes,
+                        cudaStream_t st, bool *taken);
+int run_gemm_moe_fp8b128_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                            const float *const *scales, int n, int M, int I, int O, void *ws, size_t ws_bytes,
+                            cudaStream_t st, bool *taken);
+int run_gemm_moe_fp8ue8m0_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                             const float *const *scales, int n, int M, int I, int O, void *ws, size_t ws_bytes,
+                             cudaStream_t st, bool *taken);
+int run_gemm_moe_mq4v2_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                          int n, int M, int I, int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken);
+int run_gemm_moe_mq4v1_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                          int n, int M, int I, int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken);
+int run_gemm_moe_mq4c_tc(float *Y, const uint16_t *X, const int *row0, const int *rows, const uint8_t *const *w,
+                         int n, int M, int I, int O, void *ws, size_t ws_bytes, cudaStream_t st, bool *taken);
+
 int run_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, int gs, cudaStream_t st);
 int run_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, cudaStream_t st);
 int run_encode_mq4_one_header(uint8_t *blocks, const float *w, int O, int I, bool fp16_header, cudaStream_t st);
