@@ -56,6 +56,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 
 #include "common.cuh"
@@ -370,8 +371,15 @@ struct Args {
     float *xscale;        // 2^F[m] per token row (padded to whole 256-token blocks)
     int *wexp;            // E[o] per weight row (per group and row when grouped)
     int *err;
+};
+
+// The grouped kernel's arguments: the table travels only with it, so the
+// single-matrix kernels keep their small argument block.
+struct GroupedArgs : Args {
     Groups grp;
 };
+template <bool GR>
+using KArgs = typename std::conditional<GR, GroupedArgs, Args>::type;
 
 // 2^k as an f32, |k| <= 126.
 __device__ __forceinline__ float exp2_int(int k) { return __int_as_float((k + 127) << 23); }
@@ -417,10 +425,12 @@ __device__ __forceinline__ void tile_coords(long long t, int MB, int cluster, in
 struct TileLoc {
     int m0, mend, nb, g;
 };
-template <int BT>
-__device__ __forceinline__ TileLoc tile_loc(const Args &a, long long t) {
+// GR: the kernel is compiled for grouped calls (the single-matrix kernel
+// keeps the matrix's bounds in the kernel arguments, no group lookup).
+template <int BT, bool GR>
+__device__ __forceinline__ TileLoc tile_loc(const KArgs<GR> &a, long long t) {
     TileLoc L;
-    if (a.grp.n == 0) {
+    if constexpr (!GR) {
         int mb, nb;
         tile_coords(t, a.MB, a.cluster, mb, nb);
         L.m0 = mb * BT;
@@ -428,7 +438,7 @@ __device__ __forceinline__ TileLoc tile_loc(const Args &a, long long t) {
         L.nb = nb;
         L.g = 0;
         return L;
-    }
+    } else {
     int g = 0;
     while (g + 1 < a.grp.n && t >= a.grp.tile0[g + 1]) ++g;   // groups hold at least one tile
     const int local = (int)(t - a.grp.tile0[g]);
@@ -438,10 +448,17 @@ __device__ __forceinline__ TileLoc tile_loc(const Args &a, long long t) {
     L.nb = local / mbg;
     L.g = g;
     return L;
+    }
 }
-__device__ __forceinline__ const uint8_t *group_w(const Args &a, int g) { return a.grp.n ? a.grp.w[g] : a.w; }
-__device__ __forceinline__ const float *group_scales(const Args &a, int g) {
-    return a.grp.n ? a.grp.scales[g] : a.scales;
+template <bool GR>
+__device__ __forceinline__ const uint8_t *group_w(const KArgs<GR> &a, int g) {
+    if constexpr (GR) return a.grp.w[g];
+    else return a.w;
+}
+template <bool GR>
+__device__ __forceinline__ const float *group_scales(const KArgs<GR> &a, int g) {
+    if constexpr (GR) return a.grp.scales[g];
+    else return a.scales;
 }
 
 // Segment of a block's range that starts at unit u: tile t, K steps [ks, ke).
@@ -474,8 +491,8 @@ __device__ __forceinline__ void load_xscale16(const float *p, float (&xs)[16]) {
 // for the accumulator, then either store it to Y (the whole K range is this
 // block's) or go through the partial slots.  `et` numbers the 128
 // participating threads.
-template <int BT>
-__device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, const uint32_t seg, const uint32_t tmem,
+template <int BT, bool GR>
+__device__ __forceinline__ void epilogue_segment(const KArgs<GR> &a, const Seg g, const uint32_t seg, const uint32_t tmem,
                                               const int q, const int lane, const int et, const long long cta,
                                               const long long U, const long long P, const int Kt,
                                               uint64_t *acc_full, uint64_t *acc_empty, volatile uint32_t *flag,
@@ -484,7 +501,7 @@ __device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, con
     using C = Cfg<BT>;
     const int row = q * 32 + lane;          // accumulator row = weight row within the tile
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-    const TileLoc L = tile_loc<BT>(a, g.t);
+    const TileLoc L = tile_loc<BT, GR>(a, g.t);
     const int m0 = L.m0, o = L.nb * kMmaM + row;
     const float pe = o < a.O ? exp2_int(-a.wexp[(size_t)L.g * a.O + o]) : 0.f;   // 2^-E of this row
     // The tile's token scales into shared memory, once every epilogue warp is
@@ -606,8 +623,8 @@ __device__ __forceinline__ void epilogue_segment(const Args &a, const Seg g, con
 // The part of a whole tile's store that a dequantizing warp takes once its
 // block has no K steps left: chunks slot, slot + nslots, ... of its lane
 // quarter, after the accumulator is complete.
-template <int BT>
-__device__ __forceinline__ void store_tile_slice(const Args &a, const Seg g, const uint32_t tmem, const int q,
+template <int BT, bool GR>
+__device__ __forceinline__ void store_tile_slice(const KArgs<GR> &a, const Seg g, const uint32_t tmem, const int q,
                                                  const int lane, const int slot, const int nslots,
                                                  uint64_t *acc_full, volatile uint32_t *abort, const float *sxs,
                                                  uint64_t *xs_ready, const float pe) {
@@ -615,7 +632,7 @@ __device__ __forceinline__ void store_tile_slice(const Args &a, const Seg g, con
     if (lane == 0) ok = mbar_wait_backoff(acc_full, 0u, abort) && mbar_wait_backoff(xs_ready, 0u, abort);
     if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) && lane == 0) raise_device_error(a.err, kErrTimeout);
     tc_fence_after();
-    const TileLoc L = tile_loc<BT>(a, g.t);
+    const TileLoc L = tile_loc<BT, GR>(a, g.t);
     const int o = L.nb * kMmaM + q * 32 + lane, m0 = L.m0;
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
@@ -635,9 +652,9 @@ __device__ __forceinline__ void store_tile_slice(const Args &a, const Seg g, con
     tc_fence_before();
 }
 
-template <class F, int BT>
+template <class F, int BT, bool GR>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, KArgs<GR> a) {
     using C = Cfg<BT>;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_base = smem_addr(smem_raw);
@@ -698,7 +715,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
             uint32_t it = 0;
             for (long long u = ub; u < ue;) {
                 const Seg g = segment_at(u, ue, Kt);
-                const int m0 = tile_loc<BT>(a, g.t).m0;
+                const int m0 = tile_loc<BT, GR>(a, g.t).m0;
                 for (int k = g.ks; k < g.ke; ++k, ++it) {
                     const uint32_t s = it % C::kStages, r = it / C::kStages;
                     const bool half = a.tail_half && k == Kt - 1;
@@ -765,7 +782,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         uint32_t seg = 0;
         for (long long u = ub; u < ue; ++seg) {
             const Seg g = segment_at(u, ue, Kt);
-            epilogue_segment<BT>(a, g, seg, tmem, warp & 3, lane, threadIdx.x - 32 * kWarpEpi, cta, U, P, Kt,
+            epilogue_segment<BT, GR>(a, g, seg, tmem, warp & 3, lane, threadIdx.x - 32 * kWarpEpi, cta, U, P, Kt,
                                     acc_full, acc_empty, flag, abort, whole_only ? kEpiSlots : 1, sxs, xs_ready);
             u = g.t * Kt + g.ke;
         }
@@ -784,8 +801,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         long long pu = ub, pt = ub / Kt;
         int pk = (int)(ub - pt * Kt);
         auto set_tile = [&]() {
-            const TileLoc L = tile_loc<BT>(a, pt);
-            F::row_begin(a, group_w(a, L.g), group_scales(a, L.g), L.nb * kMmaM + R, kq, pk, row);
+            const TileLoc L = tile_loc<BT, GR>(a, pt);
+            F::row_begin(a, group_w<GR>(a, L.g), group_scales<GR>(a, L.g), L.nb * kMmaM + R, kq, pk, row);
         };
         if (pu < ue) set_tile();
         auto fetch = [&](Fetch &f) {
@@ -808,7 +825,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
         int st_k = (int)(ub - st_t * Kt), e = 0;
         float p2 = 0.f;
         auto load_exp = [&]() {
-            const TileLoc L = tile_loc<BT>(a, st_t);
+            const TileLoc L = tile_loc<BT, GR>(a, st_t);
             const int o = L.nb * kMmaM + R;
             e = o < a.O ? a.wexp[(size_t)L.g * a.O + o] : 0;
             p2 = exp2_int(e);
@@ -854,7 +871,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
             ++u;
         }
         if (whole_only)
-            store_tile_slice<BT>(a, segment_at(ub, ue, Kt), tmem, q, lane, 1 + kq, kEpiSlots, acc_full, abort, sxs,
+            store_tile_slice<BT, GR>(a, segment_at(ub, ue, Kt), tmem, q, lane, 1 + kq, kEpiSlots, acc_full, abort, sxs,
                                  xs_ready, exp2_int(-e));
     }
 
@@ -895,8 +912,9 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 v, float sc) {
     return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
-template <class F>
-__global__ void __launch_bounds__(kPrepThreads, 8) gemm_tc_prep_kernel(Args a, const uint16_t *__restrict__ X, int I) {
+template <class F, bool GR>
+__global__ void __launch_bounds__(kPrepThreads, 8) gemm_tc_prep_kernel(KArgs<GR> a, const uint16_t *__restrict__ X,
+                                                                         int I) {
     // The main kernel may launch once every block of this one runs (its
     // blocks take an SM as this kernel's leave it); it waits for this grid's
     // completion before it reads what this one writes.
@@ -909,8 +927,10 @@ __global__ void __launch_bounds__(kPrepThreads, 8) gemm_tc_prep_kernel(Args a, c
         // weight row o of group g (one group when the call is not grouped)
         const int go = (blockIdx.x - a.M) * (kPrepThreads / 32) + wid;
         const int g = go / a.O, o = go - g * a.O;
-        if (g < (a.grp.n ? a.grp.n : 1)) {
-            const int e = range_exponent(F::row_bound(a, group_w(a, g), group_scales(a, g), o, lane));
+        int ngroups = 1;
+        if constexpr (GR) ngroups = a.grp.n;
+        if (g < ngroups) {
+            const int e = range_exponent(F::row_bound(a, group_w<GR>(a, g), group_scales<GR>(a, g), o, lane));
             if (lane == 0) a.wexp[go] = e;
         }
         return;
@@ -1069,14 +1089,14 @@ inline Plan choose_plan(int M, int I, int O) {
     return best;
 }
 
-template <class F, int BT>
-int launch_tile(const Plan &p, const CUtensorMap &tmX, const Args &args, cudaStream_t st) {
+template <class F, int BT, bool GR>
+int launch_tile(const Plan &p, const CUtensorMap &tmX, const KArgs<GR> &args, cudaStream_t st) {
     using C = Cfg<BT>;
     static std::once_flag attr_once[64];
     int dev = 0;
     cudaGetDevice(&dev);
     std::call_once(attr_once[dev & 63], [] {
-        cudaFuncSetAttribute(gemm_tc_kernel<F, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gemm_tc_kernel<F, BT, GR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::kSmemBytes);
     });
     cudaLaunchConfig_t cfg = {};
@@ -1093,14 +1113,14 @@ int launch_tile(const Plan &p, const CUtensorMap &tmX, const Args &args, cudaStr
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = p.cluster ? 2 : 1;
-    cudaLaunchKernelEx(&cfg, gemm_tc_kernel<F, BT>, tmX, args);
+    cudaLaunchKernelEx(&cfg, gemm_tc_kernel<F, BT, GR>, tmX, args);
     return check_launch(F::kName);
 }
 
 // Launch plan `p` for X [M, I] bf16 and Y [M, O] f32; `args` carries the
 // format's fields (w, scales, gs, ng, nbi) and is completed here.
-template <class F>
-int launch_plan(const Plan &p, float *Y, const uint16_t *X, Args args, int M, int I, int O, void *ws,
+template <class F, bool GR = false>
+int launch_plan(const Plan &p, float *Y, const uint16_t *X, KArgs<GR> args, int M, int I, int O, void *ws,
                 cudaStream_t st) {
     auto encode = encode_fn();
     if (!encode) {
@@ -1139,7 +1159,8 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, Args args, int M, in
         return check_launch(F::kName);
     {
         cudaLaunchConfig_t cfg = {};
-        const long long wrows = (long long)(args.grp.n ? args.grp.n : 1) * O;
+        long long wrows = O;
+        if constexpr (GR) wrows *= args.grp.n;
         cfg.gridDim = dim3((unsigned)(M + (wrows + kPrepThreads / 32 - 1) / (kPrepThreads / 32)));
         cfg.blockDim = dim3(kPrepThreads);
         cfg.stream = st;
@@ -1148,14 +1169,14 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, Args args, int M, in
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, gemm_tc_prep_kernel<F>, args, X, I);
+        cudaLaunchKernelEx(&cfg, gemm_tc_prep_kernel<F, GR>, args, X, I);
         const int rc = check_launch(F::kName);
         if (rc != kOk) return rc;
     }
     switch (p.tile) {
-        case kT256: return launch_tile<F, 256>(p, tmX, args, st);
-        case kT128: return launch_tile<F, 128>(p, tmX, args, st);
-        default: return launch_tile<F, 64>(p, tmX, args, st);
+        case kT256: return launch_tile<F, 256, GR>(p, tmX, args, st);
+        case kT128: return launch_tile<F, 128, GR>(p, tmX, args, st);
+        default: return launch_tile<F, 64, GR>(p, tmX, args, st);
     }
 }
 
@@ -1198,7 +1219,7 @@ inline Plan group_plan(const int *rows, int n, int M, int I, int O) {
 // except the weights; group g is rows [row0[g], row0[g] + rows[g]) of X and
 // Y with weights w[g] / scales[g] (rows[g] > 0, n <= kMaxGroups).
 template <class F>
-int launch_grouped(float *Y, const uint16_t *X, Args args, const int *row0, const int *rows,
+int launch_grouped(float *Y, const uint16_t *X, const Args &base, const int *row0, const int *rows,
                    const uint8_t *const *w, const float *const *scales, int n, int M, int I, int O, void *ws,
                    size_t ws_bytes, cudaStream_t st) {
     const Plan p = group_plan(rows, n, M, I, O);
@@ -1207,6 +1228,8 @@ int launch_grouped(float *Y, const uint16_t *X, Args args, const int *row0, cons
                          ws == nullptr ? (size_t)0 : ws_bytes);
         return kEWorkspace;
     }
+    GroupedArgs args{};
+    static_cast<Args &>(args) = base;
     args.grp.n = n;
     int t = 0;
     for (int g = 0; g < n; ++g) {
@@ -1218,7 +1241,7 @@ int launch_grouped(float *Y, const uint16_t *X, Args args, const int *row0, cons
         t += ((rows[g] + p.bt - 1) / p.bt) * p.NB;
     }
     args.grp.tile0[n] = t;
-    return launch_plan<F>(p, Y, X, args, M, I, O, ws, st);
+    return launch_plan<F, true>(p, Y, X, args, M, I, O, ws, st);
 }
 
 }  // namespace tc
