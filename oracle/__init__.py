@@ -68,6 +68,10 @@ def _declare(lib):
     lib.oracle_encode_mq4v1.argtypes = [P, P, i, i]
     lib.oracle_encode_mq4c.argtypes = [P, P, i, i]
     lib.oracle_qgemv_moe.argtypes = [i, P, P, P, z, P, P, i, P, i, i, i, i, i]
+    lib.oracle_q2_0_weight.argtypes = [P, i]
+    lib.oracle_q2_0_weight.restype = ctypes.c_double
+    lib.oracle_qgemv_q2_0.argtypes = [P, P, P, P, i, i, i]
+    lib.oracle_encode_q2_0.argtypes = [P, P, i, i]
     lib.oracle_qgemm_moe.argtypes = [i, P, P, P, P, P, i, P, P, i, i, i, i]
     lib.oracle_fwht256.argtypes = [P, P, P, z]
     lib.oracle_ifwht256.argtypes = [P, P, P, z]
@@ -257,6 +261,29 @@ class Oracle:
         w = np.ascontiguousarray(w, np.float32)
         blocks = np.empty((O, (I // 256) * 136), np.uint8)
         self.lib.oracle_encode_mq4c(_p(blocks), _p(w), O, I)
+        return blocks
+
+    # Q2_0 -------------------------------------------------------------------
+    def q2_0_weight(self, block: np.ndarray, e: int) -> float:
+        block = np.ascontiguousarray(block, np.uint8)
+        return self.lib.oracle_q2_0_weight(_p(block), e)
+
+    def qgemv_q2_0(self, x_bf16, blocks, S, I, O, rows=None):
+        x = np.ascontiguousarray(x_bf16, np.uint16)
+        blocks = np.ascontiguousarray(blocks, np.uint8)
+        o0, o1 = rows if rows is not None else (0, O)
+        rowbytes = (I // 64) * 18
+        bs = np.ascontiguousarray(blocks.reshape(O, rowbytes)[o0:o1])
+        n = o1 - o0
+        y = np.empty((S, n), np.float64)
+        mag = np.empty((S, n), np.float64)
+        self.lib.oracle_qgemv_q2_0(_p(y), _p(mag), _p(x), _p(bs), S, I, n)
+        return y, mag
+
+    def encode_q2_0(self, w, O, I):
+        w = np.ascontiguousarray(w, np.float32)
+        blocks = np.empty((O, (I // 64) * 18), np.uint8)
+        self.lib.oracle_encode_q2_0(_p(blocks), _p(w), O, I)
         return blocks
 
     # routed experts -----------------------------------------------------------

@@ -17,6 +17,7 @@
  *   [colibri #528]  "fmt=7: fp8-e4m3-b128 passthrough weight format", Design
  *                   (f32 block scales, and the UE8M0 scale encoding it names)
  *   [hipfire MQ4V2] "MQ4 V2" docs, sections 1b, 1c, 1e, 2, 3, 4, 9
+ *   [strata Q2_0]   strata review, "convert_k256_q2_0.cpp vs ref_quant.cpp" (2.5)
  *
  * No function here blocks, fuses or reorders beyond what its definition
  * states; loops run in the order the definition reads.
@@ -249,6 +250,93 @@ void oracle_qgemv_fp8b128(double *y, double *mag, const uint16_t *x, const uint8
             mag[(size_t)s * O + o] = m;
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q2_0 ([strata Q2_0]: the ggml Q2_0 codec the review checks)                */
+/*                                                                           : 18 bytes per 64 weights, little-endian:                  */
+/*     [0,2)   fp16 d                                                         */
+/*     [2,18)  16 bytes of 2-bit codes; weight e of the block sits in byte    */
+/*             2 + e/4 at bit 2*(e%4)                                         */
+/*   w_e = (code_e - 1) * d   (the asymmetric grid {-1, 0, 1, 2} * d).        */
+/*   Row o holds I/64 blocks back to back; I must be a multiple of 64.        */
+/* ------------------------------------------------------------------------ */
+double oracle_q2_0_weight(const uint8_t *block, int e)
+{
+    double d = oracle_f16_value((uint16_t)(block[0] | (block[1] << 8)));
+    int code = (block[2 + e / 4] >> (2 * (e % 4))) & 3;
+    return (double)(code - 1) * d;
+}
+
+void oracle_qgemv_q2_0(double *y, double *mag, const uint16_t *x, const uint8_t *blocks, int S, int I, int O)
+{
+    const size_t nb = (size_t)I / 64;
+    for (int s = 0; s < S; ++s)
+        for (int o = 0; o < O; ++o) {
+            double acc = 0.0, m = 0.0;
+            for (int i = 0; i < I; ++i) {
+                double t = oracle_q2_0_weight(blocks + ((size_t)o * nb + (size_t)(i / 64)) * 18, i % 64) *
+                           oracle_bf16_value(x[(size_t)s * I + i]);
+                acc += t;
+                m += fabs(t);
+            }
+            y[(size_t)s * O + o] = acc;
+            mag[(size_t)s * O + o] = m;
+        }
+}
+
+/* Encoder (the same review, 2.5: "searches d in {0.5 ... 1.0} * amax (9
+ * steps) for minimal SSE on the asymmetric {-1,0,1,2} grid ... the error is
+ * evaluated with the unrounded d").  Reading: per block amax = max |w|
+ * (binary32); for k = 0..8 the candidate d_k = amax * (0.5 + k/16) (binary32),
+ * codes c = clamp(rint(w / d_k) + 1, 0, 3) (binary32 division and rint),
+ * SSE = sum (w - (c - 1) d_k)^2 in double; the first candidate with the
+ * smallest SSE wins; its codes are stored with fp16(d_k) (round to nearest
+ * even).  An all-zero block stores d = 0 and codes 1.                        */
+void oracle_encode_q2_0(uint8_t *blocks, const float *w, int O, int I)
+{
+    const size_t nb = (size_t)I / 64;
+    for (int o = 0; o < O; ++o)
+        for (size_t b = 0; b < nb; ++b) {
+            const float *v = w + (size_t)o * I + b * 64;
+            uint8_t *out = blocks + ((size_t)o * nb + b) * 18;
+            float amax = 0.0f;
+            for (int e = 0; e < 64; ++e)
+                amax = fabsf(v[e]) > amax ? fabsf(v[e]) : amax;
+            int best_code[64];
+            float best_d = 0.0f;
+            for (int e = 0; e < 64; ++e)
+                best_code[e] = 1;
+            if (amax > 0.0f) {
+                double best_sse = INFINITY;
+                for (int k = 0; k <= 8; ++k) {
+                    volatile float frac = 0.5f + (float)k / 16.0f;
+                    volatile float d = amax * frac;
+                    int code[64];
+                    double sse = 0.0;
+                    for (int e = 0; e < 64; ++e) {
+                        volatile float r = v[e] / d;
+                        float q = rintf(r) + 1.0f;
+                        int c = q < 0.0f ? 0 : q > 3.0f ? 3 : (int)q;
+                        code[e] = c;
+                        double err = (double)v[e] - (double)(c - 1) * (double)d;
+                        sse += err * err;
+                    }
+                    if (sse < best_sse) {
+                        best_sse = sse;
+                        best_d = d;
+                        for (int e = 0; e < 64; ++e)
+                            best_code[e] = code[e];
+                    }
+                }
+            }
+            uint16_t d16 = oracle_f16_from_f32(best_d);
+            out[0] = (uint8_t)(d16 & 0xFF);
+            out[1] = (uint8_t)(d16 >> 8);
+            for (int j = 0; j < 16; ++j)
+                out[2 + j] = (uint8_t)(best_code[4 * j] | (best_code[4 * j + 1] << 2) | (best_code[4 * j + 2] << 4) |
+                                       (best_code[4 * j + 3] << 6));
+        }
 }
 
 /* ------------------------------------------------------------------------ */

@@ -653,6 +653,94 @@ def pin_mq4c_encoder(orc):
 # FWHT rotation
 # ---------------------------------------------------------------------------
 
+def _dequant_q2_0_numpy(blocks, O, I):
+    """numpy decode of Q2_0 rows from the layout description."""
+    nb = I // 64
+    b = np.asarray(blocks, np.uint8).reshape(O, nb, 18)
+    d = b[:, :, 0:2].copy().view(np.float16)[:, :, 0].astype(np.float64)          # [O, nb]
+    qs = b[:, :, 2:18].astype(np.int64)                                            # [O, nb, 16]
+    codes = np.stack([(qs >> (2 * k)) & 3 for k in range(4)], axis=-1).reshape(O, nb, 64)   # element 4j + k
+    return ((codes - 1) * d[:, :, None]).reshape(O, I)
+
+
+def pin_q2_0_golden(orc):
+    g = _golden("q2_0_hand.json")
+    for c in g["cases"]:
+        I = c["I"]
+        blocks = np.zeros(I // 64 * 18, np.uint8)
+        if "d_bits" in c:
+            blocks[0:2] = np.array([c["d_bits"]], np.uint16).view(np.uint8)
+            blocks[2:18] = c["fill"]
+            for k, v in c["codes"].items():
+                blocks[2 + int(k)] = v
+        else:
+            blocks[2:18] = 0x55                                   # block 0: weights 0
+            blocks[18:20] = np.array([c["block1_d_bits"]], np.uint16).view(np.uint8)
+            for k, v in c["block1_codes"].items():
+                blocks[18 + 2 + int(k)] = v
+        x = np.zeros(I, np.float32)
+        for k, v in c["x"].items():
+            x[int(k)] = v
+        y, mag = orc.qgemv_q2_0(synth.bf16_bits(x), blocks, 1, I, 1)
+        assert y[0, 0] == c["y"] and mag[0, 0] == c["mag"], (c["name"], y, mag)
+
+
+def pin_q2_0_size_and_bruteforce(orc):
+    """18 bytes per 64 weights; oracle GEMV == numpy decode + matmul on random
+    codes and fp16 d over several blocks and rows."""
+    rng = np.random.default_rng(61)
+    for (O, I, S) in [(1, 64, 1), (3, 128, 2), (4, 640, 3), (2, 2560, 8)]:
+        w = synth.normal(int(rng.integers(1 << 30)), O * I, 0.02)
+        blocks = orc.encode_q2_0(w, O, I)
+        assert blocks.size == 18 * O * I // 64
+        b = blocks.reshape(O, I // 64, 18)
+        b[:, :, 2:] = rng.integers(0, 256, (O, I // 64, 16), dtype=np.uint8)
+        b[:, :, 0:2] = rng.uniform(1e-3, 1e-1, (O, I // 64, 1)).astype(np.float16).view(np.uint8)
+        xb = synth.bf16_bits(rng.standard_normal(S * I).astype(np.float32))
+        y, mag = orc.qgemv_q2_0(xb, blocks, S, I, O)
+        W = _dequant_q2_0_numpy(blocks, O, I)
+        X = synth.bf16_to_f32(xb).reshape(S, I).astype(np.float64)
+        _close(y, X @ W.T, np.abs(X) @ np.abs(W).T, what=f"q2_0 O={O} I={I}")
+
+
+def pin_q2_0_encoder(orc):
+    """Codes on the grid; a block whose weights are (c - 1) * d with an
+    fp16-exact d and at least one code 3 round-trips bit-exactly (amax = 2d is
+    the first candidate, SSE 0); an all-zero block stores d = 0, codes 1; the
+    stored codes give the smallest SSE of the nine candidates (recomputed here
+    with numpy)."""
+    rng = np.random.default_rng(62)
+    O, I = 3, 192
+    d = np.array([0.25, 0.0625, 1.5], np.float16).astype(np.float32)
+    codes = rng.integers(0, 4, (O, I)).astype(np.int64)
+    codes[:, ::64] = 3
+    w = ((codes - 1) * d[:, None]).astype(np.float32)
+    blocks = orc.encode_q2_0(w, O, I)
+    assert np.array_equal(_dequant_q2_0_numpy(blocks, O, I), w.astype(np.float64))
+    z = orc.encode_q2_0(np.zeros((1, 64), np.float32), 1, 64)
+    assert z[0, 0] == 0 and z[0, 1] == 0 and (z[0, 2:] == 0x55).all()
+    w = synth.normal(63, 8 * 256, 0.02).reshape(8, 256)
+    blocks = orc.encode_q2_0(w, 8, 256)
+    W = _dequant_q2_0_numpy(blocks, 8, 256)
+    vb = w.reshape(8, 4, 64).astype(np.float32)
+    for o in range(8):
+        for b in range(4):
+            v = vb[o, b]
+            amax = np.float32(np.abs(v).max())
+            sses = []
+            for k in range(9):
+                dk = np.float32(amax * np.float32(np.float32(0.5) + np.float32(k) / np.float32(16)))
+                c = np.clip(np.rint(v / dk) + 1, 0, 3)
+                sses.append(float(((v.astype(np.float64) - (c - 1) * np.float64(dk)) ** 2).sum()))
+            best = int(np.argmin(sses))
+            dk = np.float32(amax * np.float32(np.float32(0.5) + np.float32(best) / np.float32(16)))
+            want_codes = np.clip(np.rint(v / dk) + 1, 0, 3).astype(np.int64)
+            got = blocks.reshape(8, 4, 18)[o, b]
+            got_codes = np.stack([(got[2:].astype(np.int64) >> (2 * k)) & 3 for k in range(4)], -1).reshape(64)
+            assert np.array_equal(got_codes, want_codes), (o, b)
+            assert got[0:2].copy().view(np.float16)[0] == np.float16(dk)
+
+
 def _moe_experts(rng, fmt, n_experts, O, I, gs):
     """Random experts of one format: (weights, scales, numpy dequantizer)."""
     ws, ss, deq = [], [], []

@@ -52,6 +52,14 @@ MUTATIONS = [
      "double sc = (double)scale_inv[((size_t)(o / 128) * nbi + (size_t)(i / 64)) % (nbi * (((size_t)O + 127) / 128))];"),
     ("moe_gemm_rows_from_zero", "const uint16_t *xg = X + (size_t)off[g] * I;", "const uint16_t *xg = X;"),
     ("moe_gemm_expert_of_slot", "const int e = group_expert[g];", "const int e = group_expert[0];"),
+    # Q2_0
+    ("q2_0_no_offset", "    return (double)(code - 1) * d;\n}", "    return (double)code * d;\n}"),
+    ("q2_0_shift_k", "int code = (block[2 + e / 4] >> (2 * (e % 4))) & 3;", "int code = (block[2 + e / 4] >> (e % 4)) & 3;"),
+    ("q2_0_byte_transposed", "int code = (block[2 + e / 4] >> (2 * (e % 4))) & 3;",
+     "int code = (block[2 + (e % 16)] >> (2 * (e / 16))) & 3;"),
+    ("q2_0_stride_16", "double t = oracle_q2_0_weight(blocks + ((size_t)o * nb + (size_t)(i / 64)) * 18, i % 64) *",
+     "double t = oracle_q2_0_weight(blocks + ((size_t)o * nb + (size_t)(i / 64)) * 16, i % 64) *"),
+    ("q2_0_encoder_steps_8", "volatile float frac = 0.5f + (float)k / 16.0f;", "volatile float frac = 0.5f + (float)k / 8.0f;"),
     # UE8M0 scales
     ("e8m0_bias_126", "return ldexp(1.0, (int)e - 127);", "return ldexp(1.0, (int)e - 126);"),
     ("e8m0_no_nan", "    if (e == 255)\n        return NAN;\n    return ldexp", "    if (e == 256)\n        return NAN;\n    return ldexp"),
