@@ -11,6 +11,8 @@
  *   MQ4-V2 (qt=44)          hipfire docs "MQ4 V2", sections 2, 3, 4
  *   MQ4 v1 (qt=13),         hipfire docs "MQ4 V2", sections 1b, 1c, 1e
  *   MQ4C pad (qt=45)
+ *   Q2_0                    strata review, "convert_k256_q2_0.cpp vs
+ *                           ref_quant.cpp" (2.5)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -90,7 +92,8 @@ enum {
                             /* the page's second scale encoding; a library id) */
     QG_FMT_MQ4V1 = 13,      /* MQ4 v1 (qt=13)                                  */
     QG_FMT_MQ4V2 = 44,      /* MQ4-V2 (qt=44)                                  */
-    QG_FMT_MQ4C = 45        /* MQ4C pad (qt=45)                                */
+    QG_FMT_MQ4C = 45,       /* MQ4C pad (qt=45)                                */
+    QG_FMT_Q2_0 = 20        /* Q2_0 codec, 2.25 bits per weight (a library id) */
 };
 
 /* Bytes of workspace that the GEMV entry point of format `fmt` needs for
@@ -179,6 +182,23 @@ int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *sc
 /* ------------------------------------------------------------------------ */
 int qgemv_fp8ue8m0(float *y, const uint16_t *x, const uint8_t *w, const uint8_t *scale_e8m0,
                    int S, int I, int O, void *ws, size_t ws_bytes, qg_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Q2_0 codec, decode GEMV                                                  */
+/* strata review, "convert_k256_q2_0.cpp vs ref_quant.cpp" (2.5): the ggml  */
+/* Q2_0 layout of the routed experts it checks.                             */
+/*                                                                          */
+/*   blocks  uint8 [O, I/64 * 18]: each 64-weight block is an fp16 d (bytes  */
+/*           0-1, little-endian) and 16 bytes of 2-bit codes; weight e of   */
+/*           the block sits in byte 2 + e/4 at bit 2*(e%4)                  */
+/*   x       bf16 [S, I];  y  f32 [S, O]                                    */
+/*   y[s,o] = sum_i (code(o,i) - 1) * d(o, i/64) * x[s,i]                    */
+/*   I       multiple of 64 (else QG_ESHAPE); S any >= 1                     */
+/* Alignment: y 4-byte, x and blocks 2-byte.  Workspace: qg_workspace_bytes */
+/* (QG_FMT_Q2_0, ...) when the row is split across thread blocks.           */
+/* ------------------------------------------------------------------------ */
+int qgemv_q2_0(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O,
+               void *ws, size_t ws_bytes, qg_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Routed experts: many decode GEMVs of one format and shape in one launch  */

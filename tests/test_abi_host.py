@@ -34,7 +34,7 @@ def test_header_lists_the_entry_points():
     for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qgemm_fp8b128", "qgemm_mq4v2",
                  "qg_workspace_bytes", "qg_gemm_workspace_bytes", "qg_device_status",
                  "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256",
-                 "qgemv_moe", "qgemm_moe"]:
+                 "qgemv_moe", "qgemm_moe", "qgemv_q2_0"]:
         assert must in names, names
 
 
@@ -101,6 +101,15 @@ def test_fp8ue8m0_refusals(qg):
     assert qg.qgemv_fp8ue8m0(P, P, P, P, 1, 256, 0, stream=0) == qg.QG_EINVAL
     assert qg.qgemm_fp8ue8m0(P, P, P, P, 0, 256, 4, stream=0) == qg.QG_EINVAL
     assert qg.qgemm_fp8ue8m0(P + 2, P, P, P, 4, 256, 4, stream=0) == qg.QG_EALIGN
+
+
+def test_q2_0_refusals(qg):
+    P = POISON
+    assert qg.qgemv_q2_0(P, P, P, 1, 100, 4, stream=0) == qg.QG_ESHAPE
+    assert "100" in qg.last_error()
+    assert qg.qgemv_q2_0(P, P, P + 1, 1, 128, 4, stream=0) == qg.QG_EALIGN
+    assert qg.qgemv_q2_0(P, P, None, 1, 128, 4, stream=0) == qg.QG_EINVAL
+    assert qg.qgemv_q2_0(P, P, P, 0, 128, 4, stream=0) == qg.QG_EINVAL
 
 
 def test_moe_refusals(qg):

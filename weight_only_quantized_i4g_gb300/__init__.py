@@ -25,7 +25,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 QG_OK, QG_EINVAL, QG_EGS, QG_ESHAPE, QG_EALIGN, QG_EWORKSPACE, QG_ECUDA, QG_ETIMEOUT, QG_EEXPERT = (
     0, -1, -2, -3, -4, -5, -6, -7, -8)
-QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_FP8UE8M0, QG_FMT_MQ4V1, QG_FMT_MQ4V2, QG_FMT_MQ4C = 4, 7, 71, 13, 44, 45
+QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_FP8UE8M0, QG_FMT_MQ4V1, QG_FMT_MQ4V2, QG_FMT_MQ4C, QG_FMT_Q2_0 = (
+    4, 7, 71, 13, 44, 45, 20)
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -48,6 +49,7 @@ _SIGNATURES = {
     "qgemv_mq4c": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_mq4v1": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_mq4c": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
+    "qgemv_q2_0": ([_P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_fp8ue8m0": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemm_fp8ue8m0": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_moe": ([_I, _P, _P, _Z, _P, _I, _P, _I, _I, _I, _I, _I, _P], _I),
@@ -130,6 +132,10 @@ def qgemv_i4g(y, x, w, scales, S, I, O, gs, ws=None, ws_bytes=0, stream=None) ->
 
 def qgemv_i4g_noalloc(y, x, w, scales, S, I, O, gs, stream=None) -> int:
     return _lib.qgemv_i4g_noalloc(_ptr(y), _ptr(x), _ptr(w), _ptr(scales), S, I, O, gs, _stream(stream))
+
+
+def qgemv_q2_0(y, x, blocks, S, I, O, ws=None, ws_bytes=0, stream=None) -> int:
+    return _lib.qgemv_q2_0(_ptr(y), _ptr(x), _ptr(blocks), S, I, O, _ptr(ws), ws_bytes, _stream(stream))
 
 
 def qgemv_fp8ue8m0(y, x, w, scale_e8m0, S, I, O, ws=None, ws_bytes=0, stream=None) -> int:

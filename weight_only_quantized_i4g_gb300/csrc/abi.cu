@@ -176,6 +176,7 @@ size_t qg_workspace_bytes(int fmt, int S, int I, int O, int gs) {
         case QG_FMT_MQ4V2: return (I % 256 == 0) ? ws_mq4v2(S, I, O) : 0;
         case QG_FMT_MQ4V1: return (I % 256 == 0) ? ws_mq4v1(S, I, O) : 0;
         case QG_FMT_MQ4C: return (I % 256 == 0) ? ws_mq4c(S, I, O) : 0;
+        case QG_FMT_Q2_0: return (I % 64 == 0) ? ws_q2_0(S, I, O) : 0;
         default: return 0;
     }
 }
@@ -218,6 +219,20 @@ int qgemv_fp8b128(float *y, const uint16_t *x, const uint8_t *w, const float *sc
     if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
     cudaGetLastError();
     return run_gemv_fp8b128(y, x, w, scale_inv, S, I, O, ws, ws_bytes, as_stream(stream));
+}
+
+int qgemv_q2_0(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws, size_t ws_bytes,
+               qg_stream_t stream) {
+    const char *fn = "qgemv_q2_0";
+    int rc = check_dims(fn, "S", S, I, O);
+    if (rc) return rc;
+    if (I % 64) QG_REFUSE(kEShape, "%s: I = %d is not a multiple of 64", fn, I);
+    if (!y || !x || !blocks) QG_REFUSE(kEInval, "%s: y, x and blocks must be non-NULL", fn);
+    if (!aligned(y, 4) || !aligned(x, 2) || !aligned(blocks, 2))
+        QG_REFUSE(kEAlign, "%s: y must be 4-byte, x and blocks 2-byte aligned", fn);
+    if (ws && !aligned(ws, 256)) QG_REFUSE(kEAlign, "%s: workspace must be 256-byte aligned", fn);
+    cudaGetLastError();
+    return run_gemv_q2_0(y, x, blocks, S, I, O, ws, ws_bytes, as_stream(stream));
 }
 
 int qgemv_fp8ue8m0(float *y, const uint16_t *x, const uint8_t *w, const uint8_t *scale_e8m0, int S, int I, int O,

@@ -23,6 +23,8 @@
 // Output: out[(split * S + s) * O + o]; split 0 of an unsplit call is y.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace qg {
@@ -37,6 +39,17 @@ inline int next_pow2(int x) {
 
 template <int X> struct NextPow2 {
     static constexpr int value = X <= 1 ? 1 : X <= 2 ? 2 : X <= 4 ? 4 : X <= 8 ? 8 : X <= 16 ? 16 : 32;
+};
+
+// A unit's words: NW 32-bit streaming loads, or the format's own load when it
+// defines load_unit (units that are only 2-byte aligned).
+template <class F, int NW, class = void>
+struct CsLoad {
+    __device__ static Words<NW> load(const void *p) { return ld_stream<NW>(p); }
+};
+template <class F, int NW>
+struct CsLoad<F, NW, std::void_t<decltype(&F::template load_unit<NW>)>> {
+    __device__ static Words<NW> load(const void *p) { return F::template load_unit<NW>(p); }
 };
 
 template <class F, int S, int NW, int U, int RB>
@@ -86,7 +99,7 @@ gemv_cs_kernel(const typename F::Params p, float *__restrict__ out, int units, i
 #pragma unroll
             for (int j = 0; j < U; ++j) {
                 if (o < p.O && uok[j]) {
-                    raw[r][j] = ld_stream<NW>(F::unit_ptr(p, o, uidx[j], XU));
+                    raw[r][j] = CsLoad<F, NW>::load(F::unit_ptr(p, o, uidx[j], XU));
                     aux[r][j] = F::unit_aux(p, o, uidx[j], tc[j]);
                 } else {
 #pragma unroll

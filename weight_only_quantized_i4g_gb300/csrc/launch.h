@@ -26,6 +26,7 @@ size_t ws_fp8ue8m0(int S, int I, int O);
 size_t ws_mq4v2(int S, int I, int O);
 size_t ws_mq4v1(int S, int I, int O);
 size_t ws_mq4c(int S, int I, int O);
+size_t ws_q2_0(int S, int I, int O);
 
 int run_gemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,
                  int gs, void *ws, size_t ws_bytes, cudaStream_t st);
@@ -38,6 +39,8 @@ int run_gemv_mq4v2(float *y, const uint16_t *x, const uint8_t *blocks, int S, in
 int run_gemv_mq4v1(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
                    size_t ws_bytes, cudaStream_t st);
 int run_gemv_mq4c(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
+                  size_t ws_bytes, cudaStream_t st);
+int run_gemv_q2_0(float *y, const uint16_t *x, const uint8_t *blocks, int S, int I, int O, void *ws,
                   size_t ws_bytes, cudaStream_t st);
 
 
