@@ -67,6 +67,8 @@ def weight_bytes(fmt, O, I):
         return O * I + ((O + 127) // 128) * ((I + 127) // 128) * 4
     if fmt == "fp8ue8m0":
         return O * I + ((O + 127) // 128) * ((I + 127) // 128)
+    if fmt == "q2_0":
+        return O * (I // 64) * 18
     return O * (I // 256) * 136
 
 
@@ -560,7 +562,7 @@ def _prefill_inputs(qg, torch, dev, stream, fmt, O, I, M):
 PREFILL_OTHER = (("fp8", 7168, 16384), ("fp8", 24576, 7168), ("fp8ue8m0", 7168, 16384), ("fp8ue8m0", 24576, 7168),
                  ("mq4", 5120, 17408), ("mq4", 17408, 5120), ("mq4v1", 5120, 17408), ("mq4v1", 17408, 5120),
                  ("mq4c", 5120, 17408), ("mq4c", 17408, 5120))
-FMT_ID = {"i4g": 4, "fp8": 7, "fp8ue8m0": 71, "mq4": 44, "mq4v1": 13, "mq4c": 45}
+FMT_ID = {"i4g": 4, "fp8": 7, "fp8ue8m0": 71, "mq4": 44, "mq4v1": 13, "mq4c": 45, "q2_0": 20}
 # MQ4 block formats: V2 (a header per 128-weight half), v1 (one f32 header),
 # pad (one fp16 header and four zero bytes); 136 bytes per 256 weights each
 MQ4_ENCODE = {"mq4": lambda qg: qg.qg_encode_mq4v2, "mq4v1": lambda qg: qg.qg_encode_mq4v1,
@@ -697,26 +699,38 @@ def _graph_per_call(torch, stream, reps, issue):
 
 
 ONE_HEADER = (("mq4v1", 5120, 17408), ("mq4v1", 17408, 5120), ("mq4c", 5120, 17408), ("mq4c", 17408, 5120),
-              ("fp8ue8m0", 7168, 16384), ("fp8ue8m0", 24576, 7168))
+              ("fp8ue8m0", 7168, 16384), ("fp8ue8m0", 24576, 7168),
+              ("q2_0", 2560, 640), ("q2_0", 640, 2560), ("q2_0", 2048, 7168), ("q2_0", 7168, 2048))
 
 
 def one_header_breakdown(qg, torch, stream, hbm_peak, dev):
     """Kernel-only batch-1 GEMV time of the format variants: the one-header
     MQ4 block formats (v1: f32 scale and zero per 256 weights; pad: fp16 pair
     and four zero bytes) on the MQ4-V2 decode shapes and fmt=7 with UE8M0
-    block scales on the fmt=7 decode shapes; same weight recipes and timing
-    scheme as per_format_breakdown (graph of calls over >= 3x L2 of weight
-    copies)."""
+    block scales on the fmt=7 decode shapes and the Q2_0 codec (random codes,
+    d = 0.01) on the routed-expert shapes of the strata review and of the
+    fmt=4 configs; same timing scheme as per_format_breakdown (graph of calls
+    over >= 3x L2 of weight copies)."""
     out = {}
     l2 = 129 * 2 ** 20
     lib = qg._lib
     st = stream.cuda_stream
     with torch.cuda.stream(stream):
         for fmt, O, I in ONE_HEADER:
-            weights, X = _prefill_inputs(qg, torch, dev, stream, fmt, O, I, 1)
+            if fmt == "q2_0":           # random codes, d = fp16 0.01 (no device encoder)
+                g = torch.Generator(device=dev)
+                g.manual_seed(6000 + O + I)
+                blocks = torch.randint(0, 256, (O * (I // 64), 18), generator=g, device=dev,
+                                       dtype=torch.int32).to(torch.uint8)
+                blocks[:, 0:2] = torch.tensor([0x1F, 0x21], dtype=torch.uint8, device=dev)
+                weights = (blocks.reshape(-1),)
+                X = torch.randn(1, I, generator=g, device=dev).to(torch.bfloat16).view(torch.int16)
+            else:
+                weights, X = _prefill_inputs(qg, torch, dev, stream, fmt, O, I, 1)
             y = torch.empty(O, dtype=torch.float32, device=dev)
-            assert qg.qg_workspace_bytes(FMT_ID[fmt], 1, I, O, 0) == 0
-            nbytes = weight_bytes(fmt if fmt == "fp8ue8m0" else "mq4", O, I)
+            nws = qg.qg_workspace_bytes(FMT_ID[fmt], 1, I, O, 0)
+            wsb = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+            nbytes = weight_bytes(fmt if fmt in ("fp8ue8m0", "q2_0") else "mq4", O, I)
             copies = min(64, max(1, -(-3 * l2 // nbytes)))
             wcopies = [weights[0]] + [weights[0].clone() for _ in range(copies - 1)]
 
@@ -724,6 +738,9 @@ def one_header_breakdown(qg, torch, stream, hbm_peak, dev):
                 wp = wcopies[r % copies].data_ptr()
                 if fmt == "fp8ue8m0":
                     rc = lib.qgemv_fp8ue8m0(y.data_ptr(), X.data_ptr(), wp, weights[1].data_ptr(), 1, I, O, None, 0, st)
+                elif fmt == "q2_0":
+                    rc = lib.qgemv_q2_0(y.data_ptr(), X.data_ptr(), wp, 1, I, O, wsb.data_ptr() if nws else None, nws,
+                                        st)
                 else:
                     rc = getattr(lib, MQ4_GEMV[fmt])(y.data_ptr(), X.data_ptr(), wp, 1, I, O, None, 0, st)
                 if rc:
