@@ -69,3 +69,37 @@ def test_q2_0_every_code_and_position(qg):
     y = run(qg, x, blocks, 1, I, O)[0]
     want = np.array([((r // 64) % 4 - 1) * 2.0 ** -(r % 7) for r in range(O)])
     assert np.array_equal(y, want)
+
+
+def test_q2_0_staged_every_code_and_position(qg):
+    """The staged kernel (one token, I a multiple of 512): row r holds code
+    (r // 512) % 4 at weight r % 512 of its row, code 1 (weight 0) elsewhere,
+    d = 2^-(r % 5) in every block; x = ones: y[r] = (code - 1) * d exactly."""
+    O, I = 2048, 512
+    blocks = np.zeros((O, I // 64, 18), np.uint8)
+    blocks[:, :, 2:] = 0x55
+    for r in range(O):
+        blocks[r, :, 0:2] = np.array([2.0 ** -(r % 5)], np.float16).view(np.uint8)
+        e, c = r % I, (r // I) % 4
+        b, byte = e // 64, 2 + (e % 64) // 4
+        sh = 2 * (e % 4)
+        blocks[r, b, byte] = (int(blocks[r, b, byte]) & (0xFF ^ (3 << sh))) | (c << sh)
+    blocks = blocks.reshape(O, -1)
+    x = synth.bf16_bits(np.ones(I, np.float32)).reshape(1, I)
+    y = run(qg, x, blocks, 1, I, O)[0]
+    want = np.array([((r // I) % 4 - 1) * 2.0 ** -(r % 5) for r in range(O)])
+    assert np.array_equal(y, want)
+
+
+@pytest.mark.parametrize("span", [0, 40, 120])
+def test_q2_0_activation_range(qg, span):
+    """Activations whose magnitudes span 2^-span .. 2^span (the staged kernel
+    rescales x by a power of two per thread before its fp16 products)."""
+    O, I, S = 512, 4096, 1
+    x = (synth.normal(9100 + span, I) * np.exp2(span * (2 * synth.uniform(9150 + span, I) - 1))).astype(np.float32)
+    xb = synth.bf16_bits(x).reshape(S, I)
+    w = synth.normal(9200 + span, O * I, 0.02).reshape(O, I)
+    blocks = orc().encode_q2_0(w, O, I)
+    y = run(qg, xb, blocks, S, I, O)
+    ref, mag = par_rows(orc().qgemv_q2_0, O, xb, blocks, S, I, O)
+    compare(y, ref, mag, what=f"q2_0 x span 2^{span}")
