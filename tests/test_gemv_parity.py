@@ -187,6 +187,19 @@ def test_fp8_batch(qg, S):
     compare(y, ref, mag, what=f"fp8 S={S}")
 
 
+@pytest.mark.parametrize("span", [0, 40, 120])
+def test_fp8_activation_range(qg, span):
+    """Batch-1 activations whose magnitudes span 2^-span .. 2^span (the
+    one-token kernel carries x as fp16 scaled by a power of two per thread)."""
+    O, I, S = 384, 4096, 1
+    codes, scales, _ = fp8_inputs(O, I, S, tag=300 + span)
+    x = (synth.normal(9300 + span, I) * np.exp2(span * (2 * synth.uniform(9350 + span, I) - 1))).astype(np.float32)
+    xb = synth.bf16_bits(x).reshape(S, I)
+    y = run_fp8(qg, xb, codes, scales, S, I, O)
+    ref, mag = par_rows(orc().qgemv_fp8b128, O, xb, codes, scales, S, I, O, step=128)
+    compare(y, ref, mag, what=f"fp8 x span 2^{span}")
+
+
 def test_fp8_nan_rows(qg):
     O, I, S = 130, 256, 2
     codes, scales, x = fp8_inputs(O, I, S, tag=11)

@@ -162,6 +162,115 @@ struct FmtFp8 {
 // ---------------------------------------------------------------------------
 // General kernel: any shape and alignment.  One warp per row.
 // ---------------------------------------------------------------------------
+// One token: the products in fma.rn.f32.f16.  The e4m3 pair converts to an
+// exact fp16 pair (one cvt); the bf16 activations are carried as fp16 pairs
+// scaled by 2^A, A putting the thread's largest finite |x| in [2^14, 2^15)
+// (bf16's 8-bit significand fits fp16's 11; values more than 2^29 below that
+// maximum lose bits as fp16 subnormals, more than 2^40 below it become zero).  fp16 x fp16 products are exact in f32,
+// so the sum differs from the f32 form only in rounding order; the 2^-A goes
+// back with the block scale.  Three instructions per weight pair instead of
+// four (cvt, two f16 -> f32 cvts, f32x2 FMA), and half the x registers.
+template <class SC>
+struct FmtFp8H : FmtFp8<SC> {
+    typedef typename FmtFp8<SC>::Params Params;
+    static constexpr int kPairsPerWord = 1;     // one 64-bit register = two fp16 pairs per word
+
+    // raw bf16 pairs in memory order: xp[w] = (x[4w], x[4w+1]) | (x[4w+2], x[4w+3]) << 32
+    template <int XU, int NP>
+    __device__ static void load_x(const Params &p, int s, int u, uint64_t (&xp)[NP], float &xsum) {
+        static_assert(NP == XU / 4, "four activations per 64-bit register");
+        xsum = 0.f;
+#pragma unroll
+        for (int v = 0; v < XU / 8; ++v) {
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (u >= 0) q = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)s * p.I + (size_t)u * XU) + v);
+            xp[2 * v] = (uint64_t)q.x | ((uint64_t)q.y << 32);
+            xp[2 * v + 1] = (uint64_t)q.z | ((uint64_t)q.w << 32);
+        }
+    }
+
+    typedef Pow2Pair ThreadScale;   // 2^-A as two factors
+
+    __device__ static uint32_t bf16x2_to_scaled_f16x2(uint32_t b, float k1, float k2) {
+        const float lo = __uint_as_float(b << 16) * k1 * k2, hi = __uint_as_float(b & 0xFFFF0000u) * k1 * k2;
+        uint32_t r;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+
+    template <int U, int S, int NP>
+    __device__ static ThreadScale prepare_x(uint64_t (&xp)[U][S][NP], float (&)[U][S]) {
+        uint32_t m = 0;   // largest finite |x| as a bf16 magnitude pattern
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+#pragma unroll
+                for (int i = 0; i < NP; ++i)
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const uint32_t v = (uint32_t)(xp[j][s][i] >> (16 * h)) & 0x7FFFu;
+                        if (v < 0x7F80u && v > m) m = v;
+                    }
+        int F = (int)(m >> 7);
+        if (F < 1) F = 1;
+        const int A = 141 - F;                       // in [-113, 140]
+        const float k1 = pow2i(A >> 1), k2 = pow2i(A - (A >> 1));
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int s = 0; s < S; ++s)
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                    const uint32_t lo = (uint32_t)xp[j][s][i], hi = (uint32_t)(xp[j][s][i] >> 32);
+                    xp[j][s][i] = (uint64_t)bf16x2_to_scaled_f16x2(lo, k1, k2) |
+                                  ((uint64_t)bf16x2_to_scaled_f16x2(hi, k1, k2) << 32);
+                }
+        const int c = -A;
+        return Pow2Pair{pow2i(c >> 1), pow2i(c - (c >> 1))};
+    }
+
+    __device__ static uint32_t e4m3x2_to_f16x2(uint32_t two) {
+        uint32_t h;
+        asm("{.reg .b16 lo, hi;\n\t"
+            "mov.b32 {lo, hi}, %1;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, lo;}" : "=r"(h) : "r"(two));
+        return h;
+    }
+
+    __device__ static void fma_mixed2(float &a0, float &a1, uint32_t w2, uint32_t x2) {
+        asm("{.reg .f16 wl, wh, xl, xh;\n\t"
+            "mov.b32 {wl, wh}, %2;\n\t"
+            "mov.b32 {xl, xh}, %3;\n\t"
+            "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+            "fma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
+            : "+f"(a0), "+f"(a1)
+            : "r"(w2), "r"(x2));
+    }
+
+    template <int S, int NW, int NP>
+    __device__ static void accumulate(const Words<NW> &wd, float sc, const uint64_t (&xp)[S][NP],
+                                      const float (&)[S], ThreadScale ts, float *part) {
+        uint32_t h[NW][2];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            h[w][0] = e4m3x2_to_f16x2(wd.w[w]);
+            h[w][1] = e4m3x2_to_f16x2(wd.w[w] >> 16);
+        }
+        const float scs = sc * ts.p1;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                fma_mixed2(a0, a1, h[w][0], (uint32_t)xp[s][w]);
+                fma_mixed2(a0, a1, h[w][1], (uint32_t)(xp[s][w] >> 32));
+            }
+            part[s] = fmaf(scs, (a0 + a1) * ts.p2, part[s]);
+        }
+    }
+};
+
 __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
     return e4m3x2_to_f32x2((uint32_t)c).x;
 }
@@ -264,15 +373,17 @@ void launch_tma_fp8_u(const typename FmtFp8<SC>::Params &p, float *out, const Tm
     constexpr int NW = S <= 4 ? 4 : 2;
     if constexpr (S == 1) {
         if (pl.U == 2) {
-            launch_tma<FmtFp8<SC>, S, NW, 2, RB>(p, out, pl, st, moe);
+            launch_tma<FmtFp8H<SC>, S, NW, 2, RB>(p, out, pl, st, moe);
             return;
         }
         if (pl.U == 3) {
-            launch_tma<FmtFp8<SC>, S, NW, 3, RB>(p, out, pl, st, moe);
+            launch_tma<FmtFp8H<SC>, S, NW, 3, RB>(p, out, pl, st, moe);
             return;
         }
+        launch_tma<FmtFp8H<SC>, S, NW, 1, RB>(p, out, pl, st, moe);
+    } else {
+        launch_tma<FmtFp8<SC>, S, NW, 1, RB>(p, out, pl, st, moe);
     }
-    launch_tma<FmtFp8<SC>, S, NW, 1, RB>(p, out, pl, st, moe);
 }
 
 template <class SC, int S>
@@ -285,7 +396,8 @@ void launch_tma_fp8_s(const typename FmtFp8<SC>::Params &p, float *out, const Tm
         }
     }
     if (pl.rb == 2) {
-        launch_tma<FmtFp8<SC>, S, (S <= 4 ? 4 : 2), 1, 2>(p, out, pl, st, moe);
+        if constexpr (S == 1) launch_tma<FmtFp8H<SC>, S, 4, 1, 2>(p, out, pl, st, moe);
+        else launch_tma<FmtFp8<SC>, S, (S <= 4 ? 4 : 2), 1, 2>(p, out, pl, st, moe);
         return;
     }
     launch_tma_fp8_u<SC, S, 4>(p, out, pl, st, moe);
