@@ -207,12 +207,17 @@ bool tma_plan_rows(const TmaGeom &g, int S, int O, int U_max, TmaPlan *pl) {
     // block loads the whole activation row: with several blocks per SM that
     // load rivals the weights the SM streams (fmt=4 2048x7168 with f32 x:
     // 28 KB of x per block against 54 KB of weights per SM).  One block per
-    // SM with 8-row batches measured 30% faster there (6.2 -> 4.3 us).
+    // SM with 8-row batches measured 30% faster there (6.2 -> 4.3 us); 4- and
+    // 2-row batches were slower (5.1, 6.2 us).  A matrix with fewer 8-row
+    // batches than SMs (under 1216 rows) takes 4-row batches on the same plan
+    // (Q2_0 640x2560: 3.25 -> 2.85 us) before the general plan below.
     if (S <= 2 && (double)O * (g.rowbytes + g.arowbytes) < 32e6) {
-        TmaPlan t;
-        if (tma_plan(g, S, O, 8, next_pow2(8 * S), U_max, &t, 1, 6) && (long)t.nrowb * t.splits >= num_sms()) {
-            *pl = t;
-            return true;
+        for (int rb = 8; rb >= 4; rb /= 2) {
+            TmaPlan t;
+            if (tma_plan(g, S, O, rb, next_pow2(rb * S), U_max, &t, 1, 6) && (long)t.nrowb * t.splits >= num_sms()) {
+                *pl = t;
+                return true;
+            }
         }
     }
     const int cands[3] = {8, 4, 2};
