@@ -165,6 +165,28 @@ def pin_i4g_bruteforce(orc):
                 _close(mag, refmag, refmag, what="i4g mag")
 
 
+def pin_i4g_gemm_bruteforce(orc):
+    """Batched prefill (colibri PR #457, section 4: the large-batch path computes
+    the grouped product of section 3 for every token row): Y and the tolerance
+    denominator mag = sum |w x| against numpy dequantize + matmul with bf16
+    activations, tiny shapes, every gs of the loader's list, odd I."""
+    rng = np.random.default_rng(13)
+    for O in (1, 3):
+        for I in (1, 39, 64, 65, 201, 512):
+            for gs in (16, 32, 48, 64, 96, 128, 192, 256):
+                rb, ng = (I + 1) // 2, (I + gs - 1) // gs
+                w = rng.integers(0, 256, O * rb, dtype=np.uint8)
+                sc = rng.uniform(-2, 2, O * ng).astype(np.float32)
+                M = 3
+                xb = synth.bf16_bits(rng.standard_normal(M * I).astype(np.float32))
+                Y, mag = orc.qgemm_i4g(xb, w, sc, M, I, O, gs)
+                W = _dequant_i4g_numpy(w, sc, O, I, gs)
+                X = synth.bf16_to_f32(xb).reshape(M, I).astype(np.float64)
+                refmag = np.abs(X) @ np.abs(W).T
+                _close(Y, X @ W.T, refmag, what=f"i4g gemm O={O} I={I} gs={gs}")
+                _close(mag, refmag, refmag, what=f"i4g gemm mag O={O} I={I} gs={gs}")
+
+
 def pin_i4g_single_group(orc):
     """gs >= I: one scale per row, y = scale * sum (n-8) x (the per-row form)."""
     rng = np.random.default_rng(12)
@@ -282,6 +304,7 @@ def pin_fp8_bruteforce(orc):
         W = _dequant_fp8_numpy(codes, sc, O, I)
         X = synth.bf16_to_f32(xb).reshape(S, I).astype(np.float64)
         _close(y, X @ W.T, np.abs(X) @ np.abs(W).T, what=f"fp8 O={O} I={I}")
+        _close(mag, np.abs(X) @ np.abs(W).T, np.abs(X) @ np.abs(W).T, what=f"fp8 mag O={O} I={I}")
 
 
 def pin_e8m0_vs_torch(orc):
@@ -330,6 +353,7 @@ def pin_fp8ue8m0_bruteforce(orc):
         W = _dequant_fp8_numpy(codes, f32, O, I)
         X = synth.bf16_to_f32(xb).reshape(S, I).astype(np.float64)
         _close(y, X @ W.T, np.abs(X) @ np.abs(W).T, what=f"fp8ue8m0 O={O} I={I}")
+        _close(mag, np.abs(X) @ np.abs(W).T, np.abs(X) @ np.abs(W).T, what=f"fp8ue8m0 mag O={O} I={I}")
         y2, _ = orc.qgemv_fp8b128(xb, codes, f32, S, I, O)
         assert np.array_equal(y, y2)
 
@@ -416,6 +440,7 @@ def pin_mq4v2_size_and_bruteforce(orc):
         W = _dequant_mq4v2_numpy(blocks, O, I)
         X = synth.bf16_to_f32(xb).reshape(S, I).astype(np.float64)
         _close(y, X @ W.T, np.abs(X) @ np.abs(W).T, what=f"mq4v2 O={O} I={I}")
+        _close(mag, np.abs(X) @ np.abs(W).T, np.abs(X) @ np.abs(W).T, what=f"mq4v2 mag O={O} I={I}")
 
 
 def pin_mq4v2_equal_halves_match_v1(orc):
@@ -580,6 +605,7 @@ def pin_mq4_one_header_bruteforce(orc):
             y, mag = fn(xb, blocks, S, I, O)
             W = ref(blocks, O, I)
             _close(y, X @ W.T, np.abs(X) @ np.abs(W).T, what=f"one-header O={O} I={I}")
+            _close(mag, np.abs(X) @ np.abs(W).T, np.abs(X) @ np.abs(W).T, what=f"one-header mag O={O} I={I}")
 
 
 def pin_mq4_three_layouts_agree(orc):
@@ -701,6 +727,7 @@ def pin_q2_0_size_and_bruteforce(orc):
         W = _dequant_q2_0_numpy(blocks, O, I)
         X = synth.bf16_to_f32(xb).reshape(S, I).astype(np.float64)
         _close(y, X @ W.T, np.abs(X) @ np.abs(W).T, what=f"q2_0 O={O} I={I}")
+        _close(mag, np.abs(X) @ np.abs(W).T, np.abs(X) @ np.abs(W).T, what=f"q2_0 mag O={O} I={I}")
 
 
 def pin_q2_0_encoder(orc):
@@ -840,6 +867,8 @@ def pin_moe_gemm_bruteforce(orc):
         for g, e in enumerate(ge):
             r = slice(off[g], off[g + 1])
             _close(Y[r], X[r] @ deq[e].T, np.abs(X[r]) @ np.abs(deq[e]).T, what=f"moe gemm fmt={fmt} group {g}")
+            _close(mag[r], np.abs(X[r]) @ np.abs(deq[e]).T, np.abs(X[r]) @ np.abs(deq[e]).T,
+                   what=f"moe gemm mag fmt={fmt} group {g}")
         assert not np.isnan(Y).any()
 
 

@@ -33,6 +33,27 @@ MUTATIONS = [
      "size_t rb = ((size_t)I) / 2;\n    size_t ng = ((size_t)I + (size_t)gs - 1) / (size_t)gs;\n    for (int s = 0; s < S; ++s) {\n        for (int o = 0; o < O; ++o) {\n            double acc = 0.0, m = 0.0;\n            for (int i = 0; i < I; ++i) {\n                double q = (double)i4g_value(w, rb, o, i);\n                double sc = (double)scales[(size_t)o * ng + (size_t)(i / gs)];\n                double t = q * sc * (double)x"),
     ("i4g_mag_signed", "acc += t;\n                m += fabs(t);\n            }\n            y[(size_t)s * O + o] = acc;\n            mag[(size_t)s * O + o] = m;\n        }\n    }\n}\n\n/* Batched",
      "acc += t;\n                m += t;\n            }\n            y[(size_t)s * O + o] = acc;\n            mag[(size_t)s * O + o] = m;\n        }\n    }\n}\n\n/* Batched"),
+    ("i4g_gemm_mag_signed",
+     "double t = q * sc * oracle_bf16_value(X[(size_t)s * I + i]);\n                acc += t;\n                m += fabs(t);",
+     "double t = q * sc * oracle_bf16_value(X[(size_t)s * I + i]);\n                acc += t;\n                m += t;"),
+    ("i4g_gemm_mag_x1000",
+     "double t = q * sc * oracle_bf16_value(X[(size_t)s * I + i]);\n                acc += t;\n                m += fabs(t);",
+     "double t = q * sc * oracle_bf16_value(X[(size_t)s * I + i]);\n                acc += t;\n                m += 1000.0 * fabs(t);"),
+    ("i4g_gemm_group_off_by_one",
+     "double sc = (double)scales[(size_t)o * ng + (size_t)(i / gs)];\n                double t = q * sc * oracle_bf16_value",
+     "double sc = (double)scales[(size_t)o * ng + (size_t)(i / gs > 0 ? i / gs - 1 : 0)];\n"
+     "                double t = q * sc * oracle_bf16_value"),
+    ("moe_gemm_mag_rows_from_zero", "double *mg = mag + (size_t)off[g] * O;", "double *mg = mag;"),
+    ("fp8_mag_signed",
+     "double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];\n                double t = wv * sc * oracle_bf16_value(x[(size_t)s * I + i]);\n                acc += t;\n                m += fabs(t);",
+     "double sc = (double)scale_inv[(size_t)(o / 128) * nbi + (size_t)(i / 128)];\n                double t = wv * sc * oracle_bf16_value(x[(size_t)s * I + i]);\n                acc += t;\n                m += t;"),
+    ("fp8ue8m0_mag_x2",
+     "double sc = oracle_e8m0_value(scale_e8m0[(size_t)(o / 128) * nbi + (size_t)(i / 128)]);\n                double t = wv * sc * oracle_bf16_value(x[(size_t)s * I + i]);\n                acc += t;\n                m += fabs(t);",
+     "double sc = oracle_e8m0_value(scale_e8m0[(size_t)(o / 128) * nbi + (size_t)(i / 128)]);\n                double t = wv * sc * oracle_bf16_value(x[(size_t)s * I + i]);\n                acc += t;\n                m += 2.0 * fabs(t);"),
+    ("q2_0_mag_signed", "i % 64) *\n                           oracle_bf16_value(x[(size_t)s * I + i]);\n                acc += t;\n                m += fabs(t);",
+     "i % 64) *\n                           oracle_bf16_value(x[(size_t)s * I + i]);\n                acc += t;\n                m += t;"),
+    ("mq4v2_mag_signed", "                    acc += t;\n                    m += fabs(t);", "                    acc += t;\n                    m += t;"),
+    ("mq4_one_header_mag_signed", "sum_abs += fabs(t);", "sum_abs += t;"),
     ("quant_divisor_8", "volatile float sc = amax / 7.0f;", "volatile float sc = amax / 8.0f;"),
     ("quant_truncate", "float qr = rintf(r);\n                    if (qr < -8.0f)", "float qr = truncf(r);\n                    if (qr < -8.0f)"),
     # E4M3
