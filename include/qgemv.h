@@ -141,9 +141,11 @@ int qgemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales,
  * allocator, and for host code that must not call cudaMalloc on the decode
  * path (it can wait for the whole device).  Shapes needing more than 4 MiB
  * of scratch (qg_workspace_bytes(QG_FMT_I4G, ...) > 4 MiB) are refused with
- * QG_EWORKSPACE.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress); make that first call before any stream
- * capture.  Every call on a device shares the array and leaves its contents
+ * QG_EWORKSPACE.  The first call in a CUDA context (the device's primary
+ * context, a new one after cudaDeviceReset, or a driver-API context of the
+ * caller's) looks up the array's device address there
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call on a device shares the array and leaves its contents
  * behind; calls whose kernels may run at the same time (different streams or
  * host threads) race on it and must be ordered by the caller.  Allocates
  * nothing; every GPU that loads the library holds the 4 MiB until exit. */

@@ -1,8 +1,9 @@
 """Batched-prefill dequant-GEMMs of the three formats against the oracle
 (needs a GPU).
 
-Small shapes are compared in full; the M=512 prefill workloads are compared
-on a seeded sample of token rows (every output column of those rows).  The
+Small shapes and the fmt=4 M=512 prefill workloads are compared in full;
+the fmt=7 and MQ4-V2 GEMMs on their decode shapes at M=512 on a seeded
+sample of token rows (every output column of those rows).  The
 fmt=7 and MQ4-V2 GEMMs compute the same sums as their GEMVs over M tokens,
 so the oracle's GEMV functions with S = M are their references."""
 import numpy as np
@@ -63,13 +64,17 @@ def test_gemm_small(qg, M, I, O, gs):
 
 
 @pytest.mark.parametrize("O", [7168, 2048])
-def test_gemm_prefill_workload_sampled(qg, O):
+def test_gemm_prefill_workload_full(qg, O):
+    """The M=512 prefill workloads in full, in the launch shape the bench times
+    (7168x7168: whole tiles per block; 2048x7168: K ranges split over the SMs),
+    every one of the 512 x O outputs against the oracle (colibri PR #457,
+    section 4: the large-batch GEMM computes the grouped product of section 3
+    for every token row)."""
     M, I, gs = 512, 7168, 64
     X, wq, sc = gemm_inputs(M, I, O, gs, O)
     Y = run_gemm(qg, X, wq, sc, M, I, O, gs)
-    rows = np.sort(np.random.default_rng(O).choice(M, 12, replace=False))
-    ref, mag = par_rows(orc().qgemm_i4g, O, np.ascontiguousarray(X[rows]), wq, sc, len(rows), I, O, gs)
-    compare(Y[rows], ref, mag, what=f"gemm prefill O={O}")
+    ref, mag = par_rows(orc().qgemm_i4g, O, X, wq, sc, M, I, O, gs)
+    compare(Y, ref, mag, what=f"gemm prefill {M}x{I}x{O}")
 
 
 def test_gemm_tc_needs_workspace(qg):

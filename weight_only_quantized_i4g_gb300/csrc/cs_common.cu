@@ -6,6 +6,8 @@
 #include <cmath>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "gemv_cs.cuh"
 #include "gemv_tma.cuh"
 #include "launch.h"
@@ -17,24 +19,44 @@ namespace qg {
 // reads and clears it with qg_device_status().
 __device__ int g_device_error = 0;
 
-int *device_error_word() {
-    static std::mutex mu;
-    static int *cache[64] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        cudaGetLastError();
-        return nullptr;
-    }
-    std::lock_guard<std::mutex> lk(mu);
-    if (cache[dev] == nullptr) {
+unsigned long long current_context_id() {
+    typedef CUresult (*GetCurrentFn)(CUcontext *);
+    typedef CUresult (*GetIdFn)(CUcontext, unsigned long long *);
+    static std::once_flag once;
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    std::call_once(once, [] {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+        cudaGetLastError();
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+int *device_error_word() {
+    static PerContext<int *> cache;
+    int *w = nullptr;
+    const int rc = cache.get(&w, [](int **out) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess || p == nullptr) {
             cudaGetLastError();
-            return nullptr;
+            return (int)kECuda;
         }
-        cache[dev] = static_cast<int *>(p);
-    }
-    return cache[dev];
+        *out = static_cast<int *>(p);
+        return (int)kOk;
+    });
+    return rc == kOk ? w : nullptr;
 }
 
 int read_device_error(int *status) {

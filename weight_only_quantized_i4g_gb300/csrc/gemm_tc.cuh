@@ -153,38 +153,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// As tma_load_2d, written to the same offset in the shared memory of every
-// block of the cluster in `mask`, each of whose barrier at `bar`'s offset
-// counts the bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                                      uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "h"(mask)
-        : "memory");
-}
-
-// As mma_commit, arriving on the barrier at `bar`'s offset in every block of
-// the cluster in `mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_addr(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 // 32 consecutive f32 columns of this warp's 32 tensor-memory lanes.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -363,7 +331,6 @@ struct Args {
     float *partials;      // 2 slots per block
     int M, O, gs, ng, nbi, MB, Kt;
     int tail_half;        // the last K step of every tile is 64 wide (I % 128 == 64)
-    int cluster;          // pairs of blocks share X by multicast (one whole tile per block)
     long long rowbytes;   // bytes of one weight row (fmt=4 and fmt=7; MQ4-V2: I/256 * 136)
     long long U;          // (tile, K step) units
     // Written by the preparation kernel:
@@ -405,19 +372,10 @@ __device__ __forceinline__ int range_exponent(float v) {
 }
 
 
-// Token block and output tile of tile index t.  Normally t = nb * MB + mb;
-// with clusters of two blocks the pair (2j, 2j+1) takes token block j % MB
-// and the neighbouring output tiles 2 (j / MB) and 2 (j / MB) + 1, so both
-// blocks stream the same X.
-__device__ __forceinline__ void tile_coords(long long t, int MB, int cluster, int &mb, int &nb) {
-    if (cluster) {
-        const long long j = t >> 1;
-        mb = (int)(j % MB);
-        nb = (int)(2 * (j / MB) + (t & 1));
-    } else {
-        mb = (int)(t % MB);
-        nb = (int)(t / MB);
-    }
+// Token block and output tile of tile index t = nb * MB + mb.
+__device__ __forceinline__ void tile_coords(long long t, int MB, int &mb, int &nb) {
+    mb = (int)(t % MB);
+    nb = (int)(t / MB);
 }
 
 // Where tile t sits: its first token row m0, the end of its token rows (the
@@ -432,7 +390,7 @@ __device__ __forceinline__ TileLoc tile_loc(const KArgs<GR> &a, long long t) {
     TileLoc L;
     if constexpr (!GR) {
         int mb, nb;
-        tile_coords(t, a.MB, a.cluster, mb, nb);
+        tile_coords(t, a.MB, mb, nb);
         L.m0 = mb * BT;
         L.mend = a.M;
         L.nb = nb;
@@ -673,7 +631,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, KArgs<GR> a) {
         griddep_launch_dependents();
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1 + kNumDeqWarps);
-            mbar_init(&empty[s], a.cluster ? 2 : 1);   // with a cluster: both blocks' MMAs
+            mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kNumEpiWarps);
@@ -694,10 +652,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, KArgs<GR> a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // With a cluster, the peer's copies and commits reach this block's
-    // barriers: both blocks initialize theirs first.
-    if (a.cluster) cluster_sync();
-    const uint32_t crank = a.cluster ? cluster_rank() : 0u;
 
     const long long P = gridDim.x, cta = blockIdx.x, U = a.U;
     const long long ub = sk::range_begin(cta, U, P), ue = sk::range_begin(cta + 1, U, P);
@@ -723,28 +677,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, KArgs<GR> a) {
                         raise_device_error(a.err, kErrTimeout);
                     mbar_arrive_expect_tx(&full[s], half ? C::kBoxBytes : C::kXBytes);
                     const uint32_t st = sbase + s * C::kXBytes;
-                    if (a.cluster) {
-                        // This block's half of the tokens, into both blocks.
-                        const uint32_t off = crank * (uint32_t)(BT / 2) * 128u;
-                        const int mr = m0 + (int)crank * (BT / 2);
-                        tma_load_2d_multicast(st + off, &tmX, k * kBK, mr, &full[s], 0x3);
-                        if (!half)
-                            tma_load_2d_multicast(st + C::kBoxBytes + off, &tmX, k * kBK + kBKBox, mr, &full[s], 0x3);
-                    } else {
-                        tma_load_2d(st, &tmX, k * kBK, m0, &full[s]);
-                        if (!half) tma_load_2d(st + C::kBoxBytes, &tmX, k * kBK + kBKBox, m0, &full[s]);
-                    }
+                    tma_load_2d(st, &tmX, k * kBK, m0, &full[s]);
+                    if (!half) tma_load_2d(st + C::kBoxBytes, &tmX, k * kBK + kBKBox, m0, &full[s]);
                 }
                 u = g.t * Kt + g.ke;
             }
-            // Every copy issued must have landed before the block exits, and
-            // with a cluster every commit of the peer's MMAs must have
-            // arrived here too.
-            for (uint32_t j = it > (uint32_t)C::kStages ? it - C::kStages : 0; j < it; ++j) {
+            // Every copy issued must have landed before the block exits.
+            for (uint32_t j = it > (uint32_t)C::kStages ? it - C::kStages : 0; j < it; ++j)
                 if (!mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1)) raise_device_error(a.err, kErrTimeout);
-                if (a.cluster && !mbar_wait(&empty[j % C::kStages], (j / C::kStages) & 1))
-                    raise_device_error(a.err, kErrTimeout);
-            }
         }
     } else if (warp == kWarpMma) {
         if (lane == 0) {
@@ -766,10 +706,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, KArgs<GR> a) {
                         if (kk < nk)
                             mma_f16_ts(tmem, at + kk * 8, sw128_desc(xa + (kk >> 2) * C::kBoxBytes + (kk & 3) * 32),
                                         C::kIdesc, (k > g.ks || kk > 0) ? 1u : 0u);
-                    if (a.cluster)
-                        mma_commit_multicast(&empty[s], 0x3);   // frees the stage in both blocks
-                    else
-                        mma_commit(&empty[s]);
+                    mma_commit(&empty[s]);
                 }
                 mma_commit(acc_full);
                 u = g.t * Kt + g.ke;
@@ -877,7 +814,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, KArgs<GR> a) {
 
     tc_fence_before();
     __syncthreads();
-    if (a.cluster) cluster_sync();   // the peer no longer writes into this block
     if (warp == kWarpMma) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols)
@@ -1007,7 +943,6 @@ constexpr int kTileBT[kNumTiles] = {256, 128, 64};
 
 struct Plan {
     int tile, bt, MB, NB, Kt, P;
-    int cluster;          // whole tiles in pairs sharing X by multicast
     long long T, U;
     // Workspace: tile counters, partial slots (split plans only), 2^F per
     // token (padded to whole 256-token blocks; the tail is never stored),
@@ -1042,11 +977,6 @@ inline Plan make_plan(int tile, int M, int I, int O, int nsm) {
     // One tile per block when the tiles fit in one wave; otherwise an even
     // split of the units over all SMs.
     p.P = (int)std::min<long long>(p.T <= nsm ? p.T : nsm, p.U);
-    // Pairs of whole tiles sharing X by multicast (cluster = 1) measured no
-    // faster on GB300: the bytes each SM receives per K step, not the copies
-    // it issues, bound the step, and multicast leaves those unchanged.  The
-    // planner does not pick it.
-    p.cluster = 0;
     plan_layout(p, M, I, O);
     return p;
 }
@@ -1057,7 +987,7 @@ inline Plan make_plan(int tile, int M, int I, int O, int nsm) {
 // K range is split over blocks costs ~14000 cycles per contributor for the
 // partial sums (written, then read back by the block that finishes it).
 inline double plan_cost(const Plan &p) {
-    const double step = (p.bt == 256 ? 2300.0 : 2150.0) * (p.cluster ? 0.75 : 1.0);
+    const double step = p.bt == 256 ? 2300.0 : 2150.0;
     const double steps = (double)((p.U + p.P - 1) / p.P);
     const bool split = (p.U / p.P) % p.Kt != 0 || p.U % p.P != 0;
     const double contributors = (double)p.Kt / std::max(1.0, (double)(p.U / p.P)) + 1.0;
@@ -1076,7 +1006,6 @@ inline Plan choose_plan(int M, int I, int O) {
             if (mode == 1) {
                 if (p.T >= nsm) continue;   // already the split over all SMs
                 p.P = (int)std::min<long long>(nsm, p.U);
-                p.cluster = 0;
                 plan_layout(p, M, I, O);
             }
             const double c = plan_cost(p);
@@ -1092,27 +1021,27 @@ inline Plan choose_plan(int M, int I, int O) {
 template <class F, int BT, bool GR>
 int launch_tile(const Plan &p, const CUtensorMap &tmX, const KArgs<GR> &args, cudaStream_t st) {
     using C = Cfg<BT>;
-    static std::once_flag attr_once[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    std::call_once(attr_once[dev & 63], [] {
+    // The shared-memory limit is an attribute of the kernel in the current
+    // context: set once per context.
+    static PerContext<char> attr_set;
+    char done = 0;
+    attr_set.get(&done, [](char *v) {
         cudaFuncSetAttribute(gemm_tc_kernel<F, BT, GR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::kSmemBytes);
+        cudaGetLastError();
+        *v = 1;
+        return (int)kOk;
     });
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.P);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = p.cluster ? 2 : 1;
+    cfg.numAttrs = 1;
     cudaLaunchKernelEx(&cfg, gemm_tc_kernel<F, BT, GR>, tmX, args);
     return check_launch(F::kName);
 }
@@ -1134,7 +1063,7 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, KArgs<GR> args, int 
     CUtensorMap tmX;
     const cuuint64_t dims[2] = {(cuuint64_t)I, (cuuint64_t)M};
     const cuuint64_t strides[1] = {(cuuint64_t)I * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBKBox, (cuuint32_t)(p.cluster ? p.bt / 2 : p.bt)};
+    const cuuint32_t box[2] = {(cuuint32_t)kBKBox, (cuuint32_t)p.bt};
     const cuuint32_t es[2] = {1, 1};
     CUresult r = encode(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, args.xh, dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1151,7 +1080,6 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, KArgs<GR> args, int 
     args.MB = p.MB;
     args.Kt = p.Kt;
     args.tail_half = (I % kBK) != 0 ? 1 : 0;
-    args.cluster = p.cluster;
     args.U = p.U;
     args.err = device_error_word();
     // Tile counters are only read when a tile's K range is split over blocks.
@@ -1210,7 +1138,6 @@ inline Plan group_plan(const int *rows, int n, int M, int I, int O) {
     for (int g = 0; g < n; ++g) p.T += (long long)((rows[g] + p.bt - 1) / p.bt) * p.NB;
     p.U = p.T * p.Kt;
     p.P = (int)std::min<long long>(p.T <= nsm ? p.T : nsm, p.U);
-    p.cluster = 0;
     plan_layout(p, M, I, O, n);
     return p;
 }

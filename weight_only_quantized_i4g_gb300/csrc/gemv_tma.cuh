@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "gemv_cs.cuh"
+#include "launch.h"
 #include "pipeline.cuh"
 
 namespace qg {
@@ -562,14 +563,16 @@ void launch_tma(const typename F::Params &p, float *out, const TmaPlan &pl, cuda
     auto kern = gemv_tma_kernel<F, S, NW, U, RB, TG>;
     auto kern_moe = gemv_tma_moe_kernel<F, S, NW, U, RB, TG>;
     const void *kfn = moe ? reinterpret_cast<const void *>(kern_moe) : reinterpret_cast<const void *>(kern);
-    static int attr_set_mask[2] = {0, 0};   // one bit per device ordinal (< 31), per kernel
-    int &mask = attr_set_mask[moe ? 1 : 0];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 31 && !(__atomic_load_n(&mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+    // The shared-memory limit is an attribute of the kernel in the current
+    // context: set once per context and kernel.
+    static PerContext<char> attr_set[2];
+    char done = 0;
+    attr_set[moe ? 1 : 0].get(&done, [kfn](char *v) {
         cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-        __atomic_fetch_or(&mask, 1 << dev, __ATOMIC_ACQ_REL);
-    }
+        cudaGetLastError();
+        *v = 1;
+        return (int)kOk;
+    });
     const int threads = 32 * (pl.nc + 1);
     int per_sm = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, threads, pl.L.total) != cudaSuccess ||

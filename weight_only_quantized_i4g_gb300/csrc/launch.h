@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace qg {
 
 // Status codes mirror qg_status in include/qgemv.h.
@@ -19,6 +21,52 @@ int check_launch(const char *what);
 
 // Reads and clears this device's kernel error word (0 or a qg status).
 int read_device_error(int *status);
+
+// A process-unique id of the CUDA context current on this thread (the
+// driver's context id), 0 when no context is current or the driver cannot
+// say.  Device addresses of the library's __device__ variables and kernel
+// attributes belong to a context, not to a device ordinal: after
+// cudaDeviceReset the runtime creates a new primary context, and a caller
+// may make its own driver-API context current.  Host caches of either are
+// therefore keyed on this id.
+unsigned long long current_context_id();
+
+// One cached value per context, for up to kSlots contexts (the oldest entry
+// is reused after that).  get() returns the value of the current context,
+// computing it with fill(&value) -> status the first time that context asks;
+// fill runs with the context current and under the cache's lock.
+template <class T, int kSlots = 16>
+class PerContext {
+  public:
+    template <class Fill>
+    int get(T *out, Fill fill) {
+        std::lock_guard<std::mutex> lk(mu_);
+        unsigned long long id = current_context_id();
+        if (id != 0)
+            for (int i = 0; i < kSlots; ++i)
+                if (ids_[i] == id) {
+                    *out = vals_[i];
+                    return kOk;
+                }
+        T v{};
+        const int rc = fill(&v);
+        if (rc != kOk) return rc;
+        if (id == 0) id = current_context_id();   // fill may have created the primary context
+        if (id != 0) {
+            ids_[next_] = id;
+            vals_[next_] = v;
+            next_ = (next_ + 1) % kSlots;
+        }
+        *out = v;
+        return kOk;
+    }
+
+  private:
+    std::mutex mu_;
+    unsigned long long ids_[kSlots] = {};
+    T vals_[kSlots] = {};
+    int next_ = 0;
+};
 
 size_t ws_i4g(int S, int I, int O, int gs);
 size_t ws_fp8b128(int S, int I, int O);

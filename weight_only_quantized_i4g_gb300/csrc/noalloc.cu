@@ -12,8 +12,6 @@
 // the previous call's contents; calls whose kernels overlap on the GPU
 // (several streams, or several host threads) race on it and must be ordered
 // by the caller.
-#include <mutex>
-
 #include "../../include/qgemv.h"
 #include "launch.h"
 
@@ -27,34 +25,33 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 namespace {
 
-// Device address of the scratch array for the current device.  In host code
+// Device address of the scratch array in the current context.  In host code
 // `g_noalloc_scratch` names a host-side stand-in, not device memory, so the
-// address is looked up once per device (with that device current) and cached.
+// address is looked up with cudaGetSymbolAddress, with the caller's device
+// current, the first time a context calls, and cached per context: a context
+// made after cudaDeviceReset, or a driver-API context of the caller's own,
+// gets its own address rather than a stale one.
 int noalloc_scratch(void **out) {
-    static std::mutex mu;
-    static void *cache[64] = {nullptr};
+    static PerContext<void *> cache;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
-        set_error_detail("qgemv_i4g_noalloc: no current device (%s)",
-                         e != cudaSuccess ? cudaGetErrorString(e) : "device ordinal out of range");
+    if (e != cudaSuccess) {
+        set_error_detail("qgemv_i4g_noalloc: no current device (%s)", cudaGetErrorString(e));
         cudaGetLastError();
         return kECuda;
     }
-    std::lock_guard<std::mutex> lk(mu);
-    if (cache[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
+    return cache.get(out, [dev](void **p) {
+        void *a = nullptr;
+        const cudaError_t r = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+        if (r != cudaSuccess || a == nullptr) {
             set_error_detail("qgemv_i4g_noalloc: cannot locate the scratch array on device %d (%s)", dev,
-                             cudaGetErrorString(e));
+                             cudaGetErrorString(r));
             cudaGetLastError();
-            return kECuda;
+            return (int)kECuda;
         }
-        cache[dev] = p;
-    }
-    *out = cache[dev];
-    return kOk;
+        *p = a;
+        return (int)kOk;
+    });
 }
 
 }  // namespace
