@@ -84,6 +84,13 @@ const char *qg_last_error(void);
  * status, or QG_ECUDA. */
 int qg_device_status(int *status);
 
+/* Number of kernels this library has launched in this process, over all
+ * devices and threads (every entry point counts the launches it enqueues:
+ * one per GEMV, plus one for a split reduction's summing pass; two per
+ * tensor-core GEMM).  For profiling and launch accounting; the pages have no
+ * counterpart.  Never fails. */
+unsigned long long qg_launch_count(void);
+
 /* Format ids for qg_workspace_bytes. */
 enum {
     QG_FMT_I4G = 4,         /* grouped int4 (fmt=4)                            */

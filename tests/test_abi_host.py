@@ -26,7 +26,7 @@ def qg():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(q[a-z_0-9]+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:[a-z_0-9]+\s+)+\*?\s*(q[a-z_0-9]+)\s*\(", text, flags=re.M)))
 
 
 def test_header_lists_the_entry_points():
@@ -34,7 +34,7 @@ def test_header_lists_the_entry_points():
     for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qgemm_fp8b128", "qgemm_mq4v2",
                  "qg_workspace_bytes", "qg_gemm_workspace_bytes", "qg_device_status",
                  "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256",
-                 "qgemv_moe", "qgemm_moe", "qgemv_q2_0"]:
+                 "qgemv_moe", "qgemm_moe", "qgemv_q2_0", "qg_launch_count", "qgemv_i4g_noalloc"]:
         assert must in names, names
 
 
@@ -165,10 +165,14 @@ def test_gemm_and_prep_refusals(qg):
 
 
 def test_workspace_query_is_pure(qg):
-    # no split for the decode shapes of the workloads
+    # no split for these decode shapes of the workloads
     assert qg.qg_workspace_bytes(qg.QG_FMT_I4G, 1, 7168, 2048, 64) == 0
     assert qg.qg_workspace_bytes(qg.QG_FMT_FP8B128, 1, 16384, 7168) == 0
-    assert qg.qg_workspace_bytes(qg.QG_FMT_MQ4V2, 1, 17408, 5120) == 0
+    assert qg.qg_workspace_bytes(qg.QG_FMT_MQ4V2, 1, 5120, 17408) == 0
+    # 17408 MQ4 columns are more than one block's warps hold: the reduction
+    # splits, splits * S * O floats
+    n = qg.qg_workspace_bytes(qg.QG_FMT_MQ4V2, 1, 17408, 5120)
+    assert n > 0 and n % (5120 * 4) == 0
     # a short-O / long-I shape splits the reduction and needs splits*S*O floats
     n = qg.qg_workspace_bytes(qg.QG_FMT_I4G, 1, 16384, 64, 64)
     assert n > 0 and n % (64 * 4) == 0

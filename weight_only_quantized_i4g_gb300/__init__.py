@@ -38,6 +38,7 @@ _SIGNATURES = {
     "qg_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
     "qg_gemm_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
     "qg_device_status": ([ctypes.POINTER(_I)], _I),
+    "qg_launch_count": ([], ctypes.c_ulonglong),
     "qgemv_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_i4g_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "qgemv_fp8b128": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
@@ -115,6 +116,11 @@ def qg_device_status() -> tuple[int, int]:
     st = _I(0)
     rc = _lib.qg_device_status(ctypes.byref(st))
     return rc, st.value
+
+
+def qg_launch_count() -> int:
+    """Kernels the library has launched in this process."""
+    return _lib.qg_launch_count()
 
 
 def qg_workspace_bytes(fmt: int, S: int, I: int, O: int, gs: int = 0) -> int:

@@ -157,6 +157,8 @@ const char *qg_strerror(int status) {
 
 const char *qg_last_error(void) { return error_detail(); }
 
+unsigned long long qg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
 int qg_device_status(int *status) {
     if (!status) QG_REFUSE(kEInval, "qg_device_status: status must be non-NULL");
     cudaError_t e = cudaDeviceSynchronize();

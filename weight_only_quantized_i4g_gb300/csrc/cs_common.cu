@@ -308,6 +308,7 @@ void launch_splitk_reduce(float *y, const float *ws, int splits, int S, int O, c
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, y, ws, splits, n);
+    count_launch();
 }
 
 }  // namespace qg

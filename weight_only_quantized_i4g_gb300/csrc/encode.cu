@@ -57,6 +57,7 @@ int run_quantize_i4g(uint8_t *wq, float *scales, const float *w, int O, int I, i
     size_t blocks = (total + 255) / 256;
     if (blocks > 65535) blocks = 65535;
     quantize_i4g_kernel<<<(unsigned)blocks, 256, 0, st>>>(wq, scales, w, O, I, gs);
+    count_launch();
     return check_launch("qg_quantize_i4g");
 }
 
@@ -110,6 +111,7 @@ int run_encode_mq4v2(uint8_t *blocks, const float *w, int O, int I, cudaStream_t
     size_t nblk = (total + 255) / 256;
     if (nblk > 65535) nblk = 65535;
     encode_mq4v2_kernel<<<(unsigned)nblk, 256, 0, st>>>(blocks, w, O, I);
+    count_launch();
     return check_launch("qg_encode_mq4v2");
 }
 
@@ -170,9 +172,11 @@ int run_encode_mq4_one_header(uint8_t *blocks, const float *w, int O, int I, boo
     if (nblk > 65535) nblk = 65535;
     if (fp16_header) {
         encode_mq4_one_header_kernel<true><<<(unsigned)nblk, 128, 0, st>>>(blocks, w, O, I);
+        count_launch();
         return check_launch("qg_encode_mq4c");
     }
     encode_mq4_one_header_kernel<false><<<(unsigned)nblk, 128, 0, st>>>(blocks, w, O, I);
+    count_launch();
     return check_launch("qg_encode_mq4v1");
 }
 
@@ -218,6 +222,7 @@ int run_fwht256(float *out, const float *in, const int8_t *signs, size_t nblocks
     if (blocks > 65535) blocks = 65535;
     if (blocks < 1) blocks = 1;
     fwht256_kernel<<<(unsigned)blocks, 256, 0, st>>>(out, in, signs, nblocks);
+    count_launch();
     return check_launch("qg_fwht256");
 }
 

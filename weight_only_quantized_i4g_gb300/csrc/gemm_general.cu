@@ -116,6 +116,7 @@ int launch_general(float *Y, const uint16_t *X, const W &wat, int M, int I, int 
                    const char *what) {
     dim3 grid((O + kGT - 1) / kGT, (M + kGT - 1) / kGT);
     gemm_general_kernel<W><<<grid, 256, 0, st>>>(Y, X, wat, M, I, O);
+    count_launch();
     return check_launch(what);
 }
 

@@ -1043,6 +1043,7 @@ int launch_tile(const Plan &p, const CUtensorMap &tmX, const KArgs<GR> &args, cu
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaLaunchKernelEx(&cfg, gemm_tc_kernel<F, BT, GR>, tmX, args);
+    count_launch();
     return check_launch(F::kName);
 }
 
@@ -1098,6 +1099,7 @@ int launch_plan(const Plan &p, float *Y, const uint16_t *X, KArgs<GR> args, int 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         cudaLaunchKernelEx(&cfg, gemm_tc_prep_kernel<F, GR>, args, X, I);
+        count_launch();
         const int rc = check_launch(F::kName);
         if (rc != kOk) return rc;
     }

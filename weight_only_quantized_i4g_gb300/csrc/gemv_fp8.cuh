@@ -347,6 +347,7 @@ void launch_cs_fp8(const typename FmtFp8<SC>::Params &p, float *out, const CsPla
     dim3 grid(pl.grid_x, pl.splits);
     gemv_cs_kernel<FmtFp8<SC>, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
                                                                          pl.nrowb);
+    count_launch();
 }
 
 template <class SC, int S>
@@ -432,7 +433,7 @@ int gemv_fp8_chunk(float *y, const uint16_t *x, const uint8_t *w, const typename
         const int cap = num_sms() * 16;
         const int grid = blocks_needed < cap ? blocks_needed : cap;
         switch (S) {
-#define QG_CASE(SS) case SS: gemv_fp8_general_kernel<SC, SS><<<grid, 256, 0, st>>>(y, x, w, scale_inv, I, O); break;
+#define QG_CASE(SS) case SS: gemv_fp8_general_kernel<SC, SS><<<grid, 256, 0, st>>>(y, x, w, scale_inv, I, O); count_launch(); break;
             QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
 #undef QG_CASE
         }

@@ -15,12 +15,17 @@
 // Two elements at a time with packed f32x2 add and fma.
 //
 // Paths, fastest first:
+//   mma      gemv_mma.cuh: nibbles as fp16 operands of the warp-level MMA,
+//            f32 activations as an fp16 high and low part (two MMA columns
+//            per token, four tokens per launch); needs 16-byte aligned w, x
+//            and scales, I % 64 == 0, gs 64 or 128 and ceil(I/gs) % 4 == 0
 //   staged   gemv_tma.cuh: bulk copies of whole rows (and their scales) into
 //            a shared-memory ring; needs 16-byte aligned w, x and scales,
 //            I % 32 == 0, gs a multiple of the unit and ceil(I/gs) % 4 == 0
 //   direct   gemv_cs.cuh: the same decode with 16-, 8- or 4-byte global loads
 //   general  any shape and alignment, byte loads
 #include "gemv_cs.cuh"
+#include "gemv_mma.cuh"
 #include "gemv_tma.cuh"
 #include "launch.h"
 
@@ -200,6 +205,52 @@ struct FmtI4G {
     }
 };
 
+// Warp-MMA decode (gemv_mma.cuh).  A scale unit is one 64-weight span, which
+// lies inside one group (gs = 64 or 128).  The C operand starts every unit's
+// sum at -8 sum(x), so D = sum((n - 8) x) and acc += scale * D.  Each token
+// takes two MMA columns: x = high + low, both fp16 (x * 2^k rounded to fp16,
+// and the rounding remainder rounded to fp16), which keeps 22 significant
+// bits of the f32 activation.
+template <int LG>   // gs = 64 << LG
+struct MmaI4G {
+    static constexpr bool kHiLo = true;
+    static constexpr bool kNeg8 = true;
+    static constexpr int kSpansPerUnit = 1;
+    static constexpr bool kFenceUnits = true;
+    static constexpr int kMaxConsumerWarps = 14;   // 7168 columns; 136 registers a thread
+    typedef FmtI4G::Params Params;
+    typedef float Side;
+    __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.rb; }
+    __device__ static uint32_t aux_row_bytes(const Params &p) { return (uint32_t)p.ng * 4u; }
+    __device__ static const void *w_src(const Params &p, int o, uint32_t col) { return p.w + (size_t)o * p.rb + col; }
+    __device__ static const void *a_src(const Params &p, int o) { return p.scales + (size_t)o * p.ng; }
+    __host__ __device__ static uint32_t span_byte(int sp) { return 32u * (uint32_t)sp; }
+    __device__ static uint32_t span_off(int sp_local) { return 32u * (uint32_t)sp_local; }
+    static constexpr int kXWords = 8;   // eight f32 activations
+    __device__ static const void *x_src(const Params &p, int tok, int col) { return p.x + (size_t)tok * p.I + col; }
+    __device__ static float abs_max8(const uint32_t (&w)[8]) {
+        float m = fabsf(__uint_as_float(w[0]));
+#pragma unroll
+        for (int e = 1; e < 8; ++e) m = fmaxf(m, fabsf(__uint_as_float(w[e])));
+        return m;
+    }
+    __device__ static uint64_t pair(const uint32_t (&w)[8], int i) {
+        return (uint64_t)w[2 * i] | ((uint64_t)w[2 * i + 1] << 32);
+    }
+    // byte offset of unit u's group scale in the staged scale row (a group
+    // is 2^LG spans; the warp's first span is a multiple of 8)
+    __device__ static uint32_t side_off(int sp_abs0, int, int u) {
+        return ((uint32_t)(sp_abs0 >> LG) + (uint32_t)(u >> LG)) << 2;
+    }
+    __device__ static Side side(uint32_t, uint32_t row_a, uint32_t off) { return lds_f32_at(row_a + off); }
+    __device__ static void apply(float (&acc)[4], const float (&d)[4], Side s0, Side s1, const float (&)[2]) {
+        acc[0] = fmaf(s0, d[0], acc[0]);
+        acc[1] = fmaf(s0, d[1], acc[1]);
+        acc[2] = fmaf(s1, d[2], acc[2]);
+        acc[3] = fmaf(s1, d[3], acc[3]);
+    }
+};
+
 // ---------------------------------------------------------------------------
 // General kernel: any I, any even gs, any alignment.  One warp per row; lanes
 // walk the elements; byte loads.
@@ -255,6 +306,18 @@ bool i4g_tma_ok(const float *x, const uint8_t *w, const float *scales, int I, in
            ((uintptr_t)x % 16 == 0) && ((uintptr_t)scales % 16 == 0);
 }
 
+bool i4g_mma_ok(const float *x, const uint8_t *w, const float *scales, int I, int gs) {
+    const int ng = (I + gs - 1) / gs;
+    return (I % 64 == 0) && (gs == 64 || gs == 128) && (ng % 4 == 0) && ((uintptr_t)w % 16 == 0) &&
+           ((uintptr_t)x % 16 == 0) && ((uintptr_t)scales % 16 == 0);
+}
+
+// S <= 4 tokens per launch (two MMA columns each)
+bool i4g_mma_plan(int S, int I, int O, int gs, MmaPlan *pl) {
+    return mma_plan(I / 64, 8, (uint32_t)(I / 2), (uint32_t)((I + gs - 1) / gs) * 4u, 4u, S, O, 16,
+                    MmaI4G<0>::kMaxConsumerWarps, [](int sp) { return 32u * (uint32_t)sp; }, pl);
+}
+
 bool i4g_tma_plan(int S, int I, int O, int gs, TmaPlan *pl) {
     const int nw = i4g_nw(S);
     TmaGeom g;
@@ -283,6 +346,7 @@ void launch_cs_i4g(const FmtI4G::Params &p, float *out, const CsPlan &pl, int un
     dim3 grid(pl.grid_x, pl.splits);
     gemv_cs_kernel<FmtI4G, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
                                                                      pl.nrowb);
+    count_launch();
 }
 
 template <int S>
@@ -356,7 +420,7 @@ int gemv_i4g_chunk(float *y, const float *x, const uint8_t *w, const float *scal
         const int cap = num_sms() * 16;
         const int grid = blocks_needed < cap ? blocks_needed : cap;
         switch (S) {
-#define QG_CASE(SS) case SS: gemv_i4g_general_kernel<SS><<<grid, 256, 0, st>>>(y, x, w, scales, I, O, gs); break;
+#define QG_CASE(SS) case SS: gemv_i4g_general_kernel<SS><<<grid, 256, 0, st>>>(y, x, w, scales, I, O, gs); count_launch(); break;
             QG_CASE(1) QG_CASE(2) QG_CASE(3) QG_CASE(4) QG_CASE(5) QG_CASE(6) QG_CASE(7) QG_CASE(8)
 #undef QG_CASE
         }
@@ -385,6 +449,11 @@ int gemv_i4g_chunk(float *y, const float *x, const uint8_t *w, const float *scal
 
 size_t ws_i4g(int S, int I, int O, int gs) {
     const int s = S < 8 ? S : 8;
+    size_t mma_need = 0;
+    MmaPlan mp;
+    if (I % 64 == 0 && (gs == 64 || gs == 128) && ((I + gs - 1) / gs) % 4 == 0 &&
+        i4g_mma_plan(s < 4 ? s : 4, I, O, gs, &mp) && mp.splits > 1)
+        mma_need = (size_t)mp.splits * (s < 4 ? s : 4) * O * sizeof(float);
     if (I % (8 * i4g_nw(s)) != 0 || gs % (8 * i4g_nw(s)) != 0) return 0;  // general kernel: none
     // the larger of the staged and the direct plan (the pointers decide the path)
     size_t need = 0;
@@ -393,11 +462,39 @@ size_t ws_i4g(int S, int I, int O, int gs) {
         need = (size_t)tp.splits * s * O * sizeof(float);
     int U = 1;
     const size_t cs = cs_ws_bytes(i4g_plan(s, I, O, &U), s, O);
-    return need > cs ? need : cs;
+    return std::max(mma_need, need > cs ? need : cs);
 }
 
 int run_gemv_i4g(float *y, const float *x, const uint8_t *w, const float *scales, int S, int I, int O,
                  int gs, void *ws, size_t ws_bytes, cudaStream_t st) {
+    // The warp-MMA kernel from two tokens on; at one token the staged kernel
+    // is faster on the 8 MB decode shapes (measured on GB300: 2048x7168 4.3
+    // against 5.8 us, 7168x2048 4.35 against 4.9).
+    if (S > 1 && i4g_mma_ok(x, w, scales, I, gs)) {
+        FmtI4G::Params p;
+        p.w = w; p.scales = scales; p.I = I; p.O = O; p.gs = gs;
+        p.ng = (I + gs - 1) / gs; p.rb = ((size_t)I + 1) / 2;
+        for (int s0 = 0; s0 < S; s0 += 4) {
+            const int sc = S - s0 < 4 ? S - s0 : 4;
+            MmaPlan mp;
+            if (!i4g_mma_plan(sc, I, O, gs, &mp)) break;   // the staged / direct paths below
+            const size_t need = mp.splits > 1 ? (size_t)mp.splits * sc * O * sizeof(float) : 0;
+            if (need > 0 && (ws == nullptr || ws_bytes < need)) {
+                set_error_detail("qgemv_i4g: this shape splits the reduction and needs %zu bytes of workspace "
+                                 "(got %zu)", need, ws == nullptr ? (size_t)0 : ws_bytes);
+                return kEWorkspace;
+            }
+            p.x = x + (size_t)s0 * I;
+            float *yc = y + (size_t)s0 * O;
+            float *out = mp.splits > 1 ? static_cast<float *>(ws) : yc;
+            if (gs == 64) launch_mma<MmaI4G<0>, kMmaSpansPerWarp, 16>(p, out, mp, st);
+            else launch_mma<MmaI4G<1>, kMmaSpansPerWarp, 16>(p, out, mp, st);
+            if (mp.splits > 1) launch_splitk_reduce(yc, static_cast<float *>(ws), mp.splits, sc, O, st);
+            const int rc = check_launch("qgemv_i4g");
+            if (rc != kOk) return rc;
+            if (s0 + sc >= S) return kOk;
+        }
+    }
     for (int s0 = 0; s0 < S; s0 += 8) {
         const int sc = S - s0 < 8 ? S - s0 : 8;
         const int rc = gemv_i4g_chunk(y + (size_t)s0 * O, x + (size_t)s0 * I, w, scales, sc, I, O, gs, ws,

@@ -287,6 +287,7 @@ void launch_q2(const FmtQ2::Params &p, float *out, const CsPlan &pl, int units, 
     dim3 grid(pl.grid_x, pl.splits);
     gemv_cs_kernel<FmtQ2, S, 1, U, q2_rb(S)><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
                                                                          pl.nrowb);
+    count_launch();
 }
 
 template <int S>

@@ -602,6 +602,7 @@ void launch_tma(const typename F::Params &p, float *out, const TmaPlan &pl, cuda
     else
         cudaLaunchKernelEx(&cfg, kern, p, out, pl.units, pl.units_per_split, pl.nrowb, pl.nst, pl.L,
                            device_error_word());
+    count_launch();
 }
 
 }  // namespace qg

@@ -6,6 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 namespace qg {
@@ -18,6 +19,11 @@ void set_error_detail(const char *fmt, ...);
 
 // Reports launch errors of the kernels just enqueued.
 int check_launch(const char *what);
+
+// Kernel launches of this library in this process (qg_launch_count()); every
+// launch site counts itself.
+inline std::atomic<unsigned long long> g_launches{0};
+inline void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // Reads and clears this device's kernel error word (0 or a qg status).
 int read_device_error(int *status);
