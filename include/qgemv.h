@@ -91,6 +91,21 @@ int qg_device_status(int *status);
  * counterpart.  Never fails. */
 unsigned long long qg_launch_count(void);
 
+/* Test aid for the failure path above (no counterpart in the pages, whose
+ * fp8 page asks that failures be loud and every refusal name its condition).
+ * Runs one block of the staging pipeline on the current device in which a
+ * consumer waits for a batch that is never issued: its bounded wait gives up
+ * after spin_limit polls (1 .. 4194304, the kernels' own limit) instead of
+ * 4194304, records QG_ETIMEOUT in the device error word and ends the other
+ * wait of the block, whose producer first lands the copy it issued.
+ * Synchronizes the device; *observed receives what the block saw (bit 0: the
+ * consumer gave up on the missing batch; bit 1: the producer's wait ended on
+ * the block's abort flag; bit 2: the issued copy landed before the block
+ * exited), and the error word is left for qg_device_status to read.
+ * Nothing faults and the context stays usable.  Returns QG_OK, QG_EINVAL
+ * (NULL observed or spin_limit out of range) or QG_ECUDA. */
+int qg_selftest_wait_timeout(int spin_limit, int *observed);
+
 /* Format ids for qg_workspace_bytes. */
 enum {
     QG_FMT_I4G = 4,         /* grouped int4 (fmt=4)                            */

@@ -34,7 +34,8 @@ def test_header_lists_the_entry_points():
     for must in ["qgemv_i4g", "qgemv_fp8b128", "qgemv_mq4v2", "qgemm_i4g", "qgemm_fp8b128", "qgemm_mq4v2",
                  "qg_workspace_bytes", "qg_gemm_workspace_bytes", "qg_device_status",
                  "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256",
-                 "qgemv_moe", "qgemm_moe", "qgemv_q2_0", "qg_launch_count", "qgemv_i4g_noalloc"]:
+                 "qgemv_moe", "qgemm_moe", "qgemv_q2_0", "qg_launch_count", "qgemv_i4g_noalloc",
+                 "qg_selftest_wait_timeout"]:
         assert must in names, names
 
 
@@ -191,3 +192,14 @@ def test_gemm_workspace_query(qg):
     assert qg.qg_gemm_workspace_bytes(qg.QG_FMT_FP8B128, 64, 1000, 256) == 0
     assert qg.qg_gemm_workspace_bytes(qg.QG_FMT_MQ4V2, 64, 300, 256) == 0
     assert qg.qg_gemm_workspace_bytes(qg.QG_FMT_MQ4V2, 0, 256, 256) == 0
+
+
+def test_selftest_refusals(qg):
+    """Bad arguments are refused on the host, before any launch."""
+    lib = ctypes.CDLL(qg.LIB_PATH)
+    lib.qg_selftest_wait_timeout.argtypes = [ctypes.c_int, ctypes.c_void_p]
+    v = ctypes.c_int(0)
+    assert lib.qg_selftest_wait_timeout(1024, None) == qg.QG_EINVAL
+    assert lib.qg_selftest_wait_timeout(0, ctypes.byref(v)) == qg.QG_EINVAL
+    assert lib.qg_selftest_wait_timeout((1 << 22) + 1, ctypes.byref(v)) == qg.QG_EINVAL
+    assert "spin_limit" in qg.last_error()

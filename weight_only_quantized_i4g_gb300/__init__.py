@@ -39,6 +39,7 @@ _SIGNATURES = {
     "qg_gemm_workspace_bytes": ([_I, _I, _I, _I, _I], _Z),
     "qg_device_status": ([ctypes.POINTER(_I)], _I),
     "qg_launch_count": ([], ctypes.c_ulonglong),
+    "qg_selftest_wait_timeout": ([_I, ctypes.POINTER(_I)], _I),
     "qgemv_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_i4g_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "qgemv_fp8b128": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
@@ -121,6 +122,13 @@ def qg_device_status() -> tuple[int, int]:
 def qg_launch_count() -> int:
     """Kernels the library has launched in this process."""
     return _lib.qg_launch_count()
+
+
+def qg_selftest_wait_timeout(spin_limit: int) -> tuple[int, int]:
+    """(status, observed bits) of the failure-path test aid."""
+    v = _I(0)
+    rc = _lib.qg_selftest_wait_timeout(spin_limit, ctypes.byref(v))
+    return rc, v.value
 
 
 def qg_workspace_bytes(fmt: int, S: int, I: int, O: int, gs: int = 0) -> int:

@@ -33,10 +33,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-// Wait for the phase of the given parity to complete; false after kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// Wait for the phase of the given parity to complete; false after `limit`
+// polls (kSpinLimit unless a test asks for a short wait).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = kSpinLimit) {
     const uint32_t a = smem_addr(bar);
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    for (uint32_t it = 0; it < limit; ++it) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
@@ -54,9 +55,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
 // 256 tries), and sets *abort itself when it runs out of tries, so that one
 // timed-out wait ends the other waits of the block quickly.  Polls without
 // sleeping: for the waits on a pipeline's critical path.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort) {
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, volatile uint32_t *abort,
+                                                   uint32_t limit = kSpinLimit) {
     const uint32_t a = smem_addr(bar);
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    for (uint32_t it = 0; it < limit; ++it) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
