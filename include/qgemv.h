@@ -62,8 +62,11 @@ typedef enum {
     QG_EWORKSPACE = -5,  /* workspace NULL or smaller than required          */
     QG_ECUDA = -6,       /* CUDA runtime error (no device, launch failure)   */
     QG_ETIMEOUT = -7,    /* a kernel gave up waiting (see qg_device_status)  */
-    QG_EEXPERT = -8      /* qgemv_moe: a slot's expert id was out of range   */
+    QG_EEXPERT = -8,     /* qgemv_moe: a slot's expert id was out of range   */
                          /* or its weights misaligned (qg_device_status)     */
+    QG_EBOUNDS = -9      /* bounds-checking build only: a kernel formed an   */
+                         /* index outside its arrays and skipped the access  */
+                         /* (qg_device_status; never raised by libqgemv.so)  */
 } qg_status;
 
 /* Static name of a status code ("QG_EGS: ..."). Never NULL. */

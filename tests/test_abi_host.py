@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(qg):
 
 
 def test_strerror(qg):
-    for code in range(0, -9, -1):
+    for code in range(0, -10, -1):
         assert qg.strerror(code).startswith("QG_")
     assert "unknown" in qg.strerror(-99)
 

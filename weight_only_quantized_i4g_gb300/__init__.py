@@ -23,8 +23,8 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-QG_OK, QG_EINVAL, QG_EGS, QG_ESHAPE, QG_EALIGN, QG_EWORKSPACE, QG_ECUDA, QG_ETIMEOUT, QG_EEXPERT = (
-    0, -1, -2, -3, -4, -5, -6, -7, -8)
+QG_OK, QG_EINVAL, QG_EGS, QG_ESHAPE, QG_EALIGN, QG_EWORKSPACE, QG_ECUDA, QG_ETIMEOUT, QG_EEXPERT, QG_EBOUNDS = (
+    0, -1, -2, -3, -4, -5, -6, -7, -8, -9)
 QG_FMT_I4G, QG_FMT_FP8B128, QG_FMT_FP8UE8M0, QG_FMT_MQ4V1, QG_FMT_MQ4V2, QG_FMT_MQ4C, QG_FMT_Q2_0 = (
     4, 7, 71, 13, 44, 45, 20)
 

@@ -73,6 +73,55 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
     return LIB
 
 
+# Translation units of the decode GEMVs: the bounds-checking build compiles
+# these with -DQG_BOUNDS_CHECK (every index a kernel forms is guarded; a guard
+# that fails records QG_EBOUNDS and skips its access) and links them with the
+# normal objects of the other units.
+BC_UNITS = ("cs_common.cu", "gemv_i4g.cu", "gemv_fp8b128.cu", "gemv_fp8ue8m0.cu", "gemv_mq4v2.cu", "gemv_mq4v1.cu",
+            "gemv_mq4c.cu", "gemv_q2_0.cu", "noalloc.cu")
+BUILD_BC = os.path.join(PKG, "_build_bc")
+LIB_BC = os.path.join(PKG, "libqgemv_bc.so")
+
+
+def build_bounds_check(verbose: bool = False) -> str:
+    """libqgemv_bc.so: the library with index guards in its decode GEMVs (for
+    tests; slower than libqgemv.so, same results)."""
+    build(verbose=verbose)
+    os.makedirs(BUILD_BC, exist_ok=True)
+    headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
+        glob.glob(os.path.join(PKG, "..", "include", "*.h"))
+    objs, jobs = [], []
+    for s in sources():
+        name = os.path.basename(s)
+        if name not in BC_UNITS:
+            objs.append(os.path.join(BUILD, name[:-3] + ".o"))
+            continue
+        o = os.path.join(BUILD_BC, name[:-3] + ".o")
+        objs.append(o)
+        if not _newer(o, [s, *headers]):
+            jobs.append([NVCC, *ARCH, *NVFLAGS, "-DQG_BOUNDS_CHECK", "-c", s, "-o", o])
+    with ThreadPoolExecutor(max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
+        results = list(ex.map(lambda c: (c, subprocess.run(c, capture_output=True, text=True)), jobs))
+    failed = [c[-3] for c, r in results if r.returncode != 0]
+    for c, r in results:
+        if verbose or r.returncode != 0:
+            print(" ".join(c))
+            print(r.stdout + r.stderr)
+    if failed:
+        raise RuntimeError("nvcc (bounds-checking build) failed for: " + ", ".join(failed))
+    if jobs or not _newer(LIB_BC, objs):
+        tmp = LIB_BC + ".tmp%d" % os.getpid()
+        r = subprocess.run([NVCC, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+                            "-Xlinker", "-rpath,/usr/local/cuda/lib64"], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("link failed (bounds-checking build):\n" + r.stdout + r.stderr)
+        os.replace(tmp, LIB_BC)
+    return LIB_BC
+
+
 if __name__ == "__main__":
     import sys
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, ptxas_info="--ptxas" in sys.argv))
+    if "--bounds-check" in sys.argv:
+        print(build_bounds_check(verbose="-v" in sys.argv))
+    else:
+        print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, ptxas_info="--ptxas" in sys.argv))

@@ -151,6 +151,7 @@ const char *qg_strerror(int status) {
         case QG_ECUDA: return "QG_ECUDA: CUDA runtime error";
         case QG_ETIMEOUT: return "QG_ETIMEOUT: a kernel gave up waiting on a barrier";
         case QG_EEXPERT: return "QG_EEXPERT: a routed slot named a missing expert or one with misaligned weights";
+        case QG_EBOUNDS: return "QG_EBOUNDS: a kernel formed an index outside its arrays (bounds-checking build)";
         default: return "unknown qg_status";
     }
 }

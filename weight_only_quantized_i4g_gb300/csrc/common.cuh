@@ -127,6 +127,21 @@ __device__ __forceinline__ int reduce_scatter_index(int lane) {
     return (lane >> (5 - kLog)) & (N - 1);
 }
 
+// Index guards of the bounds-checking build (compiled with -DQG_BOUNDS_CHECK,
+// the stand-in for a memory checker): a guard whose condition is false records
+// QG_EBOUNDS in the device error word `err` and the access it protects is
+// skipped.  In the normal build every guard is the constant true and costs
+// nothing.
+constexpr int kErrBounds = -9;
+#ifdef QG_BOUNDS_CHECK
+__device__ __forceinline__ bool qg_guard(bool ok, int *err) {
+    if (!ok && err != nullptr) atomicExch(err, kErrBounds);
+    return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool qg_guard(bool, int *) { return true; }
+#endif
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);

@@ -44,6 +44,25 @@ unsigned long long current_context_id() {
     return id;
 }
 
+void set_max_dynamic_smem(const void *kernel, int bytes) {
+    struct Entry { unsigned long long ctx; const void *fn; };
+    static std::mutex mu;
+    static Entry table[512];
+    static int n = 0, next = 0;
+    const unsigned long long ctx = current_context_id();
+    std::lock_guard<std::mutex> lk(mu);
+    if (ctx != 0)
+        for (int i = 0; i < n; ++i)
+            if (table[i].ctx == ctx && table[i].fn == kernel) return;
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    cudaGetLastError();
+    const unsigned long long id = ctx != 0 ? ctx : current_context_id();
+    if (id == 0) return;
+    table[next] = Entry{id, kernel};
+    next = (next + 1) % 512;
+    if (n < 512) ++n;
+}
+
 int *device_error_word() {
     static PerContext<int *> cache;
     int *w = nullptr;

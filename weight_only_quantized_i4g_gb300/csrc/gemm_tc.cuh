@@ -1023,15 +1023,7 @@ int launch_tile(const Plan &p, const CUtensorMap &tmX, const KArgs<GR> &args, cu
     using C = Cfg<BT>;
     // The shared-memory limit is an attribute of the kernel in the current
     // context: set once per context.
-    static PerContext<char> attr_set;
-    char done = 0;
-    attr_set.get(&done, [](char *v) {
-        cudaFuncSetAttribute(gemm_tc_kernel<F, BT, GR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::kSmemBytes);
-        cudaGetLastError();
-        *v = 1;
-        return (int)kOk;
-    });
+    set_max_dynamic_smem(reinterpret_cast<const void *>(gemm_tc_kernel<F, BT, GR>), (int)C::kSmemBytes);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.P);
     cfg.blockDim = dim3(kThreads);

@@ -45,17 +45,34 @@ template <int X> struct NextPow2 {
 // defines load_unit (units that are only 2-byte aligned).
 template <class F, int NW, class = void>
 struct CsLoad {
+    static constexpr uint32_t kBytes = 4u * NW;     // bytes a unit load reads
     __device__ static Words<NW> load(const void *p) { return ld_stream<NW>(p); }
 };
 template <class F, int NW>
 struct CsLoad<F, NW, std::void_t<decltype(&F::template load_unit<NW>)>> {
+    static constexpr uint32_t kBytes = 2u * NW;     // 16-bit units
     __device__ static Words<NW> load(const void *p) { return F::template load_unit<NW>(p); }
 };
+
+// Guards of the bounds-checking build for a unit access of row o: the unit's
+// bytes lie inside the row, its side data inside its array; activations of
+// token s, unit u lie inside x.
+template <class F, int NW>
+__device__ __forceinline__ bool cs_unit_in_bounds(const typename F::Params &p, int o, int u, int XU,
+                                                  const typename F::ThreadConst &tc) {
+    const long off = (long)((const uint8_t *)F::unit_ptr(p, o, u, XU) - (const uint8_t *)F::w_src(p, o, 0u));
+    return o >= 0 && o < p.O && u >= 0 && off >= 0 && off + (long)CsLoad<F, NW>::kBytes <= (long)F::row_bytes(p) &&
+           F::aux_ok(p, o, tc);
+}
+template <class F>
+__device__ __forceinline__ bool x_unit_in_bounds(const typename F::Params &p, int s, int S, int u, int XU) {
+    return s >= 0 && s < S && (u < 0 || (long)(u + 1) * XU <= (long)p.I);
+}
 
 template <class F, int S, int NW, int U, int RB>
 __global__ void __launch_bounds__(kCsMaxThreads)
 gemv_cs_kernel(const typename F::Params p, float *__restrict__ out, int units, int units_per_split,
-               int nrowb)
+               int nrowb, int *err)
 {
     constexpr int XU = NW * F::kElemsPerWord;           // elements per unit
     constexpr int NV = NextPow2<RB * S>::value;          // reduced values per batch
@@ -83,8 +100,11 @@ gemv_cs_kernel(const typename F::Params p, float *__restrict__ out, int units, i
         uok[j] = uidx[j] < uend;
         tc[j] = F::thread_const(p, uok[j] ? uidx[j] : 0, XU);
 #pragma unroll
-        for (int s = 0; s < S; ++s)
-            F::template load_x<XU>(p, s, uok[j] ? uidx[j] : -1, xs[j][s], xsum[j][s]);
+        for (int s = 0; s < S; ++s) {
+            const int ux = uok[j] ? uidx[j] : -1;
+            F::template load_x<XU>(p, s, qg_guard(x_unit_in_bounds<F>(p, s, S, ux, XU), err) ? ux : -1, xs[j][s],
+                                   xsum[j][s]);
+        }
     }
 
     // ---- walk the row batches ---------------------------------------------
@@ -98,7 +118,7 @@ gemv_cs_kernel(const typename F::Params p, float *__restrict__ out, int units, i
             const int o = o0 + r;
 #pragma unroll
             for (int j = 0; j < U; ++j) {
-                if (o < p.O && uok[j]) {
+                if (o < p.O && uok[j] && qg_guard(cs_unit_in_bounds<F, NW>(p, o, uidx[j], XU, tc[j]), err)) {
                     raw[r][j] = CsLoad<F, NW>::load(F::unit_ptr(p, o, uidx[j], XU));
                     aux[r][j] = F::unit_aux(p, o, uidx[j], tc[j]);
                 } else {
@@ -127,7 +147,7 @@ gemv_cs_kernel(const typename F::Params p, float *__restrict__ out, int units, i
             const int o = o0 + r;
             float acc = 0.f;
             for (int w = 0; w < nwarps; ++w) acc += red[buf][w][tid];
-            if (o < p.O) out[((size_t)split * S + s) * p.O + o] = acc;
+            if (o < p.O && qg_guard(split < (int)gridDim.y && s < S, err)) out[((size_t)split * S + s) * p.O + o] = acc;
         }
     }
 }

@@ -57,6 +57,10 @@ struct FmtFp8 {
         return SC::get(p.scale_inv, (size_t)(o >> 7) * p.nbi + tc.ib);
     }
     __device__ static Aux zero_aux() { return 0.f; }
+    // the unit's block scale lies inside the [ceil(O/128), ceil(I/128)] array
+    __device__ static bool aux_ok(const Params &p, int o, ThreadConst tc) {
+        return tc.ib >= 0 && tc.ib < p.nbi && (o >> 7) < (p.O + 127) / 128;
+    }
 
     // xs: natural element order, f32
     template <int XU>
@@ -346,7 +350,7 @@ void launch_cs_fp8(const typename FmtFp8<SC>::Params &p, float *out, const CsPla
     constexpr int RB = S <= 2 ? (U == 1 ? 8 : 4) : 4;
     dim3 grid(pl.grid_x, pl.splits);
     gemv_cs_kernel<FmtFp8<SC>, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
-                                                                         pl.nrowb);
+                                                                         pl.nrowb, device_error_word());
     count_launch();
 }
 

@@ -55,6 +55,8 @@ struct FmtI4G {
         return ld_nc_f32(p.scales + (size_t)o * p.ng + tc.g);
     }
     __device__ static Aux zero_aux() { return 0.f; }
+    // the unit's group scale lies inside the row's scales (bounds-checking build)
+    __device__ static bool aux_ok(const Params &p, int, ThreadConst tc) { return tc.g >= 0 && tc.g < p.ng; }
 
     // xs layout: pair i = 4*w + q holds elements (8w + q, 8w + q + 4), both
     // scaled by 16^-q, at xs[2i], xs[2i+1].
@@ -345,7 +347,7 @@ void launch_cs_i4g(const FmtI4G::Params &p, float *out, const CsPlan &pl, int un
     constexpr int RB = S <= 2 ? (U == 1 ? 8 : 4) : 4;
     dim3 grid(pl.grid_x, pl.splits);
     gemv_cs_kernel<FmtI4G, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
-                                                                     pl.nrowb);
+                                                                     pl.nrowb, device_error_word());
     count_launch();
 }
 

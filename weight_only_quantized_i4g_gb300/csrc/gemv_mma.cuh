@@ -205,8 +205,13 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
         const int slot = k % nst;
         const int o0 = (b + k * Gx) * RB;
         const int rows = min(RB, p.O - o0);
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)rows * (seg_bytes + arowbytes));
+        // the batch's rows lie inside the matrix and the segment inside a row
+        // (bounds-checking build); a refused batch is armed with no bytes
+        const bool in = qg_guard(o0 >= 0 && rows >= 1 && o0 + rows <= p.O && seg_col + seg_bytes <= F::row_bytes(p),
+                                 err);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], in ? (uint32_t)rows * (seg_bytes + arowbytes) : 0u);
         __syncwarp();
+        if (!in) return;
         uint8_t *dw = stage_w + (size_t)slot * L.stage_w;
         if (nsplit == 1) {
             // whole rows: four consecutive rows are consecutive in memory
@@ -261,7 +266,8 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
         if (lane == 0) mbar_arrive_expect_tx(x_full, (uint32_t)S * xseg_bytes);
         __syncwarp();
         for (int s = lane; s < S; s += 32)
-            bulk_copy_g2s(xstage + (size_t)s * L.x_stride, F::x_src(p, s, sp_begin * 64), xseg_bytes, x_full);
+            if (qg_guard((long)sp_begin * 64 + (long)(xseg_bytes / kXElem) <= (long)p.I, err))
+                bulk_copy_g2s(xstage + (size_t)s * L.x_stride, F::x_src(p, s, sp_begin * 64), xseg_bytes, x_full);
         for (int k = 1; k < nw0; ++k) issue(k);
         // The slots under the activations, once every consumer has its fragments.
         if (nw0 < first) {
@@ -298,7 +304,8 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
                     if (ri[v] >= 0) acc[v] += rs[((size_t)w * RB + ri[v]) * 8 + si[v]];
 #pragma unroll
             for (int v = 0; v < 4; ++v)
-                if (ri[v] >= 0 && o0 + ri[v] < p.O) out[((size_t)split * S + si[v]) * p.O + o0 + ri[v]] = acc[v];
+                if (ri[v] >= 0 && o0 + ri[v] < p.O && qg_guard(split < nsplit && si[v] < S, err))
+                    out[((size_t)split * S + si[v]) * p.O + o0 + ri[v]] = acc[v];
             __syncwarp();
         }
         return;
@@ -611,14 +618,7 @@ bool mma_plan(int nsp, int granule, uint32_t rowbytes, uint32_t arowbytes, uint3
 template <class F, int NS, int RB>
 void launch_mma(const typename F::Params &p, float *out, const MmaPlan &pl, cudaStream_t st) {
     auto kern = gemv_mma_kernel<F, NS, RB>;
-    static PerContext<char> attr_set;
-    char done = 0;
-    attr_set.get(&done, [kern](char *v) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-        cudaGetLastError();
-        *v = 1;
-        return (int)kOk;
-    });
+    set_max_dynamic_smem(reinterpret_cast<const void *>(kern), 232448);
     const int threads = 32 * (pl.nc + 1);
     int per_sm = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, pl.L.total) != cudaSuccess ||

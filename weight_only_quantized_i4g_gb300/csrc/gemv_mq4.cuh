@@ -101,6 +101,10 @@ struct FmtMq4 {
         return Hdr::load_global(p.blocks + (size_t)o * p.rowbytes + tc.hoff);
     }
     __device__ static Aux zero_aux() { return Hdr::zero_raw(); }
+    // the unit's header lies inside the row (bounds-checking build)
+    __device__ static bool aux_ok(const Params &p, int, ThreadConst tc) {
+        return tc.hoff >= 0 && (size_t)tc.hoff + sizeof(Aux) <= p.rowbytes;
+    }
 
     template <int XU>
     __device__ static void load_x(const Params &p, int s, int u, float (&xs)[XU], float &xsum) {
@@ -512,7 +516,7 @@ void launch_cs_mq4(const Mq4Params &p, float *out, const CsPlan &pl, int units, 
     constexpr int RB = S <= 2 ? (U == 1 ? 8 : 4) : 4;
     dim3 grid(pl.grid_x, pl.splits);
     gemv_cs_kernel<FmtMq4<HK>, S, NW, U, RB><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
-                                                                       pl.nrowb);
+                                                                       pl.nrowb, device_error_word());
     count_launch();
 }
 

@@ -40,6 +40,14 @@ struct FmtQ2 {
         return f16_bits_to_f32(h);
     }
     __device__ static Aux zero_aux() { return 0.f; }
+    // the unit's d lies inside the row (bounds-checking build)
+    __device__ static bool aux_ok(const Params &p, int, ThreadConst tc) {
+        return tc.doff >= 0 && (size_t)tc.doff + 2 <= p.rowbytes;
+    }
+    __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.rowbytes; }
+    __device__ static const void *w_src(const Params &p, int o, uint32_t col) {
+        return p.blocks + (size_t)o * p.rowbytes + col;
+    }
     template <int NW>
     __device__ static Words<NW> load_unit(const void *ptr) {
         static_assert(NW == 1, "a Q2_0 unit is one 16-bit load");
@@ -286,7 +294,7 @@ template <int S, int U>
 void launch_q2(const FmtQ2::Params &p, float *out, const CsPlan &pl, int units, cudaStream_t st) {
     dim3 grid(pl.grid_x, pl.splits);
     gemv_cs_kernel<FmtQ2, S, 1, U, q2_rb(S)><<<grid, pl.threads, 0, st>>>(p, out, units, pl.units_per_split,
-                                                                         pl.nrowb);
+                                                                         pl.nrowb, device_error_word());
     count_launch();
 }
 

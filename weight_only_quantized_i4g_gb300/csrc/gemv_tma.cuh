@@ -306,7 +306,11 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
             const int o0 = (b + k * G) * RB;
             const int rows = min(RB, p.O - o0);
             const uint32_t wb = (uint32_t)rows * seg_bytes, ab = (uint32_t)rows * arowbytes;
-            mbar_arrive_expect_tx(&full[slot], wb + ab);
+            // the batch's rows lie inside the matrix and the segment inside a row
+            // (bounds-checking build); a refused batch is armed with no bytes
+            const bool in = qg_guard(o0 >= 0 && rows >= 1 && o0 + rows <= p.O && seg_col + seg_bytes <= rowbytes, err);
+            mbar_arrive_expect_tx(&full[slot], in ? wb + ab : 0u);
+            if (!in) return;
             uint8_t *dw = stage_w + (size_t)slot * L.stage_w;
             if (nsplit == 1) {
                 bulk_copy_g2s(dw, F::w_src(p, o0, 0u), wb, &full[slot]);
@@ -338,7 +342,8 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
                 const float *rs = red + (size_t)slot * nc * NV + lane;
                 float acc = 0.f;
                 for (int w = 0; w < nc; ++w) acc += rs[(size_t)w * NV];
-                if (o0 + r < p.O) out[((size_t)split * S + s) * p.O + o0 + r] = acc;
+                if (o0 + r < p.O && qg_guard(split < nsplit && s < S, err))
+                    out[((size_t)split * S + s) * p.O + o0 + r] = acc;
             }
             __syncwarp();
             if (lane == 0 && k + nst < n_my) issue(k + nst);
@@ -365,8 +370,9 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
 #pragma unroll
         for (int s = 0; s < ST; ++s) {
             const int tok = tg * ST + s;              // a padding token (tok >= S) reads zeros
-            F::template load_x<XU, NP>(p, tok < S ? tok : 0, (uok[j] && tok < S) ? uidx[j] : -1, xp[j][s],
-                                       xsum[j][s]);
+            const int tx = tok < S ? tok : 0, ux = (uok[j] && tok < S) ? uidx[j] : -1;
+            F::template load_x<XU, NP>(p, tx, qg_guard(x_unit_in_bounds<F>(p, tx, S, ux, XU), err) ? ux : -1,
+                                       xp[j][s], xsum[j][s]);
         }
     }
     const typename F::ThreadScale ts = F::template prepare_x<U, ST, NP>(xp, xsum);
@@ -565,14 +571,7 @@ void launch_tma(const typename F::Params &p, float *out, const TmaPlan &pl, cuda
     const void *kfn = moe ? reinterpret_cast<const void *>(kern_moe) : reinterpret_cast<const void *>(kern);
     // The shared-memory limit is an attribute of the kernel in the current
     // context: set once per context and kernel.
-    static PerContext<char> attr_set[2];
-    char done = 0;
-    attr_set[moe ? 1 : 0].get(&done, [kfn](char *v) {
-        cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-        cudaGetLastError();
-        *v = 1;
-        return (int)kOk;
-    });
+    set_max_dynamic_smem(kfn, 232448);
     const int threads = 32 * (pl.nc + 1);
     int per_sm = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kfn, threads, pl.L.total) != cudaSuccess ||

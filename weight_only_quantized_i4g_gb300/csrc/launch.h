@@ -74,6 +74,14 @@ class PerContext {
     int next_ = 0;
 };
 
+// Sets a kernel's dynamic shared-memory limit (bytes) in the current context,
+// once per (context, kernel).  The record lives in one table of this library
+// (not in a static of a template function: those are merged across every
+// loaded copy of a library by the dynamic loader, so a second copy -- such as
+// the bounds-checking build in a test process -- would see the first copy's
+// kernels as configured and skip its own).
+void set_max_dynamic_smem(const void *kernel, int bytes);
+
 size_t ws_i4g(int S, int I, int O, int gs);
 size_t ws_fp8b128(int S, int I, int O);
 size_t ws_fp8ue8m0(int S, int I, int O);
