@@ -86,8 +86,11 @@ __global__ void encode_mq4v2_kernel(uint8_t *__restrict__ blocks, const float *_
         const float zf = __half2float(z16);
         const uint32_t hd = (uint32_t)__half_as_ushort(sc16) | ((uint32_t)__half_as_ushort(z16) << 16);
         // Header and payload go out as aligned 32-bit words (the block base is
-        // 8-byte aligned): single-byte stores of the fp16 bits were observed
-        // to lose the low byte on this toolchain, whole words never did.
+        // 8-byte aligned).  An 8-bit store of the low byte of an fp16
+        // conversion result stores 0 on this toolchain (the .b16 result
+        // register straight into st.global.b8; reproduced by
+        // tests/f16_byte_store_repro.cu), so the header bytes are never stored
+        // one by one.
         reinterpret_cast<uint32_t *>(blk)[h] = hd;
         uint32_t *pay = reinterpret_cast<uint32_t *>(blk + 8 + 64 * h);
         for (int k = 0; k < 16; ++k) {            // word k holds weights 8k..8k+7 of the half
