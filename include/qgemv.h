@@ -22,6 +22,14 @@
  *   per-device caches (SM count, that word's address, kernel attributes).
  * - Calls are asynchronous on `stream` (0 = legacy default stream).  No call
  *   synchronises the host.  Outputs are fully overwritten, never accumulated.
+ * - A call's kernels may start while the previous kernel on `stream` is still
+ *   running (programmatic dependent launch) and stream the weights, scales
+ *   and the expert table's matrices into shared memory before they wait for
+ *   it; activations, routing ids and workspace are read, and outputs
+ *   written, only after that kernel has completed.  So weights that a kernel
+ *   writes (qg_encode_* included) must not come from the kernel just before
+ *   the call on `stream`: put another kernel, an event wait or a host
+ *   synchronisation between them.
  * - Activations x are row-major [S, I]; outputs y are row-major f32 [S, O]
  *   (y[s*O + o]).  bf16 activations are passed as their raw 16-bit patterns.
  * - Every argument is validated on the host BEFORE any pointer is touched or
