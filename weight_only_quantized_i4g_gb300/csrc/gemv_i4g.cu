@@ -220,6 +220,7 @@ struct MmaI4G {
     static constexpr int kSpansPerUnit = 1;
     static constexpr bool kFenceUnits = true;
     static constexpr int kMaxConsumerWarps = 14;   // 7168 columns; 136 registers a thread
+    static constexpr int kRedStride = 4;           // four tokens per launch
     typedef FmtI4G::Params Params;
     typedef float Side;
     __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.rb; }
@@ -321,7 +322,8 @@ bool i4g_mma_ok(const float *x, const uint8_t *w, const float *scales, int I, in
 // S <= 4 tokens per launch (two MMA columns each)
 bool i4g_mma_plan(int S, int I, int O, int gs, MmaPlan *pl) {
     return mma_plan(I / 64, 8, (uint32_t)(I / 2), (uint32_t)((I + gs - 1) / gs) * 4u, 4u, S, O, 16,
-                    MmaI4G<0>::kMaxConsumerWarps, [](int sp) { return 32u * (uint32_t)sp; }, pl);
+                    MmaI4G<0>::kMaxConsumerWarps, MmaI4G<0>::kRedStride, [](int sp) { return 32u * (uint32_t)sp; },
+                    pl);
 }
 
 bool i4g_tma_plan(int S, int I, int O, int gs, TmaPlan *pl) {

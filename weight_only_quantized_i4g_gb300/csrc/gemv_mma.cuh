@@ -120,6 +120,8 @@ __device__ __forceinline__ Pow2Split pow2_split(int k) { return Pow2Split{pow2i(
 //   Side, side(row_w, row_a, off)   side data of (row, unit)
 //   kNeg8           D starts at -8 sum(x) (fmt=4's offset nibbles)
 //   kMaxConsumerWarps  consumer warps of a block (the register budget)
+//   kRedStride      floats per (warp, batch row) of the partial sums: the
+//                   most tokens one launch carries (4 with kHiLo, else 8)
 //   kFenceUnits     keep each unit's shared loads after the previous unit
 //                   (register pressure)
 //   apply(acc, d, s0, s1, X)        fold a unit's D into the accumulators
@@ -129,7 +131,7 @@ struct MmaLayout {
     uint32_t group_pitch;  // bytes between the staged groups of four rows (32 mod 128)
     uint32_t stage_w;      // bytes per ring slot, weights
     uint32_t stage_a;      // bytes per ring slot, side data
-    uint32_t red_off;      // partial sums: [pass parity][slot][warp][RB][8] floats
+    uint32_t red_off;      // partial sums: [pass parity][slot][warp][RB][F::kRedStride] floats
     uint32_t bar_off;      // full[nst], empty[nst], x_full, x_free
     uint32_t x_stride;     // bytes between the staged activation rows
     uint32_t total;
@@ -182,6 +184,8 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
     uint8_t *stage_a = smem + (size_t)nst * L.stage_w;
     uint8_t *xstage = smem + (size_t)(nst - nxs) * L.stage_w;   // the activations, then ring slots again
     float *red = reinterpret_cast<float *>(smem + L.red_off);
+    constexpr int RS = F::kRedStride;
+    static_assert(RS >= (F::kHiLo ? 4 : 8), "a batch row holds every token's partial sum");
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bar_off);
     uint64_t *empty = full + nst;
     uint64_t *x_full = empty + nst, *x_free = x_full + 1;
@@ -296,12 +300,12 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
             // pass parity, which batch k + nst does not write.
             if (k + nst < n_my) issue(k + nst);
             const int o0 = (b + k * Gx) * RB;
-            const float *rs = red + (size_t)((((k / nst) & 1) * nst + slot) * nc) * RB * 8;
+            const float *rs = red + (size_t)((((k / nst) & 1) * nst + slot) * nc) * RB * RS;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             for (int w = 0; w < nc; ++w)
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
-                    if (ri[v] >= 0) acc[v] += rs[((size_t)w * RB + ri[v]) * 8 + si[v]];
+                    if (ri[v] >= 0) acc[v] += rs[((size_t)w * RB + ri[v]) * RS + si[v]];
 #pragma unroll
             for (int v = 0; v < 4; ++v)
                 if (ri[v] >= 0 && o0 + ri[v] < p.O && qg_guard(split < nsplit && si[v] < S, err))
@@ -462,7 +466,7 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
     const Pow2Split u0 = pow2_split(10 + Fd0), u1 = pow2_split(10 + Fd1);
 
     const uint32_t sw0 = smem_addr(stage_w), sa0 = smem_addr(stage_a);
-    float *redw = red + (size_t)cw * RB * 8;
+    float *redw = red + (size_t)cw * RB * RS;
     // MMA rows g and g + 8 of this lane: batch rows batch_row(g), batch_row(g + 8)
     const int row_lo = batch_row(g), row_hi = batch_row(g + 8);
     const uint32_t rw_lo = staged_row_off(row_lo, L.group_pitch, seg_bytes);
@@ -477,7 +481,7 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
         }
         const uint32_t swb = sw0 + (uint32_t)slot * L.stage_w;
         const uint32_t sab = sa0 + (uint32_t)slot * L.stage_a;
-        float *rslot = redw + (size_t)((((k / nst) & 1) * nst + slot) * nc) * RB * 8;
+        float *rslot = redw + (size_t)((((k / nst) & 1) * nst + slot) * nc) * RB * RS;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
@@ -510,17 +514,17 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
         // partial sums of this warp's spans, unscaled, per (batch row, token)
         if constexpr (F::kHiLo) {
             if (t < S) {
-                rslot[(size_t)row_lo * 8 + t] = (acc[0] + acc[1]) * u0.a * u0.b;
-                rslot[(size_t)row_hi * 8 + t] = (acc[2] + acc[3]) * u0.a * u0.b;
+                rslot[(size_t)row_lo * RS + t] = (acc[0] + acc[1]) * u0.a * u0.b;
+                rslot[(size_t)row_hi * RS + t] = (acc[2] + acc[3]) * u0.a * u0.b;
             }
         } else {
             if (2 * t < S) {
-                rslot[(size_t)row_lo * 8 + 2 * t] = acc[0] * u0.a * u0.b;
-                rslot[(size_t)row_hi * 8 + 2 * t] = acc[2] * u0.a * u0.b;
+                rslot[(size_t)row_lo * RS + 2 * t] = acc[0] * u0.a * u0.b;
+                rslot[(size_t)row_hi * RS + 2 * t] = acc[2] * u0.a * u0.b;
             }
             if (2 * t + 1 < S) {
-                rslot[(size_t)row_lo * 8 + 2 * t + 1] = acc[1] * u1.a * u1.b;
-                rslot[(size_t)row_hi * 8 + 2 * t + 1] = acc[3] * u1.a * u1.b;
+                rslot[(size_t)row_lo * RS + 2 * t + 1] = acc[1] * u1.a * u1.b;
+                rslot[(size_t)row_hi * RS + 2 * t + 1] = acc[3] * u1.a * u1.b;
             }
         }
         __syncwarp();
@@ -551,11 +555,12 @@ struct MmaPlan {
 
 // Plan for rows of nsp spans (64 weights each), `granule` spans per column
 // split boundary, rowbytes / arowbytes staged per row (whole row), xelem
-// bytes per activation, and span_bytes(sp) the byte offset of span sp.
+// bytes per activation, red_stride = the format's kRedStride, and
+// span_bytes(sp) the byte offset of span sp.
 // False if the shape does not fit.
 template <class SpanBytes>
 bool mma_plan(int nsp, int granule, uint32_t rowbytes, uint32_t arowbytes, uint32_t xelem, int S, int O, int RB,
-              int max_warps, SpanBytes span_bytes, MmaPlan *pl) {
+              int max_warps, int red_stride, SpanBytes span_bytes, MmaPlan *pl) {
     if (nsp < 1 || RB != 16) return false;
     int splits = (nsp + kMmaSpansPerWarp * max_warps - 1) / (kMmaSpansPerWarp * max_warps);
     int sps = (nsp + splits - 1) / splits;
@@ -583,7 +588,7 @@ bool mma_plan(int nsp, int granule, uint32_t rowbytes, uint32_t arowbytes, uint3
     const uint32_t x_stride = (xseg + 127u) / 128u * 128u + 16u;
     const int x_slots = (int)(((uint32_t)S * x_stride + stage_w - 1) / stage_w);
     const uint32_t stage_a = (uint32_t)(((RB * arowbytes) + 127u) / 128u * 128u);
-    const uint32_t red = (uint32_t)nc * RB * 8u * 4u;
+    const uint32_t red = (uint32_t)nc * RB * (uint32_t)red_stride * 4u;
     const uint32_t per_slot = stage_w + stage_a + 2u * red + 16u;   // + x_full, x_free below
     // about 16 consumer warps per SM; as many slots (2..6) as fit
     int per_sm = std::max(1, 16 / nc);
@@ -593,7 +598,7 @@ bool mma_plan(int nsp, int granule, uint32_t rowbytes, uint32_t arowbytes, uint3
         if (budget > 232448) budget = 232448;
         budget -= 16;
         nst = (int)std::min<long>(6, budget / per_slot);
-        if (nst >= 2) break;
+        if (nst >= 2 && nst - x_slots >= 1) break;   // a slot left beside the activations
     }
     if (nst < 2 || nst - x_slots < 1) return false;
     pl->nc = nc;

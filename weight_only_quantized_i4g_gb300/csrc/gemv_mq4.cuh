@@ -405,6 +405,7 @@ struct MmaMq4 {
     static constexpr int kSpansPerUnit = 2;
     static constexpr bool kFenceUnits = false;
     static constexpr int kMaxConsumerWarps = 15;   // 128 registers a thread
+    static constexpr int kRedStride = 8;           // eight tokens per launch
     typedef Mq4Params Params;
     struct Side { float s, z; };
     __device__ static uint32_t row_bytes(const Params &p) { return (uint32_t)p.rowbytes; }
@@ -466,6 +467,7 @@ inline bool mq4_mma_ok(const uint16_t *x, const uint8_t *blocks) {
 inline bool mq4_mma_plan(int S, int I, int O, MmaPlan *pl) {
     // column splits on 16-byte boundaries: whole pairs of blocks (272 bytes)
     return mma_plan(I / 64, 8, (uint32_t)((I / 256) * 136), 0u, 2u, S, O, 16, MmaMq4<44>::kMaxConsumerWarps,
+                    MmaMq4<44>::kRedStride,
                     [](int sp) { return 136u * (uint32_t)(sp >> 2); }, pl);
 }
 
