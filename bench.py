@@ -1057,6 +1057,9 @@ def main():
                          "i4g/fp8/fp8ue8m0/mq4/mq4v1/mq4c, M=512) and print their prefill object")
     ap.add_argument("--prefill-reps", type=int, default=20)
     ap.add_argument("--moe-only", action="store_true", help="profiling runs: print only the routed-expert lines")
+    ap.add_argument("--stamps", action="store_true",
+                    help="profiling runs: per-block timelines of the batch-1 4-bit GEMVs (stamps build) and the "
+                         "launch-chain floor")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1073,7 +1076,9 @@ def main():
     if world is not None and int(world) != args.gpus:
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: launch one process per GPU "
                          f"(torchrun --nproc-per-node {args.gpus}) or pass the matching --gpus")
-    if args.prefill_only:
+    if args.stamps:
+        stamps_only(args)
+    elif args.prefill_only:
         prefill_only(args)
     elif args.moe_only:
         moe_only(args)
@@ -1081,6 +1086,118 @@ def main():
         reference_arm(args)
     else:
         ours_arm(args)
+
+
+STAMP_SHAPES = (("fmt4_2048x7168", "i4g", 2048, 7168), ("fmt4_7168x2048", "i4g", 7168, 2048),
+                ("mq4v2_17408x5120", "mq4", 17408, 5120))
+STAMP_PHASES = (("start_to_wait", 0, 1), ("wait_to_x", 1, 2), ("x_to_first_batch", 2, 3),
+                ("first_to_last_batch", 3, 4), ("last_batch_to_stored", 4, 5), ("block_total", 0, 5))
+FLOOR_GRIDS = ((152, 256), (608, 96), (152, 352))
+
+
+def stamps_only(args):
+    """Per-block timelines of batch-1 decode GEMVs from the stamps build of the
+    library (qg_stamps_take), and the floor of a chain of empty
+    programmatic-dependent launches (qg_selftest_pdl_chain).  Each shape runs
+    as a CUDA graph of back-to-back calls over >= 3x L2 of weight copies (the
+    per-shape timing's scheme); the stamps are those of the graph's last call,
+    whose predecessor on the stream is the same GEMV.  Prints one JSON line:
+    per shape the graph-timed us per call of the stamps build and of
+    libqgemv.so, and over the blocks the median and maximum of each phase in
+    SM cycles and in us at the median SM clock sampled meanwhile, the spread
+    of the blocks' start times (global timer) and the row batches per block;
+    per launch shape the floor in us per launch."""
+    import ctypes
+    import torch
+    import weight_only_quantized_i4g_gb300 as qg
+    from weight_only_quantized_i4g_gb300 import _build
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream()
+    slib = ctypes.CDLL(_build.build_stamps())
+    P, I_, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    slib.qgemv_i4g.argtypes = [P, P, P, P, I_, I_, I_, I_, P, Z, P]
+    slib.qgemv_i4g.restype = I_
+    slib.qgemv_mq4v2.argtypes = [P, P, P, I_, I_, I_, P, Z, P]
+    slib.qgemv_mq4v2.restype = I_
+    clocks = ClockSampler(0)
+    clocks.start()
+    l2 = 129 * 2 ** 20
+    shapes, raw_stamps = {}, {}
+    st = stream.cuda_stream
+    for name, fmt, O, I in STAMP_SHAPES:
+        raw = make_raw(name, fmt, O, I, 1 if fmt == "i4g" else 3)
+        _, _, x, y, keep, wsb, (wsp, nws) = build_device_call(qg, torch, fmt, O, I, raw, dev, stream)
+        nbytes = weight_bytes(fmt, O, I)
+        copies = min(64, max(1, -(-3 * l2 // nbytes)))
+        wsets = [keep] + [tuple(t.clone() for t in keep) for _ in range(copies - 1)]
+        xp, yp = x.data_ptr(), y.data_ptr()
+        reps = max(copies, 60)
+
+        def issue_with(lib, r):
+            k = wsets[r % len(wsets)]
+            if fmt == "i4g":
+                rc = lib.qgemv_i4g(yp, xp, k[0].data_ptr(), k[1].data_ptr(), 1, I, O, GS, wsp, nws, st)
+            else:
+                rc = lib.qgemv_mq4v2(yp, xp, k[0].data_ptr(), 1, I, O, wsp, nws, st)
+            if rc:
+                raise qg.QGError(rc)
+
+        us_normal = _graph_per_call(torch, stream, reps, lambda r: issue_with(qg._lib, r)) * 1e3
+        # the stamps build: timed replays of one graph, then one more replay
+        # whose last call leaves its stamps
+        gr = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(gr, stream=stream):
+            for r in range(reps):
+                issue_with(slib, r)
+        best = None
+        for _ in range(4):
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                ev0.record(stream)
+                gr.replay()
+                ev1.record(stream)
+            ev1.synchronize()
+            t = ev0.elapsed_time(ev1) / reps
+            best = t if best is None else min(best, t)
+        us_stamps = best * 1e3
+        rc, blocks = qg.qg_stamps_take(qg.STAMP_BLOCKS, lib=slib)      # clear
+        qg.check(rc)
+        with torch.cuda.stream(stream):
+            gr.replay()
+        rc, blocks = qg.qg_stamps_take(qg.STAMP_BLOCKS, lib=slib)
+        qg.check(rc)
+        del gr
+        raw_stamps[name] = [b for b in blocks if b[0] != 0]
+        shapes[name] = {"us_per_call": round(us_normal, 3), "us_per_call_stamps_build": round(us_stamps, 3),
+                        "calls": reps, "weight_copies": copies}
+        del wsets, keep, x, y, wsb
+        torch.cuda.empty_cache()
+    floors = {}
+    for blocks_n, threads in FLOOR_GRIDS:
+        floors[f"{blocks_n}x{threads}"] = round(
+            _graph_per_call(torch, stream, 1, lambda r: qg.check(
+                qg.qg_selftest_pdl_chain(blocks_n, threads, 2000, st))) * 1e3 / 2000, 3)
+    ck = clocks.stop()
+    mhz = ck["sm_mhz"] if ck else 2070.0
+    for name, bl in raw_stamps.items():
+        d = shapes[name]
+        d["blocks"] = len(bl)
+        d["batches_per_block"] = sorted({int(b[6]) for b in bl})
+        g0 = [b[7] for b in bl]
+        d["start_spread_us"] = round((max(g0) - min(g0)) / 1e3, 3) if g0 else None
+        for ph, a, b_ in STAMP_PHASES:
+            cyc = sorted(int(b[b_]) - int(b[a]) for b in bl if b[b_] and b[a])
+            if not cyc:
+                continue
+            med = cyc[len(cyc) // 2]
+            d[ph] = {"median_cycles": med, "max_cycles": cyc[-1], "median_us": round(med / mhz, 3),
+                     "max_us": round(cyc[-1] / mhz, 3)}
+    print(json.dumps({"stamps": shapes, "pdl_chain_floor_us_per_launch": floors, "clocks": ck,
+                      "phases": "per block, SM cycles between: start, wait for the previous kernel returned, "
+                                "activations ready, first batch landed (warp-MMA: after the activation setup), "
+                                "consumers done with the last batch, last output stored"}), flush=True)
 
 
 def moe_only(args):

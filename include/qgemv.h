@@ -117,6 +117,32 @@ unsigned long long qg_launch_count(void);
  * (NULL observed or spin_limit out of range) or QG_ECUDA. */
 int qg_selftest_wait_timeout(int spin_limit, int *observed);
 
+/* Profiling aids (no counterpart in the pages).
+ *
+ * qg_stamps_take: in the stamps build of this library (libqgemv_stamps.so,
+ * built with `_build.py --stamps`), every block of a staged or warp-MMA
+ * decode GEMV records its timeline: 8 words per block b (b < 2048, b =
+ * blockIdx.x + gridDim.x * blockIdx.y), in order the SM clock (clock64) at
+ * the block's start, when its wait for the previous kernel on the stream
+ * returned, when its activations were ready, when its first row batch had
+ * landed (warp-MMA kernel: after the activation setup), when its consumers
+ * had finished its last batch and when its last output was stored; then the
+ * number of row batches it ran and the global timer (ns) at its start.
+ * Later calls overwrite earlier ones block by block.  Synchronizes the
+ * device, copies min(max_blocks, 2048) blocks' words to `host` (8 uint64 per
+ * block) and zeroes them on the device.  Returns QG_OK, QG_EINVAL (NULL host,
+ * max_blocks < 1, or a library built without stamps) or QG_ECUDA.
+ *
+ * qg_selftest_pdl_chain: enqueues `launches` launches (1 .. 100000) of an
+ * empty kernel of `blocks` x `threads` threads (1 .. 65535, 32 .. 1024 and a
+ * multiple of 32) on `stream` with programmatic stream serialization, the
+ * launch mode of every GEMV here; each launch lets the next start early,
+ * waits for the previous one and adds one to a device word.  Its time per
+ * launch is the floor under any of these kernels that waits for its
+ * predecessor.  Returns QG_OK, QG_EINVAL or QG_ECUDA; asynchronous. */
+int qg_stamps_take(uint64_t *host, int max_blocks);
+int qg_selftest_pdl_chain(int blocks, int threads, int launches, qg_stream_t stream);
+
 /* Format ids for qg_workspace_bytes. */
 enum {
     QG_FMT_I4G = 4,         /* grouped int4 (fmt=4)                            */

@@ -35,7 +35,7 @@ def test_header_lists_the_entry_points():
                  "qg_workspace_bytes", "qg_gemm_workspace_bytes", "qg_device_status",
                  "qg_strerror", "qg_last_error", "qg_quantize_i4g", "qg_encode_mq4v2", "qg_fwht256",
                  "qgemv_moe", "qgemm_moe", "qgemv_q2_0", "qg_launch_count", "qgemv_i4g_noalloc",
-                 "qg_selftest_wait_timeout"]:
+                 "qg_selftest_wait_timeout", "qg_stamps_take", "qg_selftest_pdl_chain"]:
         assert must in names, names
 
 
@@ -203,3 +203,22 @@ def test_selftest_refusals(qg):
     assert lib.qg_selftest_wait_timeout(0, ctypes.byref(v)) == qg.QG_EINVAL
     assert lib.qg_selftest_wait_timeout((1 << 22) + 1, ctypes.byref(v)) == qg.QG_EINVAL
     assert "spin_limit" in qg.last_error()
+
+
+def test_profiling_aid_refusals(qg):
+    """The stamps reader refuses bad arguments, and refuses outright in the
+    normal build (which records no stamps); the launch chain refuses bad
+    launch shapes before any launch."""
+    n0 = qg.qg_launch_count()
+    lib = ctypes.CDLL(qg.LIB_PATH)
+    lib.qg_stamps_take.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    buf = (ctypes.c_uint64 * 8)()
+    assert lib.qg_stamps_take(None, 1) == qg.QG_EINVAL
+    assert lib.qg_stamps_take(buf, 0) == qg.QG_EINVAL
+    rc, _ = qg.qg_stamps_take(1)
+    assert rc == qg.QG_EINVAL and "without stamps" in qg.last_error()
+    for blocks, threads, launches in [(0, 256, 1), (65536, 256, 1), (152, 31, 1), (152, 48, 1), (152, 2048, 1),
+                                      (152, 256, 0), (152, 256, 100001)]:
+        assert qg.qg_selftest_pdl_chain(blocks, threads, launches, 0) == qg.QG_EINVAL
+    assert "launches" in qg.last_error()
+    assert qg.qg_launch_count() == n0

@@ -40,6 +40,8 @@ _SIGNATURES = {
     "qg_device_status": ([ctypes.POINTER(_I)], _I),
     "qg_launch_count": ([], ctypes.c_ulonglong),
     "qg_selftest_wait_timeout": ([_I, ctypes.POINTER(_I)], _I),
+    "qg_stamps_take": ([ctypes.POINTER(ctypes.c_uint64), _I], _I),
+    "qg_selftest_pdl_chain": ([_I, _I, _I, _P], _I),
     "qgemv_i4g": ([_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P], _I),
     "qgemv_i4g_noalloc": ([_P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "qgemv_fp8b128": ([_P, _P, _P, _P, _I, _I, _I, _P, _Z, _P], _I),
@@ -129,6 +131,27 @@ def qg_selftest_wait_timeout(spin_limit: int) -> tuple[int, int]:
     v = _I(0)
     rc = _lib.qg_selftest_wait_timeout(spin_limit, ctypes.byref(v))
     return rc, v.value
+
+
+STAMP_SLOTS = 8        # words per block of qg_stamps_take
+STAMP_BLOCKS = 2048    # blocks it records
+
+
+def qg_stamps_take(max_blocks: int = STAMP_BLOCKS, lib=None):
+    """(status, list of per-block 8-word lists) from qg_stamps_take of `lib`
+    (a ctypes handle of the stamps build; this package's library refuses)."""
+    lib = lib if lib is not None else _lib
+    buf = (ctypes.c_uint64 * (STAMP_SLOTS * max_blocks))()
+    f = lib.qg_stamps_take
+    f.argtypes = [ctypes.POINTER(ctypes.c_uint64), _I]
+    f.restype = _I
+    rc = f(buf, max_blocks)
+    words = list(buf)
+    return rc, [words[STAMP_SLOTS * b:STAMP_SLOTS * (b + 1)] for b in range(max_blocks)]
+
+
+def qg_selftest_pdl_chain(blocks: int, threads: int, launches: int, stream=None) -> int:
+    return _lib.qg_selftest_pdl_chain(blocks, threads, launches, _stream(stream))
 
 
 def qg_workspace_bytes(fmt: int, S: int, I: int, O: int, gs: int = 0) -> int:

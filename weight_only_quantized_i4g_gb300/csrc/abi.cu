@@ -160,6 +160,14 @@ const char *qg_last_error(void) { return error_detail(); }
 
 unsigned long long qg_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int qg_stamps_take(uint64_t *host, int max_blocks) {
+    if (host == nullptr || max_blocks < 1) {
+        set_error_detail("qg_stamps_take: host must be non-NULL and max_blocks >= 1 (got %d)", max_blocks);
+        return kEInval;
+    }
+    return stamps_take(reinterpret_cast<unsigned long long *>(host), max_blocks);
+}
+
 int qg_device_status(int *status) {
     if (!status) QG_REFUSE(kEInval, "qg_device_status: status must be non-NULL");
     cudaError_t e = cudaDeviceSynchronize();

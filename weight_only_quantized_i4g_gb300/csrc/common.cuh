@@ -142,6 +142,43 @@ __device__ __forceinline__ bool qg_guard(bool ok, int *err) {
 __device__ __forceinline__ constexpr bool qg_guard(bool, int *) { return true; }
 #endif
 
+// Timeline stamps of the stamps build (compiled with -DQG_STAMPS, for
+// profiling): block b = blockIdx.x + gridDim.x * blockIdx.y (b <
+// kStampBlocks) of a staged or warp-MMA decode GEMV writes kStampSlots 64-bit
+// words at stamp area + b * kStampSlots: clock64 when the block starts
+// (kStEntry), when its wait for the previous kernel returned (kStWaitDone),
+// when its activations were ready (kStXReady), when its first row batch had
+// landed (kStFirstBatch; on the warp-MMA kernel after the activation setup),
+// when its consumers finished the last batch (kStConsumed) and when its last
+// output was stored (kStStored); the number of row batches it ran
+// (kStBatches) and the global timer in ns at its start (kStGlobalEntry).  The
+// stamp area follows the device error word `err` (in that build its symbol is
+// an array).  Routed-expert launches (grid z) are not told apart.  In other
+// builds the calls compile to nothing.
+constexpr int kStampSlots = 8, kStampBlocks = 2048, kStampOffsetInts = 4;
+enum StampSlot {
+    kStEntry = 0, kStWaitDone = 1, kStXReady = 2, kStFirstBatch = 3, kStConsumed = 4, kStStored = 5,
+    kStBatches = 6, kStGlobalEntry = 7
+};
+#ifdef QG_STAMPS
+__device__ __forceinline__ void qg_stamp_put(int *err, int slot, unsigned long long v) {
+    const unsigned b = blockIdx.x + gridDim.x * blockIdx.y;
+    if (err != nullptr && b < (unsigned)kStampBlocks)
+        reinterpret_cast<unsigned long long *>(err + kStampOffsetInts)[(size_t)b * kStampSlots + slot] = v;
+}
+__device__ __forceinline__ void qg_stamp(int *err, int slot) { qg_stamp_put(err, slot, (unsigned long long)clock64()); }
+__device__ __forceinline__ void qg_stamp_entry(int *err) {
+    unsigned long long g;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g));
+    qg_stamp_put(err, kStEntry, (unsigned long long)clock64());
+    qg_stamp_put(err, kStGlobalEntry, g);
+}
+#else
+__device__ __forceinline__ void qg_stamp_put(int *, int, unsigned long long) {}
+__device__ __forceinline__ void qg_stamp(int *, int) {}
+__device__ __forceinline__ void qg_stamp_entry(int *) {}
+#endif
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);

@@ -16,8 +16,13 @@
 namespace qg {
 
 // One error word per device: kernels that give up waiting set it; the host
-// reads and clears it with qg_device_status().
+// reads and clears it with qg_device_status().  The stamps build keeps the
+// kernels' timeline stamps after it (common.cuh).
+#ifdef QG_STAMPS
+__device__ __align__(16) int g_device_error[kStampOffsetInts + 2 * kStampSlots * kStampBlocks];
+#else
 __device__ int g_device_error = 0;
+#endif
 
 unsigned long long current_context_id() {
     typedef CUresult (*GetCurrentFn)(CUcontext *);
@@ -61,6 +66,32 @@ void set_max_dynamic_smem(const void *kernel, int bytes) {
     table[next] = Entry{id, kernel};
     next = (next + 1) % 512;
     if (n < 512) ++n;
+}
+
+int stamps_take(unsigned long long *host, int max_blocks) {
+#ifdef QG_STAMPS
+    const int nb = max_blocks < kStampBlocks ? max_blocks : kStampBlocks;
+    void *p = nullptr;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, g_device_error);
+    unsigned long long *area =
+        p != nullptr ? reinterpret_cast<unsigned long long *>(static_cast<int *>(p) + kStampOffsetInts) : nullptr;
+    if (e == cudaSuccess)
+        e = cudaMemcpy(host, area, (size_t)nb * kStampSlots * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(area, 0, (size_t)kStampBlocks * kStampSlots * sizeof(unsigned long long));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        set_error_detail("qg_stamps_take: %s", cudaGetErrorString(e));
+        return kECuda;
+    }
+    return kOk;
+#else
+    (void)host;
+    (void)max_blocks;
+    set_error_detail("qg_stamps_take: this library was built without stamps (the stamps build is "
+                     "libqgemv_stamps.so, from _build.py --stamps)");
+    return kEInval;
+#endif
 }
 
 int *device_error_word() {

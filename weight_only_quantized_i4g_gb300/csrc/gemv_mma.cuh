@@ -238,6 +238,7 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
     const int first = min(nst, n_my), nw0 = min(nst - nxs, first);
     if (warp == 0) {
         if (lane == 0) {
+            qg_stamp_entry(err);
             griddep_launch_dependents();
             for (int s = 0; s < nst; ++s) {
                 mbar_init(&full[s], 1);
@@ -267,6 +268,7 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
         // the wait for it, ahead of the other free slots' weight copies,
         // because the consumers need them before any batch.
         griddep_wait();
+        if (lane == 0) qg_stamp(err, kStWaitDone);
         if (lane == 0) mbar_arrive_expect_tx(x_full, (uint32_t)S * xseg_bytes);
         __syncwarp();
         for (int s = lane; s < S; s += 32)
@@ -312,6 +314,10 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
                     out[((size_t)split * S + si[v]) * p.O + o0 + ri[v]] = acc[v];
             __syncwarp();
         }
+        if (lane == 0) {
+            qg_stamp(err, kStStored);
+            qg_stamp_put(err, kStBatches, (unsigned long long)n_my);
+        }
         return;
     }
 
@@ -330,6 +336,7 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
         if (lane == 0) raise_device_error(err, kErrTimeout);
         return;
     }
+    if (tid == 32) qg_stamp(err, kStXReady);
     // Setup.  The staged activations of this warp's spans are entries of
     // eight (span sp, word j, lane t: elements 16 t + 8 j .. +7 of the span)
     // per token.  All 32 lanes share the work of scaling them to fp16 in
@@ -479,6 +486,7 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
             if (lane == 0) raise_device_error(err, kErrTimeout);
             return;
         }
+        if (tid == 32 && k == 0) qg_stamp(err, kStFirstBatch);
         const uint32_t swb = sw0 + (uint32_t)slot * L.stage_w;
         const uint32_t sab = sa0 + (uint32_t)slot * L.stage_a;
         float *rslot = redw + (size_t)((((k / nst) & 1) * nst + slot) * nc) * RB * RS;
@@ -530,6 +538,7 @@ __device__ __forceinline__ void gemv_mma_body(const typename F::Params &p, float
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
     }
+    if (tid == 32) qg_stamp(err, kStConsumed);
 }
 
 // One block per SM of at most F::kMaxConsumerWarps + 1 warps: the B

@@ -279,6 +279,7 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
     uint64_t *empty = full + nst;
 
     if (tid == 0) {
+        qg_stamp_entry(err);
         griddep_launch_dependents();
         for (int s = 0; s < nst; ++s) {
             mbar_init(&full[s], 1);
@@ -348,11 +349,16 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
             __syncwarp();
             if (lane == 0 && k + nst < n_my) issue(k + nst);
         }
+        if (lane == 0) {
+            qg_stamp(err, kStStored);
+            qg_stamp_put(err, kStBatches, (unsigned long long)n_my);
+        }
         return;
     }
 
     // ------------------------------- consumers ----------------------------------
     griddep_wait();   // x may be the previous kernel's output
+    if (tid == 32) qg_stamp(err, kStWaitDone);
     const int cw = warp - 1;
     const int ct = tid - 32;
     const int tg = TG == 1 ? 0 : ct % TG;             // token group (lane % TG)
@@ -376,6 +382,7 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
         }
     }
     const typename F::ThreadScale ts = F::template prepare_x<U, ST, NP>(xp, xsum);
+    if (tid == 32) qg_stamp(err, kStXReady);
     typename F::StageConst scur[U], snext[U];
 #pragma unroll
     for (int j = 0; j < U; ++j) scur[j] = F::stage_const(p, b * RB, tc[j]);
@@ -389,6 +396,7 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
             if (lane == 0) raise_device_error(err, kErrTimeout);
             return;
         }
+        if (tid == 32 && k == 0) qg_stamp(err, kStFirstBatch);
         const uint32_t swb = sw0 + (uint32_t)slot * L.stage_w;
         const uint32_t sab = sa0 + (uint32_t)slot * L.stage_a;
         float part[NT];
@@ -446,6 +454,7 @@ __device__ __forceinline__ void gemv_tma_body(const typename F::Params &p, float
 #pragma unroll
         for (int j = 0; j < U; ++j) scur[j] = snext[j];
     }
+    if (tid == 32) qg_stamp(err, kStConsumed);
 }
 
 // A token-split kernel is capped for two blocks per SM (64 registers): the

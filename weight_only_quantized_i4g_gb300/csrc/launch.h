@@ -28,6 +28,10 @@ inline void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed);
 // Reads and clears this device's kernel error word (0 or a qg status).
 int read_device_error(int *status);
 
+// Stamps build: copies min(max_blocks, kStampBlocks) blocks' timeline stamps
+// to host and clears them (qg_stamps_take); kEInval in other builds.
+int stamps_take(unsigned long long *host, int max_blocks);
+
 // A process-unique id of the CUDA context current on this thread (the
 // driver's context id), 0 when no context is current or the driver cannot
 // say.  Device addresses of the library's __device__ variables and kernel

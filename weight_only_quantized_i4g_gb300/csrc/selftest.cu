@@ -14,6 +14,7 @@ int *device_error_word();   // cs_common.cu
 constexpr uint32_t kSelftestBytes = 4096;
 static __device__ __align__(128) uint8_t g_selftest_src[kSelftestBytes];   // copy source (zeros)
 static __device__ int g_selftest_seen;                                     // what the block observed
+static __device__ unsigned g_chain_word;                                   // counted by the launch chain
 
 // Two warps.  Warp 0 (producer) streams one batch into the ring slot with a
 // bulk copy and waits for the consumer to release the slot; warp 1 (consumer)
@@ -68,9 +69,40 @@ __global__ void __launch_bounds__(64) selftest_wait_timeout_kernel(uint32_t limi
     }
 }
 
+// One link of the launch chain: let the next launch start, wait for the
+// previous one, count.
+__global__ void selftest_pdl_chain_kernel() {
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    griddep_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0) g_chain_word += 1u;
+}
+
 }  // namespace qg
 
 using namespace qg;
+
+extern "C" int qg_selftest_pdl_chain(int blocks, int threads, int launches, qg_stream_t stream) {
+    if (blocks < 1 || blocks > 65535 || threads < 32 || threads > 1024 || threads % 32 != 0 || launches < 1 ||
+        launches > 100000) {
+        set_error_detail("qg_selftest_pdl_chain: blocks in [1, 65535], threads in [32, 1024] (a multiple of 32), "
+                         "launches in [1, 100000] (got %d, %d, %d)", blocks, threads, launches);
+        return kEInval;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    for (int i = 0; i < launches; ++i) {
+        cudaLaunchKernelEx(&cfg, selftest_pdl_chain_kernel);
+        count_launch();
+    }
+    return check_launch("qg_selftest_pdl_chain");
+}
 
 extern "C" int qg_selftest_wait_timeout(int spin_limit, int *observed) {
     if (observed == nullptr) {
