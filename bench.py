@@ -451,7 +451,13 @@ def ours_arm(args):
     # end to end through the C ABI with host buffers: every step copies its
     # activations host->device in one copy from a pinned staging buffer (each
     # call's x at a 256-byte aligned offset), runs the GEMVs on them, and
-    # copies all outputs device->host in one copy
+    # copies all outputs device->host in one copy into pinned memory.  Steps
+    # are pipelined as a serving loop would run them: two sets of device
+    # buffers, the uploads and the read-backs on their own streams, so that
+    # step i+1's upload and step i-1's read-back overlap step i's GEMVs; event
+    # waits keep each buffer's reuse in order (an upload waits until the
+    # GEMVs two steps back have read its buffer, the GEMVs wait for their
+    # upload and for the read-back that last used their output buffer).
     def packed(tensors):
         offs, n = [], 0
         for t in tensors:
@@ -461,40 +467,68 @@ def ours_arm(args):
 
     xoffs, h2d = packed([c["x"] for c in calls])
     yoffs, d2h = packed([c["y"] for c in calls])
-    xdev = torch.empty(h2d, dtype=torch.uint8, device=dev)
-    ydev = torch.zeros(d2h, dtype=torch.uint8, device=dev)
+    xdev = [torch.empty(h2d, dtype=torch.uint8, device=dev) for _ in range(2)]
+    ydev = [torch.zeros(d2h, dtype=torch.uint8, device=dev) for _ in range(2)]
     xhost = torch.empty(h2d, dtype=torch.uint8).pin_memory()
-    yhost = torch.zeros(d2h, dtype=torch.uint8).pin_memory()
+    yhost = [torch.zeros(d2h, dtype=torch.uint8).pin_memory() for _ in range(2)]
     for c, o in zip(calls, xoffs):
         xb = c["x"].contiguous().reshape(-1).view(torch.uint8).cpu()
         xhost[o:o + xb.numel()].copy_(xb)
-    e2e_ptrs = [(xdev.data_ptr() + xo, ydev.data_ptr() + yo) for xo, yo in zip(xoffs, yoffs)]
+    e2e_ptrs = [[(xdev[b].data_ptr() + xo, ydev[b].data_ptr() + yo) for xo, yo in zip(xoffs, yoffs)]
+                for b in range(2)]
+    up_stream, down_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    x_ready = [torch.cuda.Event() for _ in range(2)]
+    x_read = [torch.cuda.Event() for _ in range(2)]
+    y_ready = [torch.cuda.Event() for _ in range(2)]
+    y_out = [torch.cuda.Event() for _ in range(2)]
+    for b in range(2):          # every buffer starts free
+        x_read[b].record(stream)
+        y_out[b].record(stream)
     e_start = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
     e2e_steps = max(1, min(args.steps, 2000))
 
-    def e2e_step():
-        xdev.copy_(xhost, non_blocking=True)
-        for c, (xp, yp) in zip(calls, e2e_ptrs):
+    def e2e_step(i):
+        b = i & 1
+        up_stream.wait_event(x_read[b])
+        with torch.cuda.stream(up_stream):
+            xdev[b].copy_(xhost, non_blocking=True)
+        x_ready[b].record(up_stream)
+        stream.wait_event(x_ready[b])
+        stream.wait_event(y_out[b])
+        for c, (xp, yp) in zip(calls, e2e_ptrs[b]):
             rc = c["call"](xp, yp)
             if rc:
                 raise qg.QGError(rc)
-        yhost.copy_(ydev, non_blocking=True)
+        x_read[b].record(stream)
+        y_ready[b].record(stream)
+        down_stream.wait_event(y_ready[b])
+        with torch.cuda.stream(down_stream):
+            yhost[b].copy_(ydev[b], non_blocking=True)
+        y_out[b].record(down_stream)
+
+    def drained():
+        # the compute stream waits for the last read-backs
+        for b in range(2):
+            stream.wait_event(y_out[b])
 
     with torch.cuda.stream(stream):
-        for _ in range(min(args.warmup, 10)):
-            e2e_step()
+        for i in range(min(args.warmup, 10)):
+            e2e_step(i)
+        drained()
         barrier()
         e_start.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        up_stream.wait_event(e_start)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        drained()
         e_end.record(stream)
     barrier()
-    # the host copy of the outputs must equal the device-timed outputs
+    # the host copies of the outputs must equal the device-timed outputs
     e2e_match = all(
-        torch.equal(yhost[o:o + c["y"].numel() * c["y"].element_size()],
+        torch.equal(yhost[b][o:o + c["y"].numel() * c["y"].element_size()],
                     c["y"].contiguous().reshape(-1).view(torch.uint8).cpu())
-        for c, o in zip(calls, yoffs))
+        for b in range(min(2, e2e_steps)) for c, o in zip(calls, yoffs))
     e2e_ms = e_start.elapsed_time(e_end)
 
     if world > 1:
@@ -555,7 +589,9 @@ def ours_arm(args):
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "copies_per_step": {"h2d": 1, "d2h": 1}, "outputs_match_device_run": e2e_match},
+                    "copies_per_step": {"h2d": 1, "d2h": 1}, "outputs_match_device_run": e2e_match,
+                    "pipelining": "two device buffer sets; each step's upload and read-back run on their "
+                                  "own streams, overlapping the neighbouring steps' GEMVs"},
             "gpu_launches": launches,
             "clocks": clocks,
             "per_format": per_format,
