@@ -18,8 +18,10 @@
  * ---------------------------------------
  * - All data pointers are DEVICE pointers owned by the caller.  The library
  *   allocates no device memory and never frees anything.  Its only state is
- *   one 4-byte error word per device (see qg_device_status) and host-side
- *   per-device caches (SM count, that word's address, kernel attributes).
+ *   one 4-byte error word per device (see qg_device_status; in the stamps
+ *   build, libqgemv_stamps.so, followed by the timeline stamps of
+ *   qg_stamps_take) and host-side per-device caches (SM count, that word's
+ *   address, kernel attributes).
  * - Calls are asynchronous on `stream` (0 = legacy default stream).  No call
  *   synchronises the host.  Outputs are fully overwritten, never accumulated.
  * - A call's kernels may start while the previous kernel on `stream` is still
