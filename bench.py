@@ -356,6 +356,24 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(values, world, device=None):
+    """Each value's maximum over the ranks of the process group (the slowest
+    rank's time); the values themselves at world size 1."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_gbs(bytes_per_rank_step, world, ms_per_step):
+    """Weight GB/s of the whole job: every rank streams bytes_per_rank_step
+    per step (replicas), all in ms_per_step (the slowest rank's)."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
 def ours_arm(args):
     import torch
     import weight_only_quantized_i4g_gb300 as qg
@@ -531,15 +549,11 @@ def ours_arm(args):
         for b in range(min(2, e2e_steps)) for c, o in zip(calls, yoffs))
     e2e_ms = e_start.elapsed_time(e_end)
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = float(t[0]), float(t[1])
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], world, dev)
 
     ms_per_step = elapsed_ms / args.steps
-    value = nbytes * world / (ms_per_step * 1e-3) / 1e9
-    e2e_value = nbytes * world / (e2e_ms / e2e_steps * 1e-3) / 1e9
+    value = whole_job_gbs(nbytes, world, ms_per_step)
+    e2e_value = whole_job_gbs(nbytes, world, e2e_ms / e2e_steps)
     dom_bytes = calls[dom]["bytes"]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
 
