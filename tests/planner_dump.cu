@@ -1,0 +1,48 @@
+// planner_dump.cu -- prints the launch plans the decode GEMVs would choose
+// for a sweep of shapes and token counts: host code only, linked against
+// libqgemv.so, no GPU needed (the planners assume 152 SMs without a device).
+// One CSV line per plan; tests/test_planners.py checks each plan's
+// shared-memory layout.
+#include <cstdio>
+
+#include "gemv_fp8.cuh"
+#include "gemv_mma.cuh"
+#include "gemv_mq4.cuh"
+#include "gemv_tma.cuh"
+
+namespace qg {
+bool plan_i4g_mma(int S, int I, int O, int gs, MmaPlan *pl);   // gemv_i4g.cu
+bool plan_i4g_tma(int S, int I, int O, int gs, TmaPlan *pl);
+}  // namespace qg
+
+using namespace qg;
+
+static void dump_mma(const char *fmt, int S, int I, int O, const MmaPlan &p) {
+    printf("mma,%s,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%u,%u,%u,%u,%u,%u,%u\n", fmt, S, I, O, p.nc, p.splits, p.per_sm,
+           p.G.nsp, p.G.sps, p.G.nrowb, p.G.nst, p.G.x_slots, p.L.group_pitch, p.L.stage_w, p.L.stage_a, p.L.red_off,
+           p.L.bar_off, p.L.x_stride, p.L.total);
+}
+
+static void dump_tma(const char *fmt, int S, int I, int O, const TmaPlan &p) {
+    printf("tma,%s,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%u,%u,%u,%u,%u\n", fmt, S, I, O, p.rb, p.units, p.U, p.nc,
+           p.splits, p.units_per_split, p.nrowb, p.nst, p.per_sm, p.L.stage_w, p.L.stage_a, p.L.red_off, p.L.bar_off,
+           p.L.total);
+}
+
+int main() {
+    const int Is[] = {256, 512, 768, 1024, 1280, 2048, 2560, 4096, 5120, 6144, 7168, 8192, 9216,
+                      12288, 16384, 17408, 24576, 32768, 61440, 65536};
+    const int Os[] = {1, 7, 16, 33, 100, 640, 1000, 2048, 2560, 5120, 7168, 17408, 24576};
+    for (int S = 1; S <= 8; ++S)
+        for (int I : Is)
+            for (int O : Os) {
+                MmaPlan mp;
+                TmaPlan tp;
+                if (mq4::mq4_mma_plan(S, I, O, &mp)) dump_mma("mq4", S, I, O, mp);
+                if (mq4::mq4_tma_plan(S, I, O, &tp)) dump_tma("mq4", S, I, O, tp);
+                if (S <= 4 && plan_i4g_mma(S, I, O, 64, &mp)) dump_mma("i4g", S, I, O, mp);
+                if (plan_i4g_tma(S, I, O, 64, &tp)) dump_tma("i4g", S, I, O, tp);
+                if (fp8_tma_plan(S, I, O, &tp)) dump_tma("fp8", S, I, O, tp);
+            }
+    return 0;
+}

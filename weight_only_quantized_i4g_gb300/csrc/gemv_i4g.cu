@@ -455,6 +455,11 @@ int gemv_i4g_chunk(float *y, const float *x, const uint8_t *w, const float *scal
 
 }  // namespace
 
+// The fmt=4 decode planners above, exported (host code) for the test suite's
+// checks of the shared-memory layouts they choose over a sweep of shapes.
+bool plan_i4g_mma(int S, int I, int O, int gs, MmaPlan *pl) { return i4g_mma_plan(S, I, O, gs, pl); }
+bool plan_i4g_tma(int S, int I, int O, int gs, TmaPlan *pl) { return i4g_tma_plan(S, I, O, gs, pl); }
+
 size_t ws_i4g(int S, int I, int O, int gs) {
     const int s = S < 8 ? S : 8;
     size_t mma_need = 0;
