@@ -1,5 +1,6 @@
-"""The launch plans of the staged and warp-MMA decode GEMVs, checked on the
-CPU over a sweep of shapes (O x I x S: 13 x 20 x 8, every format).
+"""The launch plans of the staged and warp-MMA decode GEMVs (O x I x S: 13 x
+20 x 8, every format) and of the tensor-core prefill GEMM (M x I x O: 11 x 20
+x 13, and 200 routed-expert calls of seeded group sizes), checked on the CPU.
 
 tests/planner_dump.cu calls the library's own planners (host code, linked
 against libqgemv.so; without a GPU they plan for 152 SMs) and prints every
@@ -8,7 +9,12 @@ limit and the share of an SM its block count was sized for, keep every
 region 16-byte aligned for the bulk copies and 8-byte aligned for the
 mbarriers, keep its regions apart (ring slots, side data, partial sums,
 barriers; the activations inside the last ring slots), cover every row and
-every column of the matrix once, and respect the kernels' static limits."""
+every column of the matrix once, and respect the kernels' static limits.  A
+prefill plan's tiles must cover the output, its blocks split the (tile, K
+step) units without going past the SMs, and its workspace regions (tile
+counters, partial slots when a tile's K range is shared, token scales,
+weight-row exponents, the fp16 copy of X) must be 256-byte aligned, in order
+and large enough."""
 import os
 import shutil
 import subprocess
@@ -128,9 +134,52 @@ def test_tma_plans(plans):
 
 def test_decode_shapes_are_planned(plans):
     """The decode workloads' shapes get a plan on the paths they run."""
-    have = {(r[0], r[1], int(r[2]), int(r[3]), int(r[4])) for r in plans}
+    have = {(r[0], r[1], int(r[2]), int(r[3]), int(r[4])) for r in plans if r[0] in ("mma", "tma")}
     for key in [("tma", "i4g", 1, 7168, 2048), ("tma", "i4g", 1, 2048, 7168), ("tma", "fp8", 1, 16384, 7168),
                 ("tma", "fp8", 1, 7168, 24576), ("tma", "mq4", 1, 17408, 5120), ("mma", "mq4", 1, 5120, 17408),
                 ("mma", "mq4", 8, 5120, 17408), ("mma", "mq4", 8, 17408, 5120), ("mma", "i4g", 4, 2048, 7168),
                 ("mma", "i4g", 4, 7168, 2048)]:
         assert key in have, key
+
+
+GEMM_BT = (256, 128, 64)
+
+
+def check_gemm(r, grouped, tiles=None):
+    M, I, O, n, tile, bt, MB, NB, Kt, P = map(int, r[1:11])
+    T, U, counter, xscale, wexp, xh, ws = map(int, r[11:18])
+    what = f"{r[0]} M={M} I={I} O={O} groups={n}: {r[5:]}"
+    assert bt == GEMM_BT[tile], what
+    assert NB == cdiv(O, 128) and Kt == cdiv(I, 128), what
+    if grouped:
+        assert T == tiles, what                      # every group's token blocks times the output tiles
+    else:
+        assert MB == cdiv(M, bt) and T == MB * NB, what
+    assert U == T * Kt and 1 <= P <= min(U, 152), what
+    split = not (U % P == 0 and (U // P) % Kt == 0)
+    for off in (counter, xscale, wexp, xh, ws):
+        assert off % 256 == 0, what
+    assert counter >= 4 * T, what
+    assert xscale >= counter + (2 * P * 128 * bt * 4 if split else 0), what
+    assert wexp - xscale >= (cdiv(M, 256) + (1 if grouped else 0)) * 256 * 4, what
+    assert xh - wexp >= (n if grouped else 1) * O * 4, what
+    assert ws - xh >= M * I * 2, what
+
+
+def test_gemm_plans(plans):
+    n = 0
+    for r in plans:
+        if r[0] == "gemm":
+            check_gemm(r, False)
+            n += 1
+    assert n > 2000
+
+
+def test_grouped_gemm_plans(plans):
+    n = 0
+    for r, nxt in zip(plans, plans[1:]):
+        if r[0] == "ggemm":
+            assert nxt[0] == "gtiles"
+            check_gemm(r, True, int(nxt[1]))
+            n += 1
+    assert n == 200
