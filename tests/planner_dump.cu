@@ -11,6 +11,7 @@
 #include "gemv_mq4.cuh"
 #include "gemv_tma.cuh"
 #include "gemm_tc.cuh"
+#include "../../include/qgemv.h"
 
 namespace qg {
 bool plan_i4g_mma(int S, int I, int O, int gs, MmaPlan *pl);   // gemv_i4g.cu
@@ -19,16 +20,22 @@ bool plan_i4g_tma(int S, int I, int O, int gs, TmaPlan *pl);
 
 using namespace qg;
 
+// the workspace the C ABI asks callers for at this shape (last field)
+static size_t ws_query(const char *fmt, int S, int I, int O) {
+    const int id = fmt[0] == 'i' ? QG_FMT_I4G : fmt[0] == 'm' ? QG_FMT_MQ4V2 : QG_FMT_FP8B128;
+    return qg_workspace_bytes(id, S, I, O, 64);
+}
+
 static void dump_mma(const char *fmt, int S, int I, int O, const MmaPlan &p) {
-    printf("mma,%s,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%u,%u,%u,%u,%u,%u,%u\n", fmt, S, I, O, p.nc, p.splits, p.per_sm,
-           p.G.nsp, p.G.sps, p.G.nrowb, p.G.nst, p.G.x_slots, p.L.group_pitch, p.L.stage_w, p.L.stage_a, p.L.red_off,
-           p.L.bar_off, p.L.x_stride, p.L.total);
+    printf("mma,%s,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%u,%u,%u,%u,%u,%u,%u,%zu\n", fmt, S, I, O, p.nc, p.splits,
+           p.per_sm, p.G.nsp, p.G.sps, p.G.nrowb, p.G.nst, p.G.x_slots, p.L.group_pitch, p.L.stage_w, p.L.stage_a,
+           p.L.red_off, p.L.bar_off, p.L.x_stride, p.L.total, ws_query(fmt, S, I, O));
 }
 
 static void dump_tma(const char *fmt, int S, int I, int O, const TmaPlan &p) {
-    printf("tma,%s,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%u,%u,%u,%u,%u\n", fmt, S, I, O, p.rb, p.units, p.U, p.nc,
+    printf("tma,%s,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%d,%u,%u,%u,%u,%u,%zu\n", fmt, S, I, O, p.rb, p.units, p.U, p.nc,
            p.splits, p.units_per_split, p.nrowb, p.nst, p.per_sm, p.L.stage_w, p.L.stage_a, p.L.red_off, p.L.bar_off,
-           p.L.total);
+           p.L.total, ws_query(fmt, S, I, O));
 }
 
 static void dump_gemm(const char *kind, int M, int I, int O, int n, const tc::Plan &p) {

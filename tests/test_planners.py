@@ -9,7 +9,9 @@ limit and the share of an SM its block count was sized for, keep every
 region 16-byte aligned for the bulk copies and 8-byte aligned for the
 mbarriers, keep its regions apart (ring slots, side data, partial sums,
 barriers; the activations inside the last ring slots), cover every row and
-every column of the matrix once, and respect the kernels' static limits.  A
+every column of the matrix once, respect the kernels' static limits, and,
+where it splits rows over blocks, get at least its workspace from
+qg_workspace_bytes.  A
 prefill plan's tiles must cover the output, its blocks split the (tile, K
 step) units without going past the SMs, and its workspace regions (tile
 counters, partial slots when a tile's K range is shared, token scales,
@@ -100,6 +102,9 @@ def test_mma_plans(plans):
         assert bar_off == red_off + 2 * nst * red and bar_off % 16 == 0, what
         assert total == bar_off + 16 * nst + 16, what
         assert total <= SMEM_BLOCK and per_sm >= 1 and total <= SMEM_SM // per_sm - 1024, what
+        # a split writes its segments' sums to the caller's workspace: the size query covers it
+        if splits > 1:
+            assert int(r[20]) >= splits * S * O * 4, what
     assert n > 500
 
 
@@ -129,6 +134,9 @@ def test_tma_plans(plans):
         assert bar_off >= red_off + nst * nc * next_pow2(rb * S) * 4 and bar_off % 16 == 0, what
         assert total == bar_off + 16 * nst, what
         assert total <= SMEM_BLOCK and per_sm >= 1 and total <= SMEM_SM // per_sm - 1024, what
+        # a split writes its segments' sums to the caller's workspace: the size query covers it
+        if splits > 1:
+            assert int(r[19]) >= splits * S * O * 4, what
     assert n > 2000
 
 
