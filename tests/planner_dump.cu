@@ -53,8 +53,8 @@ static unsigned long long mix(unsigned long long &s) {
 
 int main() {
     const int Is[] = {256, 512, 768, 1024, 1280, 2048, 2560, 4096, 5120, 6144, 7168, 8192, 9216,
-                      12288, 16384, 17408, 24576, 32768, 61440, 65536};
-    const int Os[] = {1, 7, 16, 33, 100, 640, 1000, 2048, 2560, 5120, 7168, 17408, 24576};
+                      12288, 16384, 17408, 24576, 32768, 61440, 65536, 1 << 20, 1 << 22};
+    const int Os[] = {1, 7, 16, 33, 100, 640, 1000, 2048, 2560, 5120, 7168, 17408, 24576, 1 << 20, 1 << 24};
     for (int S = 1; S <= 8; ++S)
         for (int I : Is)
             for (int O : Os) {

@@ -1,6 +1,7 @@
-"""The launch plans of the staged and warp-MMA decode GEMVs (O x I x S: 13 x
-20 x 8, every format) and of the tensor-core prefill GEMM (M x I x O: 11 x 20
-x 13, and 200 routed-expert calls of seeded group sizes), checked on the CPU.
+"""The launch plans of the staged and warp-MMA decode GEMVs (O x I x S: 15 x
+22 x 8, every format, up to 2^24 rows and 2^22 columns) and of the
+tensor-core prefill GEMM (M x I x O: 11 x 22 x 15, and 200 routed-expert
+calls of seeded group sizes), checked on the CPU.
 
 tests/planner_dump.cu calls the library's own planners (host code, linked
 against libqgemv.so; without a GPU they plan for 152 SMs) and prints every
